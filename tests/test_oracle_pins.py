@@ -1,0 +1,286 @@
+"""Pins of the CPU oracle to facts fixed outside itself.
+
+Each check is a function of the oracle's outputs, so the same check is run
+on planted mistakes (a dropped column, a transposed operand, a missing
+scale) to show it would catch them.  Citations name sections/equations of
+"PuzzleKV: Page-Wise Low-Rank Decomposition for KV Cache Compression".
+"""
+import itertools
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden", "pages_printed_values.json")
+
+
+def _page(P, d, seed, k=6, n_out=2):
+    spec = synth.KVSpec(layers=1, kv_heads=1, head_dim=d, page_size=P, inner_rank=k,
+                        n_outliers=n_out, dtype=torch.float32)
+    K, _ = synth.prefill_kv(spec, P, seq=seed)
+    return K[0, 0].double().numpy()
+
+
+# ---------------------------------------------------------------- SVD pins
+
+def eckart_young_defect(X, L, R, S, r):
+    """| ||X - L R||_F^2 - sum_{i>r} S_i^2 | / ||X||_F^2  (§3.2: the rank-r
+    truncation attains the discarded singular-value energy)."""
+    err = np.sum((X - L @ R) ** 2)
+    tail = np.sum(S[r:] ** 2)
+    tot = np.sum(X ** 2)
+    return max(abs(err - tail), abs(tot - np.sum(S ** 2))) / max(tot, 1e-300)
+
+
+def orthonormality_defect(L, R, S, r):
+    """max of |L^T L - I| and |R R^T - diag(S_r^2)| / S_1^2."""
+    a = np.abs(L.T @ L - np.eye(r)).max()
+    b = np.abs(R @ R.T - np.diag(S[:r] ** 2)).max() / max(S[0] ** 2, 1e-300)
+    return max(a, b)
+
+
+@pytest.mark.parametrize("P,d,r", [(4, 4, 1), (4, 4, 2), (16, 32, 5), (32, 64, 8), (32, 64, 32), (64, 128, 16), (64, 128, 24)])
+def test_eckart_young_and_orthonormality(P, d, r):
+    for seed in range(3):
+        X = _page(P, d, seed, k=min(6, P))
+        L, R, S = oracle.factorize(X, r)
+        assert eckart_young_defect(X, L, R, S, r) < 1e-12
+        assert orthonormality_defect(L, R, S, r) < 1e-12
+        assert np.all(np.diff(S) <= 0)
+
+
+def test_singular_values_match_lapack():
+    rng = np.random.default_rng(1)
+    for P, d in [(4, 4), (8, 8), (32, 64), (64, 128)]:
+        X = rng.standard_normal((P, d)) * rng.uniform(0.1, 10, size=(1, d))
+        _, S, _, sweeps = oracle.svd(X)
+        ref = np.linalg.svd(X, compute_uv=False)
+        assert sweeps > 0
+        assert np.abs(S - ref).max() <= 1e-12 * ref[0]
+
+
+def test_two_by_two_closed_form():
+    """Singular values of a 2 x d page from the closed-form eigenvalues of
+    the 2 x 2 Gram X X^T: (tr +- sqrt(tr^2 - 4 det)) / 2."""
+    rng = np.random.default_rng(2)
+    for d in (2, 3, 8):
+        X = rng.standard_normal((2, d))
+        G = X @ X.T
+        tr, det = G[0, 0] + G[1, 1], G[0, 0] * G[1, 1] - G[0, 1] ** 2
+        disc = math.sqrt(max(tr * tr - 4 * det, 0.0))
+        lam = np.array([(tr + disc) / 2, (tr - disc) / 2])
+        _, S, _, _ = oracle.svd(X)
+        assert np.allclose(S ** 2, lam, rtol=1e-12, atol=1e-12 * tr)
+
+
+def _best_sampled_error(X, r, samples, rng):
+    """Smallest ||X - Q Q^T X||^2 over random orthonormal P x r frames Q."""
+    P = X.shape[0]
+    best = np.inf
+    for _ in range(samples):
+        Q, _ = np.linalg.qr(rng.standard_normal((P, r)))
+        best = min(best, np.sum((X - Q @ (Q.T @ X)) ** 2))
+    return best
+
+
+@pytest.mark.parametrize("r", [1, 2])
+def test_brute_force_4x4(r):
+    """Eckart-Young on 4 x 4 pages by brute force over frames on the sphere:
+    no sampled rank-r projection beats the oracle, and the sampled minimum,
+    refined by alternating projection from its frame, reaches it."""
+    rng = np.random.default_rng(3 + r)
+    for _ in range(4):
+        X = rng.standard_normal((4, 4))
+        L, R, S = oracle.factorize(X, r)
+        opt = np.sum((X - L @ R) ** 2)
+        best = _best_sampled_error(X, r, 20000, rng)
+        assert best >= opt * (1 - 1e-12)
+        assert best <= opt + 0.05 * np.sum(X ** 2)
+        # local refinement: orthogonal iteration started from a random frame
+        Q, _ = np.linalg.qr(rng.standard_normal((4, r)))
+        for _ in range(2000):
+            Q, _ = np.linalg.qr(X @ (X.T @ Q))
+        refined = np.sum((X - Q @ (Q.T @ X)) ** 2)
+        assert abs(refined - opt) <= 1e-9 * np.sum(X ** 2)
+
+
+def test_degenerate_pages():
+    """All-zero page: zero factors, orthonormal L; rank-1 page: exact at r=1."""
+    X = np.zeros((8, 16))
+    L, R, S = oracle.factorize(X, 3)
+    assert np.all(S == 0) and np.all(R == 0)
+    assert np.abs(L.T @ L - np.eye(3)).max() == 0
+    rng = np.random.default_rng(4)
+    u, v = rng.standard_normal(8), rng.standard_normal(16)
+    X = np.outer(u, v)
+    L, R, S = oracle.factorize(X, 1)
+    assert np.abs(X - L @ R).max() < 1e-12 * np.abs(X).max()
+    assert abs(S[0] - np.linalg.norm(u) * np.linalg.norm(v)) < 1e-12 * S[0]
+
+
+def test_planted_factor_mistakes_are_caught():
+    X = _page(32, 64, 5)
+    r = 8
+    L, R, S = oracle.factorize(X, r)
+    L_drop = L.copy(); L_drop[:, 3] = 0.0                   # dropped column
+    assert eckart_young_defect(X, L_drop, R, S, r) > 1e-6
+    R_sign = R.copy(); R_sign[2] *= -1.0                     # wrong sign
+    assert eckart_young_defect(X, L, R_sign, S, r) > 1e-6
+    L_perm = L[:, ::-1].copy()                               # wrong index order
+    assert eckart_young_defect(X, L_perm, R, S, r) > 1e-6
+    L_bad = L + 1e-3 * np.random.default_rng(0).standard_normal(L.shape)
+    assert orthonormality_defect(L_bad, R, S, r) > 1e-6
+
+
+# ---------------------------------------------------------- attention pins
+
+def test_attention_special_cases():
+    rng = np.random.default_rng(6)
+    d = 16
+    q = rng.standard_normal((3, d))
+    # one key: softmax of a single score is 1
+    K1, V1 = rng.standard_normal((1, d)), rng.standard_normal((1, d))
+    assert np.allclose(oracle.attention(q, K1, V1), np.repeat(V1, 3, 0), rtol=0, atol=1e-15)
+    # identical keys: uniform weights, output is the mean value row
+    K = np.repeat(rng.standard_normal((1, d)), 7, 0)
+    V = rng.standard_normal((7, d))
+    assert np.allclose(oracle.attention(q, K, V), np.repeat(V.mean(0, keepdims=True), 3, 0), atol=1e-14)
+    # two keys: logistic weight of the score difference, scores scaled by 1/sqrt(d)
+    K2, V2 = rng.standard_normal((2, d)), rng.standard_normal((2, d))
+    out = oracle.attention(q, K2, V2)
+    for g in range(3):
+        s = K2 @ q[g] / math.sqrt(d)
+        w = 1.0 / (1.0 + math.exp(s[1] - s[0]))
+        assert np.allclose(out[g], w * V2[0] + (1 - w) * V2[1], atol=1e-14)
+    # a dominant key takes all the weight
+    Kd = np.zeros((5, d)); Kd[2] = q[0] * 1e4
+    Vd = rng.standard_normal((5, d))
+    assert np.allclose(oracle.attention(q[:1], Kd, Vd)[0], Vd[2], atol=1e-12)
+    # permuting tokens leaves the output unchanged
+    K5, V5 = rng.standard_normal((9, d)), rng.standard_normal((9, d))
+    perm = rng.permutation(9)
+    assert np.allclose(oracle.attention(q, K5, V5), oracle.attention(q, K5[perm], V5[perm]), atol=1e-14)
+
+
+def test_planted_missing_scale_is_caught():
+    rng = np.random.default_rng(7)
+    d = 64
+    q, K, V = rng.standard_normal((2, d)), rng.standard_normal((2, d)), rng.standard_normal((2, d))
+    out = oracle.attention(q, K, V)
+    unscaled = oracle.attention(q * math.sqrt(d), K, V)  # as if 1/sqrt(d) were dropped
+    s = K @ q[0] / math.sqrt(d)
+    w = 1.0 / (1.0 + math.exp(s[1] - s[0]))
+    ref = w * V[0] + (1 - w) * V[1]
+    assert np.allclose(out[0], ref, atol=1e-14)
+    assert not np.allclose(unscaled[0], ref, atol=1e-6)
+
+
+def _cache(T, P, d, G, r, seed, window=64, sink=4):
+    spec = synth.KVSpec(layers=1, kv_heads=1, head_dim=d, page_size=P, inner_rank=6,
+                        n_outliers=2, dtype=torch.float32)
+    K, V = synth.prefill_kv(spec, T, seq=seed)
+    K, V = K[0, 0].double().numpy(), V[0, 0].double().numpy()
+    q = synth.queries(1, G, d, step=seed, dtype=torch.float32)[0].double().numpy()
+    kinds = oracle.page_kinds(T, P, sink, window)
+    n = len(kinds)
+    LK = np.zeros((n, P, r)); RK = np.zeros((n, r, d))
+    LV = np.zeros((n, P, r)); RV = np.zeros((n, r, d))
+    for p in range(n):
+        if kinds[p] == oracle.FACTORED:
+            LK[p], RK[p], _ = oracle.factorize(K[p * P:(p + 1) * P], r)
+            LV[p], RV[p], _ = oracle.factorize(V[p * P:(p + 1) * P], r)
+    return q, K, V, kinds, LK, RK, LV, RV
+
+
+def test_full_rank_factorized_attention_equals_dense():
+    """r = min(P, d): every factorized page reconstructs exactly, so mixed
+    attention equals dense attention (§3.3 ④ with eq. (2) at full rank)."""
+    T, P, d, G = 300, 32, 64, 4
+    q, K, V, kinds, LK, RK, LV, RV = _cache(T, P, d, G, r=P, seed=11)
+    assert (kinds == oracle.FACTORED).sum() >= 4
+    mixed = oracle.decode_head(q, kinds, K, V, LK, RK, LV, RV, T, P)
+    dense = oracle.attention(q, K, V)
+    assert np.abs(mixed - dense).max() <= 1e-6 * np.abs(dense).max()
+    assert np.abs(mixed - dense).max() <= 1e-12 * np.abs(dense).max()
+
+
+def test_low_rank_attention_uses_reconstruction():
+    """At r < P the mixed result equals dense attention over the rows L R
+    rebuilt by hand (page-by-page products)."""
+    T, P, d, G, r = 200, 32, 64, 4, 8
+    q, K, V, kinds, LK, RK, LV, RV = _cache(T, P, d, G, r=r, seed=12)
+    Kh, Vh = K.copy(), V.copy()
+    for p in np.nonzero(kinds == oracle.FACTORED)[0]:
+        Kh[p * P:(p + 1) * P] = LK[p] @ RK[p]
+        Vh[p * P:(p + 1) * P] = LV[p] @ RV[p]
+    mixed = oracle.decode_head(q, kinds, K, V, LK, RK, LV, RV, T, P)
+    assert np.abs(mixed - oracle.attention(q, Kh, Vh)).max() <= 1e-12 * np.abs(mixed).max()
+    # a transposed factor or a skipped page changes the result
+    LKt = LK.copy(); f = int(np.nonzero(kinds == oracle.FACTORED)[0][0])
+    LKt[f] = LKt[f][::-1]
+    assert np.abs(oracle.decode_head(q, kinds, K, V, LKt, RK, LV, RV, T, P) - mixed).max() > 1e-6
+
+
+# ------------------------------------------------------ classification pins
+
+def token_level_kinds(T, P, sink, W):
+    """Re-derivation by tokens: a token is dense if it is among the first
+    `sink` tokens or the last W; a page is dense if it holds a dense token or
+    is incomplete (§3.3 ①②③: sink page, local window, page still filling)."""
+    dense_tok = [(t < sink) or (t >= T - W) for t in range(T)]
+    kinds = []
+    for p in range((T + P - 1) // P):
+        toks = range(p * P, min((p + 1) * P, T))
+        incomplete = len(toks) < P
+        kinds.append(oracle.DENSE if incomplete or any(dense_tok[t] for t in toks) else oracle.FACTORED)
+    return np.array(kinds, dtype=np.int32)
+
+
+def test_classification_exhaustive():
+    for P, sink, W in itertools.product((4, 32, 64), (0, 4, 64), (0, 64, 128)):
+        for T in range(1, 700):
+            assert np.array_equal(oracle.page_kinds(T, P, sink, W), token_level_kinds(T, P, sink, W)), (T, P, sink, W)
+
+
+@pytest.mark.parametrize("T,P,sink,W,dense", [
+    (1024, 32, 4, 64, [0, 30, 31]),          # tiny shape
+    (32768, 64, 4, 128, [0, 510, 511]),      # 32K context, P = 64
+    (131072, 64, 4, 128, [0, 2046, 2047]),   # 128K context, P = 64
+    (32769, 64, 4, 128, [0, 510, 511, 512]),
+    (32832, 64, 4, 128, [0, 511, 512]),      # page 510 has left the window
+])
+def test_classification_config_values(T, P, sink, W, dense):
+    kinds = oracle.page_kinds(T, P, sink, W)
+    assert list(np.nonzero(kinds == oracle.DENSE)[0]) == dense
+
+
+# ---------------------------------------------------- printed-value pins
+
+def test_printed_storage_ratios():
+    g = json.load(open(GOLDEN))
+    c = g["storage_ratio_default"]
+    ratio = oracle.page_storage_ratio(c["P"], c["d"], c["rk"], c["rv"])
+    assert round(ratio, c["printed_digits"]) == c["printed"]
+    a = g["storage_ratio_page_size_ablation"]
+    for P, rk, rv in a["configs"]:
+        # "near 63%" printed to whole percent: within half a percent point
+        assert abs(100 * oracle.page_storage_ratio(P, a["d"], rk, rv) - a["printed_percent"]) <= 0.5 + 1e-9
+
+
+def test_printed_footprint_and_kv_size():
+    g = json.load(open(GOLDEN))
+    f = g["steady_state_footprint"]
+    n_pages = f["T"] // f["P"]
+    rho = oracle.page_storage_ratio(f["P"], f["d"], f["rk"], f["rv"])
+    footprint = ((n_pages - f["dense_pages"]) * rho + f["dense_pages"]) / n_pages
+    assert abs(100 * footprint - f["printed_percent"]) < 0.02
+    assert abs(100 * (footprint - rho) - f["printed_gap_pp"]) < 0.02
+    s = g["dense_kv_size"]
+    nbytes = oracle.dense_kv_elements(s["layers"], s["kv_heads"], s["T"], s["d"]) * s["bytes_per_element"]
+    assert nbytes / 2 ** 30 == s["printed_gib"]
