@@ -1,0 +1,209 @@
+/*
+ * puzzlekv.h -- C ABI of the GB300 (sm_103a) PuzzleKV hot path.
+ *
+ * Page-wise low-rank KV cache compression as described in "PuzzleKV:
+ * Page-Wise Low-Rank Decomposition for KV Cache Compression" (cited below as
+ * [PuzzleKV] with its section and equation numbers):
+ *   - every completed page of P tokens of each layer's per-KV-head key and
+ *     value cache, outside a dense sink page and a dense local window, is
+ *     factorized into rank-r factors L (P x r, orthonormal columns) and
+ *     R = L^T X (r x d), through the P x P Gram matrix and its top-r
+ *     eigenvectors                                  [PuzzleKV §3.3 ①②③, eq. (2)]
+ *   - decode attention runs directly over dense and factorized pages with one
+ *     online softmax, never reconstructing a page   [PuzzleKV §3.3 ④, eqs. (4)-(5)]
+ *   - each decoded token is appended to the newest dense page; a page that
+ *     leaves the local window is factorized once    [PuzzleKV §3.3 ⑤]
+ *
+ * Conventions shared by every entry point:
+ *   - All functions are extern "C", never throw and never abort; they return a
+ *     puzzlekv_status.  puzzlekv_last_error() gives a message for the calling
+ *     thread's most recent failure.
+ *   - Arguments are checked on the host before anything is launched; on a
+ *     host-side error nothing is launched and no store state changes.
+ *   - Device work is asynchronous on the given stream (a cudaStream_t passed
+ *     as void*; NULL = legacy default stream).  A CUDA error raised by a
+ *     launch is returned as PUZZLEKV_ERR_CUDA.
+ *   - "device" pointers must point to memory of the current CUDA device and be
+ *     16-byte aligned.  "host" pointers are read before the call returns.
+ *   - The caller allocates and frees every device buffer; the library only
+ *     borrows them.  It allocates no device memory itself.
+ *   - Storage dtype: PUZZLEKV_BF16 (bf16 dense pages and factors, tensor-core
+ *     path) or PUZZLEKV_F32 (fp32, CUDA-core path).  Outputs are fp32.
+ *   - Supported shapes: head_dim d in {64, 128}; page size P in {16, 32, 64}
+ *     with P <= d; 1 <= rank <= P; query heads per KV head G = Hq / H in
+ *     1..8.  Key/value ranks are stored padded to a multiple of 8 (the
+ *     padding is zero and never changes a result).
+ */
+#ifndef PUZZLEKV_H
+#define PUZZLEKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    PUZZLEKV_OK = 0,
+    PUZZLEKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad index or size */
+    PUZZLEKV_ERR_UNSUPPORTED = 2,   /* shape outside the supported set above */
+    PUZZLEKV_ERR_CAPACITY = 3,      /* sequence would exceed max_tokens_per_seq */
+    PUZZLEKV_ERR_NOT_CONVERGED = 4, /* an eigensolve hit its sweep cap (results kept) */
+    PUZZLEKV_ERR_CUDA = 5,          /* a CUDA launch or copy failed */
+    PUZZLEKV_ERR_DEVICE_TIMEOUT = 6 /* a kernel's bounded wait ran out (error flag set) */
+} puzzlekv_status;
+
+typedef enum { PUZZLEKV_F32 = 0, PUZZLEKV_BF16 = 1 } puzzlekv_dtype;
+
+/* Page kinds as stored in the page table [PuzzleKV §3.3 ①②③]. */
+enum { PUZZLEKV_PAGE_FACTORED = 0, PUZZLEKV_PAGE_DENSE = 1 };
+
+/*
+ * Store configuration.  sink_tokens: the first tokens kept dense; the sink
+ * is every page holding one of them.  recent_tokens: width W of the dense
+ * local window; every page holding one of the last W tokens stays dense, and
+ * so does the incomplete last page [PuzzleKV §3.3 ①②③].  max_batch: number
+ * of sequence slots.  max_tokens_per_seq: capacity per sequence.
+ */
+typedef struct {
+    int32_t num_layers;
+    int32_t num_kv_heads;
+    int32_t num_q_heads;
+    int32_t head_dim;
+    int32_t page_size;
+    int32_t rank_k;
+    int32_t rank_v;
+    int32_t sink_tokens;
+    int32_t recent_tokens;
+    int32_t max_batch;
+    int32_t max_tokens_per_seq;
+    int32_t kv_dtype; /* puzzlekv_dtype */
+} puzzlekv_config;
+
+typedef struct puzzlekv_store puzzlekv_store; /* opaque host handle */
+
+/*
+ * Byte sizes of the four device buffers a store borrows for `cfg`:
+ *   dense_pool: dense pages (sink, window, page being filled) for every
+ *               (layer, sequence, KV head), K and V;
+ *   factor_pool: one preallocated factor record per (layer, sequence, KV
+ *               head, page) [PuzzleKV §3.3 ⑤ "preallocated storage"];
+ *   page_table: per (sequence, layer): current length and one descriptor
+ *               per page (kind, slot);
+ *   workspace:  split-K partial softmax states and the device status word.
+ * Host-only; needs no GPU.
+ */
+puzzlekv_status puzzlekv_query_sizes(const puzzlekv_config *cfg, size_t *dense_pool_bytes,
+                                     size_t *factor_pool_bytes, size_t *page_table_bytes,
+                                     size_t *workspace_bytes);
+
+/*
+ * Create a store over caller-allocated device buffers of at least the sizes
+ * puzzlekv_query_sizes reports (all 256-byte aligned).  The buffers stay owned
+ * by the caller and must outlive the store.  The call zero-fills the dense
+ * pool, page table and workspace on `stream` (the factor pool is written
+ * before it is read).  All sequence slots start empty.
+ */
+puzzlekv_status puzzlekv_store_create(const puzzlekv_config *cfg, void *dense_pool, void *factor_pool,
+                                      void *page_table, void *workspace, void *stream,
+                                      puzzlekv_store **out);
+
+/* Free the host handle (not the device buffers). NULL is accepted. */
+puzzlekv_status puzzlekv_store_destroy(puzzlekv_store *store);
+
+/*
+ * Prefill compression of one sequence [PuzzleKV §3.3 ①②③]: given its dense
+ * prompt cache, partition every layer and KV head into pages, copy the dense
+ * pages (sink, local window, incomplete last page) into the dense pool and
+ * factorize every other page -- all layers, heads, keys and values in one
+ * batched launch -- into the factor pool.
+ *   k, v: device, [num_layers][num_kv_heads][T][head_dim] in kv_dtype,
+ *         read-only, may be freed once the stream passes this call.
+ *   seq:  sequence slot in [0, max_batch); any previous content is dropped.
+ *   T:    prompt length, 1 <= T <= max_tokens_per_seq.
+ */
+puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *store, int32_t seq, const void *k,
+                                         const void *v, int32_t T, void *stream);
+
+/*
+ * Stateless batched page factorization [PuzzleKV §3.3 ③ and eq. (2)]:
+ * for each of n independent pages X_i (P x d), G_i = X_i X_i^T in fp32, its
+ * eigenvectors by cyclic Jacobi, L_i = top-r eigenvectors (P x r),
+ * R_i = L_i^T X_i (r x d).
+ *   X:      device, [n][P][d] in x_dtype (row = token).
+ *   L, R:   device, [n][P][r] and [n][r][d] in out_dtype.
+ *   sigma:  device fp32 [n][P] or NULL: sqrt of the eigenvalues (clamped at
+ *           0), descending -- the singular values of X_i.
+ *   status: device int32 or NULL; on return of the stream work, nonzero if
+ *           any page hit the sweep cap (its factors are still written).
+ */
+puzzlekv_status puzzlekv_factorize_batch(const void *X, int32_t x_dtype, int64_t n, int32_t P, int32_t d,
+                                         int32_t r, void *L, void *R, int32_t out_dtype, float *sigma,
+                                         int32_t *status, void *stream);
+
+/*
+ * Append one decoded token per listed sequence to `layer` [PuzzleKV §3.3 ⑤]:
+ * the new key/value rows go into the newest dense page and take part in the
+ * next attention call at once.  When the append moves a completed page out
+ * of the local window, that page (keys and values of every KV head of this
+ * layer) is factorized on `stream` into its preallocated factor record and
+ * its dense slot is released -- at most one page per (sequence, layer) per
+ * call; factorized pages are never revisited.
+ *   k, v:    device, [B][num_kv_heads][head_dim] in kv_dtype.
+ *   seq_ids: host, B distinct sequence slots, each already holding a prompt.
+ */
+puzzlekv_status puzzlekv_append_token(puzzlekv_store *store, int32_t layer, const void *k, const void *v,
+                                      const int32_t *seq_ids, int32_t B, void *stream);
+
+/*
+ * Decode attention of one layer over the hybrid cache [PuzzleKV §3.3 ④]:
+ * for each listed sequence and query head, softmax(q K^T / sqrt(d)) V over all
+ * T cached tokens, with factorized pages evaluated as (q R_K^T) L_K^T and
+ * (p L_V) R_V (eq. (4)) and all pages merged by one online softmax (eq. (5)).
+ * Query head h reads KV head h / G.
+ *   q:       device, [B][num_q_heads][head_dim] in kv_dtype.
+ *   out:     device fp32, [B][num_q_heads][head_dim].
+ *   seq_ids: host, B distinct sequence slots with T >= 1.
+ */
+puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *store, int32_t layer, const void *q, float *out,
+                                          const int32_t *seq_ids, int32_t B, void *stream);
+
+/*
+ * Host-side accounting of one (sequence, layer) from the store's host mirror
+ * (no device access): current length, dense and factorized page counts, and
+ * the bytes those pages occupy (factors at the configured ranks plus the valid
+ * rows of dense pages) [PuzzleKV §4.5 Memory Footprint].
+ */
+puzzlekv_status puzzlekv_store_stats(const puzzlekv_store *store, int32_t seq, int32_t layer, int32_t *length,
+                                     int64_t *dense_pages, int64_t *factored_pages, int64_t *bytes_live);
+
+/*
+ * Synchronise `stream`, read the device status word and clear it.  Returns
+ * PUZZLEKV_ERR_NOT_CONVERGED if an eigensolve hit its sweep cap since the last
+ * check, PUZZLEKV_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out.
+ */
+puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *store, void *stream);
+
+/*
+ * Host-only page classification, the rule the store and its kernels apply
+ * [PuzzleKV §3.3 ①②③, ⑤]: writes PUZZLEKV_PAGE_DENSE or
+ * PUZZLEKV_PAGE_FACTORED for each of the ceil(T/P) pages of a T-token
+ * sequence into kinds[0..cap).  Returns the page count, or -1 on bad
+ * arguments or when cap is too small.
+ */
+int32_t puzzlekv_classify_pages(int32_t T, int32_t P, int32_t sink_tokens, int32_t recent_tokens,
+                                int32_t *kinds, int32_t cap);
+
+/* Storage of one factorized key-value page pair relative to dense,
+ * (r_K + r_V)(P + d) / (2 P d) [PuzzleKV §3.3 eq. (3)]. Host-only. */
+double puzzlekv_page_storage_ratio(int32_t P, int32_t d, int32_t rank_k, int32_t rank_v);
+
+/* Message of the calling thread's most recent failure ("" if none). */
+const char *puzzlekv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PUZZLEKV_H */

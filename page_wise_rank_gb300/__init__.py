@@ -1,0 +1,183 @@
+"""PuzzleKV page-wise low-rank KV cache compression on GB300 (sm_103a).
+
+Python face of the C ABI in include/puzzlekv.h.  The functions here only
+marshal arguments (shapes, dtypes, pointers, the current CUDA stream) into
+the CUDA library; PyTorch provides device memory and streams.  Citations name
+sections/equations of "PuzzleKV: Page-Wise Low-Rank Decomposition for KV
+Cache Compression".
+"""
+from __future__ import annotations
+
+import ctypes
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _lib
+from ._lib import BF16, F32, PAGE_DENSE, PAGE_FACTORED, PuzzleKVError, check, last_error, lib  # noqa: F401
+
+_DT = {torch.float32: F32, torch.bfloat16: BF16}
+_TORCH = {F32: torch.float32, BF16: torch.bfloat16}
+
+
+@dataclass(frozen=True)
+class StoreConfig:
+    num_layers: int
+    num_kv_heads: int
+    num_q_heads: int
+    head_dim: int
+    page_size: int
+    rank_k: int
+    rank_v: int
+    sink_tokens: int
+    recent_tokens: int
+    max_batch: int
+    max_tokens_per_seq: int
+    kv_dtype: torch.dtype = torch.bfloat16
+
+    def c(self) -> _lib.Config:
+        c = _lib.Config()
+        for f in _lib.Config._fields_:
+            name = f[0]
+            setattr(c, name, _DT[self.kv_dtype] if name == "kv_dtype" else getattr(self, name))
+        return c
+
+
+def _stream(stream: Optional[torch.cuda.Stream]) -> ctypes.c_void_p:
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t: torch.Tensor) -> ctypes.c_void_p:
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _need(t: torch.Tensor, shape, dtype, name: str) -> None:
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if tuple(t.shape) != tuple(shape) or t.dtype != dtype or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
+
+
+def _seq_ids(seq_ids: Sequence[int]):
+    arr = (ctypes.c_int32 * len(seq_ids))(*[int(s) for s in seq_ids])
+    return arr, len(seq_ids)
+
+
+def query_sizes(cfg: StoreConfig) -> dict:
+    """Byte sizes of the dense pool, factor pool, page table and workspace."""
+    s = [ctypes.c_size_t() for _ in range(4)]
+    c = cfg.c()
+    check(lib().puzzlekv_query_sizes(ctypes.byref(c), *[ctypes.byref(x) for x in s]))
+    return dict(zip(("dense_pool", "factor_pool", "page_table", "workspace"), (x.value for x in s)))
+
+
+def classify_pages(T: int, P: int, sink_tokens: int, recent_tokens: int) -> np.ndarray:
+    """PAGE_DENSE / PAGE_FACTORED per page of a T-token sequence (host-only)."""
+    n = (T + P - 1) // P
+    out = (ctypes.c_int32 * max(n, 1))()
+    got = lib().puzzlekv_classify_pages(T, P, sink_tokens, recent_tokens, out, n)
+    if got != n:
+        raise ValueError("bad arguments to classify_pages")
+    return np.frombuffer(out, dtype=np.int32, count=n).copy()
+
+
+def page_storage_ratio(P: int, d: int, rank_k: int, rank_v: int) -> float:
+    """(r_K + r_V)(P + d) / (2 P d), eq. (3)."""
+    return float(lib().puzzlekv_page_storage_ratio(P, d, rank_k, rank_v))
+
+
+def factorize_batch(X: torch.Tensor, r: int, out_dtype: torch.dtype = torch.float32, sigma: bool = True,
+                    stream: Optional[torch.cuda.Stream] = None):
+    """Factorize independent pages X[n, P, d] -> (L[n, P, r], R[n, r, d], sigma[n, P] or None, status[1]).
+
+    ``status`` (int32 on the device) is nonzero if an eigensolve hit its sweep cap.
+    """
+    if X.dim() != 3:
+        raise ValueError("X must be [n, P, d]")
+    n, P, d = X.shape
+    _need(X, (n, P, d), X.dtype, "X")
+    if X.dtype not in _DT:
+        raise ValueError("X must be float32 or bfloat16")
+    L = torch.empty(n, P, r, dtype=out_dtype, device=X.device)
+    R = torch.empty(n, r, d, dtype=out_dtype, device=X.device)
+    S = torch.empty(n, P, dtype=torch.float32, device=X.device) if sigma else None
+    status = torch.zeros(1, dtype=torch.int32, device=X.device)
+    check(lib().puzzlekv_factorize_batch(_ptr(X), _DT[X.dtype], n, P, d, r, _ptr(L), _ptr(R), _DT[out_dtype],
+                                         _ptr(S) if S is not None else None, _ptr(status), _stream(stream)))
+    return L, R, S, status
+
+
+class Store:
+    """Paged factor store over four torch-allocated device buffers."""
+
+    def __init__(self, cfg: StoreConfig, device="cuda", stream: Optional[torch.cuda.Stream] = None):
+        self.cfg = cfg
+        sizes = query_sizes(cfg)
+        self.sizes = sizes
+        # 256-byte aligned device buffers (the caching allocator aligns to 512)
+        self.dense_pool = torch.empty(sizes["dense_pool"], dtype=torch.uint8, device=device)
+        self.factor_pool = torch.empty(sizes["factor_pool"], dtype=torch.uint8, device=device)
+        self.page_table = torch.empty(sizes["page_table"], dtype=torch.uint8, device=device)
+        self.workspace = torch.empty(sizes["workspace"], dtype=torch.uint8, device=device)
+        h = ctypes.c_void_p()
+        c = cfg.c()
+        check(lib().puzzlekv_store_create(ctypes.byref(c), _ptr(self.dense_pool), _ptr(self.factor_pool),
+                                          _ptr(self.page_table), _ptr(self.workspace), _stream(stream),
+                                          ctypes.byref(h)))
+        self._h = h
+
+    def close(self) -> None:
+        if getattr(self, "_h", None):
+            lib().puzzlekv_store_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    @property
+    def handle(self) -> ctypes.c_void_p:
+        return self._h
+
+    def factorize_pages(self, seq: int, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+        """Prefill compression of sequence `seq` from dense k, v [L, H, T, d] (§3.3 ①②③)."""
+        c = self.cfg
+        T = k.shape[2]
+        shape = (c.num_layers, c.num_kv_heads, T, c.head_dim)
+        _need(k, shape, c.kv_dtype, "k")
+        _need(v, shape, c.kv_dtype, "v")
+        check(lib().puzzlekv_factorize_pages(self._h, seq, _ptr(k), _ptr(v), T, _stream(stream)))
+
+    def append_token(self, layer: int, k: torch.Tensor, v: torch.Tensor, seq_ids: Sequence[int], stream=None) -> None:
+        """Append one token per sequence to `layer`; converts pages leaving the window (§3.3 ⑤)."""
+        c = self.cfg
+        ids, B = _seq_ids(seq_ids)
+        _need(k, (B, c.num_kv_heads, c.head_dim), c.kv_dtype, "k")
+        _need(v, (B, c.num_kv_heads, c.head_dim), c.kv_dtype, "v")
+        check(lib().puzzlekv_append_token(self._h, layer, _ptr(k), _ptr(v), ids, B, _stream(stream)))
+
+    def decode_attention(self, layer: int, q: torch.Tensor, out: torch.Tensor, seq_ids: Sequence[int],
+                         stream=None) -> torch.Tensor:
+        """Mixed dense/factorized decode attention of one layer (§3.3 ④, eqs. (4)-(5))."""
+        c = self.cfg
+        ids, B = _seq_ids(seq_ids)
+        _need(q, (B, c.num_q_heads, c.head_dim), c.kv_dtype, "q")
+        _need(out, (B, c.num_q_heads, c.head_dim), torch.float32, "out")
+        check(lib().puzzlekv_decode_attention(self._h, layer, _ptr(q), _ptr(out), ids, B, _stream(stream)))
+        return out
+
+    def stats(self, seq: int, layer: int) -> dict:
+        n = ctypes.c_int32()
+        nd, nf, nb = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        check(lib().puzzlekv_store_stats(self._h, seq, layer, ctypes.byref(n), ctypes.byref(nd), ctypes.byref(nf),
+                                         ctypes.byref(nb)))
+        return {"length": n.value, "dense_pages": nd.value, "factored_pages": nf.value, "bytes_live": nb.value}
+
+    def check_device_status(self, stream=None) -> int:
+        """Synchronise and return the status code (raises nothing; OK = 0)."""
+        return lib().puzzlekv_check_device_status(self._h, _stream(stream))

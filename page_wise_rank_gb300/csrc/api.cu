@@ -1,0 +1,423 @@
+// C ABI of the PuzzleKV store (declared in include/puzzlekv.h).
+//
+// Host responsibilities: validate every argument before launching anything,
+// keep a host mirror of each (sequence, layer) length so that page
+// classification -- which pages are dense, which page an append converts --
+// is decided without reading device memory, and launch the kernels on the
+// caller's stream.  The library never allocates device memory.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cstdarg>
+#include <cstdio>
+#include <cstring>
+#include <string>
+#include <vector>
+
+#include "../../include/puzzlekv.h"
+#include "kernels.h"
+#include "layout.h"
+
+using namespace pkv;
+
+namespace {
+
+thread_local std::string g_last_error;
+
+puzzlekv_status fail(puzzlekv_status st, const char *fmt, ...) {
+    char buf[512];
+    va_list ap;
+    va_start(ap, fmt);
+    vsnprintf(buf, sizeof(buf), fmt, ap);
+    va_end(ap);
+    g_last_error = buf;
+    return st;
+}
+
+puzzlekv_status cuda_fail(cudaError_t e, const char *what) {
+    return fail(PUZZLEKV_ERR_CUDA, "%s: %s", what, cudaGetErrorString(e));
+}
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+bool aligned256(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 255u) == 0; }
+
+int sm_count() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 132;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0) return 132;
+    return n;
+}
+
+int host_page_kind(int p, int T, int P, int sink, int W) { return page_kind(p, T, P, sink, W); }
+
+puzzlekv_status validate_config(const puzzlekv_config *c) {
+    if (!c) return fail(PUZZLEKV_ERR_INVALID_ARG, "config is NULL");
+    if (c->num_layers < 1 || c->num_kv_heads < 1 || c->num_q_heads < 1 || c->max_batch < 1 ||
+        c->max_tokens_per_seq < 1)
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "layers, heads, max_batch and max_tokens_per_seq must be >= 1");
+    if (c->num_q_heads % c->num_kv_heads != 0)
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+    int G = c->num_q_heads / c->num_kv_heads;
+    if (G > 8) return fail(PUZZLEKV_ERR_UNSUPPORTED, "at most 8 query heads per KV head (got %d)", G);
+    if (c->head_dim != 64 && c->head_dim != 128)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "head_dim must be 64 or 128 (got %d)", c->head_dim);
+    if (c->page_size != 16 && c->page_size != 32 && c->page_size != 64)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "page_size must be 16, 32 or 64 (got %d)", c->page_size);
+    if (c->page_size > c->head_dim) return fail(PUZZLEKV_ERR_UNSUPPORTED, "page_size must be <= head_dim");
+    if (c->rank_k < 1 || c->rank_k > c->page_size || c->rank_v < 1 || c->rank_v > c->page_size)
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "ranks must be in [1, page_size]");
+    if (c->sink_tokens < 0 || c->recent_tokens < 0)
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "sink_tokens and recent_tokens must be >= 0");
+    if (c->kv_dtype != PUZZLEKV_F32 && c->kv_dtype != PUZZLEKV_BF16)
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "kv_dtype must be PUZZLEKV_F32 or PUZZLEKV_BF16");
+    if (c->max_batch > (1 << 16) || c->max_tokens_per_seq > (1 << 24))
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "max_batch or max_tokens_per_seq too large");
+    int P = c->page_size;
+    int sink_pages = (c->sink_tokens + P - 1) / P;
+    int ring = (c->recent_tokens + P - 1) / P + 2;
+    if (sink_pages + ring > MAX_DENSE_PAGES)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "sink + window span more than %d dense pages", MAX_DENSE_PAGES - 2);
+    int n_pg = (c->max_tokens_per_seq + P - 1) / P;
+    if ((long)(n_pg + MAX_CHUNK_PAGES - 1) / MAX_CHUNK_PAGES > MAX_SPLITS)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "max_tokens_per_seq too large for the split-K workspace");
+    return PUZZLEKV_OK;
+}
+
+void layout_from(Layout &y, const puzzlekv_config *c) {
+    make_layout(y, c->num_layers, c->num_kv_heads, c->num_q_heads, c->head_dim, c->page_size, c->rank_k,
+                c->rank_v, c->sink_tokens, c->recent_tokens, c->max_batch, c->max_tokens_per_seq, c->kv_dtype);
+}
+
+}  // namespace
+
+struct puzzlekv_store {
+    puzzlekv_config cfg;
+    Layout y;
+    char *dense_pool, *factor_pool, *page_table, *workspace;
+    std::vector<int> len;    // host mirror [seq][layer]; -1 = empty slot
+    int num_sms;
+};
+
+static int *lengths_ptr(puzzlekv_store *s) { return reinterpret_cast<int *>(s->page_table); }
+static int *desc_ptr(puzzlekv_store *s) { return reinterpret_cast<int *>(s->page_table + s->y.desc_offset); }
+static int *status_ptr(puzzlekv_store *s) { return reinterpret_cast<int *>(s->workspace); }
+
+extern "C" {
+
+const char *puzzlekv_last_error(void) { return g_last_error.c_str(); }
+
+int32_t puzzlekv_classify_pages(int32_t T, int32_t P, int32_t sink_tokens, int32_t recent_tokens, int32_t *kinds,
+                                int32_t cap) {
+    if (T < 0 || P < 1 || sink_tokens < 0 || recent_tokens < 0 || (!kinds && cap > 0)) return -1;
+    int n = (T + P - 1) / P;
+    if (n > cap) return -1;
+    for (int p = 0; p < n; ++p) kinds[p] = host_page_kind(p, T, P, sink_tokens, recent_tokens);
+    return n;
+}
+
+double puzzlekv_page_storage_ratio(int32_t P, int32_t d, int32_t rank_k, int32_t rank_v) {
+    if (P < 1 || d < 1) return 0.0;
+    return (double)(rank_k + rank_v) * (double)(P + d) / (2.0 * P * d);
+}
+
+puzzlekv_status puzzlekv_query_sizes(const puzzlekv_config *cfg, size_t *dense_pool_bytes, size_t *factor_pool_bytes,
+                                     size_t *page_table_bytes, size_t *workspace_bytes) {
+    puzzlekv_status st = validate_config(cfg);
+    if (st != PUZZLEKV_OK) return st;
+    Layout y;
+    layout_from(y, cfg);
+    if (dense_pool_bytes) *dense_pool_bytes = y.dense_pool_bytes;
+    if (factor_pool_bytes) *factor_pool_bytes = y.factor_pool_bytes;
+    if (page_table_bytes) *page_table_bytes = y.page_table_bytes;
+    if (workspace_bytes) *workspace_bytes = y.workspace_bytes;
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_store_create(const puzzlekv_config *cfg, void *dense_pool, void *factor_pool,
+                                      void *page_table, void *workspace, void *stream, puzzlekv_store **out) {
+    if (!out) return fail(PUZZLEKV_ERR_INVALID_ARG, "out is NULL");
+    *out = nullptr;
+    puzzlekv_status st = validate_config(cfg);
+    if (st != PUZZLEKV_OK) return st;
+    if (!dense_pool || !factor_pool || !page_table || !workspace)
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "device buffers must not be NULL");
+    if (!aligned256(dense_pool) || !aligned256(factor_pool) || !aligned256(page_table) || !aligned256(workspace))
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "device buffers must be 256-byte aligned");
+    puzzlekv_store *s = new puzzlekv_store();
+    s->cfg = *cfg;
+    layout_from(s->y, cfg);
+    s->dense_pool = static_cast<char *>(dense_pool);
+    s->factor_pool = static_cast<char *>(factor_pool);
+    s->page_table = static_cast<char *>(page_table);
+    s->workspace = static_cast<char *>(workspace);
+    s->len.assign((size_t)cfg->max_batch * cfg->num_layers, -1);
+    s->num_sms = sm_count();
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaMemsetAsync(dense_pool, 0, s->y.dense_pool_bytes, strm);
+    if (e == cudaSuccess) e = cudaMemsetAsync(page_table, 0, s->y.page_table_bytes, strm);
+    if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, s->y.workspace_bytes, strm);
+    if (e != cudaSuccess) {
+        delete s;
+        return cuda_fail(e, "store_create memset");
+    }
+    *out = s;
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_store_destroy(puzzlekv_store *store) {
+    delete store;
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const void *k, const void *v, int32_t T,
+                                         void *stream) {
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    const Layout &y = s->y;
+    if (seq < 0 || seq >= y.Bmax) return fail(PUZZLEKV_ERR_INVALID_ARG, "seq %d out of range", seq);
+    if (T < 1) return fail(PUZZLEKV_ERR_INVALID_ARG, "T must be >= 1");
+    if (T > y.Tmax) return fail(PUZZLEKV_ERR_CAPACITY, "T=%d exceeds max_tokens_per_seq=%d", T, y.Tmax);
+    if (!k || !v || !aligned16(k) || !aligned16(v))
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "k and v must be non-NULL and 16-byte aligned");
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    const int n_pages = (T + y.P - 1) / y.P;
+    SeqInitParams ip{};
+    ip.y = y;
+    ip.lengths = lengths_ptr(s);
+    ip.desc = desc_ptr(s);
+    ip.dense_pool = s->dense_pool;
+    ip.k_src = static_cast<const char *>(k);
+    ip.v_src = static_cast<const char *>(v);
+    ip.seq = seq;
+    ip.T = T;
+    int f_lo = -1, f_hi = -1;
+    for (int p = 0; p < n_pages; ++p) {
+        if (host_page_kind(p, T, y.P, y.sink_tokens, y.W) == KIND_DENSE) {
+            if (ip.n_dense >= MAX_DENSE_PAGES) return fail(PUZZLEKV_ERR_UNSUPPORTED, "too many dense pages");
+            ip.dense_pages[ip.n_dense++] = p;
+        } else {
+            if (f_lo < 0) f_lo = p;
+            if (f_hi >= 0 && f_hi != p) return fail(PUZZLEKV_ERR_INVALID_ARG, "factorized pages not contiguous");
+            f_hi = p + 1;
+        }
+    }
+    cudaError_t e = launch_seq_init(ip, strm);
+    if (e != cudaSuccess) return cuda_fail(e, "seq_init launch");
+    if (f_lo >= 0) {
+        FactorParams fp{};
+        fp.mode = FACT_MODE_PREFILL;
+        fp.max_sweeps = 24;
+        fp.status = status_ptr(s);
+        fp.y = y;
+        fp.P = y.P;
+        fp.d = y.d;
+        fp.x_esz = y.esz;
+        fp.factor_pool = s->factor_pool;
+        fp.k_src = ip.k_src;
+        fp.v_src = ip.v_src;
+        fp.seq = seq;
+        fp.T = T;
+        fp.p_lo = f_lo;
+        fp.p_hi = f_hi;
+        fp.n_jobs = (long)y.L * y.H * 2 * (f_hi - f_lo);
+        e = launch_factorize(fp, s->num_sms, strm);
+        if (e != cudaSuccess) return cuda_fail(e, "factorize launch");
+    }
+    for (int l = 0; l < y.L; ++l) s->len[(size_t)seq * y.L + l] = T;
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_factorize_batch(const void *X, int32_t x_dtype, int64_t n, int32_t P, int32_t d, int32_t r,
+                                         void *L, void *R, int32_t out_dtype, float *sigma, int32_t *status,
+                                         void *stream) {
+    if (n < 0) return fail(PUZZLEKV_ERR_INVALID_ARG, "n must be >= 0");
+    if ((x_dtype != PUZZLEKV_F32 && x_dtype != PUZZLEKV_BF16) || (out_dtype != PUZZLEKV_F32 && out_dtype != PUZZLEKV_BF16))
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "dtype must be PUZZLEKV_F32 or PUZZLEKV_BF16");
+    if ((P != 16 && P != 32 && P != 64) || (d != 64 && d != 128) || P > d)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "need P in {16,32,64}, d in {64,128}, P <= d");
+    if (r < 1 || r > P) return fail(PUZZLEKV_ERR_INVALID_ARG, "rank must be in [1, P]");
+    if (n == 0) return PUZZLEKV_OK;
+    if (!X || !L || !R || !aligned16(X)) return fail(PUZZLEKV_ERR_INVALID_ARG, "X, L, R must be non-NULL, X 16-byte aligned");
+    FactorParams fp{};
+    fp.mode = FACT_MODE_BATCH;
+    fp.n_jobs = (long)n;
+    fp.max_sweeps = 24;
+    fp.status = status;
+    fp.x_base = static_cast<const char *>(X);
+    fp.x_esz = x_dtype == PUZZLEKV_BF16 ? 2 : 4;
+    fp.out_esz = out_dtype == PUZZLEKV_BF16 ? 2 : 4;
+    fp.P = P;
+    fp.d = d;
+    fp.r = r;
+    fp.L_out = static_cast<char *>(L);
+    fp.R_out = static_cast<char *>(R);
+    fp.sigma = sigma;
+    cudaError_t e = launch_factorize(fp, sm_count(), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "factorize_batch launch");
+    return PUZZLEKV_OK;
+}
+
+static puzzlekv_status check_call(puzzlekv_store *s, int32_t layer, const int32_t *seq_ids, int32_t B) {
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    if (layer < 0 || layer >= s->y.L) return fail(PUZZLEKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+    if (B < 1 || B > MAX_CALL_BATCH) return fail(PUZZLEKV_ERR_INVALID_ARG, "B must be in [1, %d]", MAX_CALL_BATCH);
+    if (!seq_ids) return fail(PUZZLEKV_ERR_INVALID_ARG, "seq_ids is NULL");
+    for (int i = 0; i < B; ++i) {
+        int b = seq_ids[i];
+        if (b < 0 || b >= s->y.Bmax) return fail(PUZZLEKV_ERR_INVALID_ARG, "seq id %d out of range", b);
+        if (s->len[(size_t)b * s->y.L + layer] < 1)
+            return fail(PUZZLEKV_ERR_INVALID_ARG, "sequence %d holds no tokens", b);
+        for (int j = 0; j < i; ++j)
+            if (seq_ids[j] == b) return fail(PUZZLEKV_ERR_INVALID_ARG, "sequence %d listed twice", b);
+    }
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_append_token(puzzlekv_store *s, int32_t layer, const void *k, const void *v,
+                                      const int32_t *seq_ids, int32_t B, void *stream) {
+    puzzlekv_status st = check_call(s, layer, seq_ids, B);
+    if (st != PUZZLEKV_OK) return st;
+    if (!k || !v || !aligned16(k) || !aligned16(v))
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "k and v must be non-NULL and 16-byte aligned");
+    const Layout &y = s->y;
+    AppendParams ap{};
+    ap.y = y;
+    ap.lengths = lengths_ptr(s);
+    ap.desc = desc_ptr(s);
+    ap.dense_pool = s->dense_pool;
+    ap.k = static_cast<const char *>(k);
+    ap.v = static_cast<const char *>(v);
+    ap.layer = layer;
+    ap.nseq = B;
+    FactorParams fp{};
+    fp.n_conv = 0;
+    for (int i = 0; i < B; ++i) {
+        int b = seq_ids[i];
+        int T = s->len[(size_t)b * y.L + layer];
+        if (T + 1 > y.Tmax) return fail(PUZZLEKV_ERR_CAPACITY, "sequence %d is full (%d tokens)", b, T);
+        ap.seqs[i] = b;
+        ap.pos[i] = T;
+        // [PuzzleKV §3.3 ⑤]: the page that T -> T + 1 moves out of the dense region
+        int conv = -1;
+        int n_old = (T + y.P - 1) / y.P;
+        int lo = std::max(0, (T - y.W) / y.P - 1);
+        for (int p = lo; p < n_old; ++p) {
+            if (host_page_kind(p, T, y.P, y.sink_tokens, y.W) == KIND_DENSE &&
+                host_page_kind(p, T + 1, y.P, y.sink_tokens, y.W) == KIND_FACTORED) {
+                if (conv >= 0) return fail(PUZZLEKV_ERR_INVALID_ARG, "internal: two conversions in one step");
+                conv = p;
+            }
+        }
+        ap.conv_page[i] = conv;
+        if (conv >= 0) {
+            fp.conv_seq[fp.n_conv] = b;
+            fp.conv_page[fp.n_conv] = conv;
+            fp.n_conv++;
+        }
+    }
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    cudaError_t e = launch_append(ap, strm);
+    if (e != cudaSuccess) return cuda_fail(e, "append launch");
+    if (fp.n_conv > 0) {
+        fp.mode = FACT_MODE_CONVERT;
+        fp.max_sweeps = 24;
+        fp.status = status_ptr(s);
+        fp.y = y;
+        fp.P = y.P;
+        fp.d = y.d;
+        fp.x_esz = y.esz;
+        fp.factor_pool = s->factor_pool;
+        fp.dense_pool = s->dense_pool;
+        fp.layer = layer;
+        fp.n_jobs = (long)fp.n_conv * y.H * 2;
+        e = launch_factorize(fp, s->num_sms, strm);
+        if (e != cudaSuccess) return cuda_fail(e, "conversion launch");
+    }
+    for (int i = 0; i < B; ++i) s->len[(size_t)seq_ids[i] * y.L + layer] += 1;
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *s, int32_t layer, const void *q, float *out,
+                                          const int32_t *seq_ids, int32_t B, void *stream) {
+    puzzlekv_status st = check_call(s, layer, seq_ids, B);
+    if (st != PUZZLEKV_OK) return st;
+    if (!q || !out || !aligned16(q) || !aligned16(out))
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+    const Layout &y = s->y;
+    DecodeParams dp{};
+    dp.y = y;
+    dp.factor_pool = s->factor_pool;
+    dp.dense_pool = s->dense_pool;
+    dp.lengths = lengths_ptr(s);
+    dp.desc = desc_ptr(s);
+    dp.q = static_cast<const char *>(q);
+    dp.partials = reinterpret_cast<float *>(s->workspace + y.partial_offset);
+    dp.out = out;
+    dp.status = status_ptr(s);
+    dp.layer = layer;
+    dp.nseq = B;
+    long total = 0;
+    int max_pages = 0;
+    for (int i = 0; i < B; ++i) {
+        int T = s->len[(size_t)seq_ids[i] * y.L + layer];
+        int np = (T + y.P - 1) / y.P;
+        total += (long)np * y.H;
+        max_pages = std::max(max_pages, np);
+        dp.seqs[i] = seq_ids[i];
+    }
+    // split-K: about two CTAs per SM over all (sequence, KV head) page ranges
+    long target = 2L * s->num_sms;
+    int chunk = (int)std::max(1L, (total + target - 1) / target);
+    chunk = std::min(chunk, MAX_CHUNK_PAGES);
+    int splits = (max_pages + chunk - 1) / chunk;
+    while (splits > MAX_SPLITS) {
+        chunk *= 2;
+        splits = (max_pages + chunk - 1) / chunk;
+    }
+    if (chunk > MAX_CHUNK_PAGES) return fail(PUZZLEKV_ERR_UNSUPPORTED, "sequence too long for the split workspace");
+    dp.chunk = chunk;
+    cudaError_t e = launch_decode(dp, splits, s->num_sms, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_store_stats(const puzzlekv_store *s, int32_t seq, int32_t layer, int32_t *length,
+                                     int64_t *dense_pages, int64_t *factored_pages, int64_t *bytes_live) {
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    const Layout &y = s->y;
+    if (seq < 0 || seq >= y.Bmax || layer < 0 || layer >= y.L)
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "seq or layer out of range");
+    int T = std::max(0, s->len[(size_t)seq * y.L + layer]);
+    int64_t nd = 0, nf = 0, bytes = 0;
+    int n = (T + y.P - 1) / y.P;
+    for (int p = 0; p < n; ++p) {
+        if (host_page_kind(p, T, y.P, y.sink_tokens, y.W) == KIND_DENSE) {
+            ++nd;
+            int rows = std::min(y.P, T - p * y.P);
+            bytes += (int64_t)rows * 2 * y.d * y.esz * y.H;
+        } else {
+            ++nf;
+            bytes += (int64_t)(y.rk + y.rv) * (y.P + y.d) * y.esz * y.H;
+        }
+    }
+    if (length) *length = T;
+    if (dense_pages) *dense_pages = nd;
+    if (factored_pages) *factored_pages = nf;
+    if (bytes_live) *bytes_live = bytes;
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *s, void *stream) {
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    int words[STATUS_WORDS] = {0};
+    cudaError_t e = cudaStreamSynchronize(strm);
+    if (e == cudaSuccess) e = cudaMemcpy(words, status_ptr(s), sizeof(words), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(status_ptr(s), 0, sizeof(words));
+    if (e != cudaSuccess) return cuda_fail(e, "status read");
+    if (words[STATUS_TIMEOUT]) return fail(PUZZLEKV_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out");
+    if (words[STATUS_NOT_CONVERGED])
+        return fail(PUZZLEKV_ERR_NOT_CONVERGED, "%d page eigensolves hit the sweep cap", words[STATUS_NOT_CONVERGED]);
+    return PUZZLEKV_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,73 @@
+// Kernel parameter blocks and launchers (private to the library).
+#pragma once
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "layout.h"
+
+namespace pkv {
+
+enum { FACT_MODE_BATCH = 0, FACT_MODE_PREFILL = 1, FACT_MODE_CONVERT = 2 };
+
+struct FactorParams {
+    int mode;
+    long n_jobs;
+    int max_sweeps;
+    int *status;  // device status words (may be null in batch mode)
+    // batch mode: X[n][P][d] -> L[n][P][r], R[n][r][d], sigma[n][P]
+    const char *x_base;
+    int x_esz, out_esz, P, d, r;
+    char *L_out, *R_out;
+    float *sigma;
+    // store modes
+    Layout y;
+    char *factor_pool;
+    const char *dense_pool;
+    // prefill: pages [p_lo, p_hi) of sequence `seq` from k_src / v_src ([L][H][T][d])
+    const char *k_src, *v_src;
+    int seq, T, p_lo, p_hi;
+    // convert: one page per call entry of `layer`
+    int layer, n_conv;
+    int conv_seq[MAX_CALL_BATCH], conv_page[MAX_CALL_BATCH];
+};
+
+struct DecodeParams {
+    Layout y;
+    const char *factor_pool, *dense_pool;
+    const int *lengths, *desc;
+    const char *q;      // [B][Hq][d] storage dtype
+    float *partials;    // workspace split partials
+    float *out;         // [B][Hq][d]
+    int *status;
+    int layer, chunk, nseq;
+    int seqs[MAX_CALL_BATCH];
+};
+
+constexpr int MAX_DENSE_PAGES = 64;  // dense pages of one sequence (sink + window + filling)
+
+struct SeqInitParams {
+    Layout y;
+    int *lengths, *desc;
+    char *dense_pool;
+    const char *k_src, *v_src;  // [L][H][T][d]
+    int seq, T, n_dense;
+    int dense_pages[MAX_DENSE_PAGES];
+};
+
+struct AppendParams {
+    Layout y;
+    int *lengths, *desc;
+    char *dense_pool;
+    const char *k, *v;  // [B][H][d]
+    int layer, nseq;
+    int seqs[MAX_CALL_BATCH];
+    int pos[MAX_CALL_BATCH];       // token position written (old length)
+    int conv_page[MAX_CALL_BATCH]; // page converted by this call, or -1
+};
+
+cudaError_t launch_factorize(const FactorParams &p, int num_sms, cudaStream_t st);
+cudaError_t launch_seq_init(const SeqInitParams &p, cudaStream_t st);
+cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
+cudaError_t launch_decode(const DecodeParams &p, int splits, int num_sms, cudaStream_t st);
+
+}  // namespace pkv

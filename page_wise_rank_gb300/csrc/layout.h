@@ -1,0 +1,134 @@
+// Device-memory layout of the paged factor store (host and device code).
+//
+// Everything the library keeps in HBM lives in four caller-owned buffers:
+//
+//   factor pool  [layer][seq][kv_head][page] -> one factor record per page
+//                (preallocated for every page a sequence can hold, so a page
+//                converted during decoding never needs an allocation --
+//                "PuzzleKV: Page-Wise Low-Rank Decomposition for KV Cache
+//                Compression", §3.3 ⑤).
+//   dense pool   [layer][seq][dense slot][kv_head][K|V][P][d]: sink pages
+//                take slots 0..sink_pages-1, every other dense page takes
+//                slot sink_pages + (page mod ring).  The ring is wide enough
+//                for the window, the page being filled and the page being
+//                converted, so a slot is "released" simply by the page
+//                leaving the ring.
+//   page table   int32 lengths[seq][layer], then int32 desc[seq][layer][page]
+//                = kind << 30 | slot.
+//   workspace    int32 status words, then fp32 split-K partial states
+//                [seq][q_head][split][2 + d].
+//
+// Factor record of one (layer, seq, kv head, page), element type e:
+//   LK  [P][rkp]    key left factor,   row = token   (B operand of s = t L_K^T)
+//   RK  [rkp][d]    key right factor,  row = rank    (B operand of t = q R_K^T)
+//   LVt [rvp][P]    value left factor, transposed: row = rank
+//   RVt [d][rvp]    value right factor, transposed: row = head dim
+// rkp / rvp are the ranks rounded up to a multiple of 8 (zero padding).  Each
+// row is a sequence of 16-byte chunks whose order is XOR-swizzled by row
+// (swizzle_chunk below) so that eight consecutive rows read at the same
+// logical chunk hit eight distinct bank groups; dense K/V rows use the same
+// rule.  The record is contiguous, so one bulk copy brings a page into shared
+// memory already in its conflict-free layout.
+#pragma once
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__CUDACC__)
+#define PKV_HD __host__ __device__ __forceinline__
+#else
+#define PKV_HD inline
+#endif
+
+namespace pkv {
+
+constexpr int KIND_SHIFT = 30;
+constexpr int32_t SLOT_MASK = (1 << KIND_SHIFT) - 1;
+constexpr int KIND_FACTORED = 0;
+constexpr int KIND_DENSE = 1;
+constexpr int MAX_SPLITS = 128;     // split-K partials per (seq, q head)
+constexpr int MAX_CHUNK_PAGES = 512; // pages per decode CTA
+constexpr int MAX_CALL_BATCH = 64;  // sequences per append / attention call
+constexpr int STATUS_WORDS = 16;    // int32 status words at the workspace start
+constexpr int STATUS_NOT_CONVERGED = 0;
+constexpr int STATUS_TIMEOUT = 1;
+
+PKV_HD int gcd8(int c) { return (c & 7) == 0 ? 8 : ((c & 3) == 0 ? 4 : ((c & 1) == 0 ? 2 : 1)); }
+
+// Physical 16-byte chunk of logical chunk `c` in row `row` of a row made of
+// `C` chunks.  Bijective within a row; conflict-free for 8 consecutive rows.
+PKV_HD int swizzle_chunk(int row, int c, int C) {
+    int g = gcd8(C);
+    if (g == 1) return c;
+    int period = 8 / g;
+    return c ^ ((row / period) & (g - 1));
+}
+
+// Byte offset of byte `b` of row `row` in a swizzled tile whose rows are
+// `pitch` bytes (a multiple of 16).
+PKV_HD uint32_t swz_offset(int row, int b, int pitch) {
+    int C = pitch >> 4;
+    return (uint32_t)(row * pitch + (swizzle_chunk(row, b >> 4, C) << 4) + (b & 15));
+}
+
+PKV_HD int round_up8(int x) { return (x + 7) & ~7; }
+
+// Page classification [PuzzleKV §3.3 ①②③, ⑤]: dense if the page holds one of
+// the first sink_tokens tokens, one of the last W tokens, or is incomplete.
+PKV_HD int page_kind(int p, int T, int P, int sink_tokens, int W) {
+    int first = p * P;
+    int end = first + P < T ? first + P : T;
+    int sink_pages = (sink_tokens + P - 1) / P;
+    bool dense = (p < sink_pages) || (end - first < P) || (end > T - W);
+    return dense ? KIND_DENSE : KIND_FACTORED;
+}
+
+struct Layout {
+    int L, H, Hq, G, d, P, rk, rv, rkp, rvp, sink_tokens, W, Bmax, Tmax, esz, dtype;
+    int n_pg_max, sink_pages, ring, dslots;
+    size_t rec_bytes, off_RK, off_LV, off_RV;
+    size_t dense_half_bytes;  // one K or V page: P * d * esz
+    size_t factor_pool_bytes, dense_pool_bytes, page_table_bytes, workspace_bytes;
+    size_t desc_offset;       // byte offset of desc[] in the page table
+    size_t partial_offset;    // byte offset of split partials in the workspace
+
+    PKV_HD size_t record_index(int l, int b, int h, int p) const {
+        return (((size_t)l * Bmax + b) * H + h) * (size_t)n_pg_max + p;
+    }
+    PKV_HD size_t record_offset(int l, int b, int h, int p) const { return record_index(l, b, h, p) * rec_bytes; }
+    PKV_HD int dense_slot(int p) const { return p < sink_pages ? p : sink_pages + (p % ring); }
+    // byte offset of the K (kv = 0) or V (kv = 1) half of a dense slot
+    PKV_HD size_t dense_offset(int l, int b, int slot, int h, int kv) const {
+        return (((((size_t)l * Bmax + b) * dslots + slot) * H + h) * 2 + kv) * dense_half_bytes;
+    }
+    PKV_HD size_t len_index(int b, int l) const { return (size_t)b * L + l; }
+    PKV_HD size_t desc_index(int b, int l, int p) const { return ((size_t)b * L + l) * n_pg_max + p; }
+    PKV_HD size_t partial_index(int b, int hq, int s) const { return ((size_t)b * Hq + hq) * MAX_SPLITS + s; }
+};
+
+// Fill a Layout from a validated configuration.
+inline void make_layout(Layout &y, int L, int H, int Hq, int d, int P, int rk, int rv, int sink, int W,
+                        int Bmax, int Tmax, int dtype) {
+    y.L = L; y.H = H; y.Hq = Hq; y.G = Hq / H; y.d = d; y.P = P; y.rk = rk; y.rv = rv;
+    y.rkp = round_up8(rk); y.rvp = round_up8(rv);
+    y.sink_tokens = sink; y.W = W; y.Bmax = Bmax; y.Tmax = Tmax; y.dtype = dtype;
+    y.esz = dtype == 1 ? 2 : 4;
+    y.n_pg_max = (Tmax + P - 1) / P;
+    y.sink_pages = (sink + P - 1) / P;
+    y.ring = (W + P - 1) / P + 2;
+    y.dslots = y.sink_pages + y.ring;
+    size_t e = (size_t)y.esz;
+    y.off_RK = (size_t)P * y.rkp * e;
+    y.off_LV = y.off_RK + (size_t)y.rkp * d * e;
+    y.off_RV = y.off_LV + (size_t)y.rvp * P * e;
+    y.rec_bytes = y.off_RV + (size_t)d * y.rvp * e;
+    y.dense_half_bytes = (size_t)P * d * e;
+    y.factor_pool_bytes = (size_t)L * Bmax * H * y.n_pg_max * y.rec_bytes;
+    y.dense_pool_bytes = (size_t)L * Bmax * y.dslots * H * 2 * y.dense_half_bytes;
+    size_t len_bytes = ((size_t)Bmax * L * 4 + 255) & ~(size_t)255;
+    y.desc_offset = len_bytes;
+    y.page_table_bytes = len_bytes + (((size_t)Bmax * L * y.n_pg_max * 4 + 255) & ~(size_t)255);
+    y.partial_offset = 256;
+    y.workspace_bytes = y.partial_offset + (size_t)Bmax * Hq * MAX_SPLITS * (2 + d) * 4;
+}
+
+}  // namespace pkv

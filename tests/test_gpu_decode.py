@@ -1,0 +1,216 @@
+"""GPU parity of the store: prefill compression, page table, decode attention
+and incremental conversion, against the fp64 oracle on the same seeded inputs.
+
+Decode tolerance (spec reading C6), on identical factors (the oracle is
+handed the factors the GPU stored, upcast exactly): per output row
+max_i |o_i - ref_i| / max_i |ref_i| <= 2e-3 for bf16 storage, 1e-5 for fp32.
+Page classification and descriptors are compared bit-exactly.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import synth
+from gpu_helpers import HostCache, check_page_table, oracle_decode_on_store, rel_err_rows, spec_of
+
+pytestmark = pytest.mark.gpu
+
+TOL = {torch.bfloat16: 2e-3, torch.float32: 1e-5}
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    if not torch.cuda.is_available():
+        pytest.skip("needs a GPU")
+    from page_wise_rank_gb300 import build
+    build.build()
+    import page_wise_rank_gb300 as m
+    return m
+
+
+def make_cfg(pkv, **kw):
+    base = dict(num_layers=2, num_kv_heads=2, num_q_heads=8, head_dim=128, page_size=64, rank_k=16, rank_v=24,
+                sink_tokens=4, recent_tokens=128, max_batch=4, max_tokens_per_seq=6000, kv_dtype=torch.bfloat16)
+    base.update(kw)
+    return pkv.StoreConfig(**base)
+
+
+def run_decode_check(pkv, store, cfg, host, seqs, layer, step, tol, heads=None):
+    B = len(seqs)
+    q = synth.queries(B, cfg.num_q_heads, cfg.head_dim, step=step, layer=layer, dtype=cfg.kv_dtype)
+    out = torch.empty(B, cfg.num_q_heads, cfg.head_dim, dtype=torch.float32, device="cuda")
+    store.decode_attention(layer, q.cuda(), out, seqs)
+    assert store.check_device_status() == 0, pkv.last_error()
+    got = out.cpu().double().numpy()
+    G = cfg.num_q_heads // cfg.num_kv_heads
+    worst = 0.0
+    for i, s in enumerate(seqs):
+        for h in (heads if heads is not None else range(cfg.num_kv_heads)):
+            ref = oracle_decode_on_store(store, cfg, host, s, layer, h, q[i, h * G:(h + 1) * G].double().numpy())
+            worst = max(worst, rel_err_rows(got[i, h * G:(h + 1) * G], ref))
+    assert worst <= tol, worst
+    return worst
+
+
+def prefill(pkv, store, cfg, host, seq, T, rope=None, k=12, n_out=4):
+    spec = spec_of(cfg, inner_rank=k, n_outliers=n_out, rope_base=rope)
+    K, V = synth.prefill_kv(spec, T, seq=seq)
+    store.factorize_pages(seq, K.cuda(), V.cuda())
+    host.set_prefill(seq, K, V)
+    return spec
+
+
+def test_tiny_fp32_config(pkv):
+    """1 layer, 2 KV heads x 4 query heads, d = 64, fp32, T = 1024, P = 32, r = 8,
+    sink = the first 4 tokens' page, window = last 64 tokens; one decode step."""
+    cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=32, rank_k=8, rank_v=8,
+                   sink_tokens=4, recent_tokens=64, max_batch=1, max_tokens_per_seq=1024, kv_dtype=torch.float32)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    prefill(pkv, store, cfg, host, 0, 1024, k=6, n_out=2)
+    check_page_table(store, cfg, 0, 0, 1024)
+    run_decode_check(pkv, store, cfg, host, [0], 0, step=0, tol=TOL[torch.float32])
+
+
+def test_tiny_full_rank_equals_dense(pkv):
+    """r = min(P, d): mixed attention equals dense softmax attention over the
+    original rows (spec full-rank check, on the GPU path)."""
+    cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=32, rank_k=32,
+                   rank_v=32, sink_tokens=4, recent_tokens=64, max_batch=1, max_tokens_per_seq=1024,
+                   kv_dtype=torch.float32)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    prefill(pkv, store, cfg, host, 0, 1024, k=6, n_out=2)
+    q = synth.queries(1, 8, 64, step=1, dtype=torch.float32)
+    out = torch.empty(1, 8, 64, device="cuda")
+    store.decode_attention(0, q.cuda(), out, [0])
+    got = out.cpu().double().numpy()[0]
+    for h in range(2):
+        K, V = host.rows(0, 0, h)
+        ref = oracle.attention(q[0, 4 * h:4 * h + 4].double().numpy(), K, V)
+        assert rel_err_rows(got[4 * h:4 * h + 4], ref) <= 1e-5
+
+
+@pytest.mark.parametrize("T", [5000, 4097, 64 * 40, 130])
+def test_bf16_llama_shape_prefill_decode(pkv, T):
+    cfg = make_cfg(pkv, num_layers=2, num_kv_heads=4, num_q_heads=16)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    prefill(pkv, store, cfg, host, 1, T, rope=5e5)
+    for l in range(cfg.num_layers):
+        check_page_table(store, cfg, 1, l, T)
+    run_decode_check(pkv, store, cfg, host, [1], 1, step=3, tol=TOL[torch.bfloat16])
+
+
+def test_bf16_gqa8_ranks_24(pkv):
+    cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=16, rank_k=24, rank_v=24)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    prefill(pkv, store, cfg, host, 0, 3000)
+    run_decode_check(pkv, store, cfg, host, [0], 0, step=4, tol=TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("P,d,rk,rv", [(32, 128, 16, 14), (16, 64, 9, 9), (64, 64, 27, 27), (32, 64, 8, 40 // 2)])
+def test_bf16_page_and_rank_variants(pkv, P, d, rk, rv):
+    cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=8, head_dim=d, page_size=P, rank_k=rk, rank_v=rv,
+                   recent_tokens=2 * P)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    prefill(pkv, store, cfg, host, 2, 1500)
+    check_page_table(store, cfg, 2, 0, 1500)
+    run_decode_check(pkv, store, cfg, host, [2], 0, step=5, tol=TOL[torch.bfloat16])
+
+
+def test_batched_ragged(pkv):
+    cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=8)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    lens = {0: 700, 2: 2100, 3: 4500, 1: 65}
+    for s, T in lens.items():
+        prefill(pkv, store, cfg, host, s, T)
+    run_decode_check(pkv, store, cfg, host, [3, 0, 1, 2], 0, step=6, tol=TOL[torch.bfloat16])
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_incremental_conversion(pkv, dtype):
+    """Append tokens across several page boundaries: each page that leaves the
+    window is factorized once on the stream (§3.3 ⑤); the page table, the
+    converted factors and attention stay exact against the oracle."""
+    d = 128 if dtype == torch.bfloat16 else 64
+    cfg = make_cfg(pkv, num_layers=2, num_kv_heads=2, num_q_heads=8, head_dim=d, max_tokens_per_seq=2000,
+                   kv_dtype=dtype)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    spec = prefill(pkv, store, cfg, host, 0, 1000)
+    prefill(pkv, store, cfg, host, 1, 1061)
+    seqs = [1, 0]
+    cache = {}
+    for step in range(200):
+        for l in range(cfg.num_layers):
+            pos = [len(torch.cat(host.k[(s, l, 0)])) for s in seqs]
+            k, v = synth.decode_tokens(spec, l, seqs, pos, cache=cache)
+            store.append_token(l, k.cuda(), v.cuda(), seqs)
+            for i, s in enumerate(seqs):
+                host.append(s, l, k[i], v[i])
+        if step in (0, 23, 87, 199):
+            for l in range(cfg.num_layers):
+                run_decode_check(pkv, store, cfg, host, seqs, l, step=100 + step, tol=TOL[dtype])
+    for s, T0 in ((0, 1000), (1, 1061)):
+        for l in range(cfg.num_layers):
+            check_page_table(store, cfg, s, l, T0 + 200)
+            st = store.stats(s, l)
+            kinds = oracle.page_kinds(T0 + 200, 64, 4, 128)
+            assert st["length"] == T0 + 200
+            assert st["factored_pages"] == int((kinds == oracle.FACTORED).sum())
+
+
+def test_edge_lengths(pkv):
+    cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=8, max_batch=4, max_tokens_per_seq=300)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    for s, T in ((0, 1), (1, 3), (2, 64), (3, 200)):
+        prefill(pkv, store, cfg, host, s, T)
+        check_page_table(store, cfg, s, 0, T)
+    run_decode_check(pkv, store, cfg, host, [0, 1, 2, 3], 0, step=7, tol=TOL[torch.bfloat16])
+
+
+def test_no_window_no_sink(pkv):
+    """sink = 0 and W = 0: only the incomplete page stays dense; each page is
+    converted the moment it completes."""
+    cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=8, sink_tokens=0, recent_tokens=0,
+                   max_tokens_per_seq=1000)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    spec = prefill(pkv, store, cfg, host, 0, 600)
+    cache = {}
+    for step in range(70):
+        pos = [600 + step]
+        k, v = synth.decode_tokens(spec, 0, [0], pos, cache=cache)
+        store.append_token(0, k.cuda(), v.cuda(), [0])
+        host.append(0, 0, k[0], v[0])
+    check_page_table(store, cfg, 0, 0, 670)
+    run_decode_check(pkv, store, cfg, host, [0], 0, step=8, tol=TOL[torch.bfloat16])
+
+
+def test_host_errors_leave_state_unchanged(pkv):
+    cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=8, max_batch=2, max_tokens_per_seq=130)
+    store = pkv.Store(cfg)
+    host = HostCache()
+    spec = prefill(pkv, store, cfg, host, 0, 129)
+    k, v = synth.decode_tokens(spec, 0, [0], [129])
+    store.append_token(0, k.cuda(), v.cuda(), [0])
+    with pytest.raises(pkv.PuzzleKVError) as e:       # capacity
+        store.append_token(0, k.cuda(), v.cuda(), [0])
+    assert e.value.status == 3
+    with pytest.raises(pkv.PuzzleKVError):            # empty sequence slot
+        store.decode_attention(0, torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda"),
+                               torch.empty(1, 8, 128, device="cuda"), [1])
+    with pytest.raises(pkv.PuzzleKVError):            # duplicate ids
+        store.append_token(0, torch.zeros(2, 2, 128, dtype=torch.bfloat16, device="cuda"),
+                           torch.zeros(2, 2, 128, dtype=torch.bfloat16, device="cuda"), [0, 0])
+    with pytest.raises(pkv.PuzzleKVError):            # layer out of range
+        store.decode_attention(3, torch.zeros(1, 8, 128, dtype=torch.bfloat16, device="cuda"),
+                               torch.empty(1, 8, 128, device="cuda"), [0])
+    assert store.stats(0, 0)["length"] == 130
+    check_page_table(store, cfg, 0, 0, 130)

@@ -1,0 +1,105 @@
+"""CPU-side checks of the C-ABI library: it loads, exports every symbol the
+header declares, and its host-only logic (page classification, storage
+ratio, buffer sizing, argument validation) is right.  No compute calls."""
+import ctypes
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def pkv():
+    from page_wise_rank_gb300 import build
+    build.build()
+    import page_wise_rank_gb300 as m
+    return m
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "puzzlekv.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(puzzlekv_[a-z_]+)\s*\(", src)))
+
+
+def test_library_exports_every_declared_symbol(pkv):
+    from page_wise_rank_gb300 import _lib
+    declared = header_functions()
+    assert declared == sorted(_lib.EXPORTED)
+    L = pkv.lib()
+    for name in declared:
+        assert hasattr(L, name), name
+
+
+def test_classification_bit_exact_with_oracle(pkv):
+    for P in (16, 32, 64):
+        for sink, W in ((0, 0), (4, 64), (4, 128), (64, 128), (100, 7)):
+            for T in list(range(1, 400)) + [4095, 4096, 4097, 32768, 32769, 131072]:
+                a = pkv.classify_pages(T, P, sink, W)
+                b = oracle.page_kinds(T, P, sink, W)
+                assert a.dtype == np.int32 and np.array_equal(a, b), (T, P, sink, W)
+
+
+def test_storage_ratio_matches_eq3(pkv):
+    for P, d, rk, rv in [(32, 128, 16, 14), (64, 128, 16, 24), (64, 128, 24, 24), (16, 128, 9, 9)]:
+        assert pkv.page_storage_ratio(P, d, rk, rv) == oracle.page_storage_ratio(P, d, rk, rv)
+
+
+def _cfg(pkv, **kw):
+    base = dict(num_layers=32, num_kv_heads=8, num_q_heads=32, head_dim=128, page_size=64, rank_k=16, rank_v=24,
+                sink_tokens=4, recent_tokens=128, max_batch=1, max_tokens_per_seq=32768 + 256,
+                kv_dtype=torch.bfloat16)
+    base.update(kw)
+    return pkv.StoreConfig(**base)
+
+
+def test_query_sizes(pkv):
+    cfg = _cfg(pkv)
+    s = pkv.query_sizes(cfg)
+    n_pg = (cfg.max_tokens_per_seq + 63) // 64
+    rec = (16 + 24) * (64 + 128) * 2
+    assert s["factor_pool"] == 32 * 1 * 8 * n_pg * rec
+    dslots = 1 + (128 + 63) // 64 + 2
+    assert s["dense_pool"] == 32 * 1 * dslots * 8 * 2 * 64 * 128 * 2
+    assert s["workspace"] >= 256 + 32 * 128 * 130 * 4
+
+
+@pytest.mark.parametrize("bad,status", [
+    (dict(head_dim=96), 2), (dict(page_size=128), 2), (dict(num_q_heads=33), 1),
+    (dict(num_q_heads=8 * 16), 2), (dict(rank_k=0), 1), (dict(rank_v=65), 1),
+    (dict(sink_tokens=-1), 1), (dict(max_batch=0), 1),
+])
+def test_config_validation(pkv, bad, status):
+    with pytest.raises(pkv.PuzzleKVError) as e:
+        pkv.query_sizes(_cfg(pkv, **bad))
+    assert e.value.status == status
+    assert pkv.last_error()
+
+
+def test_store_create_rejects_bad_pointers_without_gpu(pkv):
+    cfg = _cfg(pkv)
+    c = cfg.c()
+    h = ctypes.c_void_p()
+    L = pkv.lib()
+    assert L.puzzlekv_store_create(ctypes.byref(c), None, None, None, None, None, ctypes.byref(h)) == 1
+    assert L.puzzlekv_store_create(ctypes.byref(c), 16, 256, 256, 256, None, ctypes.byref(h)) == 1  # misaligned
+    assert h.value is None
+    assert L.puzzlekv_factorize_pages(None, 0, None, None, 1, None) == 1
+    assert L.puzzlekv_decode_attention(None, 0, None, None, None, 1, None) == 1
+    assert L.puzzlekv_factorize_batch(None, 1, 4, 64, 96, 8, None, None, 0, None, None, None) == 2
+    assert L.puzzlekv_factorize_batch(None, 1, 0, 64, 128, 8, None, None, 0, None, None, None) == 0
+
+
+def test_binding_has_no_cpu_fallback(tmp_path, monkeypatch):
+    """Without the built library every call raises instead of computing on the CPU."""
+    from page_wise_rank_gb300 import _lib
+    monkeypatch.setattr(_lib, "LIB_PATH", str(tmp_path / "missing.so"))
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(RuntimeError, match="no CPU fallback"):
+        _lib.lib()
