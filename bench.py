@@ -1,0 +1,457 @@
+"""Benchmark of the PuzzleKV hot path on one GB300 (or N independent replicas).
+
+A step = one decode step of a Llama-3.1-8B-shaped attention stack (32 layers,
+8 KV heads, 32 query heads, d = 128, bf16, P = 64, r_K = 16, r_V = 24, sink 4
+tokens, recent 128 tokens) at a 32K-token context, batch 1: for every layer,
+append the new key/value (converting the page that leaves the window, once
+per 64 steps per layer) and run mixed dense/factorized decode attention.
+The prompt cache is factorized once before timing (pages factorized/s).
+
+Prints one JSON line (see --help).  ``--impl reference`` times the CPU oracle
+on a bounded sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+WORKLOADS = {
+    # name: (layers, kv_heads, q_heads, d, P, rk, rv, sink, recent, batch, T, rope, inner rank, outliers)
+    "llama32k": dict(layers=32, H=8, Hq=32, d=128, P=64, rk=16, rv=24, sink=4, W=128, B=1, T=32768, rope=5e5,
+                     k=12, n_out=4,
+                     desc="Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query heads, d=128, bf16, "
+                          "T=32768, batch 1, P=64, rK=16, rV=24, sink 4, recent 128"),
+    "qwen128k": dict(layers=64, H=8, Hq=64, d=128, P=64, rk=24, rv=24, sink=4, W=128, B=1, T=131072, rope=None,
+                     k=12, n_out=4,
+                     desc="Qwen3-32B-shaped attention, 64 layers, 8 KV / 64 query heads, d=128, bf16, "
+                          "T=131072, batch 1, P=64, rK=rV=24, sink 4, recent 128"),
+}
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
+    ap.add_argument("--workload", default="llama32k", choices=sorted(WORKLOADS))
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-e2e", action="store_true")
+    return ap.parse_args()
+
+
+def measured_peak_hbm():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["hbm_gbs"]), "measured"
+    except Exception:
+        return 6800.0, "fallback"
+
+
+def source_hash(names):
+    h = hashlib.sha256()
+    for n in names:
+        with open(os.path.join(ROOT, "page_wise_rank_gb300", "csrc", n), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(kernel_key, src_hash):
+    """Per-launch DRAM bytes from a committed ncu summary, if it was taken on
+    the current kernel source (else None)."""
+    try:
+        with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+            rec = json.load(f).get(kernel_key)
+        if rec and rec.get("source_hash") == src_hash:
+            return rec
+    except Exception:
+        pass
+    return None
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.path = os.path.join(ROOT, "gpurun_out", f"clocks_bench_{os.getpid()}.csv")
+
+    def start(self):
+        try:
+            os.makedirs(os.path.dirname(self.path), exist_ok=True)
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", f"--id={self.index}", f"--query-gpu={self.FIELDS}",
+                                          "--format=csv,noheader,nounits", "-lms", "100"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+        except Exception:
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:
+            self.proc.kill()
+        self.f.close()
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx), "reasons": sorted(reasons),
+                "samples": len(sm)}
+
+
+def dist_init(n):
+    if n <= 1 or "RANK" not in os.environ:
+        return 0, 1, 0
+    import torch.distributed as dist
+    dist.init_process_group("nccl")
+    return dist.get_rank(), dist.get_world_size(), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def barrier_max(x, world):
+    if world <= 1:
+        return x
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def alg_bytes(wl, T, esz=2):
+    """Algorithmic bytes of one decode-attention launch (one layer, all KV heads):
+    factors of every factorized page, valid rows of every dense page, q and out."""
+    import page_wise_rank_gb300 as pkv
+    kinds = pkv.classify_pages(T, wl["P"], wl["sink"], wl["W"])
+    n_fac = int((kinds == pkv.PAGE_FACTORED).sum())
+    n_dense_tok = T - n_fac * wl["P"]
+    per_head = n_fac * (wl["rk"] + wl["rv"]) * (wl["P"] + wl["d"]) * esz + n_dense_tok * 2 * wl["d"] * esz
+    return wl["B"] * (wl["H"] * per_head + wl["Hq"] * wl["d"] * (esz + 4))
+
+
+def gpu_arm(args, rank, world, local):
+    import page_wise_rank_gb300 as pkv
+    import synth
+    from page_wise_rank_gb300 import build as cuda_build
+
+    wl = WORKLOADS[args.workload]
+    cuda_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    L, H, Hq, d, P, B, T0 = wl["layers"], wl["H"], wl["Hq"], wl["d"], wl["P"], wl["B"], wl["T"]
+    n_steps_total = args.warmup + args.steps * (1 if args.no_e2e else 2)
+    cfg = pkv.StoreConfig(num_layers=L, num_kv_heads=H, num_q_heads=Hq, head_dim=d, page_size=P, rank_k=wl["rk"],
+                          rank_v=wl["rv"], sink_tokens=wl["sink"], recent_tokens=wl["W"], max_batch=B,
+                          max_tokens_per_seq=T0 + n_steps_total + 8, kv_dtype=torch.bfloat16)
+    spec = synth.KVSpec(layers=L, kv_heads=H, head_dim=d, page_size=P, inner_rank=wl["k"], n_outliers=wl["n_out"],
+                        rope_base=wl["rope"], dtype=torch.bfloat16)
+    with torch.cuda.stream(stream):
+        store = pkv.Store(cfg, device=dev, stream=stream)
+        # prompt cache -> factorized store (pages factorized/s), sequence slot 0 of this replica
+        K = torch.empty(L, H, T0, d, dtype=torch.bfloat16, device=dev)
+        V = torch.empty_like(K)
+        synth.prefill_kv(spec, T0, seq=rank, device=dev, out=(K, V))
+        kinds = pkv.classify_pages(T0, P, wl["sink"], wl["W"])
+        n_fact_pages = int((kinds == pkv.PAGE_FACTORED).sum()) * L * H * 2
+        stream.synchronize()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        store.factorize_pages(0, K, V, stream=stream)
+        e1.record(stream)
+        st = store.check_device_status(stream)
+        prefill_ms = e0.elapsed_time(e1)
+        if st != 0:
+            raise RuntimeError(f"prefill factorization status {st}: {pkv.last_error()}")
+        del K, V
+        torch.cuda.empty_cache()
+        # per-step inputs, resident in HBM before timing
+        cache = {}
+        qs, ks, vs = [], [], []
+        for s in range(n_steps_total):
+            qs.append(torch.stack([synth.queries(B, Hq, d, step=s, layer=l, device=dev) for l in range(L)]))
+            kl, vl = [], []
+            for l in range(L):
+                k, v = synth.decode_tokens(spec, l, [rank], [T0 + s], device=dev, cache=cache)
+                kl.append(k)
+                vl.append(v)
+            ks.append(torch.stack(kl))
+            vs.append(torch.stack(vl))
+        out = torch.empty(L, B, Hq, d, dtype=torch.float32, device=dev)
+        seqs = [0]
+        stream.synchronize()
+
+    launches = [0]
+
+    def step(s, ev=None, q_src=None, k_src=None, v_src=None, out_dst=None):
+        qq = qs[s] if q_src is None else q_src
+        kk = ks[s] if k_src is None else k_src
+        vv = vs[s] if v_src is None else v_src
+        T = store_len[0]
+        conv = any(pkv.classify_pages(T, P, wl["sink"], wl["W"])[p] == pkv.PAGE_DENSE and
+                   pkv.classify_pages(T + 1, P, wl["sink"], wl["W"])[p] == pkv.PAGE_FACTORED
+                   for p in range(max(0, (T - wl["W"]) // P - 1), (T + P - 1) // P))
+        for l in range(L):
+            store.append_token(l, kk[l], vv[l], seqs, stream=stream)
+            if ev is not None:
+                ev[l][0].record(stream)
+            store.decode_attention(l, qq[l], out[l], seqs, stream=stream)
+            if ev is not None:
+                ev[l][1].record(stream)
+        launches[0] += L * 3 + (L if conv else 0)
+        store_len[0] = T + 1
+        if out_dst is not None:
+            out_dst.copy_(out, non_blocking=True)
+
+    store_len = [T0]
+    with torch.cuda.stream(stream):
+        for s in range(args.warmup):
+            step(s)
+        stream.synchronize()
+        # ---- timed region: K steps, device-resident inputs
+        evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
+               for _ in range(args.steps)]
+        t_lens = []
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
+        barrier(world)
+        stream.synchronize()
+        launches[0] = 0
+        s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        s0.record(stream)
+        for i in range(args.steps):
+            t_lens.append(store_len[0] + 1)
+            step(args.warmup + i, ev=evs[i])
+        s1.record(stream)
+        stream.synchronize()
+        barrier(world)
+        clk = clocks.stop()
+        gpu_launches = launches[0]
+        ms_total = barrier_max(s0.elapsed_time(s1), world)
+        st = store.check_device_status(stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {pkv.last_error()}")
+        dec_ms = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(args.steps) for l in range(L)]
+        dec_bytes = [alg_bytes(wl, t_lens[i]) for i in range(args.steps) for l in range(L)]
+        # ---- e2e: same steps through the public API with pinned host buffers
+        e2e = None
+        if not args.no_e2e:
+            hq = [qs[args.warmup + i].cpu().pin_memory() for i in range(args.steps)]
+            hk = [ks[args.warmup + i].cpu().pin_memory() for i in range(args.steps)]
+            hv = [vs[args.warmup + i].cpu().pin_memory() for i in range(args.steps)]
+            hout = torch.empty(args.steps, L, B, Hq, d, dtype=torch.float32).pin_memory()
+            dq, dk, dv = torch.empty_like(qs[0]), torch.empty_like(ks[0]), torch.empty_like(vs[0])
+            stream.synchronize()
+            barrier(world)
+            x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            x0.record(stream)
+            for i in range(args.steps):
+                dq.copy_(hq[i], non_blocking=True)
+                dk.copy_(hk[i], non_blocking=True)
+                dv.copy_(hv[i], non_blocking=True)
+                step(args.warmup + args.steps + i, q_src=dq, k_src=dk, v_src=dv, out_dst=hout[i])
+            x1.record(stream)
+            stream.synchronize()
+            e2e_ms = barrier_max(x0.elapsed_time(x1), world)
+            e2e = {"value": 1000.0 * e2e_ms / args.steps, "unit": "us/step",
+                   "h2d_bytes_per_step": int(dq.numel() * 2 + dk.numel() * 2 + dv.numel() * 2),
+                   "d2h_bytes_per_step": int(out.numel() * 4)}
+    us_step = 1000.0 * ms_total / args.steps
+    dec_us = 1000.0 * sum(dec_ms) / len(dec_ms)
+    achieved = sum(dec_bytes) / (sum(dec_ms) * 1e-3) / 1e9
+    peak, peak_kind = measured_peak_hbm()
+    src_hash = source_hash(["decode.cu", "common.cuh", "layout.h"])
+    traffic = recorded_traffic(f"decode_bf16:{args.workload}", src_hash)
+    pages_per_s = n_fact_pages / (prefill_ms * 1e-3)
+    result = {
+        "metric": "mixed decode attention us/step (all layers) & % HBM roofline; pages factorized/s",
+        "value": round(us_step, 3),
+        "unit": "us/step",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": round(ms_total / args.steps, 6),
+        "higher_is_better": False,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic (seeded low-rank-plus-noise pages, RoPE keys)",
+        "config": {"workload": wl["desc"], "global_batch": wl["B"] * world, "seq_len": wl["T"],
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "l2": f"inputs larger than L2: {alg_bytes(wl, T0) * L / 1e9:.2f} GB read per step"},
+        "decode_attention_us_per_layer": round(dec_us, 3),
+        "pages_factorized_per_s": round(pages_per_s, 1),
+        "prefill_factorization": {"pages": n_fact_pages, "ms": round(prefill_ms, 3)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "kernel": "decode_bf16_kernel + merge_splits_kernel (one decode_attention call)",
+                     "traffic": (traffic["bytes_per_launch"] if traffic else None),
+                     "algorithmic_bytes_per_launch": int(statistics.mean(dec_bytes))},
+        "e2e": e2e,
+        "gpu_launches": gpu_launches,
+        "clocks": clk,
+    }
+    if rank == 0 and not args.no_cpu_baseline:
+        result["cpu_baseline"] = cpu_baseline_sample(wl)
+    store.close()
+    return result
+
+
+def _oracle_sample(wl, layer_heads, nthreads):
+    """Oracle factorization of every eligible page of the sampled (layer, KV head)
+    pairs (timed, all host threads) and oracle decode of each pair (timed, one
+    thread).  Returns (pages/s, seconds per (layer, head) decode, pages)."""
+    import oracle
+    import synth
+
+    T, P, d = wl["T"], wl["P"], wl["d"]
+    spec = synth.KVSpec(layers=1, kv_heads=wl["H"], head_dim=d, page_size=P, inner_rank=wl["k"],
+                        n_outliers=wl["n_out"], rope_base=wl["rope"], dtype=torch.bfloat16)
+    kinds = oracle.page_kinds(T, P, wl["sink"], wl["W"])
+    fac = np.nonzero(kinds == oracle.FACTORED)[0]
+    n = len(kinds)
+    t_fact, n_pages, t_dec = 0.0, 0, []
+    for (layer, h) in layer_heads:
+        # layer index only selects the seed; generate that layer's cache on the host
+        g = synth.KVSpec(**{**spec.__dict__, "layers": layer + 1})
+        K, V = synth.prefill_kv(g, T)
+        Kh, Vh = K[layer, h].double().numpy(), V[layer, h].double().numpy()
+        del K, V
+        Xk = np.stack([Kh[p * P:(p + 1) * P] for p in fac])
+        Xv = np.stack([Vh[p * P:(p + 1) * P] for p in fac])
+        t0 = time.perf_counter()
+        LKf, RKf, _ = oracle.factorize_pages(Xk, wl["rk"], nthreads)
+        LVf, RVf, _ = oracle.factorize_pages(Xv, wl["rv"], nthreads)
+        t_fact += time.perf_counter() - t0
+        n_pages += 2 * len(fac)
+        LK, RK = np.zeros((n, P, wl["rk"])), np.zeros((n, wl["rk"], d))
+        LV, RV = np.zeros((n, P, wl["rv"])), np.zeros((n, wl["rv"], d))
+        LK[fac], RK[fac], LV[fac], RV[fac] = LKf, RKf, LVf, RVf
+        G = wl["Hq"] // wl["H"]
+        q = synth.queries(1, wl["Hq"], d, step=0, layer=layer)[0, h * G:(h + 1) * G].double().numpy()
+        t0 = time.perf_counter()
+        oracle.decode_head(q, kinds, Kh, Vh, LK, RK, LV, RV, T, P)
+        t_dec.append(time.perf_counter() - t0)
+    return n_pages / t_fact, statistics.mean(t_dec), n_pages
+
+
+def cpu_baseline_sample(wl):
+    nthreads = os.cpu_count() or 1
+    pairs = [(0, 0), (wl["layers"] - 1, wl["H"] - 1)]
+    pages_s, t_head, n_pages = _oracle_sample(wl, pairs, nthreads)
+    heads = wl["layers"] * wl["H"] * wl["B"]
+    # per step: attention over every (layer, KV head), plus on average 2 H L / P page conversions
+    conv_per_step = 2.0 * wl["H"] * wl["layers"] * wl["B"] / wl["P"]
+    us_step = 1e6 * (heads * t_head + conv_per_step / pages_s)
+    return {"value": round(us_step, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
+            "sample": f"oracle decode of {len(pairs)} (layer, KV head) pairs at T={wl['T']} on 1 thread, "
+                      f"scaled to {heads} pairs per step, plus {conv_per_step:.0f} page conversions per step "
+                      f"at the oracle's factorization rate",
+            "pages_factorized_per_s": round(pages_s, 1), "pages_cores": nthreads, "pages_sample": n_pages}
+
+
+def reference_arm(args, rank, world):
+    if rank != 0:
+        return None
+    wl = WORKLOADS[args.workload]
+    import oracle
+    import synth
+
+    T, P, d, layers, H = wl["T"], wl["P"], wl["d"], wl["layers"], wl["H"]
+    nthreads = os.cpu_count() or 1
+    pages_s, _, n_pages = _oracle_sample(wl, [(0, 0)], nthreads)
+    # per step: oracle decode of one (layer, KV head) pair, scaled to all pairs
+    spec = synth.KVSpec(layers=1, kv_heads=H, head_dim=d, page_size=P, inner_rank=wl["k"], n_outliers=wl["n_out"],
+                        rope_base=wl["rope"], dtype=torch.bfloat16)
+    K, V = synth.prefill_kv(spec, T)
+    Kh, Vh = K[0, 0].double().numpy(), V[0, 0].double().numpy()
+    kinds = oracle.page_kinds(T, P, wl["sink"], wl["W"])
+    fac = np.nonzero(kinds == oracle.FACTORED)[0]
+    n = len(kinds)
+    LK, RK = np.zeros((n, P, wl["rk"])), np.zeros((n, wl["rk"], d))
+    LV, RV = np.zeros((n, P, wl["rv"])), np.zeros((n, wl["rv"], d))
+    a, b, _ = oracle.factorize_pages(np.stack([Kh[p * P:(p + 1) * P] for p in fac]), wl["rk"], nthreads)
+    LK[fac], RK[fac] = a, b
+    a, b, _ = oracle.factorize_pages(np.stack([Vh[p * P:(p + 1) * P] for p in fac]), wl["rv"], nthreads)
+    LV[fac], RV[fac] = a, b
+    G = wl["Hq"] // H
+    times = []
+    for s in range(args.warmup + args.steps):
+        q = synth.queries(1, wl["Hq"], d, step=s, layer=0)[0, :G].double().numpy()
+        t0 = time.perf_counter()
+        oracle.decode_head(q, kinds, Kh, Vh, LK, RK, LV, RV, T, P)
+        if s >= args.warmup:
+            times.append(time.perf_counter() - t0)
+    heads = layers * H * wl["B"]
+    conv_per_step = 2.0 * H * layers * wl["B"] / P
+    us_step = 1e6 * (heads * statistics.mean(times) + conv_per_step / pages_s)
+    sample = (f"per step: oracle decode of 1 (layer, KV head) pair at T={T} on 1 thread, scaled to {heads} pairs, "
+              f"plus {conv_per_step:.0f} conversions at the oracle factorization rate ({n_pages} pages sampled "
+              f"on {nthreads} threads)")
+    return {"impl": "reference", "metric": "mixed decode attention us/step (all layers) & % HBM roofline; "
+                                           "pages factorized/s",
+            "value": round(us_step, 1), "unit": "us/step", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(us_step / 1000.0, 3), "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": wl["desc"], "global_batch": wl["B"], "seq_len": T, "parallelism": "cpu oracle"},
+            "cpu_baseline": {"value": round(us_step, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
+                             "sample": sample, "pages_factorized_per_s": round(pages_s, 1)},
+            "e2e": {"value": round(us_step, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+            "gpu_launches": 0}
+
+
+def main():
+    args = parse()
+    rank, world, local = dist_init(args.gpus)
+    if args.impl == "reference":
+        res = reference_arm(args, rank, world)
+    else:
+        res = gpu_arm(args, rank, world, local)
+    if rank == 0 and res is not None:
+        print(json.dumps(res), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -91,6 +91,14 @@ int oracle_svd(const double *X, int n, int d, double *U, double *S, double *Y)
     for (int i = 0; i < n; ++i)
         for (int j = 0; j < n; ++j)
             u[i * n + j] = (i == j) ? 1.0 : 0.0;
+    /* Rows whose norm falls below 1e-14 ||X||_F are zero to working
+     * precision (what is left of them is rounding noise); rotating them
+     * changes nothing in exact arithmetic and can go on forever in floating
+     * point, so they take part in no rotation. */
+    double frob2 = 0.0;
+    for (size_t i = 0; i < (size_t)n * d; ++i)
+        frob2 += X[i] * X[i];
+    const double negligible = 1e-28 * frob2;
 
     while (!converged && sweeps < max_sweeps) {
         int rotated = 0;
@@ -100,7 +108,8 @@ int oracle_svd(const double *X, int n, int d, double *U, double *S, double *Y)
                 double alpha = dot(yp, yp, d);
                 double beta = dot(yq, yq, d);
                 double gamma = dot(yp, yq, d);
-                if (gamma == 0.0 || fabs(gamma) <= tol * sqrt(alpha * beta))
+                if (gamma == 0.0 || fabs(gamma) <= tol * sqrt(alpha * beta) || alpha <= negligible ||
+                    beta <= negligible)
                     continue;
                 /* tan of the angle that zeroes the rotated rows' inner product
                  * (smaller root of t^2 + 2 zeta t - 1 = 0). */

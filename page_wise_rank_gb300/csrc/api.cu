@@ -364,18 +364,8 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *s, int32_t layer, cons
         max_pages = std::max(max_pages, np);
         dp.seqs[i] = seq_ids[i];
     }
-    // split-K: about two CTAs per SM over all (sequence, KV head) page ranges
-    long target = 2L * s->num_sms;
-    int chunk = (int)std::max(1L, (total + target - 1) / target);
-    chunk = std::min(chunk, MAX_CHUNK_PAGES);
-    int splits = (max_pages + chunk - 1) / chunk;
-    while (splits > MAX_SPLITS) {
-        chunk *= 2;
-        splits = (max_pages + chunk - 1) / chunk;
-    }
-    if (chunk > MAX_CHUNK_PAGES) return fail(PUZZLEKV_ERR_UNSUPPORTED, "sequence too long for the split workspace");
-    dp.chunk = chunk;
-    cudaError_t e = launch_decode(dp, splits, s->num_sms, static_cast<cudaStream_t>(stream));
+    dp.tickets = reinterpret_cast<int *>(s->workspace + y.ticket_offset);
+    cudaError_t e = launch_decode(dp, total, max_pages, s->num_sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     return PUZZLEKV_OK;
 }
@@ -413,6 +403,8 @@ puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *s, void *stream) {
     cudaError_t e = cudaStreamSynchronize(strm);
     if (e == cudaSuccess) e = cudaMemcpy(words, status_ptr(s), sizeof(words), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemset(status_ptr(s), 0, sizeof(words));
+    if (e == cudaSuccess && words[STATUS_TIMEOUT])  // a CTA that gave up never took its split ticket
+        e = cudaMemset(s->workspace + s->y.ticket_offset, 0, (size_t)s->y.Bmax * s->y.H * 4);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     if (words[STATUS_TIMEOUT]) return fail(PUZZLEKV_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out");
     if (words[STATUS_NOT_CONVERGED])

@@ -42,6 +42,7 @@ struct DecodeShared {
     int n_units;
     int issued;
     int failed;
+    int last;
 };
 
 __device__ __forceinline__ int dense_half_valid(int T, int p, int P, int half) {
@@ -96,6 +97,87 @@ __device__ bool build_units(DecodeShared &sh, const DecodeParams &prm, int b, in
     }
     __syncthreads();
     return true;
+}
+
+
+// Write this CTA's state for the G query heads of (b, h) -- the NWC warp
+// states in `comb` ([warp][g][m, l, o...], D + 2 floats per row) merged by
+// eq. (5) -- to the workspace; then, if this CTA is the last of the `ns`
+// CTAs of (b, h) to get there (atomic ticket, no waiting), merge all ns
+// partial states into `out` and reset the ticket for the next launch.
+// `scratch` holds 3 * MAX_SPLITS * 8 + 16 floats of shared memory.
+template <int D>
+__device__ void finish_split(const DecodeParams &prm, const float *comb, int b_idx, int b, int h, int split, int ns,
+                             float *scratch, int *last) {
+    const Layout &y = prm.y;
+    const int G = y.G, S = y.part_stride;
+    for (int e = threadIdx.x; e < G * (D + 2); e += blockDim.x) {
+        int gg = e / (D + 2), k = e % (D + 2);
+        float M = -INFINITY;
+        for (int w = 0; w < NWC; ++w) M = fmaxf(M, comb[(w * 8 + gg) * (D + 2)]);
+        float acc = 0.f;
+        if (k == 0) {
+            acc = M;
+        } else {
+            for (int w = 0; w < NWC; ++w) {
+                float mw = comb[(w * 8 + gg) * (D + 2)];
+                acc += (mw == -INFINITY ? 0.f : exp2f(mw - M)) * comb[(w * 8 + gg) * (D + 2) + k];
+            }
+        }
+        prm.partials[y.partial_index(b, h * G + gg, split) * S + (k < 2 ? k : k + 2)] = acc;
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        int old = atomicAdd(prm.tickets + y.ticket_index(b, h), 1);
+        *last = (old == ns - 1);
+    }
+    __syncthreads();
+    if (!*last) return;
+    __threadfence();
+    float *sm = scratch, *sl = scratch + MAX_SPLITS * 8, *wt = sl + MAX_SPLITS * 8, *Mg = wt + MAX_SPLITS * 8;
+    float *iL = Mg + 8;
+    for (int e = threadIdx.x; e < ns * G; e += blockDim.x) {
+        int sp = e / G, g = e % G;
+        const float *row = prm.partials + y.partial_index(b, h * G + g, sp) * S;
+        sm[sp * 8 + g] = __ldcg(row);
+        sl[sp * 8 + g] = __ldcg(row + 1);
+    }
+    __syncthreads();
+    if (threadIdx.x < G) {
+        int g = threadIdx.x;
+        float M = -INFINITY, L = 0.f;
+        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, sm[sp * 8 + g]);
+        for (int sp = 0; sp < ns; ++sp) {
+            float m = sm[sp * 8 + g];
+            L += (m == -INFINITY ? 0.f : exp2f(m - M)) * sl[sp * 8 + g];
+        }
+        Mg[g] = M;
+        iL[g] = 1.f / L;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < ns * G; e += blockDim.x) {
+        int sp = e / G, g = e % G;
+        float m = sm[sp * 8 + g];
+        wt[sp * 8 + g] = (m == -INFINITY ? 0.f : exp2f(m - Mg[g])) * iL[g];
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < G * (D / 4); e += blockDim.x) {
+        int g = e / (D / 4), k4 = e % (D / 4);
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+        for (int sp = 0; sp < ns; ++sp) {
+            const float4 v = __ldcg(reinterpret_cast<const float4 *>(
+                                        prm.partials + y.partial_index(b, h * G + g, sp) * S + 4) + k4);
+            float c = wt[sp * 8 + g];
+            acc.x = fmaf(c, v.x, acc.x);
+            acc.y = fmaf(c, v.y, acc.y);
+            acc.z = fmaf(c, v.z, acc.z);
+            acc.w = fmaf(c, v.w, acc.w);
+        }
+        reinterpret_cast<float4 *>(prm.out + ((size_t)b_idx * y.Hq + h * G + g) * D)[k4] = acc;
+    }
+    if (threadIdx.x == 0) prm.tickets[y.ticket_index(b, h)] = 0;
 }
 
 // ---------------------------------------------------------------- bf16 tensor-core path
@@ -441,23 +523,11 @@ __global__ void __launch_bounds__((NWC + 1) * 32) decode_bf16_kernel(const Decod
         }
     }
     __syncthreads();
-    // merge the NWC warp states of each query head; write the CTA's partial state
-    const float *comb = reinterpret_cast<const float *>(stages);
-    for (int e = threadIdx.x; e < y.G * (D + 2); e += blockDim.x) {
-        int gg = e / (D + 2), k = e % (D + 2);
-        float M = -INFINITY;
-        for (int ww = 0; ww < NWC; ++ww) M = fmaxf(M, comb[(ww * 8 + gg) * (D + 2)]);
-        float acc = 0.f;
-        if (k == 0) {
-            acc = M;
-        } else {
-            for (int ww = 0; ww < NWC; ++ww) {
-                float mw = comb[(ww * 8 + gg) * (D + 2)];
-                float sc = mw == -INFINITY ? 0.f : exp2f(mw - M);
-                acc += sc * comb[(ww * 8 + gg) * (D + 2) + k];
-            }
-        }
-        prm.partials[y.partial_index(b, h * y.G + gg, split) * (D + 2) + k] = acc;
+    {
+        const float *comb = reinterpret_cast<const float *>(stages);
+        float *scratch = reinterpret_cast<float *>(stages) + NWC * 8 * (D + 2);
+        const int ns = (n_pages + prm.chunk - 1) / prm.chunk;
+        finish_split<D>(prm, comb, b_idx, b, h, split, ns, scratch, &sh.last);
     }
 }
 
@@ -478,6 +548,8 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
     constexpr int DPL = D / 32;         // head dims per lane
     const float scale = rsqrtf((float)D);
     __shared__ float comb[NWC][8][D + 2];
+    __shared__ float scratch[3 * MAX_SPLITS * 8 + 16];
+    __shared__ int last;
 
     float q[8][DPL];  // this lane's head dims of each query row
     const float *qb = reinterpret_cast<const float *>(prm.q) + ((size_t)b_idx * y.Hq + (size_t)h * G) * D;
@@ -496,7 +568,7 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
         float s[8][TPL];
         if (kind == KIND_FACTORED) {
             const char *rec = prm.factor_pool + y.record_offset(prm.layer, b, h, slot);
-            const int rkp = y.rkp, rvp = y.rvp;
+            const int rkp = y.rkp;
             // t = q R_K^T: full dot products by warp reduction, one rank at a time
             float t[8][2];  // lane j holds rank j and j + 32
             for (int g = 0; g < 8; ++g) t[g][0] = t[g][1] = 0.f;
@@ -589,7 +661,7 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
             }
         }
     }
-    // warp states -> shared, then one partial per query head (m kept in log2 units)
+    // warp states -> shared (m kept in log2 units), then the split hand-off
     for (int g = 0; g < 8; ++g) {
         if (lane == 0) {
             comb[warp][g][0] = m[g] * LOG2E;
@@ -598,79 +670,59 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
         for (int e = 0; e < DPL; ++e) comb[warp][g][2 + lane + 32 * e] = o[g][e];
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < G * (D + 2); e += blockDim.x) {
-        int g = e / (D + 2), k = e % (D + 2);
-        float M = -INFINITY;
-        for (int w = 0; w < NWC; ++w) M = fmaxf(M, comb[w][g][0]);
-        float acc = 0.f;
-        if (k == 0) {
-            acc = M;
-        } else {
-            for (int w = 0; w < NWC; ++w) {
-                float mw = comb[w][g][0];
-                acc += (mw == -INFINITY ? 0.f : exp2f(mw - M)) * comb[w][g][k];
-            }
-        }
-        prm.partials[y.partial_index(b, h * G + g, split) * (D + 2) + k] = acc;
-    }
-}
-
-// ---------------------------------------------------------------- split merge, eq. (5)
-
-__global__ void merge_splits_kernel(const DecodeParams prm) {
-    const Layout &y = prm.y;
-    const int b_idx = blockIdx.x, b = prm.seqs[b_idx], hq = blockIdx.y;
-    const int T = prm.lengths[y.len_index(b, prm.layer)];
-    const int n_pages = (T + y.P - 1) / y.P;
     const int ns = (n_pages + prm.chunk - 1) / prm.chunk;
-    const float *part = prm.partials + y.partial_index(b, hq, 0) * (y.d + 2);
-    float M = -INFINITY;
-    for (int s = 0; s < ns; ++s) M = fmaxf(M, part[(size_t)s * (y.d + 2)]);
-    for (int k = threadIdx.x; k < y.d; k += blockDim.x) {
-        float L = 0.f, O = 0.f;
-        for (int s = 0; s < ns; ++s) {
-            const float *ps = part + (size_t)s * (y.d + 2);
-            float sc = ps[0] == -INFINITY ? 0.f : exp2f(ps[0] - M);
-            L += sc * ps[1];
-            O += sc * ps[2 + k];
-        }
-        prm.out[((size_t)b_idx * y.Hq + hq) * y.d + k] = O / L;
-    }
+    finish_split<D>(prm, &comb[0][0][0], b_idx, b, h, split, ns, scratch, &last);
 }
 
 // ---------------------------------------------------------------- launch
 
+static void choose_chunk(DecodeParams &p, long total_pages, int max_pages, int ctas_per_wave, int &splits) {
+    int chunk = (int)((total_pages + ctas_per_wave - 1) / ctas_per_wave);
+    chunk = chunk < 1 ? 1 : (chunk > MAX_CHUNK ? MAX_CHUNK : chunk);
+    while ((max_pages + chunk - 1) / chunk > MAX_SPLITS) ++chunk;
+    p.chunk = chunk;
+    splits = (max_pages + chunk - 1) / chunk;
+}
+
 template <int P, int D, int MAXRT, int NS>
-static cudaError_t launch_bf16(const DecodeParams &p, dim3 grid, cudaStream_t st) {
+static cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     const Layout &y = p.y;
     size_t stage_bytes = ((y.rec_bytes > (size_t)P * D * 2 ? y.rec_bytes : (size_t)P * D * 2) + 127) & ~(size_t)127;
-    size_t comb_bytes = (size_t)NWC * 8 * (D + 2) * 4;
-    if (NS * stage_bytes < comb_bytes) return cudaErrorInvalidValue;
+    size_t tail_bytes = (size_t)NWC * 8 * (D + 2) * 4 + (3 * MAX_SPLITS * 8 + 16) * 4;  // comb + merge scratch
+    if (NS * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
     size_t smem = NS * stage_bytes + 2 * NS * sizeof(uint64_t) + sizeof(DecodeShared);
     auto k = decode_bf16_kernel<P, D, MAXRT, NS>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
+    int occ = 1;
+    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, (NWC + 1) * 32, smem) != cudaSuccess || occ < 1) occ = 1;
+    int splits = 1;
+    choose_chunk(p, total_pages, max_pages, num_sms * occ, splits);
+    dim3 grid((unsigned)splits, (unsigned)y.H, (unsigned)p.nseq);
     k<<<grid, (NWC + 1) * 32, smem, st>>>(p);
     return cudaGetLastError();
 }
 
 template <int P, int D>
-static cudaError_t launch_p_d(const DecodeParams &p, dim3 grid, cudaStream_t st) {
+static cudaError_t launch_p_d(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     if (p.y.dtype == 0) {
-        decode_f32_kernel<P, D><<<grid, NWC * 32, 0, st>>>(p);
+        auto k = decode_f32_kernel<P, D>;
+        int occ = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, NWC * 32, 0) != cudaSuccess || occ < 1) occ = 1;
+        int splits = 1;
+        choose_chunk(p, total_pages, max_pages, num_sms * occ, splits);
+        dim3 grid((unsigned)splits, (unsigned)p.y.H, (unsigned)p.nseq);
+        k<<<grid, NWC * 32, 0, st>>>(p);
         return cudaGetLastError();
     }
     int maxrt = (p.y.rkp > p.y.rvp ? p.y.rkp : p.y.rvp) / 8;
-    if (maxrt <= 4) return launch_bf16<P, D, 4, 8>(p, grid, st);
-    return launch_bf16<P, D, 8, 4>(p, grid, st);
+    if (maxrt <= 4) return launch_bf16<P, D, 4, 8>(p, total_pages, max_pages, num_sms, st);
+    return launch_bf16<P, D, 8, 4>(p, total_pages, max_pages, num_sms, st);
 }
 
-cudaError_t launch_decode(const DecodeParams &p, int splits, int num_sms, cudaStream_t st) {
-    (void)num_sms;
-    dim3 grid((unsigned)splits, (unsigned)p.y.H, (unsigned)p.nseq);
-    cudaError_t e = cudaErrorInvalidValue;
+cudaError_t launch_decode(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
 #define PKV_DEC_CASE(PP, DD) \
-    if (p.y.P == PP && p.y.d == DD) e = launch_p_d<PP, DD>(p, grid, st);
+    if (p.y.P == PP && p.y.d == DD) return launch_p_d<PP, DD>(p, total_pages, max_pages, num_sms, st);
     PKV_DEC_CASE(16, 64)
     PKV_DEC_CASE(32, 64)
     PKV_DEC_CASE(64, 64)
@@ -678,9 +730,7 @@ cudaError_t launch_decode(const DecodeParams &p, int splits, int num_sms, cudaSt
     PKV_DEC_CASE(32, 128)
     PKV_DEC_CASE(64, 128)
 #undef PKV_DEC_CASE
-    if (e != cudaSuccess) return e;
-    merge_splits_kernel<<<dim3((unsigned)p.nseq, (unsigned)p.y.Hq), 128, 0, st>>>(p);
-    return cudaGetLastError();
+    return cudaErrorInvalidValue;
 }
 
 }  // namespace pkv

@@ -172,7 +172,7 @@ __device__ int jacobi(FactorSmem<T, P, D> &s, int max_sweeps) {
                 if (gpq != 0.f && fabsf(gpq) > JACOBI_TOL * sqrtf(fabsf(gpp * gqq))) {
                     float zeta = (gqq - gpp) / (2.f * gpq);
                     t = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(1.f + zeta * zeta));
-                    c = rsqrtf(1.f + t * t);
+                    c = 1.f / sqrtf(1.f + t * t);
                     sn = t * c;
                     rot = 1;
                 }
@@ -255,9 +255,25 @@ __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lo
     }
     __syncthreads();
     const int r = v.r;
+    if (v.sigma && tid < P) v.sigma[tid] = sqrtf(fmaxf(s.lam[s.order[tid]], 0.f));
+    __syncthreads();
     for (int e = tid; e < P * P; e += FT_THREADS) {
         int i = e / P, j = e % P;
         s.G[i][j] = s.V[i][s.order[j]];
+    }
+    __syncthreads();
+    // Hundreds of rounds of fp32 rotations let the eigenvector norms drift by
+    // ~1e-5; scale the kept columns back to unit length (their mutual
+    // orthogonality is already at fp32 rounding level).
+    if (tid < v.r) {
+        float n2 = 0.f;
+        for (int i = 0; i < P; ++i) n2 = fmaf(s.G[i][tid], s.G[i][tid], n2);
+        s.lam[tid] = n2 > 0.f ? 1.f / sqrtf(n2) : 1.f;  // lam[] is free once order[] is set
+    }
+    __syncthreads();
+    for (int e = tid; e < P * v.r; e += FT_THREADS) {
+        int i = e / v.r, j = e % v.r;
+        s.G[i][j] *= s.lam[j];
     }
     __syncthreads();
 
@@ -280,7 +296,6 @@ __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lo
             store_elem<float>(v.L, (size_t)i * r + j, val);
         }
     }
-    if (v.sigma && tid < P) v.sigma[tid] = sqrtf(fmaxf(s.lam[s.order[tid]], 0.f));
     // R = Q_r^T X in fp32: thread -> head-dim column k, a group of ranks
     constexpr int PITCH = D * (int)sizeof(T);
     constexpr int GROUPS = FT_THREADS / D;

@@ -37,6 +37,7 @@ struct DecodeParams {
     const int *lengths, *desc;
     const char *q;      // [B][Hq][d] storage dtype
     float *partials;    // workspace split partials
+    int *tickets;       // workspace split tickets, zero between launches
     float *out;         // [B][Hq][d]
     int *status;
     int layer, chunk, nseq;
@@ -68,6 +69,8 @@ struct AppendParams {
 cudaError_t launch_factorize(const FactorParams &p, int num_sms, cudaStream_t st);
 cudaError_t launch_seq_init(const SeqInitParams &p, cudaStream_t st);
 cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
-cudaError_t launch_decode(const DecodeParams &p, int splits, int num_sms, cudaStream_t st);
+// Chooses pages per CTA (p.chunk) for one wave over total_pages pages
+// (all listed sequences and KV heads), then launches.
+cudaError_t launch_decode(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st);
 
 }  // namespace pkv

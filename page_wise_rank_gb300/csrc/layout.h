@@ -15,8 +15,9 @@
 //                leaving the ring.
 //   page table   int32 lengths[seq][layer], then int32 desc[seq][layer][page]
 //                = kind << 30 | slot.
-//   workspace    int32 status words, then fp32 split-K partial states
-//                [seq][q_head][split][2 + d].
+//   workspace    int32 status words, int32 split tickets [seq][kv_head], then
+//                fp32 split-K partial states [seq][q_head][split][4 + d]
+//                (m, l, two pad words, o[d]: 16-byte aligned rows).
 //
 // Factor record of one (layer, seq, kv head, page), element type e:
 //   LK  [P][rkp]    key left factor,   row = token   (B operand of s = t L_K^T)
@@ -89,7 +90,9 @@ struct Layout {
     size_t dense_half_bytes;  // one K or V page: P * d * esz
     size_t factor_pool_bytes, dense_pool_bytes, page_table_bytes, workspace_bytes;
     size_t desc_offset;       // byte offset of desc[] in the page table
+    size_t ticket_offset;     // byte offset of the per-(seq, kv head) split tickets in the workspace
     size_t partial_offset;    // byte offset of split partials in the workspace
+    int part_stride;          // floats per partial row: m, l, 2 pad, o[d]
 
     PKV_HD size_t record_index(int l, int b, int h, int p) const {
         return (((size_t)l * Bmax + b) * H + h) * (size_t)n_pg_max + p;
@@ -103,6 +106,7 @@ struct Layout {
     PKV_HD size_t len_index(int b, int l) const { return (size_t)b * L + l; }
     PKV_HD size_t desc_index(int b, int l, int p) const { return ((size_t)b * L + l) * n_pg_max + p; }
     PKV_HD size_t partial_index(int b, int hq, int s) const { return ((size_t)b * Hq + hq) * MAX_SPLITS + s; }
+    PKV_HD size_t ticket_index(int b, int h) const { return (size_t)b * H + h; }
 };
 
 // Fill a Layout from a validated configuration.
@@ -127,8 +131,10 @@ inline void make_layout(Layout &y, int L, int H, int Hq, int d, int P, int rk, i
     size_t len_bytes = ((size_t)Bmax * L * 4 + 255) & ~(size_t)255;
     y.desc_offset = len_bytes;
     y.page_table_bytes = len_bytes + (((size_t)Bmax * L * y.n_pg_max * 4 + 255) & ~(size_t)255);
-    y.partial_offset = 256;
-    y.workspace_bytes = y.partial_offset + (size_t)Bmax * Hq * MAX_SPLITS * (2 + d) * 4;
+    y.ticket_offset = 256;
+    y.partial_offset = y.ticket_offset + (((size_t)Bmax * H * 4 + 255) & ~(size_t)255);
+    y.part_stride = d + 4;
+    y.workspace_bytes = y.partial_offset + (size_t)Bmax * Hq * MAX_SPLITS * y.part_stride * 4;
 }
 
 }  // namespace pkv

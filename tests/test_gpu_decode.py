@@ -75,7 +75,12 @@ def test_tiny_fp32_config(pkv):
 
 def test_tiny_full_rank_equals_dense(pkv):
     """r = min(P, d): mixed attention equals dense softmax attention over the
-    original rows (spec full-rank check, on the GPU path)."""
+    original rows (spec full-rank check, on the GPU path).
+
+    Against the original rows the bound is 5e-5, not the 1e-5 of identical
+    factors: the fp32 eigensolve rebuilds each page only to ~1e-6 of its norm
+    (test_full_rank_reconstructs), which moves scores |q||k|/sqrt(d) ~ 10 by
+    ~1e-5.  On the factors the GPU stored the 1e-5 bar applies unchanged."""
     cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=8, head_dim=64, page_size=32, rank_k=32,
                    rank_v=32, sink_tokens=4, recent_tokens=64, max_batch=1, max_tokens_per_seq=1024,
                    kv_dtype=torch.float32)
@@ -89,7 +94,9 @@ def test_tiny_full_rank_equals_dense(pkv):
     for h in range(2):
         K, V = host.rows(0, 0, h)
         ref = oracle.attention(q[0, 4 * h:4 * h + 4].double().numpy(), K, V)
-        assert rel_err_rows(got[4 * h:4 * h + 4], ref) <= 1e-5
+        assert rel_err_rows(got[4 * h:4 * h + 4], ref) <= 5e-5
+        same = oracle_decode_on_store(store, cfg, host, 0, 0, h, q[0, 4 * h:4 * h + 4].double().numpy())
+        assert rel_err_rows(got[4 * h:4 * h + 4], same) <= 1e-5
 
 
 @pytest.mark.parametrize("T", [5000, 4097, 64 * 40, 130])

@@ -99,7 +99,9 @@ def test_degenerate_pages(pkv):
         _, _, So = oracle.factorize(Xd, r)
         e_star = math.sqrt(np.sum(So[r:] ** 2))
         e = np.linalg.norm(Xd - L[i].double().cpu().numpy() @ R[i].double().cpu().numpy())
-        assert e <= e_star * (1 + 1e-3) + 1e-5 * np.linalg.norm(Xd), (i, e, e_star)
+        # fp32 Gram floor: eigenvalues carry ~eps32 * ||X||^2 of rounding, so a page
+        # whose discarded energy sits below that can only be matched to it
+        assert e ** 2 <= e_star ** 2 * (1 + 2e-3) + 1e-7 * np.sum(Xd ** 2), (i, e, e_star)
 
 
 def test_bf16_output_is_rounded_fp32_output(pkv):

@@ -284,3 +284,22 @@ def test_printed_footprint_and_kv_size():
     s = g["dense_kv_size"]
     nbytes = oracle.dense_kv_elements(s["layers"], s["kv_heads"], s["T"], s["d"]) * s["bytes_per_element"]
     assert nbytes / 2 ** 30 == s["printed_gib"]
+
+
+def test_exactly_rank_deficient_pages_converge():
+    """Repeated rows, a single constant channel, bf16-rounded rank-1 pages:
+    exact rank deficiency must not stall the sweeps, and the pins still hold."""
+    rng = np.random.default_rng(8)
+    pages = []
+    X = np.zeros((64, 128)); X[:, 5] = 3.0; pages.append(X)
+    X = rng.standard_normal((64, 128)); X[32:] = X[:32]; pages.append(X)
+    u, w = rng.standard_normal(64), rng.standard_normal(128)
+    pages.append(torch.from_numpy(np.outer(u, w)).to(torch.bfloat16).double().numpy())
+    X = pages[-1].copy(); X[10:] = 0; pages.append(X)
+    for X in pages:
+        for r in (1, 16):
+            L, R, S = oracle.factorize(X, r)
+            assert eckart_young_defect(X, L, R, S, r) < 1e-12
+            assert np.abs(L.T @ L - np.eye(r)).max() < 1e-12
+            ref = np.linalg.svd(X, compute_uv=False)
+            assert np.abs(S - ref).max() <= 1e-12 * ref[0]
