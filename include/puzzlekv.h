@@ -170,6 +170,33 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *store, int32_t layer, 
                                           const int32_t *seq_ids, int32_t B, void *stream);
 
 /*
+ * Same computation and arguments as puzzlekv_decode_attention, for callers
+ * that cannot allocate device memory where they decode (runtimes that forbid
+ * allocation once serving has started, so that their footprint stays fixed
+ * and no request fails on or waits for the allocator; embedders whose device
+ * memory is owned by an allocator this layer cannot reach).  The page has no
+ * counterpart: this is a deployment variant, not part of the method.
+ *   - The split-K scratch (partial softmax states and split tickets) comes
+ *     from a 16 MiB array compiled into the library, one per GPU that loads
+ *     it, kept until the process exits; the store's workspace is not used
+ *     for it.  Nothing is allocated by this call.
+ *   - Stores needing more than 16 MiB of scratch (4 bytes x (max_batch x
+ *     num_kv_heads, rounded up to 64) + 4 bytes x max_batch x num_q_heads x
+ *     128 x (head_dim + 4)) are rejected with PUZZLEKV_ERR_CAPACITY before
+ *     anything is launched.
+ *   - The first call on a device looks up the array's device address
+ *     (cudaGetSymbolAddress) with that device current; make that first call
+ *     before any stream capture begins.
+ *   - Every call shares the one array and clears its split tickets on
+ *     `stream` before launching; calls whose kernels overlap on the GPU
+ *     (other streams, other threads) race on it and must be serialised by
+ *     the caller.
+ */
+puzzlekv_status puzzlekv_decode_attention_static_scratch(puzzlekv_store *store, int32_t layer, const void *q,
+                                                         float *out, const int32_t *seq_ids, int32_t B,
+                                                         void *stream);
+
+/*
  * Host-side accounting of one (sequence, layer) from the store's host mirror
  * (no device access): current length, dense and factorized page counts, and
  * the bytes those pages occupy (factors at the configured ranks plus the valid

@@ -171,6 +171,18 @@ class Store:
         check(lib().puzzlekv_decode_attention(self._h, layer, _ptr(q), _ptr(out), ids, B, _stream(stream)))
         return out
 
+    def decode_attention_static_scratch(self, layer: int, q: torch.Tensor, out: torch.Tensor,
+                                        seq_ids: Sequence[int], stream=None) -> torch.Tensor:
+        """decode_attention with its split-K scratch in the library's static
+        device array (no per-call scratch buffer; see include/puzzlekv.h)."""
+        c = self.cfg
+        ids, B = _seq_ids(seq_ids)
+        _need(q, (B, c.num_q_heads, c.head_dim), c.kv_dtype, "q")
+        _need(out, (B, c.num_q_heads, c.head_dim), torch.float32, "out")
+        check(lib().puzzlekv_decode_attention_static_scratch(self._h, layer, _ptr(q), _ptr(out), ids, B,
+                                                             _stream(stream)))
+        return out
+
     def stats(self, seq: int, layer: int) -> dict:
         n = ctypes.c_int32()
         nd, nf, nb = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()

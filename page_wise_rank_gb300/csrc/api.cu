@@ -11,6 +11,7 @@
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
+#include <mutex>
 #include <string>
 #include <vector>
 
@@ -413,3 +414,88 @@ puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *s, void *stream) {
 }
 
 }  // extern "C"
+
+// ---------------------------------------------------------------------------
+// Decode attention with split-K scratch in a static device array.
+//
+// Some callers cannot allocate device memory at the point where they decode:
+// serving runtimes that forbid allocation once they have started (so that the
+// memory footprint stays fixed and no request can fail on, or wait for, the
+// allocator), and embedders whose device memory belongs to another framework's
+// allocator that this layer cannot reach.  Such callers cannot set aside a
+// per-call scratch buffer for the split-K partial softmax states, so this
+// entry point takes that scratch from a file-scope array instead.
+namespace {
+
+constexpr size_t kStaticScratchBytes = (size_t)16 << 20;  // 16 MiB per device
+
+// Held by every GPU that loads this library, until the process exits.  In
+// host code this name is only a host-side stand-in: its device address comes
+// from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_decode_scratch[kStaticScratchBytes];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+void *g_scratch_addr[kMaxDevices] = {nullptr};
+
+}  // namespace
+
+extern "C" puzzlekv_status puzzlekv_decode_attention_static_scratch(puzzlekv_store *s, int32_t layer, const void *q,
+                                                                    float *out, const int32_t *seq_ids, int32_t B,
+                                                                    void *stream) {
+    puzzlekv_status st = check_call(s, layer, seq_ids, B);
+    if (st != PUZZLEKV_OK) return st;
+    if (!q || !out || !aligned16(q) || !aligned16(out))
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
+    const Layout &y = s->y;
+    const size_t ticket_bytes = ((size_t)y.Bmax * y.H * 4 + 255) & ~(size_t)255;
+    const size_t need = ticket_bytes + (size_t)y.Bmax * y.Hq * MAX_SPLITS * y.part_stride * 4;
+    if (need > kStaticScratchBytes)
+        return fail(PUZZLEKV_ERR_CAPACITY,
+                    "static decode scratch holds %zu bytes; this store needs %zu (max_batch x num_q_heads too large)",
+                    kStaticScratchBytes, need);
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(PUZZLEKV_ERR_UNSUPPORTED, "device index %d too large", dev);
+    void *base = nullptr;
+    {
+        std::lock_guard<std::mutex> lock(g_scratch_mu);
+        if (!g_scratch_addr[dev]) {  // first call on this device: look up the array's device address
+            void *p = nullptr;
+            e = cudaGetSymbolAddress(&p, g_decode_scratch);
+            if (e != cudaSuccess) return cuda_fail(e, "cudaGetSymbolAddress(static decode scratch)");
+            g_scratch_addr[dev] = p;
+        }
+        base = g_scratch_addr[dev];
+    }
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    // split tickets must start at zero; the array keeps the previous call's contents
+    e = cudaMemsetAsync(base, 0, ticket_bytes, strm);
+    if (e != cudaSuccess) return cuda_fail(e, "static scratch ticket reset");
+    DecodeParams dp{};
+    dp.y = y;
+    dp.factor_pool = s->factor_pool;
+    dp.dense_pool = s->dense_pool;
+    dp.lengths = lengths_ptr(s);
+    dp.desc = desc_ptr(s);
+    dp.q = static_cast<const char *>(q);
+    dp.tickets = static_cast<int *>(base);
+    dp.partials = reinterpret_cast<float *>(static_cast<char *>(base) + ticket_bytes);
+    dp.out = out;
+    dp.status = status_ptr(s);
+    dp.layer = layer;
+    dp.nseq = B;
+    long total = 0;
+    int max_pages = 0;
+    for (int i = 0; i < B; ++i) {
+        int T = s->len[(size_t)seq_ids[i] * y.L + layer];
+        int np = (T + y.P - 1) / y.P;
+        total += (long)np * y.H;
+        max_pages = std::max(max_pages, np);
+        dp.seqs[i] = seq_ids[i];
+    }
+    e = launch_decode(dp, total, max_pages, s->num_sms, strm);
+    if (e != cudaSuccess) return cuda_fail(e, "decode launch (static scratch)");
+    return PUZZLEKV_OK;
+}
