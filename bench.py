@@ -51,6 +51,7 @@ def parse():
     ap.add_argument("--workload", default="llama32k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
     return ap.parse_args()
 
 
@@ -173,7 +174,10 @@ def gpu_arm(args, rank, world, local):
     import synth
     from page_wise_rank_gb300 import build as cuda_build
 
-    wl = WORKLOADS[args.workload]
+    wl = dict(WORKLOADS[args.workload])
+    if args.layers:
+        wl["layers"] = args.layers
+        wl["desc"] += f" (first {args.layers} layers only)"
     cuda_build.build()
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
@@ -227,20 +231,29 @@ def gpu_arm(args, rank, world, local):
         kk = ks[s] if k_src is None else k_src
         vv = vs[s] if v_src is None else v_src
         T = store_len[0]
-        conv = any(pkv.classify_pages(T, P, wl["sink"], wl["W"])[p] == pkv.PAGE_DENSE and
-                   pkv.classify_pages(T + 1, P, wl["sink"], wl["W"])[p] == pkv.PAGE_FACTORED
-                   for p in range(max(0, (T - wl["W"]) // P - 1), (T + P - 1) // P))
+        conv = (T + 1) % P == 0  # this step completes a page (batched factorization)
         for l in range(L):
-            store.append_token(l, kk[l], vv[l], seqs, stream=stream)
             if ev is not None:
                 ev[l][0].record(stream)
-            store.decode_attention(l, qq[l], out[l], seqs, stream=stream)
+            store.decode_step(l, qq[l], kk[l], vv[l], out[l], seqs, stream=stream)
             if ev is not None:
                 ev[l][1].record(stream)
-        launches[0] += L * 3 + (L if conv else 0)
+        # pages completed by this step: factorize them now, in one batched launch
+        # over all layers, ahead of their leaving the window
+        if (T + 1) % P == 0:
+            if ev is not None:
+                ev[L][0].record(stream)
+            store.convert_ready_pages(stream=stream)
+            if ev is not None:
+                ev[L][1].record(stream)
+            launches[0] += 1
+        else:
+            store.convert_ready_pages(stream=stream)  # host bookkeeping only
+        launches[0] += L
         store_len[0] = T + 1
         if out_dst is not None:
             out_dst.copy_(out, non_blocking=True)
+        return conv
 
     store_len = [T0]
     with torch.cuda.stream(stream):
@@ -248,7 +261,7 @@ def gpu_arm(args, rank, world, local):
             step(s)
         stream.synchronize()
         # ---- timed region: K steps, device-resident inputs
-        evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L)]
+        evs = [[[torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)] for _ in range(L + 1)]
                for _ in range(args.steps)]
         t_lens = []
         clocks = ClockSampler(torch.cuda.current_device())
@@ -258,9 +271,10 @@ def gpu_arm(args, rank, world, local):
         launches[0] = 0
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         s0.record(stream)
+        conv_steps = []
         for i in range(args.steps):
             t_lens.append(store_len[0] + 1)
-            step(args.warmup + i, ev=evs[i])
+            conv_steps.append(step(args.warmup + i, ev=evs[i]))
         s1.record(stream)
         stream.synchronize()
         barrier(world)
@@ -270,8 +284,10 @@ def gpu_arm(args, rank, world, local):
         st = store.check_device_status(stream)
         if st != 0:
             raise RuntimeError(f"device status {st}: {pkv.last_error()}")
+        # every decode_step launch (page conversions run in the separate batched call)
         dec_ms = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(args.steps) for l in range(L)]
         dec_bytes = [alg_bytes(wl, t_lens[i]) for i in range(args.steps) for l in range(L)]
+        conv_ms = [evs[i][L][0].elapsed_time(evs[i][L][1]) for i in range(args.steps) if conv_steps[i]]
         # ---- e2e: same steps through the public API with pinned host buffers
         e2e = None
         if not args.no_e2e:
@@ -319,11 +335,12 @@ def gpu_arm(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {alg_bytes(wl, T0) * L / 1e9:.2f} GB read per step"},
         "decode_attention_us_per_layer": round(dec_us, 3),
+        "batched_conversion_us": round(1000.0 * statistics.mean(conv_ms), 1) if conv_ms else None,
         "pages_factorized_per_s": round(pages_per_s, 1),
         "prefill_factorization": {"pages": n_fact_pages, "ms": round(prefill_ms, 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "kernel": "decode_bf16_kernel + merge_splits_kernel (one decode_attention call)",
+                     "kernel": "decode_bf16_kernel (one decode_step call: append + attention + split merge)",
                      "traffic": (traffic["bytes_per_launch"] if traffic else None),
                      "algorithmic_bytes_per_launch": int(statistics.mean(dec_bytes))},
         "e2e": e2e,

@@ -170,6 +170,35 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *store, int32_t layer, 
                                           const int32_t *seq_ids, int32_t B, void *stream);
 
 /*
+ * Factorize ahead of time, in one batched launch over all sequences and
+ * layers, every page that is complete but has no factors yet (pages inside
+ * the local window included) [PuzzleKV §3.3 ⑤].  A page's content is final
+ * once its P tokens are present, W tokens before it leaves the window; when
+ * it leaves, puzzlekv_append_token / puzzlekv_decode_step then only switch it
+ * to its factors instead of factorizing one page per layer on the critical
+ * path.  Calling this is optional (without it those calls factorize the page
+ * themselves) and cheap when nothing is pending (host bookkeeping only);
+ * calling it once per decode step, after the last layer, is the intended use.
+ * Pages whose dense slot might be reused are never listed: a page reaches
+ * the window's end before its slot comes round again.
+ */
+puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *store, void *stream);
+
+/*
+ * One decode step of one layer in a single attention launch [PuzzleKV §3.3
+ * ④ and ⑤]: append the new key/value row of each listed sequence (as
+ * puzzlekv_append_token) and attend over the grown cache (as
+ * puzzlekv_decode_attention), the new token included.  If the append moves a
+ * completed page out of the local window, that page is factorized on
+ * `stream` first, so this step already attends over its factors.
+ *   q:   device, [B][num_q_heads][head_dim];  k, v: device, [B][num_kv_heads][head_dim]
+ *   out: device fp32, [B][num_q_heads][head_dim]; seq_ids: host, B distinct slots.
+ * Equivalent to puzzlekv_append_token followed by puzzlekv_decode_attention.
+ */
+puzzlekv_status puzzlekv_decode_step(puzzlekv_store *store, int32_t layer, const void *q, const void *k,
+                                     const void *v, float *out, const int32_t *seq_ids, int32_t B, void *stream);
+
+/*
  * Same computation and arguments as puzzlekv_decode_attention, for callers
  * that cannot allocate device memory where they decode (runtimes that forbid
  * allocation once serving has started, so that their footprint stays fixed

@@ -171,6 +171,25 @@ class Store:
         check(lib().puzzlekv_decode_attention(self._h, layer, _ptr(q), _ptr(out), ids, B, _stream(stream)))
         return out
 
+    def decode_step(self, layer: int, q: torch.Tensor, k: torch.Tensor, v: torch.Tensor, out: torch.Tensor,
+                    seq_ids: Sequence[int], stream=None) -> torch.Tensor:
+        """Append (k, v) and attend with q in one launch (§3.3 ④⑤); converts the
+        page leaving the window first."""
+        c = self.cfg
+        ids, B = _seq_ids(seq_ids)
+        _need(q, (B, c.num_q_heads, c.head_dim), c.kv_dtype, "q")
+        _need(k, (B, c.num_kv_heads, c.head_dim), c.kv_dtype, "k")
+        _need(v, (B, c.num_kv_heads, c.head_dim), c.kv_dtype, "v")
+        _need(out, (B, c.num_q_heads, c.head_dim), torch.float32, "out")
+        check(lib().puzzlekv_decode_step(self._h, layer, _ptr(q), _ptr(k), _ptr(v), _ptr(out), ids, B,
+                                         _stream(stream)))
+        return out
+
+    def convert_ready_pages(self, stream=None) -> None:
+        """Factorize every complete, not yet factorized page of all sequences and
+        layers in one batched launch (ahead of its leaving the window)."""
+        check(lib().puzzlekv_convert_ready_pages(self._h, _stream(stream)))
+
     def decode_attention_static_scratch(self, layer: int, q: torch.Tensor, out: torch.Tensor,
                                         seq_ids: Sequence[int], stream=None) -> torch.Tensor:
         """decode_attention with its split-K scratch in the library's static

@@ -25,6 +25,8 @@ EXPORTED = (
     "puzzlekv_factorize_batch",
     "puzzlekv_append_token",
     "puzzlekv_decode_attention",
+    "puzzlekv_decode_step",
+    "puzzlekv_convert_ready_pages",
     "puzzlekv_decode_attention_static_scratch",
     "puzzlekv_store_stats",
     "puzzlekv_check_device_status",
@@ -70,6 +72,8 @@ def lib() -> ctypes.CDLL:
         "puzzlekv_append_token": ([vp, i32, vp, vp, i32p, i32, vp], i32),
         "puzzlekv_decode_attention": ([vp, i32, vp, vp, i32p, i32, vp], i32),
         "puzzlekv_decode_attention_static_scratch": ([vp, i32, vp, vp, i32p, i32, vp], i32),
+        "puzzlekv_decode_step": ([vp, i32, vp, vp, vp, vp, i32p, i32, vp], i32),
+        "puzzlekv_convert_ready_pages": ([vp, vp], i32),
         "puzzlekv_store_stats": ([vp, i32, i32, i32p, i64p, i64p, i64p], i32),
         "puzzlekv_check_device_status": ([vp, vp], i32),
         "puzzlekv_classify_pages": ([i32, i32, i32, i32, i32p, i32], i32),

@@ -71,8 +71,8 @@ puzzlekv_status validate_config(const puzzlekv_config *c) {
         return fail(PUZZLEKV_ERR_INVALID_ARG, "sink_tokens and recent_tokens must be >= 0");
     if (c->kv_dtype != PUZZLEKV_F32 && c->kv_dtype != PUZZLEKV_BF16)
         return fail(PUZZLEKV_ERR_INVALID_ARG, "kv_dtype must be PUZZLEKV_F32 or PUZZLEKV_BF16");
-    if (c->max_batch > (1 << 16) || c->max_tokens_per_seq > (1 << 24))
-        return fail(PUZZLEKV_ERR_UNSUPPORTED, "max_batch or max_tokens_per_seq too large");
+    if (c->max_batch > (1 << 16) || c->max_tokens_per_seq > (1 << 24) || c->num_layers > 255)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "max_batch, max_tokens_per_seq or num_layers too large");
     int P = c->page_size;
     int sink_pages = (c->sink_tokens + P - 1) / P;
     int ring = (c->recent_tokens + P - 1) / P + 2;
@@ -96,6 +96,8 @@ struct puzzlekv_store {
     Layout y;
     char *dense_pool, *factor_pool, *page_table, *workspace;
     std::vector<int> len;    // host mirror [seq][layer]; -1 = empty slot
+    std::vector<int> conv_upto;  // [seq][layer]: pages below this index (past the sink) have factor records
+    std::vector<int2> job_host;  // staging of the batched-conversion job list
     int num_sms;
 };
 
@@ -152,6 +154,7 @@ puzzlekv_status puzzlekv_store_create(const puzzlekv_config *cfg, void *dense_po
     s->page_table = static_cast<char *>(page_table);
     s->workspace = static_cast<char *>(workspace);
     s->len.assign((size_t)cfg->max_batch * cfg->num_layers, -1);
+    s->conv_upto.assign((size_t)cfg->max_batch * cfg->num_layers, 0);
     s->num_sms = sm_count();
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(dense_pool, 0, s->y.dense_pool_bytes, strm);
@@ -223,7 +226,10 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const v
         e = launch_factorize(fp, s->num_sms, strm);
         if (e != cudaSuccess) return cuda_fail(e, "factorize launch");
     }
-    for (int l = 0; l < y.L; ++l) s->len[(size_t)seq * y.L + l] = T;
+    for (int l = 0; l < y.L; ++l) {
+        s->len[(size_t)seq * y.L + l] = T;
+        s->conv_upto[(size_t)seq * y.L + l] = f_lo >= 0 ? f_hi : y.sink_pages;
+    }
     return PUZZLEKV_OK;
 }
 
@@ -255,6 +261,48 @@ puzzlekv_status puzzlekv_factorize_batch(const void *X, int32_t x_dtype, int64_t
     cudaError_t e = launch_factorize(fp, sm_count(), static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "factorize_batch launch");
     return PUZZLEKV_OK;
+}
+
+// [PuzzleKV §3.3 ⑤]: the page (if any) that growing a sequence from T to
+// T + 1 tokens moves out of the dense region; at most one per step.
+static int converted_page(const Layout &y, int T) {
+    int conv = -1;
+    const int n_old = (T + y.P - 1) / y.P;
+    for (int p = std::max(0, (T - y.W) / y.P - 1); p < n_old; ++p)
+        if (host_page_kind(p, T, y.P, y.sink_tokens, y.W) == KIND_DENSE &&
+            host_page_kind(p, T + 1, y.P, y.sink_tokens, y.W) == KIND_FACTORED)
+            conv = p;
+    return conv;
+}
+
+// Decode-kernel parameters for one call (lengths from the host mirror).
+static void fill_decode_params(puzzlekv_store *s, int32_t layer, const void *q, float *out, const int32_t *seq_ids,
+                               int32_t B, int extra_tokens, DecodeParams &dp, long &total, int &max_pages) {
+    const Layout &y = s->y;
+    dp = DecodeParams{};
+    dp.y = y;
+    dp.factor_pool = s->factor_pool;
+    dp.dense_pool = s->dense_pool;
+    dp.lengths = reinterpret_cast<const int *>(s->page_table);
+    dp.desc = reinterpret_cast<const int *>(s->page_table + y.desc_offset);
+    dp.q = static_cast<const char *>(q);
+    dp.partials = reinterpret_cast<float *>(s->workspace + y.partial_offset);
+    dp.tickets = reinterpret_cast<int *>(s->workspace + y.ticket_offset);
+    dp.out = out;
+    dp.status = reinterpret_cast<int *>(s->workspace);
+    dp.layer = layer;
+    dp.nseq = B;
+    total = 0;
+    max_pages = 0;
+    for (int i = 0; i < B; ++i) {
+        const int T = s->len[(size_t)seq_ids[i] * y.L + layer] + extra_tokens;
+        const int np = (T + y.P - 1) / y.P;
+        total += (long)np * y.H;
+        max_pages = std::max(max_pages, np);
+        dp.seqs[i] = seq_ids[i];
+        dp.lens[i] = T;
+        dp.conv_page[i] = -1;
+    }
 }
 
 static puzzlekv_status check_call(puzzlekv_store *s, int32_t layer, const int32_t *seq_ids, int32_t B) {
@@ -292,27 +340,22 @@ puzzlekv_status puzzlekv_append_token(puzzlekv_store *s, int32_t layer, const vo
     FactorParams fp{};
     fp.n_conv = 0;
     for (int i = 0; i < B; ++i) {
+        const int T = s->len[(size_t)seq_ids[i] * y.L + layer];
+        if (T + 1 > y.Tmax) return fail(PUZZLEKV_ERR_CAPACITY, "sequence %d is full (%d tokens)", seq_ids[i], T);
+    }
+    for (int i = 0; i < B; ++i) {
         int b = seq_ids[i];
         int T = s->len[(size_t)b * y.L + layer];
-        if (T + 1 > y.Tmax) return fail(PUZZLEKV_ERR_CAPACITY, "sequence %d is full (%d tokens)", b, T);
         ap.seqs[i] = b;
         ap.pos[i] = T;
-        // [PuzzleKV §3.3 ⑤]: the page that T -> T + 1 moves out of the dense region
-        int conv = -1;
-        int n_old = (T + y.P - 1) / y.P;
-        int lo = std::max(0, (T - y.W) / y.P - 1);
-        for (int p = lo; p < n_old; ++p) {
-            if (host_page_kind(p, T, y.P, y.sink_tokens, y.W) == KIND_DENSE &&
-                host_page_kind(p, T + 1, y.P, y.sink_tokens, y.W) == KIND_FACTORED) {
-                if (conv >= 0) return fail(PUZZLEKV_ERR_INVALID_ARG, "internal: two conversions in one step");
-                conv = p;
-            }
-        }
-        ap.conv_page[i] = conv;
-        if (conv >= 0) {
+        const int conv = converted_page(y, T);
+        ap.conv_page[i] = conv;  // descriptor flip
+        int &upto = s->conv_upto[(size_t)b * y.L + layer];
+        if (conv >= upto) {  // not factorized ahead of time: factorize it now, before attention
             fp.conv_seq[fp.n_conv] = b;
             fp.conv_page[fp.n_conv] = conv;
             fp.n_conv++;
+            upto = conv + 1;
         }
     }
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
@@ -343,31 +386,112 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *s, int32_t layer, cons
     if (st != PUZZLEKV_OK) return st;
     if (!q || !out || !aligned16(q) || !aligned16(out))
         return fail(PUZZLEKV_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
-    const Layout &y = s->y;
-    DecodeParams dp{};
-    dp.y = y;
-    dp.factor_pool = s->factor_pool;
-    dp.dense_pool = s->dense_pool;
-    dp.lengths = lengths_ptr(s);
-    dp.desc = desc_ptr(s);
-    dp.q = static_cast<const char *>(q);
-    dp.partials = reinterpret_cast<float *>(s->workspace + y.partial_offset);
-    dp.out = out;
-    dp.status = status_ptr(s);
-    dp.layer = layer;
-    dp.nseq = B;
-    long total = 0;
-    int max_pages = 0;
-    for (int i = 0; i < B; ++i) {
-        int T = s->len[(size_t)seq_ids[i] * y.L + layer];
-        int np = (T + y.P - 1) / y.P;
-        total += (long)np * y.H;
-        max_pages = std::max(max_pages, np);
-        dp.seqs[i] = seq_ids[i];
-    }
-    dp.tickets = reinterpret_cast<int *>(s->workspace + y.ticket_offset);
+    DecodeParams dp;
+    long total;
+    int max_pages;
+    fill_decode_params(s, layer, q, out, seq_ids, B, 0, dp, total, max_pages);
     cudaError_t e = launch_decode(dp, total, max_pages, s->num_sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_decode_step(puzzlekv_store *s, int32_t layer, const void *q, const void *k, const void *v,
+                                     float *out, const int32_t *seq_ids, int32_t B, void *stream) {
+    puzzlekv_status st = check_call(s, layer, seq_ids, B);
+    if (st != PUZZLEKV_OK) return st;
+    if (!q || !out || !k || !v || !aligned16(q) || !aligned16(out) || !aligned16(k) || !aligned16(v))
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "q, k, v and out must be non-NULL and 16-byte aligned");
+    const Layout &y = s->y;
+    FactorParams fp{};
+    fp.n_conv = 0;
+    for (int i = 0; i < B; ++i) {
+        const int b = seq_ids[i];
+        const int T = s->len[(size_t)b * y.L + layer];
+        if (T + 1 > y.Tmax) return fail(PUZZLEKV_ERR_CAPACITY, "sequence %d is full (%d tokens)", b, T);
+    }
+    DecodeParams dp;
+    long total;
+    int max_pages;
+    fill_decode_params(s, layer, q, out, seq_ids, B, 1, dp, total, max_pages);
+    dp.append = 1;
+    dp.k_new = static_cast<const char *>(k);
+    dp.v_new = static_cast<const char *>(v);
+    dp.lengths_out = reinterpret_cast<int *>(s->page_table);
+    dp.desc_out = reinterpret_cast<int *>(s->page_table + y.desc_offset);
+    for (int i = 0; i < B; ++i) {
+        const int b = seq_ids[i];
+        const int conv = converted_page(y, s->len[(size_t)b * y.L + layer]);
+        dp.conv_page[i] = conv;  // descriptor flip
+        int &upto = s->conv_upto[(size_t)b * y.L + layer];
+        if (conv >= upto) {  // not factorized ahead of time: factorize it now, before attention
+            fp.conv_seq[fp.n_conv] = b;
+            fp.conv_page[fp.n_conv] = conv;
+            fp.n_conv++;
+            upto = conv + 1;
+        }
+    }
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    cudaError_t e;
+    if (fp.n_conv > 0) {  // the page leaving the window is factorized before this step's attention
+        fp.mode = FACT_MODE_CONVERT;
+        fp.max_sweeps = 24;
+        fp.status = status_ptr(s);
+        fp.y = y;
+        fp.P = y.P;
+        fp.d = y.d;
+        fp.x_esz = y.esz;
+        fp.factor_pool = s->factor_pool;
+        fp.dense_pool = s->dense_pool;
+        fp.layer = layer;
+        fp.n_jobs = (long)fp.n_conv * y.H * 2;
+        e = launch_factorize(fp, s->num_sms, strm);
+        if (e != cudaSuccess) return cuda_fail(e, "conversion launch");
+    }
+    e = launch_decode(dp, total, max_pages, s->num_sms, strm);
+    if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
+    for (int i = 0; i < B; ++i) s->len[(size_t)seq_ids[i] * y.L + layer] += 1;
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    const Layout &y = s->y;
+    s->job_host.clear();
+    for (int b = 0; b < y.Bmax; ++b) {
+        for (int l = 0; l < y.L; ++l) {
+            const int T = s->len[(size_t)b * y.L + l];
+            if (T < 1) continue;
+            int &upto = s->conv_upto[(size_t)b * y.L + l];
+            const int complete = T / y.P;  // pages whose P tokens are all present
+            for (int p = std::max(upto, y.sink_pages); p < complete; ++p) {
+                if ((int)s->job_host.size() >= y.max_conv_jobs)
+                    return fail(PUZZLEKV_ERR_CAPACITY, "internal: conversion list overflow");
+                s->job_host.push_back(make_int2((b << 8) | l, p));
+            }
+            upto = std::max(upto, complete);
+        }
+    }
+    if (s->job_host.empty()) return PUZZLEKV_OK;
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    int2 *dev_jobs = reinterpret_cast<int2 *>(s->workspace + y.jobs_offset);
+    // pageable source: the copy has consumed job_host when cudaMemcpyAsync returns
+    cudaError_t e = cudaMemcpyAsync(dev_jobs, s->job_host.data(), s->job_host.size() * sizeof(int2),
+                                    cudaMemcpyHostToDevice, strm);
+    if (e != cudaSuccess) return cuda_fail(e, "conversion list upload");
+    FactorParams fp{};
+    fp.mode = FACT_MODE_CONVERT_LIST;
+    fp.max_sweeps = 24;
+    fp.status = status_ptr(s);
+    fp.y = y;
+    fp.P = y.P;
+    fp.d = y.d;
+    fp.x_esz = y.esz;
+    fp.factor_pool = s->factor_pool;
+    fp.dense_pool = s->dense_pool;
+    fp.conv_list = dev_jobs;
+    fp.n_jobs = (long)s->job_host.size() * y.H * 2;
+    e = launch_factorize(fp, s->num_sms, strm);
+    if (e != cudaSuccess) return cuda_fail(e, "batched conversion launch");
     return PUZZLEKV_OK;
 }
 
@@ -473,28 +597,12 @@ extern "C" puzzlekv_status puzzlekv_decode_attention_static_scratch(puzzlekv_sto
     // split tickets must start at zero; the array keeps the previous call's contents
     e = cudaMemsetAsync(base, 0, ticket_bytes, strm);
     if (e != cudaSuccess) return cuda_fail(e, "static scratch ticket reset");
-    DecodeParams dp{};
-    dp.y = y;
-    dp.factor_pool = s->factor_pool;
-    dp.dense_pool = s->dense_pool;
-    dp.lengths = lengths_ptr(s);
-    dp.desc = desc_ptr(s);
-    dp.q = static_cast<const char *>(q);
+    DecodeParams dp;
+    long total;
+    int max_pages;
+    fill_decode_params(s, layer, q, out, seq_ids, B, 0, dp, total, max_pages);
     dp.tickets = static_cast<int *>(base);
     dp.partials = reinterpret_cast<float *>(static_cast<char *>(base) + ticket_bytes);
-    dp.out = out;
-    dp.status = status_ptr(s);
-    dp.layer = layer;
-    dp.nseq = B;
-    long total = 0;
-    int max_pages = 0;
-    for (int i = 0; i < B; ++i) {
-        int T = s->len[(size_t)seq_ids[i] * y.L + layer];
-        int np = (T + y.P - 1) / y.P;
-        total += (long)np * y.H;
-        max_pages = std::max(max_pages, np);
-        dp.seqs[i] = seq_ids[i];
-    }
     e = launch_decode(dp, total, max_pages, s->num_sms, strm);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch (static scratch)");
     return PUZZLEKV_OK;

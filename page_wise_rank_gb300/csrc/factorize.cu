@@ -8,9 +8,9 @@
 //   2. G = X X^T in fp32: bf16 pages on tensor cores (mma.sync m16n8k16,
 //      bf16 products are exact in fp32), fp32 pages on CUDA cores;
 //   3. cyclic Jacobi on G with the round-robin (circle) pairing: each round
-//      rotates P/2 disjoint pairs at once, every thread updating 2x2 blocks
-//      of G and pairs of eigenvector entries; a sweep is P-1 rounds; stop
-//      after a sweep with no rotation (relative threshold), or at the cap;
+//      rotates P/2 disjoint pairs at once (2x2 blocks of G, pairs of
+//      eigenvector rows); a sweep is P-1 rounds; stop after a sweep with no
+//      rotation (relative threshold), or at the cap;
 //   4. eigenvalues ranked descending (ties: lower index first);
 //   5. L = Q_r, R = Q_r^T X in fp32, written as bf16 or fp32 into either a
 //      factor record (swizzled store layout) or plain row-major arrays.
@@ -19,16 +19,15 @@
 
 namespace pkv {
 
-constexpr int FT_THREADS = 256;
 constexpr float JACOBI_TOL = 1e-6f;
 
 template <typename T, int P, int D>
 struct FactorSmem {
     alignas(128) unsigned char X[P * D * sizeof(T)];  // swizzled rows, pitch D * sizeof(T)
-    float G[P][P + 1];  // Gram matrix; after the eigensolve reused for Q[i][j] = V[i][order[j]]
-    float V[P][P + 1];
-    float cs[P / 2], sn[P / 2], tn[P / 2];
-    int pp[P / 2], qq[P / 2];
+    float G[P][P + 1];  // Gram matrix; after the eigensolve reused for Q[i][j] = Vt[order[j]][i]
+    alignas(16) float Vt[P][P + 4];  // eigenvectors, one per row (rows stay 16-byte aligned)
+    float4 pair[P / 2];              // per pair of the round: (p, q as int bits, cos, sin)
+    float tn[P / 2];                 // tan of the pair's angle (0: no rotation)
     float lam[P];
     int order[P];
 };
@@ -71,6 +70,17 @@ __device__ __forceinline__ JobView job_view(const FactorParams &fp, long job) {
         v.kind = kind;
         v.r = kind == 0 ? y.rk : y.rv;
         v.rec = fp.factor_pool + y.record_offset(l, fp.seq, h, pg);
+    } else if (fp.mode == FACT_MODE_CONVERT_LIST) {  // job -> (list entry, head, kind)
+        int kind = (int)(job % 2);
+        long t = job / 2;
+        int h = (int)(t % y.H);
+        const int2 e = fp.conv_list[t / y.H];
+        const int b = e.x >> 8, l = e.x & 255, pg = e.y;
+        v.x = fp.dense_pool + y.dense_offset(l, b, y.dense_slot(pg), h, kind);
+        v.x_pool = 1;
+        v.kind = kind;
+        v.r = kind == 0 ? y.rk : y.rv;
+        v.rec = fp.factor_pool + y.record_offset(l, b, h, pg);
     } else {  // FACT_MODE_CONVERT: job -> (call entry, head, kind)
         int kind = (int)(job % 2);
         long t = job / 2;
@@ -86,13 +96,13 @@ __device__ __forceinline__ JobView job_view(const FactorParams &fp, long job) {
     return v;
 }
 
-template <typename T, int P, int D>
+template <typename T, int P, int D, int NT>
 __device__ void load_page(FactorSmem<T, P, D> &s, const JobView &v) {
     // 16-byte vectors; pool pages are already swizzled, plain rows get swizzled here
     constexpr int PITCH = D * (int)sizeof(T);
     constexpr int NVEC = P * PITCH / 16;
     const uint4 *src = reinterpret_cast<const uint4 *>(v.x);
-    for (int i = threadIdx.x; i < NVEC; i += FT_THREADS) {
+    for (int i = threadIdx.x; i < NVEC; i += NT) {
         uint4 val = src[i];
         int row = (i * 16) / PITCH, b = (i * 16) % PITCH;
         uint32_t off = v.x_pool ? (uint32_t)(i * 16) : swz_offset(row, b, PITCH);
@@ -101,13 +111,13 @@ __device__ void load_page(FactorSmem<T, P, D> &s, const JobView &v) {
 }
 
 // G = X X^T, bf16 rows on tensor cores.
-template <int P, int D>
+template <int P, int D, int NT>
 __device__ void gram_bf16(FactorSmem<__nv_bfloat16, P, D> &s) {
-    constexpr int MT = P / 16, NT = P / 8, KS = D / 16, PITCH = D * 2;
+    constexpr int MT = P / 16, NTL = P / 8, KS = D / 16, PITCH = D * 2;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const uint32_t xb = smem_u32(s.X);
-    for (int tile = warp; tile < MT * NT; tile += FT_THREADS / 32) {
-        int mt = tile / NT, nt = tile % NT;
+    for (int tile = warp; tile < MT * NTL; tile += NT / 32) {
+        int mt = tile / NTL, nt = tile % NTL;
         float acc[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
@@ -131,10 +141,10 @@ __device__ void gram_bf16(FactorSmem<__nv_bfloat16, P, D> &s) {
 }
 
 // G = X X^T, fp32 rows on CUDA cores (upper triangle, mirrored).
-template <int P, int D>
+template <int P, int D, int NT>
 __device__ void gram_f32(FactorSmem<float, P, D> &s) {
     constexpr int PITCH = D * 4;
-    for (int e = threadIdx.x; e < P * P; e += FT_THREADS) {
+    for (int e = threadIdx.x; e < P * P; e += NT) {
         int i = e / P, j = e % P;
         if (j < i) continue;
         float acc = 0.f;
@@ -146,20 +156,41 @@ __device__ void gram_f32(FactorSmem<float, P, D> &s) {
     }
 }
 
-// Cyclic Jacobi eigensolve of the symmetric P x P matrix in s.G; eigenvectors
-// accumulate into s.V.  Returns the number of sweeps, or -1 at the cap.
-template <typename T, int P, int D>
+// Cyclic Jacobi eigensolve of the symmetric P x P matrix in s.G (upper
+// triangle, G[i][j] with i <= j, is the matrix); eigenvectors accumulate as
+// the rows of s.Vt.  Returns the number of sweeps, or -1 at the cap.  A round
+// rotates the P/2 disjoint pairs of the round-robin (circle) pairing at once:
+// phase A computes the angles, phase B applies G <- J^T G J to the 2x2
+// blocks of the upper triangle (each thread keeps its blocks for the whole
+// solve) and rotates pairs of eigenvector rows with 16-byte vectors.  Blocks
+// and rows of pairs that did not rotate are left alone.
+template <typename T, int P, int D, int NT>
 __device__ int jacobi(FactorSmem<T, P, D> &s, int max_sweeps) {
     constexpr int NP = P / 2;
+    constexpr int NBLK = NP * (NP + 1) / 2;
+    constexpr int BPT = (NBLK + NT - 1) / NT;  // blocks per thread
+    constexpr int V4 = P / 4;                  // float4 per eigenvector row
     const int tid = threadIdx.x;
-    for (int e = tid; e < P * P; e += FT_THREADS) s.V[e / P][e % P] = (e / P == e % P) ? 1.f : 0.f;
+    for (int e = tid; e < P * P; e += NT) s.Vt[e / P][e % P] = (e / P == e % P) ? 1.f : 0.f;
+    int my_al[BPT], my_be[BPT];
+#pragma unroll
+    for (int i = 0; i < BPT; ++i) {  // block e = tid + i * NT of the row-major upper triangle
+        int e = tid + i * NT, be = 0;
+        if (e < NBLK) {
+            while ((be + 1) * (be + 2) / 2 <= e) ++be;
+            my_al[i] = e - be * (be + 1) / 2;
+            my_be[i] = be;
+        } else {
+            my_al[i] = my_be[i] = -1;
+        }
+    }
+    const float tol2 = JACOBI_TOL * JACOBI_TOL;
     __syncthreads();
     for (int sweep = 0; sweep < max_sweeps; ++sweep) {
         int rotated_any = 0;
         for (int round = 0; round < P - 1; ++round) {
-            // Phase A: angles of the NP disjoint pairs of this round (circle method:
-            // slot 0 holds index 0, slot i >= 1 holds 1 + (i - 1 - round) mod (P - 1);
-            // slot k meets slot P - 1 - k).
+            // Phase A: slot 0 holds index 0, slot i >= 1 holds 1 + (i - 1 - round) mod (P - 1);
+            // slot k meets slot P - 1 - k.
             int rot = 0;
             if (tid < NP) {
                 int k = tid;
@@ -169,50 +200,66 @@ __device__ int jacobi(FactorSmem<T, P, D> &s, int max_sweeps) {
                 int p = a < b ? a : b, q = a < b ? b : a;
                 float gpp = s.G[p][p], gqq = s.G[q][q], gpq = s.G[p][q];
                 float c = 1.f, sn = 0.f, t = 0.f;
-                if (gpq != 0.f && fabsf(gpq) > JACOBI_TOL * sqrtf(fabsf(gpp * gqq))) {
-                    float zeta = (gqq - gpp) / (2.f * gpq);
-                    t = copysignf(1.f, zeta) / (fabsf(zeta) + sqrtf(1.f + zeta * zeta));
-                    c = 1.f / sqrtf(1.f + t * t);
+                if (gpq * gpq > tol2 * fabsf(gpp * gqq) && gpq != 0.f) {
+                    // tan of the angle that zeroes G_pq: smaller root of t^2 + 2 zeta t - 1 = 0
+                    float zeta = __fdividef(gqq - gpp, 2.f * gpq);
+                    float z2 = fmaf(zeta, zeta, 1.f);
+                    t = copysignf(__fdividef(1.f, fabsf(zeta) + z2 * rsqrtf(z2)), zeta);
+                    if (fabsf(zeta) > 1e18f) t = __fdividef(0.5f, zeta);  // z2 overflows
+                    c = rsqrtf(fmaf(t, t, 1.f));
                     sn = t * c;
                     rot = 1;
                 }
-                s.pp[k] = p;
-                s.qq[k] = q;
-                s.cs[k] = c;
-                s.sn[k] = sn;
+                s.pair[k] = make_float4(__int_as_float(p), __int_as_float(q), c, sn);
                 s.tn[k] = t;
             }
             rotated_any |= __syncthreads_or(rot);
-            // Phase B: G <- J^T G J on every 2x2 block, V <- V J.
-            for (int bi = tid; bi < NP * NP; bi += FT_THREADS) {
-                int al = bi % NP, be = bi / NP;
-                int pa = s.pp[al], qa = s.qq[al], pb = s.pp[be], qb = s.qq[be];
-                float g00 = s.G[pa][pb], g01 = s.G[pa][qb], g10 = s.G[qa][pb], g11 = s.G[qa][qb];
+            // Phase B1: 2x2 blocks of the upper triangle of G
+#pragma unroll
+            for (int i = 0; i < BPT; ++i) {
+                const int al = my_al[i], be = my_be[i];
+                if (al < 0) continue;
+                const float4 A = s.pair[al];
+                const int pa = __float_as_int(A.x), qa = __float_as_int(A.y);
                 if (al == be) {
-                    float t = s.tn[al];
+                    const float t = s.tn[al];
                     if (t != 0.f) {
+                        const float g00 = s.G[pa][pa], g01 = s.G[pa][qa], g11 = s.G[qa][qa];
                         s.G[pa][pa] = g00 - t * g01;
                         s.G[qa][qa] = g11 + t * g01;
                         s.G[pa][qa] = 0.f;
-                        s.G[qa][pa] = 0.f;
                     }
-                } else {
-                    float ca = s.cs[al], sa = s.sn[al], cb = s.cs[be], sb = s.sn[be];
-                    float h00 = ca * g00 - sa * g10, h01 = ca * g01 - sa * g11;
-                    float h10 = sa * g00 + ca * g10, h11 = sa * g01 + ca * g11;
-                    s.G[pa][pb] = cb * h00 - sb * h01;
-                    s.G[pa][qb] = sb * h00 + cb * h01;
-                    s.G[qa][pb] = cb * h10 - sb * h11;
-                    s.G[qa][qb] = sb * h10 + cb * h11;
+                    continue;
                 }
+                const float4 B = s.pair[be];
+                if (A.w == 0.f && B.w == 0.f) continue;
+                const int pb = __float_as_int(B.x), qb = __float_as_int(B.y);
+                // element (x, y) of the symmetric matrix lives at G[min][max]
+                float *e00 = pa < pb ? &s.G[pa][pb] : &s.G[pb][pa];
+                float *e01 = pa < qb ? &s.G[pa][qb] : &s.G[qb][pa];
+                float *e10 = qa < pb ? &s.G[qa][pb] : &s.G[pb][qa];
+                float *e11 = qa < qb ? &s.G[qa][qb] : &s.G[qb][qa];
+                const float ca = A.z, sa = A.w, cb = B.z, sb = B.w;
+                const float g00 = *e00, g01 = *e01, g10 = *e10, g11 = *e11;
+                const float h00 = ca * g00 - sa * g10, h01 = ca * g01 - sa * g11;
+                const float h10 = sa * g00 + ca * g10, h11 = sa * g01 + ca * g11;
+                *e00 = cb * h00 - sb * h01;
+                *e01 = sb * h00 + cb * h01;
+                *e10 = cb * h10 - sb * h11;
+                *e11 = sb * h10 + cb * h11;
             }
-            for (int e = tid; e < P * NP; e += FT_THREADS) {
-                int i = e % P, k = e / P;
-                int p = s.pp[k], q = s.qq[k];
-                float c = s.cs[k], sn = s.sn[k];
-                float vp = s.V[i][p], vq = s.V[i][q];
-                s.V[i][p] = c * vp - sn * vq;
-                s.V[i][q] = sn * vp + c * vq;
+            // Phase B2: eigenvector rows p, q of each pair, four components at a time
+            for (int e = tid; e < NP * V4; e += NT) {
+                const int k = e / V4, c4 = e % V4;
+                const float4 A = s.pair[k];
+                if (A.w == 0.f) continue;
+                const int p = __float_as_int(A.x), q = __float_as_int(A.y);
+                float4 *vp = reinterpret_cast<float4 *>(&s.Vt[p][0]) + c4;
+                float4 *vq = reinterpret_cast<float4 *>(&s.Vt[q][0]) + c4;
+                const float4 a = *vp, b = *vq;
+                const float c = A.z, sn = A.w;
+                *vp = make_float4(c * a.x - sn * b.x, c * a.y - sn * b.y, c * a.z - sn * b.z, c * a.w - sn * b.w);
+                *vq = make_float4(sn * a.x + c * b.x, sn * a.y + c * b.y, sn * a.z + c * b.z, sn * a.w + c * b.w);
             }
             __syncthreads();
         }
@@ -226,21 +273,21 @@ __device__ __forceinline__ void store_elem(char *base, size_t idx, float v) {
     reinterpret_cast<TO *>(base)[idx] = Elem<TO>::from_f32(v);
 }
 
-template <typename T, int P, int D>
+template <typename T, int P, int D, int NT>
 __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, long job) {
     const int tid = threadIdx.x;
     const JobView v = job_view(fp, job);
-    load_page<T, P, D>(s, v);
+    load_page<T, P, D, NT>(s, v);
     __syncthreads();
-    if constexpr (sizeof(T) == 2) gram_bf16<P, D>(s); else gram_f32<P, D>(s);
+    if constexpr (sizeof(T) == 2) gram_bf16<P, D, NT>(s); else gram_f32<P, D, NT>(s);
     __syncthreads();
     // the tensor-core tiles of (i, j) and (j, i) may round differently: symmetrise
-    for (int e = tid; e < P * P; e += FT_THREADS) {
+    for (int e = tid; e < P * P; e += NT) {
         int i = e / P, j = e % P;
         if (j > i) s.G[j][i] = s.G[i][j];
     }
     __syncthreads();
-    int sweeps = jacobi<T, P, D>(s, fp.max_sweeps);
+    int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps);
     if (sweeps < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
     if (tid < P) s.lam[tid] = s.G[tid][tid];
     __syncthreads();
@@ -257,9 +304,9 @@ __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lo
     const int r = v.r;
     if (v.sigma && tid < P) v.sigma[tid] = sqrtf(fmaxf(s.lam[s.order[tid]], 0.f));
     __syncthreads();
-    for (int e = tid; e < P * P; e += FT_THREADS) {
+    for (int e = tid; e < P * P; e += NT) {
         int i = e / P, j = e % P;
-        s.G[i][j] = s.V[i][s.order[j]];
+        s.G[i][j] = s.Vt[s.order[j]][i];
     }
     __syncthreads();
     // Hundreds of rounds of fp32 rotations let the eigenvector norms drift by
@@ -271,7 +318,7 @@ __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lo
         s.lam[tid] = n2 > 0.f ? 1.f / sqrtf(n2) : 1.f;  // lam[] is free once order[] is set
     }
     __syncthreads();
-    for (int e = tid; e < P * v.r; e += FT_THREADS) {
+    for (int e = tid; e < P * v.r; e += NT) {
         int i = e / v.r, j = e % v.r;
         s.G[i][j] *= s.lam[j];
     }
@@ -281,7 +328,7 @@ __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lo
     const bool rec = v.rec != nullptr;
     const int rp = rec ? (v.kind == 0 ? y.rkp : y.rvp) : r;
     // L = Q_r  (record: keys LK[token][rank], values LVt[rank][token])
-    for (int e = tid; e < P * rp; e += FT_THREADS) {
+    for (int e = tid; e < P * rp; e += NT) {
         int i = e / rp, j = e % rp;
         float val = j < r ? s.G[i][j] : 0.f;
         if (rec) {
@@ -298,7 +345,7 @@ __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lo
     }
     // R = Q_r^T X in fp32: thread -> head-dim column k, a group of ranks
     constexpr int PITCH = D * (int)sizeof(T);
-    constexpr int GROUPS = FT_THREADS / D;
+    constexpr int GROUPS = NT / D;
     const int k = tid % D, grp = tid / D;
     for (int j0 = grp; j0 < rp; j0 += GROUPS * 8) {
         float acc[8];
@@ -331,28 +378,37 @@ __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lo
     }
 }
 
-template <typename T, int P, int D>
-__global__ void __launch_bounds__(FT_THREADS) factorize_kernel(const FactorParams fp) {
+template <typename T, int P, int D, int NT>
+__global__ void __launch_bounds__(NT) factorize_kernel(const FactorParams fp) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto &s = *reinterpret_cast<FactorSmem<T, P, D> *>(smem_raw);
     for (long job = blockIdx.x; job < fp.n_jobs; job += gridDim.x) {
-        factorize_one<T, P, D>(s, fp, job);
+        factorize_one<T, P, D, NT>(s, fp, job);
         __syncthreads();
     }
 }
 
-template <typename T, int P, int D>
+template <typename T, int P, int D, int NT>
 static cudaError_t launch_t(const FactorParams &fp, int num_sms, cudaStream_t st) {
     size_t smem = sizeof(FactorSmem<T, P, D>);
-    auto k = factorize_kernel<T, P, D>;
+    auto k = factorize_kernel<T, P, D, NT>;
     cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     long blocks = fp.n_jobs;
-    long cap = (long)num_sms * 16;
+    long cap = (long)num_sms * (NT >= 1024 ? 2 : 8);
     if (blocks > cap) blocks = cap;
     if (blocks < 1) return cudaSuccess;
-    k<<<(unsigned)blocks, FT_THREADS, smem, st>>>(fp);
+    k<<<(unsigned)blocks, NT, smem, st>>>(fp);
     return cudaGetLastError();
+}
+
+// A few pages (conversions during decoding) are latency-bound: 1024 threads
+// per page.  Many pages (prefill, batches) are throughput-bound: 256 threads,
+// several pages per SM.
+template <typename T, int P, int D>
+static cudaError_t launch_nt(const FactorParams &fp, int num_sms, cudaStream_t st) {
+    if (fp.n_jobs <= 2L * num_sms) return launch_t<T, P, D, 1024>(fp, num_sms, st);
+    return launch_t<T, P, D, 256>(fp, num_sms, st);
 }
 
 cudaError_t launch_factorize(const FactorParams &fp, int num_sms, cudaStream_t st) {
@@ -360,7 +416,7 @@ cudaError_t launch_factorize(const FactorParams &fp, int num_sms, cudaStream_t s
     const bool bf = fp.x_esz == 2;
 #define PKV_FACT_CASE(PP, DD)                                                                    \
     if (fp.P == PP && fp.d == DD)                                                                \
-        return bf ? launch_t<__nv_bfloat16, PP, DD>(fp, num_sms, st) : launch_t<float, PP, DD>(fp, num_sms, st);
+        return bf ? launch_nt<__nv_bfloat16, PP, DD>(fp, num_sms, st) : launch_nt<float, PP, DD>(fp, num_sms, st);
     PKV_FACT_CASE(16, 64)
     PKV_FACT_CASE(32, 64)
     PKV_FACT_CASE(64, 64)

@@ -7,7 +7,7 @@
 
 namespace pkv {
 
-enum { FACT_MODE_BATCH = 0, FACT_MODE_PREFILL = 1, FACT_MODE_CONVERT = 2 };
+enum { FACT_MODE_BATCH = 0, FACT_MODE_PREFILL = 1, FACT_MODE_CONVERT = 2, FACT_MODE_CONVERT_LIST = 3 };
 
 struct FactorParams {
     int mode;
@@ -29,6 +29,8 @@ struct FactorParams {
     // convert: one page per call entry of `layer`
     int layer, n_conv;
     int conv_seq[MAX_CALL_BATCH], conv_page[MAX_CALL_BATCH];
+    // convert list: device int2 {seq << 8 | layer, page} per page, 2 H jobs each
+    const int2 *conv_list;
 };
 
 struct DecodeParams {
@@ -41,7 +43,16 @@ struct DecodeParams {
     float *out;         // [B][Hq][d]
     int *status;
     int layer, chunk, nseq;
+    int stages;         // shared-memory ring depth (bf16 kernel)
     int seqs[MAX_CALL_BATCH];
+    int lens[MAX_CALL_BATCH];       // tokens attended per call entry (host mirror, after any append)
+    // fused append (decode step): the token at position lens - 1 comes from
+    // k_new / v_new ([B][H][d]); the kernel writes it into its dense page and
+    // updates the device page table (new page, page converted before launch)
+    const char *k_new, *v_new;
+    int append;
+    int conv_page[MAX_CALL_BATCH];  // page converted before this launch, or -1
+    int *lengths_out, *desc_out;    // device page table (written when append)
 };
 
 constexpr int MAX_DENSE_PAGES = 64;  // dense pages of one sequence (sink + window + filling)

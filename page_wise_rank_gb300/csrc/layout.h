@@ -15,7 +15,8 @@
 //                leaving the ring.
 //   page table   int32 lengths[seq][layer], then int32 desc[seq][layer][page]
 //                = kind << 30 | slot.
-//   workspace    int32 status words, int32 split tickets [seq][kv_head], then
+//   workspace    int32 status words, int32 split tickets [seq][kv_head], the
+//                batched-conversion job list (int2 per page), then
 //                fp32 split-K partial states [seq][q_head][split][4 + d]
 //                (m, l, two pad words, o[d]: 16-byte aligned rows).
 //
@@ -47,7 +48,7 @@ constexpr int32_t SLOT_MASK = (1 << KIND_SHIFT) - 1;
 constexpr int KIND_FACTORED = 0;
 constexpr int KIND_DENSE = 1;
 constexpr int MAX_SPLITS = 128;     // split-K partials per (seq, q head)
-constexpr int MAX_CHUNK_PAGES = 512; // pages per decode CTA
+constexpr int MAX_CHUNK_PAGES = 256; // pages per decode CTA
 constexpr int MAX_CALL_BATCH = 64;  // sequences per append / attention call
 constexpr int STATUS_WORDS = 16;    // int32 status words at the workspace start
 constexpr int STATUS_NOT_CONVERGED = 0;
@@ -91,6 +92,8 @@ struct Layout {
     size_t factor_pool_bytes, dense_pool_bytes, page_table_bytes, workspace_bytes;
     size_t desc_offset;       // byte offset of desc[] in the page table
     size_t ticket_offset;     // byte offset of the per-(seq, kv head) split tickets in the workspace
+    size_t jobs_offset;       // byte offset of the batched-conversion job list in the workspace
+    int max_conv_jobs;        // entries of that list: one per (seq, layer, page) awaiting conversion
     size_t partial_offset;    // byte offset of split partials in the workspace
     int part_stride;          // floats per partial row: m, l, 2 pad, o[d]
 
@@ -132,7 +135,9 @@ inline void make_layout(Layout &y, int L, int H, int Hq, int d, int P, int rk, i
     y.desc_offset = len_bytes;
     y.page_table_bytes = len_bytes + (((size_t)Bmax * L * y.n_pg_max * 4 + 255) & ~(size_t)255);
     y.ticket_offset = 256;
-    y.partial_offset = y.ticket_offset + (((size_t)Bmax * H * 4 + 255) & ~(size_t)255);
+    y.jobs_offset = y.ticket_offset + (((size_t)Bmax * H * 4 + 255) & ~(size_t)255);
+    y.max_conv_jobs = Bmax * L * (y.ring + 1);
+    y.partial_offset = y.jobs_offset + (((size_t)y.max_conv_jobs * 8 + 255) & ~(size_t)255);
     y.part_stride = d + 4;
     y.workspace_bytes = y.partial_offset + (size_t)Bmax * Hq * MAX_SPLITS * y.part_stride * 4;
 }

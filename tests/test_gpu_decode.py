@@ -221,3 +221,54 @@ def test_host_errors_leave_state_unchanged(pkv):
                                torch.empty(1, 8, 128, device="cuda"), [0])
     assert store.stats(0, 0)["length"] == 130
     check_page_table(store, cfg, 0, 0, 130)
+
+
+@pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
+def test_decode_step_fused_append(pkv, dtype):
+    """decode_step = append + (conversion) + attention in one call: its output
+    at every checked step matches the oracle over the grown cache, the page
+    table stays exact, a twin store driven by append_token + decode_attention
+    gives the same outputs, and so does a store whose completed pages are
+    factorized ahead of time by convert_ready_pages."""
+    d = 128 if dtype == torch.bfloat16 else 64
+    cfg = make_cfg(pkv, num_layers=2, num_kv_heads=2, num_q_heads=8, head_dim=d, max_tokens_per_seq=2000,
+                   kv_dtype=dtype)
+    a, b, c = pkv.Store(cfg), pkv.Store(cfg), pkv.Store(cfg)
+    host = HostCache()
+    spec = prefill(pkv, a, cfg, host, 0, 1000)
+    prefill(pkv, a, cfg, host, 3, 1061)
+    for seq, T in ((0, 1000), (3, 1061)):
+        K, V = synth.prefill_kv(spec, T, seq=seq)
+        b.factorize_pages(seq, K.cuda(), V.cuda())
+        c.factorize_pages(seq, K.cuda(), V.cuda())
+    seqs = [3, 0]
+    cache = {}
+    G = cfg.num_q_heads // cfg.num_kv_heads
+    for step in range(150):
+        for l in range(cfg.num_layers):
+            pos = [len(torch.cat(host.k[(s, l, 0)])) for s in seqs]
+            k, v = synth.decode_tokens(spec, l, seqs, pos, cache=cache)
+            q = synth.queries(2, cfg.num_q_heads, d, step=200 + step, layer=l, dtype=dtype)
+            out_a = torch.empty(2, cfg.num_q_heads, d, device="cuda")
+            out_b = torch.empty_like(out_a)
+            out_c = torch.empty_like(out_a)
+            a.decode_step(l, q.cuda(), k.cuda(), v.cuda(), out_a, seqs)
+            b.append_token(l, k.cuda(), v.cuda(), seqs)
+            b.decode_attention(l, q.cuda(), out_b, seqs)
+            c.decode_step(l, q.cuda(), k.cuda(), v.cuda(), out_c, seqs)
+            for i, s in enumerate(seqs):
+                host.append(s, l, k[i], v[i])
+            assert torch.equal(out_a, out_b), (step, l)
+            assert torch.equal(out_a, out_c), (step, l)
+            if step in (0, 36, 37, 149) and l == 1:
+                got = out_a.cpu().double().numpy()
+                for i, s in enumerate(seqs):
+                    for h in range(cfg.num_kv_heads):
+                        ref = oracle_decode_on_store(a, cfg, host, s, l, h, q[i, h * G:(h + 1) * G].double().numpy())
+                        assert rel_err_rows(got[i, h * G:(h + 1) * G], ref) <= TOL[dtype]
+        c.convert_ready_pages()  # factorize completed pages ahead of their leaving the window
+    assert a.check_device_status() == 0 and c.check_device_status() == 0
+    for s, T0 in ((0, 1000), (3, 1061)):
+        for l in range(cfg.num_layers):
+            check_page_table(a, cfg, s, l, T0 + 150)
+            check_page_table(c, cfg, s, l, T0 + 150)
