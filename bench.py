@@ -64,6 +64,11 @@ def measured_peak_hbm():
         return 6800.0, "fallback"
 
 
+# the sources the bf16 decode kernel is built from (a recorded ncu traffic
+# figure is reported only while they are unchanged)
+DECODE_SOURCES = ("decode_impl.cuh", "decode_bf16_p64.cu", "common.cuh", "layout.h", "kernels.h")
+
+
 def source_hash(names):
     h = hashlib.sha256()
     for n in names:
@@ -183,7 +188,7 @@ def gpu_arm(args, rank, world, local):
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
     L, H, Hq, d, P, B, T0 = wl["layers"], wl["H"], wl["Hq"], wl["d"], wl["P"], wl["B"], wl["T"]
-    n_steps_total = args.warmup + args.steps * (1 if args.no_e2e else 2)
+    n_steps_total = args.warmup + args.steps * (1 if args.no_e2e else 2) + min(args.steps, 8)
     cfg = pkv.StoreConfig(num_layers=L, num_kv_heads=H, num_q_heads=Hq, head_dim=d, page_size=P, rank_k=wl["rk"],
                           rank_v=wl["rv"], sink_tokens=wl["sink"], recent_tokens=wl["W"], max_batch=B,
                           max_tokens_per_seq=T0 + n_steps_total + 8, kv_dtype=torch.bfloat16)
@@ -270,11 +275,19 @@ def gpu_arm(args, rank, world, local):
         stream.synchronize()
         launches[0] = 0
         s0, s1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        # a GPU-side sleep ahead of the start event lets the host queue work
+        # before the clock starts, so host launch latency is not timed as GPU time
+        # (if enqueueing is slower than the GPU, the queue drains and it shows)
+        torch.cuda._sleep(20_000_000)
         s0.record(stream)
         conv_steps = []
+        step_ev = [s0]
         for i in range(args.steps):
             t_lens.append(store_len[0] + 1)
-            conv_steps.append(step(args.warmup + i, ev=evs[i]))
+            conv_steps.append(step(args.warmup + i))
+            e = torch.cuda.Event(enable_timing=True)
+            e.record(stream)
+            step_ev.append(e)
         s1.record(stream)
         stream.synchronize()
         barrier(world)
@@ -284,10 +297,22 @@ def gpu_arm(args, rank, world, local):
         st = store.check_device_status(stream)
         if st != 0:
             raise RuntimeError(f"device status {st}: {pkv.last_error()}")
-        # every decode_step launch (page conversions run in the separate batched call)
-        dec_ms = [evs[i][l][0].elapsed_time(evs[i][l][1]) for i in range(args.steps) for l in range(L)]
-        dec_bytes = [alg_bytes(wl, t_lens[i]) for i in range(args.steps) for l in range(L)]
-        conv_ms = [evs[i][L][0].elapsed_time(evs[i][L][1]) for i in range(args.steps) if conv_steps[i]]
+        # decode-attention time per layer in the timed region: steps without a
+        # batched page conversion are L back-to-back decode_step launches
+        step_ms = [step_ev[i].elapsed_time(step_ev[i + 1]) for i in range(args.steps)]
+        plain = [i for i in range(args.steps) if not conv_steps[i]] or list(range(args.steps))
+        dec_ms = [step_ms[i] / L for i in plain]
+        dec_bytes = [alg_bytes(wl, t_lens[i]) for i in plain]
+        conv_ms = [step_ms[i] - statistics.mean(step_ms[j] for j in plain) for i in range(args.steps) if conv_steps[i]]
+        # the same launches one at a time (an event pair around each call stops
+        # consecutive launches from overlapping), queued behind a GPU-side sleep
+        n_prof = min(args.steps, 8)
+        iso_ms = []
+        for i in range(n_prof):
+            torch.cuda._sleep(4_000_000)
+            step(args.warmup + args.steps + i, ev=evs[i])
+            stream.synchronize()
+            iso_ms += [evs[i][l][0].elapsed_time(evs[i][l][1]) for l in range(L)]
         # ---- e2e: same steps through the public API with pinned host buffers
         e2e = None
         if not args.no_e2e:
@@ -299,12 +324,13 @@ def gpu_arm(args, rank, world, local):
             stream.synchronize()
             barrier(world)
             x0, x1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(20_000_000)
             x0.record(stream)
             for i in range(args.steps):
                 dq.copy_(hq[i], non_blocking=True)
                 dk.copy_(hk[i], non_blocking=True)
                 dv.copy_(hv[i], non_blocking=True)
-                step(args.warmup + args.steps + i, q_src=dq, k_src=dk, v_src=dv, out_dst=hout[i])
+                step(args.warmup + args.steps + n_prof + i, q_src=dq, k_src=dk, v_src=dv, out_dst=hout[i])
             x1.record(stream)
             stream.synchronize()
             e2e_ms = barrier_max(x0.elapsed_time(x1), world)
@@ -315,7 +341,7 @@ def gpu_arm(args, rank, world, local):
     dec_us = 1000.0 * sum(dec_ms) / len(dec_ms)
     achieved = sum(dec_bytes) / (sum(dec_ms) * 1e-3) / 1e9
     peak, peak_kind = measured_peak_hbm()
-    src_hash = source_hash(["decode.cu", "common.cuh", "layout.h"])
+    src_hash = source_hash(DECODE_SOURCES)
     traffic = recorded_traffic(f"decode_bf16:{args.workload}", src_hash)
     pages_per_s = n_fact_pages / (prefill_ms * 1e-3)
     result = {
@@ -335,12 +361,13 @@ def gpu_arm(args, rank, world, local):
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "l2": f"inputs larger than L2: {alg_bytes(wl, T0) * L / 1e9:.2f} GB read per step"},
         "decode_attention_us_per_layer": round(dec_us, 3),
+        "decode_step_us_per_layer_isolated": round(1000.0 * statistics.mean(iso_ms), 3),
         "batched_conversion_us": round(1000.0 * statistics.mean(conv_ms), 1) if conv_ms else None,
         "pages_factorized_per_s": round(pages_per_s, 1),
         "prefill_factorization": {"pages": n_fact_pages, "ms": round(prefill_ms, 3)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "kernel": "decode_bf16_kernel (one decode_step call: append + attention + split merge)",
+                     "kernel": "decode_bf16_kernel: one decode_step launch per layer (append + attention + split merge), mean over the timed steps without a page conversion",
                      "traffic": (traffic["bytes_per_launch"] if traffic else None),
                      "algorithmic_bytes_per_launch": int(statistics.mean(dec_bytes))},
         "e2e": e2e,

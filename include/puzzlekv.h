@@ -209,15 +209,15 @@ puzzlekv_status puzzlekv_decode_step(puzzlekv_store *store, int32_t layer, const
  *     from a 16 MiB array compiled into the library, one per GPU that loads
  *     it, kept until the process exits; the store's workspace is not used
  *     for it.  Nothing is allocated by this call.
- *   - Stores needing more than 16 MiB of scratch (4 bytes x (max_batch x
- *     num_kv_heads, rounded up to 64) + 4 bytes x max_batch x num_q_heads x
- *     128 x (head_dim + 4)) are rejected with PUZZLEKV_ERR_CAPACITY before
- *     anything is launched.
+ *   - Stores needing more than 16 MiB of scratch (8 bytes x max_batch x
+ *     num_kv_heads rounded up to 256 bytes, + 4 bytes x max_batch x
+ *     num_q_heads x 128 x (head_dim + 4)) are rejected with
+ *     PUZZLEKV_ERR_CAPACITY before anything is launched.
  *   - The first call on a device looks up the array's device address
  *     (cudaGetSymbolAddress) with that device current; make that first call
  *     before any stream capture begins.
- *   - Every call shares the one array and clears its split tickets on
- *     `stream` before launching; calls whose kernels overlap on the GPU
+ *   - Every call shares the one array and clears its counters on `stream`
+ *     before launching; calls whose kernels overlap on the GPU
  *     (other streams, other threads) race on it and must be serialised by
  *     the caller.
  */

@@ -61,9 +61,17 @@ def _need(t: torch.Tensor, shape, dtype, name: str) -> None:
         raise ValueError(f"{name}: expected contiguous {dtype} {tuple(shape)}, got {t.dtype} {tuple(t.shape)}")
 
 
+_SEQ_CACHE: dict = {}
+
+
 def _seq_ids(seq_ids: Sequence[int]):
-    arr = (ctypes.c_int32 * len(seq_ids))(*[int(s) for s in seq_ids])
-    return arr, len(seq_ids)
+    key = tuple(int(s) for s in seq_ids)
+    arr = _SEQ_CACHE.get(key)
+    if arr is None:
+        if len(_SEQ_CACHE) > 4096:
+            _SEQ_CACHE.clear()
+        arr = _SEQ_CACHE[key] = (ctypes.c_int32 * len(key))(*key)
+    return arr, len(key)
 
 
 def query_sizes(cfg: StoreConfig) -> dict:

@@ -98,6 +98,7 @@ struct puzzlekv_store {
     std::vector<int> len;    // host mirror [seq][layer]; -1 = empty slot
     std::vector<int> conv_upto;  // [seq][layer]: pages below this index (past the sink) have factor records
     std::vector<int2> job_host;  // staging of the batched-conversion job list
+    bool after_decode = false;   // the store's latest launch was a decode launch
     int num_sms;
 };
 
@@ -205,6 +206,7 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const v
         }
     }
     cudaError_t e = launch_seq_init(ip, strm);
+    s->after_decode = false;
     if (e != cudaSuccess) return cuda_fail(e, "seq_init launch");
     if (f_lo >= 0) {
         FactorParams fp{};
@@ -224,6 +226,7 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const v
         fp.p_hi = f_hi;
         fp.n_jobs = (long)y.L * y.H * 2 * (f_hi - f_lo);
         e = launch_factorize(fp, s->num_sms, strm);
+        s->after_decode = false;
         if (e != cudaSuccess) return cuda_fail(e, "factorize launch");
     }
     for (int l = 0; l < y.L; ++l) {
@@ -288,6 +291,7 @@ static void fill_decode_params(puzzlekv_store *s, int32_t layer, const void *q, 
     dp.q = static_cast<const char *>(q);
     dp.partials = reinterpret_cast<float *>(s->workspace + y.partial_offset);
     dp.tickets = reinterpret_cast<int *>(s->workspace + y.ticket_offset);
+    dp.wait_first = s->after_decode ? 0 : 1;
     dp.out = out;
     dp.status = reinterpret_cast<int *>(s->workspace);
     dp.layer = layer;
@@ -360,6 +364,7 @@ puzzlekv_status puzzlekv_append_token(puzzlekv_store *s, int32_t layer, const vo
     }
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     cudaError_t e = launch_append(ap, strm);
+    s->after_decode = false;
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
     if (fp.n_conv > 0) {
         fp.mode = FACT_MODE_CONVERT;
@@ -374,6 +379,7 @@ puzzlekv_status puzzlekv_append_token(puzzlekv_store *s, int32_t layer, const vo
         fp.layer = layer;
         fp.n_jobs = (long)fp.n_conv * y.H * 2;
         e = launch_factorize(fp, s->num_sms, strm);
+        s->after_decode = false;
         if (e != cudaSuccess) return cuda_fail(e, "conversion launch");
     }
     for (int i = 0; i < B; ++i) s->len[(size_t)seq_ids[i] * y.L + layer] += 1;
@@ -392,6 +398,7 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *s, int32_t layer, cons
     fill_decode_params(s, layer, q, out, seq_ids, B, 0, dp, total, max_pages);
     cudaError_t e = launch_decode(dp, total, max_pages, s->num_sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
+    s->after_decode = true;
     return PUZZLEKV_OK;
 }
 
@@ -445,10 +452,13 @@ puzzlekv_status puzzlekv_decode_step(puzzlekv_store *s, int32_t layer, const voi
         fp.layer = layer;
         fp.n_jobs = (long)fp.n_conv * y.H * 2;
         e = launch_factorize(fp, s->num_sms, strm);
+        s->after_decode = false;
         if (e != cudaSuccess) return cuda_fail(e, "conversion launch");
     }
+    if (fp.n_conv > 0) dp.wait_first = 1;
     e = launch_decode(dp, total, max_pages, s->num_sms, strm);
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
+    s->after_decode = true;
     for (int i = 0; i < B; ++i) s->len[(size_t)seq_ids[i] * y.L + layer] += 1;
     return PUZZLEKV_OK;
 }
@@ -491,6 +501,7 @@ puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
     fp.conv_list = dev_jobs;
     fp.n_jobs = (long)s->job_host.size() * y.H * 2;
     e = launch_factorize(fp, s->num_sms, strm);
+    s->after_decode = false;
     if (e != cudaSuccess) return cuda_fail(e, "batched conversion launch");
     return PUZZLEKV_OK;
 }
@@ -529,7 +540,7 @@ puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *s, void *stream) {
     if (e == cudaSuccess) e = cudaMemcpy(words, status_ptr(s), sizeof(words), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemset(status_ptr(s), 0, sizeof(words));
     if (e == cudaSuccess && words[STATUS_TIMEOUT])  // a CTA that gave up never took its split ticket
-        e = cudaMemset(s->workspace + s->y.ticket_offset, 0, (size_t)s->y.Bmax * s->y.H * 4);
+        e = cudaMemset(s->workspace + s->y.ticket_offset, 0, s->y.jobs_offset - s->y.ticket_offset);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     if (words[STATUS_TIMEOUT]) return fail(PUZZLEKV_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out");
     if (words[STATUS_NOT_CONVERGED])
@@ -572,7 +583,8 @@ extern "C" puzzlekv_status puzzlekv_decode_attention_static_scratch(puzzlekv_sto
     if (!q || !out || !aligned16(q) || !aligned16(out))
         return fail(PUZZLEKV_ERR_INVALID_ARG, "q and out must be non-NULL and 16-byte aligned");
     const Layout &y = s->y;
-    const size_t ticket_bytes = ((size_t)y.Bmax * y.H * 4 + 255) & ~(size_t)255;
+    // split tickets, then the partial states
+    const size_t ticket_bytes = ((size_t)y.Bmax * y.H * 8 + 255) & ~(size_t)255;
     const size_t need = ticket_bytes + (size_t)y.Bmax * y.Hq * MAX_SPLITS * y.part_stride * 4;
     if (need > kStaticScratchBytes)
         return fail(PUZZLEKV_ERR_CAPACITY,
@@ -602,8 +614,10 @@ extern "C" puzzlekv_status puzzlekv_decode_attention_static_scratch(puzzlekv_sto
     int max_pages;
     fill_decode_params(s, layer, q, out, seq_ids, B, 0, dp, total, max_pages);
     dp.tickets = static_cast<int *>(base);
+    dp.wait_first = 1;
     dp.partials = reinterpret_cast<float *>(static_cast<char *>(base) + ticket_bytes);
     e = launch_decode(dp, total, max_pages, s->num_sms, strm);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch (static scratch)");
+    s->after_decode = true;
     return PUZZLEKV_OK;
 }

@@ -46,14 +46,28 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, uint32_t parity) {
     return ok != 0;
 }
 
-// Wait for phase `parity` of `bar` to complete, giving up after a bounded
-// number of polls (each try_wait itself suspends for a short while).  On
-// give-up the device status word records a timeout and false is returned.
-constexpr uint32_t WAIT_LIMIT = 1u << 22;
+// Nanoseconds of the GPU's global timer.
+__device__ __forceinline__ uint64_t global_ns() {
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Longest time any spin-wait of the library waits before it gives up.
+constexpr uint64_t WAIT_NS = 1000000000ull;
+
+// Wait for phase `parity` of `bar` to complete, giving up after WAIT_NS of
+// polling (each try_wait itself suspends for a short while).  On give-up the
+// device status word records a timeout and false is returned.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status) {
-    for (uint32_t i = 0; i < WAIT_LIMIT; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_ns();
+    for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
-        if (i > 64) __nanosleep(64);
+        if (i >= 64) {
+            __nanosleep(64);
+            if ((i & 63) == 0 && global_ns() - t0 > WAIT_NS) break;
+        }
     }
     if (status) atomicOr(status + STATUS_TIMEOUT, 1);
     return false;
@@ -69,6 +83,44 @@ __device__ __forceinline__ void bulk_g2s(void *dst_smem, const void *src_gmem, u
         "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar))
         : "memory");
 }
+
+// Same copy with an L2 eviction-priority policy (see l2_evict_first).
+__device__ __forceinline__ void bulk_g2s_hint(void *dst_smem, const void *src_gmem, uint32_t bytes, uint64_t *bar,
+                                              uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;" ::"r"(
+            smem_u32(dst_smem)),
+        "l"(src_gmem), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// L2 policy for bytes read exactly once: first in line for eviction.
+__device__ __forceinline__ uint64_t l2_evict_first() {
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+// Ask L2 to fetch `bytes` (multiple of 16) at a 16-byte aligned global
+// address; no completion is tracked and nothing is written to the SM.
+__device__ __forceinline__ void prefetch_l2(const void *src_gmem, uint32_t bytes) {
+    asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(src_gmem), "r"(bytes) : "memory");
+}
+
+// Order this thread's earlier generic-proxy accesses to global memory
+// before its later async-proxy (bulk copy) accesses.
+__device__ __forceinline__ void fence_proxy_async_global() {
+    asm volatile("fence.proxy.async.global;" ::: "memory");
+}
+
+// Order this thread's earlier generic-proxy accesses to shared memory before
+// its later async-proxy (bulk copy) writes there.
+__device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
+
+// Programmatic dependent launch: wait until the preceding grid in the stream
+// has completed and its memory is visible / let the next grid start early.
+__device__ __forceinline__ void grid_dependency_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void grid_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 // ---------------------------------------------------------------- tensor-core fragments
 

@@ -25,7 +25,7 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
     constexpr int DPL = D / 32;         // head dims per lane
     const float scale = rsqrtf((float)D);
     __shared__ float comb[NWC][8][D + 2];
-    __shared__ float scratch[3 * MAX_SPLITS * 8 + 16];
+    __shared__ float scratch[MAX_SPLITS * 8 + 8];
     __shared__ int last;
 
     float q[8][DPL];  // this lane's head dims of each query row
@@ -166,8 +166,12 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
 template <int P, int D>
 static cudaError_t launch_f32(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     auto k = decode_f32_kernel<P, D>;
-    int occ = 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, NWC * 32, 0) != cudaSuccess || occ < 1) occ = 1;
+    static int occ = 0;  // computed once (the kernel uses static shared memory only)
+    if (occ == 0) {
+        int o = 1;
+        if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, k, NWC * 32, 0) != cudaSuccess || o < 1) o = 1;
+        occ = o;
+    }
     int splits = 1;
     choose_chunk(p, total_pages, max_pages, num_sms * occ, splits);
     dim3 grid((unsigned)splits, (unsigned)p.y.H, (unsigned)p.nseq);

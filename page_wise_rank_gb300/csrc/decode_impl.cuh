@@ -9,12 +9,13 @@
 //
 // One CTA handles one (sequence, KV head, page range).  Its pages are cut
 // into units -- a factorized page, or half of a dense page (keys and values of
-// P/2 tokens) -- each of which fits one shared-memory stage.  A producer warp
-// streams units through an NS-stage ring with one or two bulk copies per unit
-// (mbarrier transaction counts); NWC consumer warps each take every NWC-th
-// unit and keep their own running (m, l, o) for the G query heads of the KV
-// head.  At the end the warps' states are merged in shared memory and the
-// CTA's state goes to the workspace; a second kernel merges the splits.
+// P/2 tokens) -- each of which fits one shared-memory slot.  The CTA's warps
+// take its units round-robin and stream them through private slots with one
+// or two bulk copies per unit (mbarrier transaction counts), each keeping its
+// own running (m, l, o) for the G query heads of the KV head.  At the end the
+// warps' states are merged in shared memory, every CTA's state goes to the
+// workspace, and the last CTA of the (sequence, KV head) to finish merges the
+// splits and writes the output.
 //
 // bf16 storage: the four contractions of eq. (4) run on tensor cores
 // (mma.sync m16n8k16 / m16n8k8, fp32 accumulate).  The G <= 8 query heads fill
@@ -26,13 +27,18 @@
 #pragma once
 #include <math.h>
 
+#include <algorithm>
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace pkv {
 
 constexpr int NWC = 4;            // consumer warps of the fp32 kernel
-constexpr int NWC_BF16 = 8;       // consumer warps of the bf16 kernel
+constexpr int NWC_BF16 = 4;       // warps of the bf16 kernel
+constexpr int SLOTS_PER_WARP = 2; // shared-memory slots each warp streams its units through
+constexpr int CTAS_PER_SM = 1;    // resident bf16 decode CTAs per SM
 constexpr int NS_MAX = 16;        // shared-memory stages (bf16 kernel), chosen at launch
 constexpr int MAX_CHUNK = MAX_CHUNK_PAGES;
 constexpr float LOG2E = 1.4426950408889634f;
@@ -45,189 +51,170 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
+// One shared-memory slot: a factor record or half a dense page (K and V rows).
+template <int P, int D>
+__host__ __device__ inline size_t decode_stage_bytes(const Layout &y) {
+    return ((y.rec_bytes > (size_t)P * D * 2 ? y.rec_bytes : (size_t)P * D * 2) + 127) & ~(size_t)127;
+}
+
 struct DecodeShared {
-    int desc[MAX_CHUNK];
-    int cnt[MAX_CHUNK];
-    int off[MAX_CHUNK];
-    int unit[2 * MAX_CHUNK];
-    int n_units;
-    int issued;
+    uint64_t merge_bar;  // completion of the split-merge bulk copies
     int failed;
     int last;
+    int unit_info[NS_MAX];
 };
 
-__device__ __forceinline__ int dense_half_valid(int T, int p, int P, int half) {
-    int first = p * P + half * (P / 2);
-    int v = T - first;
-    return v < 0 ? 0 : (v > P / 2 ? P / 2 : v);
-}
 
-// Build the CTA's unit list: per page 1 unit (factorized) or one per non-empty
-// dense half.  Page kinds follow page_kind() at the call's length, the rule
-// the store's page table records (the host mirror passes the length, so no
-// global load precedes the first bulk copy); a factorized page's record is
-// its own preallocated slot, a dense page sits in dense_slot(page).
-// Returns the page count of the CTA (0: nothing to do).
-__device__ inline int build_units(DecodeShared &sh, const DecodeParams &prm, int b_idx, int split, int &T_out) {
-    const Layout &y = prm.y;
-    const int p0 = split * prm.chunk;
-    const int T = prm.lens[b_idx];
-    T_out = T;
-    const int n_pages = (T + y.P - 1) / y.P;
-    if (p0 >= n_pages) return 0;
-    const int np = min(prm.chunk, n_pages - p0);
-    for (int i = threadIdx.x; i < np; i += blockDim.x) {
-        const int p = p0 + i;
-        const int kind = page_kind(p, T, y.P, y.sink_tokens, y.W);
-        sh.desc[i] = (kind << KIND_SHIFT) | (kind == KIND_FACTORED ? p : y.dense_slot(p));
-        sh.cnt[i] = kind == KIND_FACTORED
-                        ? 1
-                        : (dense_half_valid(T, p0 + i, y.P, 0) > 0) + (dense_half_valid(T, p0 + i, y.P, 1) > 0);
-    }
-    __syncthreads();
-    if (threadIdx.x < 32) {  // warp 0: exclusive scan over pages, lane-contiguous segments
-        int lane = threadIdx.x;
-        int seg = (np + 31) / 32;
-        int lo = lane * seg, hi = min(lo + seg, np);
-        int sum = 0;
-        for (int i = lo; i < hi; ++i) sum += sh.cnt[i];
-        int incl = sum;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            int v = __shfl_up_sync(0xffffffffu, incl, o);
-            if (lane >= o) incl += v;
+// Walk over the units of a page range [p, pe): one per factorized page, one
+// per non-empty half of a dense page.  The range is cut into three segments
+// by the classification rule -- dense sink pages, factorized pages [a1, a2)
+// (their records are contiguous in the factor pool), dense window pages --
+// so a step costs a few integer operations.  Page kinds follow page_kind()
+// at the call's length (the host mirror passes it, so nothing is read from
+// global memory before the first bulk copy).
+struct UnitCursor {
+    int p, half, a1, a2, pe, T;
+    template <int P>
+    __device__ __forceinline__ bool next(int &pg, int &hf, bool &dense) {
+        while (p < pe) {
+            if (p >= a1 && p < a2) {
+                pg = p++;
+                hf = 0;
+                dense = false;
+                return true;
+            }
+            const int pp = p, hh = half;
+            if (half == 0) {
+                half = 1;
+            } else {
+                half = 0;
+                ++p;
+            }
+            if (T > pp * P + hh * (P / 2)) {
+                pg = pp;
+                hf = hh;
+                dense = true;
+                return true;
+            }
         }
-        int run = incl - sum;
-        for (int i = lo; i < hi; ++i) {
-            sh.off[i] = run;
-            run += sh.cnt[i];
-        }
-        if (lane == 31) sh.n_units = incl;
+        return false;
     }
-    __syncthreads();
-    for (int i = threadIdx.x; i < np; i += blockDim.x) {
-        int o = sh.off[i];
-        int kind = sh.desc[i] >> KIND_SHIFT;
-        if (kind == KIND_FACTORED) {
-            sh.unit[o] = i << 1;
-        } else {
-            int k = 0;
-            for (int half = 0; half < 2; ++half)
-                if (dense_half_valid(T, p0 + i, y.P, half) > 0) sh.unit[o + k++] = (i << 1) | half;
-        }
-    }
-    __syncthreads();
-    return np;
-}
+};
 
-// Write this CTA's state for the G query heads of (b, h) -- the NWC warp
-// states in `comb` ([warp][g][m, l, o...], D + 2 floats per row) merged by
-// eq. (5) -- to the workspace; then, if this CTA is the last of the `ns`
-// CTAs of (b, h) to get there (atomic ticket, no waiting), merge all ns
-// partial states into `out` and reset the ticket for the next launch.
-// `scratch` holds 3 * MAX_SPLITS * 8 + 16 floats of shared memory; `stage_buf`
-// (optional, `stage_cap` bytes) receives the partial rows for the merge.
+// Split hand-off, eq. (5).  `comb` holds the NW warp states of this CTA
+// ([warp][g][m, l, o...], D + 2 floats per row, m in log2 units); they are
+// merged into the CTA's state, which every CTA writes to the workspace and
+// makes visible before it takes its arrival
+// ticket for (b, h).  The CTA that takes the last ticket therefore sees every
+// state: it merges them in split order (the same sums whichever CTA that is)
+// and writes `out`, then resets the ticket.  `scratch` holds MAX_SPLITS * 8
+// + 8 floats.  With `merge_bar` (an mbarrier of count 1 in its first phase)
+// and room in `stage_buf` (16-byte aligned shared memory, `stage_cap` bytes,
+// may overlap `comb`), the states arrive by one bulk copy per query head;
+// otherwise they are read from global memory.
 template <int D, int NW>
-__device__ void finish_split(const DecodeParams &prm, const float *comb, int b_idx, int b, int h, int split, int ns,
-                             float *scratch, int *last, float *stage_buf = nullptr, size_t stage_cap = 0) {
+__device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_idx, int b, int h, int split, int ns,
+                             float *scratch, int *last, float *stage_buf = nullptr,
+                             size_t stage_cap = 0, uint64_t *merge_bar = nullptr) {
     const Layout &y = prm.y;
     const int G = y.G, S = y.part_stride;
+    int *arrivals = prm.tickets + y.ticket_index(b, h);
     for (int e = threadIdx.x; e < G * (D + 2); e += blockDim.x) {
-        int gg = e / (D + 2), k = e % (D + 2);
-        float M = -INFINITY;
-        for (int w = 0; w < NW; ++w) M = fmaxf(M, comb[(w * 8 + gg) * (D + 2)]);
+        const int gg = e / (D + 2), k = e % (D + 2);
+        float mw[NW], M = -INFINITY;
+#pragma unroll
+        for (int w = 0; w < NW; ++w) {
+            mw[w] = comb[(w * 8 + gg) * (D + 2)];
+            M = fmaxf(M, mw[w]);
+        }
         float acc = 0.f;
         if (k == 0) {
             acc = M;
         } else {
-            for (int w = 0; w < NW; ++w) {
-                float mw = comb[(w * 8 + gg) * (D + 2)];
-                acc += (mw == -INFINITY ? 0.f : exp2f(mw - M)) * comb[(w * 8 + gg) * (D + 2) + k];
-            }
+#pragma unroll
+            for (int w = 0; w < NW; ++w)
+                acc += (mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M)) * comb[(w * 8 + gg) * (D + 2) + k];
         }
         prm.partials[y.partial_index(b, h * G + gg, split) * S + (k < 2 ? k : k + 2)] = acc;
     }
+    // rows of head g are contiguous: partial_index(b, h G + g, 0 .. ns-1)
+    const bool staged = merge_bar != nullptr && stage_buf != nullptr && (size_t)G * ns * S * 4 <= stage_cap;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();
-        int old = atomicAdd(prm.tickets + y.ticket_index(b, h), 1);
-        *last = (old == ns - 1);
+        __threadfence();  // this CTA's state is visible before its ticket
+        const bool is_last = atomicAdd(arrivals, 1) == ns - 1;
+        *last = is_last;
+        if (is_last) {
+            __threadfence();
+            if (staged) {  // the states were written through the generic proxy
+                fence_proxy_async_global();
+                fence_proxy_async_shared();  // the warp states in stage_buf have been read
+                const uint32_t bytes = (uint32_t)ns * S * 4;
+                mbar_arrive_expect_tx(merge_bar, (uint32_t)G * bytes);
+                for (int g = 0; g < G; ++g)
+                    bulk_g2s(stage_buf + (size_t)g * ns * S, prm.partials + y.partial_index(b, h * G + g, 0) * S,
+                             bytes, merge_bar);
+            }
+        }
     }
     __syncthreads();
-    if (!*last) return;
-    __threadfence();
-    float *sm = scratch, *sl = scratch + MAX_SPLITS * 8, *wt = sl + MAX_SPLITS * 8, *Mg = wt + MAX_SPLITS * 8;
-    float *iL = Mg + 8;
-    // all partial rows of the G heads, staged in shared memory when they fit:
-    // every load is issued before any is used (one round trip instead of ns)
-    const int rows = ns * G, row4 = S / 4;
-    const bool staged = stage_buf != nullptr && (size_t)rows * S * 4 <= stage_cap;
-    if (staged) {
-        float4 *dst = reinterpret_cast<float4 *>(stage_buf);
-        const int total = rows * row4;
-        for (int base = threadIdx.x; base < total; base += blockDim.x * 12) {
-            float4 v[12];
-#pragma unroll
-            for (int k = 0; k < 12; ++k) {
-                int e = base + k * blockDim.x;
-                if (e < total) {
-                    int r = e / row4, c = e % row4, sp = r / G, g = r % G;
-                    v[k] = __ldcg(reinterpret_cast<const float4 *>(prm.partials +
-                                                                   y.partial_index(b, h * G + g, sp) * S) + c);
-                }
-            }
-#pragma unroll
-            for (int k = 0; k < 12; ++k) {
-                int e = base + k * blockDim.x;
-                if (e < total) dst[e] = v[k];
-            }
+    if (!*last) return false;
+    float *wt = scratch;  // weights [g][split]
+    auto merge = [&](auto ld1, auto ld4) {
+        // weight of split sp for head g: 2^(m_sp - M_g), M_g the max over the splits
+        for (int t = threadIdx.x; t < G * ns; t += blockDim.x) {
+            const int g = t / ns, sp = t - g * ns;
+            float M = -INFINITY;
+            for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, ld1(g, s2, 0));
+            const float m = ld1(g, sp, 0);
+            wt[g * MAX_SPLITS + sp] = m == -INFINITY ? 0.f : ex2_approx(m - M);
         }
         __syncthreads();
-    }
-    auto row_ptr = [&](int sp, int g) -> const float * {
-        return staged ? stage_buf + ((size_t)sp * G + g) * S : prm.partials + y.partial_index(b, h * G + g, sp) * S;
-    };
-    for (int e = threadIdx.x; e < ns * G; e += blockDim.x) {
-        int sp = e / G, g = e % G;
-        const float *row = row_ptr(sp, g);
-        sm[sp * 8 + g] = staged ? row[0] : __ldcg(row);
-        sl[sp * 8 + g] = staged ? row[1] : __ldcg(row + 1);
-    }
-    __syncthreads();
-    if (threadIdx.x < G) {
-        int g = threadIdx.x;
-        float M = -INFINITY, L = 0.f;
-        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, sm[sp * 8 + g]);
-        for (int sp = 0; sp < ns; ++sp) {
-            float m = sm[sp * 8 + g];
-            L += (m == -INFINITY ? 0.f : exp2f(m - M)) * sl[sp * 8 + g];
-        }
-        Mg[g] = M;
-        iL[g] = 1.f / L;
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < ns * G; e += blockDim.x) {
-        int sp = e / G, g = e % G;
-        float m = sm[sp * 8 + g];
-        wt[sp * 8 + g] = (m == -INFINITY ? 0.f : exp2f(m - Mg[g])) * iL[g];
-    }
-    __syncthreads();
-    for (int e = threadIdx.x; e < G * (D / 4); e += blockDim.x) {
-        int g = e / (D / 4), k4 = e % (D / 4);
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        // o: one float4 of one head per thread, summed in split order
+        for (int e = threadIdx.x; e < G * (D / 4); e += blockDim.x) {
+            const int g = e / (D / 4), j = e % (D / 4);
+            float L = 0.f;
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
-        for (int sp = 0; sp < ns; ++sp) {
-            const float4 *src = reinterpret_cast<const float4 *>(row_ptr(sp, g) + 4) + k4;
-            const float4 v = staged ? *src : __ldcg(src);
-            float c = wt[sp * 8 + g];
-            acc.x = fmaf(c, v.x, acc.x);
-            acc.y = fmaf(c, v.y, acc.y);
-            acc.z = fmaf(c, v.z, acc.z);
-            acc.w = fmaf(c, v.w, acc.w);
+            for (int sp = 0; sp < ns; ++sp) {
+                const float c = wt[g * MAX_SPLITS + sp];
+                const float4 v = ld4(g, sp, 4 + 4 * j);
+                L = fmaf(c, ld1(g, sp, 1), L);
+                acc.x = fmaf(c, v.x, acc.x);
+                acc.y = fmaf(c, v.y, acc.y);
+                acc.z = fmaf(c, v.z, acc.z);
+                acc.w = fmaf(c, v.w, acc.w);
+            }
+            const float il = 1.f / L;
+            reinterpret_cast<float4 *>(prm.out + ((size_t)b_idx * y.Hq + h * G + g) * D)[j] =
+                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
         }
-        reinterpret_cast<float4 *>(prm.out + ((size_t)b_idx * y.Hq + h * G + g) * D)[k4] = acc;
+    };
+    if (staged) {
+        mbar_wait_bounded(merge_bar, 0, prm.status);
+        const uint32_t sb = smem_u32(stage_buf);
+        merge(
+            [&](int g, int sp, int k) -> float {
+                float v;
+                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(sb + (uint32_t)(((g * ns + sp) * S + k) * 4)));
+                return v;
+            },
+            [&](int g, int sp, int k) -> float4 {
+                float4 v;
+                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                             : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                             : "r"(sb + (uint32_t)(((g * ns + sp) * S + k) * 4)));
+                return v;
+            });
+    } else {
+        const float *rows = prm.partials + y.partial_index(b, h * G, 0) * S;  // head g at + g MAX_SPLITS S
+        merge([&](int g, int sp, int k) -> float { return __ldcg(rows + ((size_t)g * MAX_SPLITS + sp) * S + k); },
+              [&](int g, int sp, int k) -> float4 {
+                  return __ldcg(reinterpret_cast<const float4 *>(rows + ((size_t)g * MAX_SPLITS + sp) * S + k));
+              });
     }
-    if (threadIdx.x == 0) prm.tickets[y.ticket_index(b, h)] = 0;
+    if (threadIdx.x == 0) arrivals[0] = 0;
+    return true;
 }
 
 // ---------------------------------------------------------------- bf16 tensor-core path
@@ -494,70 +481,126 @@ __device__ __forceinline__ void patch_new_row(const DecodeParams &prm, unsigned 
     __syncwarp();
 }
 
+// One CTA of a (sequence, KV head) group of `gridDim.x` CTAs, streaming one
+// contiguous, byte-balanced range of the sequence's pages.  The CTA's units
+// are dealt round-robin to its NWC warps; each warp streams its own units
+// through SPW private shared-memory slots, its lane 0 issuing the bulk copy of
+// the warp's next unit into the slot the warp has just finished with (one
+// mbarrier per slot, so a slot's phases are always consumed in order by the
+// warp that fills it).  Right after its first copies, lane 0 of warp 0 asks
+// L2 for the rest of the CTA's range, so the bytes in flight do not depend on
+// the slot count.
+//
+// Overlap with the neighbouring launches (programmatic dependent launch): a
+// CTA lets the next launch start as soon as its own wait for the preceding
+// launch has returned, so at most two decode grids are resident and the next
+// one fetches while this one finishes.  Before that wait only bytes no earlier
+// launch can still be writing are copied to shared memory: factor records
+// (unless the preceding launch of this store was a conversion, a prefill or an
+// append, in which case prm.wait_first makes the first copy wait) and dense
+// rows below T - 2 (the rows the preceding launch may append are T - 2 and
+// T - 1).  L2 prefetches need no such care: L2 is the point of coherence, so
+// a row written after its prefetch is still copied fresh.
+// float offset of the warp states in the ring once streaming is over (after
+// the merge scratch; a multiple of 4 floats)
+template <int D>
+__host__ __device__ constexpr int fin_comb() { return MAX_SPLITS * 8 + 8; }
+
 template <int P, int D, int RKT, int RVT>
-__global__ void __launch_bounds__((NWC_BF16 + 1) * 32) decode_bf16_kernel(const DecodeParams prm) {
-    constexpr int NWC = NWC_BF16;
+__global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel(const DecodeParams prm) {
+    constexpr int NWC = NWC_BF16, SPW = SLOTS_PER_WARP, NS = NWC * SPW;
+    constexpr int FIN_COMB = fin_comb<D>();
     extern __shared__ __align__(128) unsigned char smem[];
     const Layout &y = prm.y;
-    const int b_idx = blockIdx.z, b = prm.seqs[b_idx], h = blockIdx.y, split = blockIdx.x;
-    const int NS = prm.stages;
+    const int b_idx = blockIdx.z, b = prm.seqs[b_idx], h = blockIdx.y, rank = blockIdx.x;
+    const int T = prm.lens[b_idx];
+    const int n_pages = (T + P - 1) / P;
+    const int ns = min((int)gridDim.x, n_pages);  // CTAs taking part for this sequence
+    if (rank >= ns) return;                       // uniform over the CTA
 
-    const size_t stage_bytes = ((y.rec_bytes > (size_t)P * D * 2 ? y.rec_bytes : (size_t)P * D * 2) + 127) & ~(size_t)127;
+    const size_t stage_bytes = decode_stage_bytes<P, D>(y);
     unsigned char *stages = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
-    uint64_t *empty = full + NS_MAX;
-    DecodeShared &sh = *reinterpret_cast<DecodeShared *>(empty + NS_MAX);
+    DecodeShared &sh = *reinterpret_cast<DecodeShared *>(full + NS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    uint64_t *wfull = full + warp * SPW;
+    unsigned char *wstage = stages + (size_t)warp * SPW * stage_bytes;
+    int *winfo = sh.unit_info + warp * SPW;  // per slot: page << 2 | dense << 1 | half
 
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < NS; ++i) {
-            mbar_init(&full[i], 1);
-            mbar_init(&empty[i], 1);
+    // lane 0: this warp's cursor and next unit
+    UnitCursor cur{};
+    int n_pg = 0, n_hf = 0;
+    bool n_dense = false, have_next = false;
+    bool waited = prm.wait_first != 0;
+    uint64_t policy = 0;
+    const char *fact = prm.factor_pool + y.record_offset(prm.layer, b, h, 0);
+    auto take = [&](int skip) -> bool {  // skip units dealt to the other warps, then take one
+        int pg, hf;
+        bool dn;
+        for (int i = 0; i < skip; ++i)
+            if (!cur.next<P>(pg, hf, dn)) return false;
+        return cur.next<P>(n_pg, n_hf, n_dense);
+    };
+    auto issue = [&](int slot) {
+        winfo[slot] = (n_pg << 2) | (n_dense ? 2 : 0) | n_hf;
+        unsigned char *dst = wstage + (size_t)slot * stage_bytes;
+        if (!n_dense) {
+            mbar_arrive_expect_tx(&wfull[slot], (uint32_t)y.rec_bytes);
+            bulk_g2s_hint(dst, fact + (size_t)n_pg * y.rec_bytes, (uint32_t)y.rec_bytes, &wfull[slot], policy);
+        } else {
+            const int first = n_pg * P + n_hf * (P / 2);
+            if (!waited && first + dense_half_valid(T, n_pg, P, n_hf) >= T - 1) {
+                grid_dependency_wait();
+                waited = true;
+            }
+            const int slot_d = y.dense_slot(n_pg);
+            const uint32_t hb = (uint32_t)(P / 2) * D * 2;
+            mbar_arrive_expect_tx(&wfull[slot], 2 * hb);
+            bulk_g2s_hint(dst, prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 0) + n_hf * hb, hb,
+                          &wfull[slot], policy);
+            bulk_g2s_hint(dst + hb, prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 1) + n_hf * hb, hb,
+                          &wfull[slot], policy);
         }
+    };
+    // this CTA's pages and their factorized stretch (split on the host)
+    const int pb = prm.bounds[prm.boff[b_idx] + rank], pe = prm.bounds[prm.boff[b_idx] + rank + 1];
+    const int a1 = min(max(pb, prm.fs[b_idx]), pe), a2 = max(a1, min(pe, prm.fw[b_idx]));
+    if (threadIdx.x == 0) {
         sh.failed = 0;
-        sh.issued = 0;
+        for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
+        mbar_init(&sh.merge_bar, 1);
         fence_barrier_init();
     }
-    int T = 0;
-    const int np = build_units(sh, prm, b_idx, split, T);  // contains __syncthreads
-    if (np == 0) return;
-    const int n_pages = (T + P - 1) / P;
-    const int p0 = split * prm.chunk;
-    const int NU = sh.n_units;
-    if (prm.append && split == 0 && h == 0 && threadIdx.x == 0) append_page_table(prm, b_idx, b, T);
-
-    WarpState<P, D> w;
-    if (warp == NWC) {  // producer
-        if (lane == 0) {
-            int u = 0;
-            for (; u < NU; ++u) {
-                int stg = u % NS;
-                uint32_t ph = (u / NS) & 1;
-                if (!mbar_wait_bounded(&empty[stg], ph ^ 1, prm.status)) {
-                    sh.failed = 1;
-                    break;
-                }
-                int info = sh.unit[u];
-                int i = info >> 1, half = info & 1;
-                int d = sh.desc[i];
-                int slot = d & SLOT_MASK;
-                unsigned char *dst = stages + (size_t)stg * stage_bytes;
-                if ((d >> KIND_SHIFT) == KIND_FACTORED) {
-                    mbar_arrive_expect_tx(&full[stg], (uint32_t)y.rec_bytes);
-                    bulk_g2s(dst, prm.factor_pool + y.record_offset(prm.layer, b, h, slot), (uint32_t)y.rec_bytes,
-                             &full[stg]);
-                } else {
-                    const uint32_t hb = (uint32_t)(P / 2) * D * 2;
-                    mbar_arrive_expect_tx(&full[stg], 2 * hb);
-                    bulk_g2s(dst, prm.dense_pool + y.dense_offset(prm.layer, b, slot, h, 0) + half * hb, hb, &full[stg]);
-                    bulk_g2s(dst + hb, prm.dense_pool + y.dense_offset(prm.layer, b, slot, h, 1) + half * hb, hb,
-                             &full[stg]);
-                }
-            }
-            sh.issued = u;
+    __syncthreads();
+    int issued = 0;
+    if (lane == 0) {
+        policy = l2_evict_first();
+        if (waited) grid_dependency_wait();
+        cur = UnitCursor{pb, 0, a1, a2, pe, T};
+        have_next = take(warp);
+        while (have_next && issued < SPW) {
+            issue(issued++);
+            have_next = take(NWC - 1);
         }
-        __syncwarp();
-    } else {  // consumers
+        if (warp == NWC - 1) {  // the rest of the range: L2 prefetches
+            for (size_t off = 0, len = (size_t)(a2 - a1) * y.rec_bytes; off < len; off += 65536)
+                prefetch_l2(fact + (size_t)a1 * y.rec_bytes + off, (uint32_t)min(len - off, (size_t)65536));
+            for (int p = pb; p < pe; ++p) {
+                if (p >= a1 && p < a2) continue;
+                const int slot_d = y.dense_slot(p);
+                prefetch_l2(prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 0), (uint32_t)y.dense_half_bytes);
+                prefetch_l2(prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 1), (uint32_t)y.dense_half_bytes);
+            }
+        }
+    }
+    issued = __shfl_sync(0xffffffffu, issued, 0);
+
+    // q, the appended token and the page table may come from the preceding grid
+    grid_dependency_wait();
+    if (threadIdx.x == 0) grid_launch_dependents();  // the next launch may now become resident
+    if (prm.append && rank == 0 && h == 0 && threadIdx.x == 0) append_page_table(prm, b_idx, b, T);
+    WarpState<P, D> w;
+    {
         const int g = lane >> 2, c2 = 2 * (lane & 3);
         const __nv_bfloat16 *qrow =
             reinterpret_cast<const __nv_bfloat16 *>(prm.q) + ((size_t)b_idx * y.Hq + (size_t)h * y.G + g) * D;
@@ -566,53 +609,58 @@ __global__ void __launch_bounds__((NWC_BF16 + 1) * 32) decode_bf16_kernel(const 
             w.qf[kk][0] = g < y.G ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16 + c2) : 0u;
             w.qf[kk][1] = g < y.G ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16 + 8 + c2) : 0u;
         }
+    }
 #pragma unroll
-        for (int nt = 0; nt < D / 8; ++nt) w.o[nt][0] = w.o[nt][1] = w.o[nt][2] = w.o[nt][3] = 0.f;
-        w.m = -INFINITY;
-        w.l = 0.f;
-        const float scale_log2 = LOG2E * rsqrtf((float)D);
-        for (int u = warp; u < NU; u += NWC) {
-            int stg = u % NS;
-            uint32_t ph = (u / NS) & 1;
-            bool ok = mbar_wait_bounded(&full[stg], ph, prm.status);
-            if (!__all_sync(0xffffffffu, ok)) {
-                sh.failed = 1;
-                break;
-            }
-            int info = sh.unit[u];
-            int i = info >> 1, half = info & 1;
-            int d = sh.desc[i];
-            uint32_t st = smem_u32(stages + (size_t)stg * stage_bytes);
-            if ((d >> KIND_SHIFT) == KIND_FACTORED) {
-                factored_unit<P, D, RKT, RVT>(w, st, y, lane, scale_log2);
-            } else {
-                const int valid = dense_half_valid(T, p0 + i, P, half);
-                const int first = (p0 + i) * P + half * (P / 2);
-                if (prm.append && first + valid == T)  // this unit ends with the appended token
-                    patch_new_row<D>(prm, stages + (size_t)stg * stage_bytes, b_idx, b, h, d & SLOT_MASK,
-                                     T - 1 - (p0 + i) * P, valid - 1, lane);
-                dense_unit<P, D>(w, st, valid, lane, scale_log2);
-            }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&empty[stg]);
+    for (int nt = 0; nt < D / 8; ++nt) w.o[nt][0] = w.o[nt][1] = w.o[nt][2] = w.o[nt][3] = 0.f;
+    w.m = -INFINITY;
+    w.l = 0.f;
+    const float scale_log2 = LOG2E * rsqrtf((float)D);
+    int slot = 0, k = 0;
+    uint32_t ph = 0;
+    for (; k < issued; ++k) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wfull[slot], ph, prm.status))) break;
+        const int info = winfo[slot];
+        const int pg = info >> 2, half = info & 1;
+        const uint32_t st = smem_u32(wstage + (size_t)slot * stage_bytes);
+        if (!(info & 2)) {
+            factored_unit<P, D, RKT, RVT>(w, st, y, lane, scale_log2);
+        } else {
+            const int valid = dense_half_valid(T, pg, P, half);
+            const int first = pg * P + half * (P / 2);
+            if (prm.append && first + valid == T)  // this unit ends with the appended token
+                patch_new_row<D>(prm, wstage + (size_t)slot * stage_bytes, b_idx, b, h, y.dense_slot(pg),
+                                 T - 1 - pg * P, valid - 1, lane);
+            dense_unit<P, D>(w, st, valid, lane, scale_log2);
         }
+        __syncwarp();
+        int more = 0;
+        if (lane == 0 && have_next) {  // the slot is free again: this warp's next unit goes into it
+            fence_proxy_async_shared();
+            issue(slot);
+            have_next = take(NWC - 1);
+            more = 1;
+        }
+        issued += __shfl_sync(0xffffffffu, more, 0);
+        if (++slot == SPW) {
+            slot = 0;
+            ph ^= 1;
+        }
+    }
+    if (k < issued) {  // a bounded wait gave up: let this warp's copies land before the CTA exits
+        if (lane == 0) {
+            sh.failed = 1;
+            for (int kk = k; kk < issued; ++kk) mbar_wait_bounded(&wfull[kk % SPW], (kk / SPW) & 1, nullptr);
+        }
+        __syncwarp();
     }
     __syncthreads();
-    if (sh.failed) {
-        // a bounded wait gave up: let every issued copy land before the CTA exits
-        if (threadIdx.x == 0) {
-            for (int u = sh.issued - NS; u < sh.issued; ++u)
-                if (u >= 0) mbar_wait_bounded(&full[u % NS], (u / NS) & 1, nullptr);
-        }
-        __syncthreads();
-        return;
-    }
-    if (warp < NWC) {  // per-warp state -> shared memory (the ring is free: every copy has landed)
+    if (sh.failed) return;
+    {  // per-warp state -> shared memory (every copy has landed and been read)
         const int g = lane >> 2, c2 = 2 * (lane & 3);
         float l = w.l;
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
-        float *comb = reinterpret_cast<float *>(stages) + (size_t)warp * 8 * (D + 2);
+        float *comb = reinterpret_cast<float *>(stages) + FIN_COMB + (size_t)warp * 8 * (D + 2);
         if (g < y.G) {
             float *row = comb + g * (D + 2);
             if (c2 == 0) {
@@ -628,13 +676,12 @@ __global__ void __launch_bounds__((NWC_BF16 + 1) * 32) decode_bf16_kernel(const 
     }
     __syncthreads();
     {
-        const float *comb = reinterpret_cast<const float *>(stages);
-        float *scratch = reinterpret_cast<float *>(stages) + NWC * 8 * (D + 2);
-        float *stage_buf = scratch + 3 * MAX_SPLITS * 8 + 16;
-        const size_t used = (size_t)(NWC * 8 * (D + 2) + 3 * MAX_SPLITS * 8 + 16) * 4;
-        const size_t cap = (size_t)NS * stage_bytes > used ? (size_t)NS * stage_bytes - used : 0;
-        const int ns = (n_pages + prm.chunk - 1) / prm.chunk;
-        finish_split<D, NWC>(prm, comb, b_idx, b, h, split, ns, scratch, &sh.last, stage_buf, cap);
+        // ring reuse: merge scratch, then the warp states, which the other
+        // CTAs' states overwrite once merged
+        float *scratch = reinterpret_cast<float *>(stages);
+        float *comb = scratch + FIN_COMB;
+        const size_t cap = (size_t)NS * stage_bytes - (size_t)FIN_COMB * 4;
+        finish_split<D, NWC>(prm, comb, b_idx, b, h, rank, ns, scratch, &sh.last, comb, cap, &sh.merge_bar);
     }
 }
 
@@ -646,32 +693,97 @@ inline void choose_chunk(DecodeParams &p, long total_pages, int max_pages, int c
     splits = (max_pages + chunk - 1) / chunk;
 }
 
+// Launch set-up of one kernel instantiation on the current device, computed
+// once (shared-memory opt-in, ring depth, occupancy): none of it changes
+// between calls, and querying it per launch costs more host time than a
+// decode launch takes on the GPU.
+struct LaunchSetup {
+    int ready = 0;
+    int stages = 0;
+    size_t smem = 0;
+    int occ = 1;
+    cudaError_t err = cudaSuccess;
+};
+
 template <int P, int D, int RKT, int RVT>
 cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     const Layout &y = p.y;
-    size_t stage_bytes = ((y.rec_bytes > (size_t)P * D * 2 ? y.rec_bytes : (size_t)P * D * 2) + 127) & ~(size_t)127;
-    size_t tail_bytes = (size_t)NWC_BF16 * 8 * (D + 2) * 4 + (3 * MAX_SPLITS * 8 + 16) * 4;  // comb + merge scratch
-    size_t fixed = 2 * NS_MAX * sizeof(uint64_t) + sizeof(DecodeShared);
-    int dev = 0, optin = 0;
-    cudaGetDevice(&dev);
-    if (cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess || optin <= 0)
-        optin = 227 * 1024;
-    // as many stages as fit: bytes in flight per SM are what hide HBM latency
-    int ns = (int)(((size_t)optin - fixed) / stage_bytes);
-    ns = ns > NS_MAX ? NS_MAX : ns;
-    if (ns < 2 || ns * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
-    p.stages = ns;
-    size_t smem = ns * stage_bytes + fixed;
+    const size_t stage_bytes =
+        ((y.rec_bytes > (size_t)P * D * 2 ? y.rec_bytes : (size_t)P * D * 2) + 127) & ~(size_t)127;
     auto k = decode_bf16_kernel<P, D, RKT, RVT>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // one set-up per (device, record size): the ring depth depends on the record size
+    static std::mutex mu;
+    static LaunchSetup cache[64][4];
+    static size_t cache_key[64][4];
+    int dev = 0;
+    cudaGetDevice(&dev);
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    LaunchSetup setup;
+    {
+        std::lock_guard<std::mutex> lock(mu);
+        int slot = -1;
+        for (int i = 0; i < 4; ++i)
+            if (cache[dev][i].ready && cache_key[dev][i] == stage_bytes) slot = i;
+        if (slot < 0) {
+            for (int i = 0; i < 4 && slot < 0; ++i)
+                if (!cache[dev][i].ready) slot = i;
+            if (slot < 0) slot = 0;
+            LaunchSetup &c = cache[dev][slot];
+            c = LaunchSetup{};
+            constexpr int NS = NWC_BF16 * SLOTS_PER_WARP;
+            const size_t tail_bytes = (size_t)fin_comb<D>() * 4 + (size_t)NWC_BF16 * 8 * (D + 2) * 4;
+            if ((size_t)NS * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
+            c.stages = NS;
+            c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared);
+            c.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
+            if (c.err == cudaSuccess &&
+                (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, NWC_BF16 * 32, c.smem) != cudaSuccess ||
+                 c.occ < 1))
+                c.occ = 1;
+            c.ready = 1;
+            cache_key[dev][slot] = stage_bytes;
+        }
+        setup = cache[dev][slot];
+    }
+    if (setup.err != cudaSuccess) return setup.err;
+    p.stages = setup.stages;
+    // one CTA per SM: a group of CTAs per (sequence, KV head), each streaming
+    // one byte-balanced range of pages; the SM's other CTA slot is left to
+    // the next launch
+    const long pairs = (long)p.nseq * y.H;
+    int group = (int)((num_sms + pairs / 2) / pairs);
+    group = group < 1 ? 1 : (group > MAX_SPLITS ? MAX_SPLITS : group);
+    group = group > max_pages ? max_pages : group;
+    // page bounds of every CTA, ns + 1 per call entry (fewer CTAs if they do not fit)
+    for (;;) {
+        int need = 0;
+        for (int i = 0; i < p.nseq; ++i) need += std::min(group, (p.lens[i] + P - 1) / P) + 1;
+        if (need <= MAX_BOUNDS || group == 1) break;
+        --group;
+    }
+    for (int i = 0, off = 0; i < p.nseq; ++i) {
+        const int T = p.lens[i], n = std::min(group, (T + P - 1) / P);
+        const PageSplit split(T, P, y.sink_pages, y.sink_tokens, y.W, (long long)y.rec_bytes,
+                              (long long)P * D * 2, n);
+        p.boff[i] = off;
+        p.fs[i] = split.fs;
+        p.fw[i] = split.fw;
+        for (int r = 0; r <= n; ++r) p.bounds[off + r] = split.begin(r);
+        off += n + 1;
+    }
+    const int splits = group;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)splits, (unsigned)y.H, (unsigned)p.nseq);
+    cfg.blockDim = dim3(NWC_BF16 * 32, 1, 1);
+    cfg.dynamicSmemBytes = setup.smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;  // may start while the previous grid finishes
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    cudaError_t e = cudaLaunchKernelEx(&cfg, k, p);
     if (e != cudaSuccess) return e;
-    int occ = 1;
-    if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, k, (NWC_BF16 + 1) * 32, smem) != cudaSuccess || occ < 1)
-        occ = 1;
-    int splits = 1;
-    choose_chunk(p, total_pages, max_pages, num_sms * occ, splits);
-    dim3 grid((unsigned)splits, (unsigned)y.H, (unsigned)p.nseq);
-    k<<<grid, (NWC_BF16 + 1) * 32, smem, st>>>(p);
     return cudaGetLastError();
 }
 

@@ -14,6 +14,8 @@
 //   4. eigenvalues ranked descending (ties: lower index first);
 //   5. L = Q_r, R = Q_r^T X in fp32, written as bf16 or fp32 into either a
 //      factor record (swizzled store layout) or plain row-major arrays.
+#include <atomic>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -392,8 +394,20 @@ template <typename T, int P, int D, int NT>
 static cudaError_t launch_t(const FactorParams &fp, int num_sms, cudaStream_t st) {
     size_t smem = sizeof(FactorSmem<T, P, D>);
     auto k = factorize_kernel<T, P, D, NT>;
-    cudaError_t e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // the shared-memory opt-in is set once per device (per launch it costs
+    // more host time than a small launch takes on the GPU)
+    static std::atomic<int> attr_state[64];  // 0 = not set, 1 = set, 2 + error = failed
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return e;
+    if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    int state = attr_state[dev].load(std::memory_order_acquire);
+    if (state == 0) {
+        e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        state = e == cudaSuccess ? 1 : 2 + (int)e;
+        attr_state[dev].store(state, std::memory_order_release);
+    }
+    if (state != 1) return (cudaError_t)(state - 2);
     long blocks = fp.n_jobs;
     long cap = (long)num_sms * (NT >= 1024 ? 2 : 8);
     if (blocks > cap) blocks = cap;

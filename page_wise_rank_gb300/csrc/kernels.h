@@ -33,6 +33,8 @@ struct FactorParams {
     const int2 *conv_list;
 };
 
+constexpr int MAX_BOUNDS = 384;  // page bounds of all CTAs of one bf16 decode launch
+
 struct DecodeParams {
     Layout y;
     const char *factor_pool, *dense_pool;
@@ -40,6 +42,7 @@ struct DecodeParams {
     const char *q;      // [B][Hq][d] storage dtype
     float *partials;    // workspace split partials
     int *tickets;       // workspace split tickets, zero between launches
+    int wait_first;     // bf16 kernel: the preceding launch may have written factor records
     float *out;         // [B][Hq][d]
     int *status;
     int layer, chunk, nseq;
@@ -52,6 +55,11 @@ struct DecodeParams {
     const char *k_new, *v_new;
     int append;
     int conv_page[MAX_CALL_BATCH];  // page converted before this launch, or -1
+    // bf16 kernel, filled by its launcher: CTA r of call entry i streams pages
+    // [bounds[boff[i] + r], bounds[boff[i] + r + 1]) (PageSplit), of which
+    // [fs[i], fw[i]) are the sequence's factorized pages
+    int boff[MAX_CALL_BATCH], fs[MAX_CALL_BATCH], fw[MAX_CALL_BATCH];
+    int bounds[MAX_BOUNDS];
     int *lengths_out, *desc_out;    // device page table (written when append)
 };
 

@@ -15,8 +15,9 @@
 //                leaving the ring.
 //   page table   int32 lengths[seq][layer], then int32 desc[seq][layer][page]
 //                = kind << 30 | slot.
-//   workspace    int32 status words, int32 split tickets [seq][kv_head], the
-//                batched-conversion job list (int2 per page), then
+//   workspace    int32 status words, int32 split tickets [seq][kv_head][2] (one
+//                counter, padded),
+//                the batched-conversion job list (int2 per page), then
 //                fp32 split-K partial states [seq][q_head][split][4 + d]
 //                (m, l, two pad words, o[d]: 16-byte aligned rows).
 //
@@ -84,6 +85,68 @@ PKV_HD int page_kind(int p, int T, int P, int sink_tokens, int W) {
     return dense ? KIND_DENSE : KIND_FACTORED;
 }
 
+// Tokens in half `half` of page p (P/2 rows) of a sequence of T tokens.
+PKV_HD int dense_half_valid(int T, int p, int P, int half) {
+    int first = p * P + half * (P / 2);
+    int v = T - first;
+    return v < 0 ? 0 : (v > P / 2 ? P / 2 : v);
+}
+
+// Bytes a dense page streams in decode: a K and a V half page per non-empty half.
+PKV_HD long long dense_page_bytes(int p, int T, int P, long long half_bytes) {
+    return (dense_half_valid(T, p, P, 0) > 0 ? half_bytes : 0) + (dense_half_valid(T, p, P, 1) > 0 ? half_bytes : 0);
+}
+
+// Split of one sequence's pages over the n CTAs of a (sequence, KV head)
+// decode group, balanced by the bytes each CTA streams: page p goes to the CTA
+// whose equal share of the total holds the page's midpoint.  The kinds follow
+// the classification rule -- dense sink pages [0, fs), factorized pages
+// [fs, fw), dense window pages [fw, n_pages) -- so the factorized stretch is
+// counted in closed form and only the few dense pages are walked.
+struct PageSplit {
+    int T, P, n_pages, fs, fw, n;
+    long long rec, half, total;
+    PKV_HD PageSplit(int T_, int P_, int sink_pages, int sink_tokens, int W, long long rec_bytes,
+                     long long half_bytes, int n_)
+        : T(T_), P(P_), n(n_), rec(rec_bytes), half(half_bytes) {
+        n_pages = (T + P - 1) / P;
+        fs = sink_pages < n_pages ? sink_pages : n_pages;
+        fw = n_pages;
+        while (fw > fs && page_kind(fw - 1, T, P, sink_tokens, W) == KIND_DENSE) --fw;
+        total = (long long)(fw - fs) * rec;
+        for (int p = 0; p < fs; ++p) total += dense_page_bytes(p, T, P, half);
+        for (int p = fw; p < n_pages; ++p) total += dense_page_bytes(p, T, P, half);
+    }
+    // first page of CTA r: the pages whose midpoint lies below r / n of the
+    // bytes, i.e. n (2 before + cost) < 2 total r
+    PKV_HD int begin(int r) const {
+        if (r <= 0) return 0;
+        if (r >= n) return n_pages;
+        const long long lim = 2 * total * r;
+        long long before = 0;
+        int cnt = 0;
+        for (int p = 0; p < fs; ++p) {
+            const long long c = dense_page_bytes(p, T, P, half);
+            if (n * (2 * before + c) >= lim) return cnt;
+            before += c;
+            ++cnt;
+        }
+        // factorized pages j = 0, 1, ...: n (2 (before + j rec) + rec) < lim  <=>  j < rhs / step
+        const long long rhs = lim - n * (2 * before + rec), step = 2 * (long long)n * rec;
+        const long long k = rhs <= 0 ? 0 : (rhs + step - 1) / step;
+        if (k < fw - fs) return cnt + (int)k;
+        cnt += fw - fs;
+        before += (long long)(fw - fs) * rec;
+        for (int p = fw; p < n_pages; ++p) {
+            const long long c = dense_page_bytes(p, T, P, half);
+            if (n * (2 * before + c) >= lim) return cnt;
+            before += c;
+            ++cnt;
+        }
+        return cnt;
+    }
+};
+
 struct Layout {
     int L, H, Hq, G, d, P, rk, rv, rkp, rvp, sink_tokens, W, Bmax, Tmax, esz, dtype;
     int n_pg_max, sink_pages, ring, dslots;
@@ -109,7 +172,8 @@ struct Layout {
     PKV_HD size_t len_index(int b, int l) const { return (size_t)b * L + l; }
     PKV_HD size_t desc_index(int b, int l, int p) const { return ((size_t)b * L + l) * n_pg_max + p; }
     PKV_HD size_t partial_index(int b, int hq, int s) const { return ((size_t)b * Hq + hq) * MAX_SPLITS + s; }
-    PKV_HD size_t ticket_index(int b, int h) const { return (size_t)b * H + h; }
+    // one arrival counter per (seq, kv head), padded to two ints
+    PKV_HD size_t ticket_index(int b, int h) const { return 2 * ((size_t)b * H + h); }
 };
 
 // Fill a Layout from a validated configuration.
@@ -135,7 +199,7 @@ inline void make_layout(Layout &y, int L, int H, int Hq, int d, int P, int rk, i
     y.desc_offset = len_bytes;
     y.page_table_bytes = len_bytes + (((size_t)Bmax * L * y.n_pg_max * 4 + 255) & ~(size_t)255);
     y.ticket_offset = 256;
-    y.jobs_offset = y.ticket_offset + (((size_t)Bmax * H * 4 + 255) & ~(size_t)255);
+    y.jobs_offset = y.ticket_offset + (((size_t)Bmax * H * 8 + 255) & ~(size_t)255);
     y.max_conv_jobs = Bmax * L * (y.ring + 1);
     y.partial_offset = y.jobs_offset + (((size_t)y.max_conv_jobs * 8 + 255) & ~(size_t)255);
     y.part_stride = d + 4;
