@@ -31,6 +31,7 @@ from .generators import (  # noqa: F401
     prefill_kv,
     decode_page,
     decode_tokens,
+    decode_rows,
     queries,
     batch_lengths,
     apply_rope,

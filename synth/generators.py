@@ -145,6 +145,22 @@ def decode_tokens(spec: KVSpec, layer: int, seqs: Sequence[int], positions: Sequ
     return (torch.stack(ks).to(spec.dtype), torch.stack(vs).to(spec.dtype))
 
 
+def decode_rows(spec: KVSpec, layer: int, seq: int, first: int, n: int, device="cpu"
+                ) -> Tuple[torch.Tensor, torch.Tensor]:
+    """The rows ``decode_tokens`` gives sequence ``seq`` at positions
+    first .. first + n - 1, all at once: (K, V), each [H, n, d] in ``spec.dtype``."""
+    P = spec.page_size
+    p0, p1 = first // P, (first + n - 1) // P
+    out = []
+    for kind in (0, 1):
+        x = torch.cat([decode_page(spec, layer, kind, seq, p, device) for p in range(p0, p1 + 1)], dim=1)
+        x = x[:, first - p0 * P: first - p0 * P + n]
+        if kind == 0 and spec.rope_base is not None:
+            x = apply_rope(x, torch.arange(first, first + n, device=device), spec.rope_base)
+        out.append(x.to(spec.dtype))
+    return out[0], out[1]
+
+
 def queries(B: int, Hq: int, d: int, step: int, layer: int = 0, device="cpu",
             dtype: torch.dtype = torch.bfloat16) -> torch.Tensor:
     """[B, Hq, d] queries, N(0, 1) / sqrt(d)."""

@@ -81,7 +81,11 @@ def descriptors(store, lay: Layout, b: int, l: int, n_pages: int):
 def read_factors(fp_bytes: np.ndarray, lay: Layout, l: int, b: int, h: int, p: int):
     """(LK [P, rk], RK [rk, d], LV [P, rv], RV [rv, d]) of one record, fp64."""
     o = lay.record_offset(l, b, h, p)
-    rec = fp_bytes[o:o + lay.rec_bytes]
+    return read_record(fp_bytes[o:o + lay.rec_bytes], lay)
+
+
+def read_record(rec: np.ndarray, lay: Layout):
+    """Factors of one record given its rec_bytes bytes, fp64."""
     e, P, d = lay.esz, lay.P, lay.d
     LK = unswizzle(rec[: lay.off_RK], P, lay.rkp, e, lay.dtype)[:, : lay.rk]
     RK = unswizzle(rec[lay.off_RK: lay.off_LV], lay.rkp, d, e, lay.dtype)[: lay.rk]
