@@ -24,7 +24,7 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
     constexpr int TPL = (P + 31) / 32;  // tokens per lane
     constexpr int DPL = D / 32;         // head dims per lane
     const float scale = rsqrtf((float)D);
-    __shared__ float comb[NWC][8][D + 2];
+    __shared__ __align__(16) float comb[NWC][8][D + 4];
     __shared__ float scratch[MAX_SPLITS * 8 + 8];
     __shared__ int last;
 
@@ -154,7 +154,7 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
             comb[warp][g][0] = m[g] * LOG2E;
             comb[warp][g][1] = l[g];
         }
-        for (int e = 0; e < DPL; ++e) comb[warp][g][2 + lane + 32 * e] = o[g][e];
+        for (int e = 0; e < DPL; ++e) comb[warp][g][4 + lane + 32 * e] = o[g][e];
     }
     __syncthreads();
     const int ns = (n_pages + prm.chunk - 1) / prm.chunk;

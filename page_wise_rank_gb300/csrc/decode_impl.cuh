@@ -102,7 +102,8 @@ struct UnitCursor {
 };
 
 // Split hand-off, eq. (5).  `comb` holds the NW warp states of this CTA
-// ([warp][g][m, l, o...], D + 2 floats per row, m in log2 units); they are
+// ([warp][g][m, l, pad, pad, o...], D + 4 floats per row, 16-byte aligned, m
+// in log2 units); they are
 // merged into the CTA's state, which every CTA writes to the workspace and
 // makes visible before it takes its arrival
 // ticket for (b, h).  The CTA that takes the last ticket therefore sees every
@@ -119,23 +120,32 @@ __device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_i
     const Layout &y = prm.y;
     const int G = y.G, S = y.part_stride;
     int *arrivals = prm.tickets + y.ticket_index(b, h);
-    for (int e = threadIdx.x; e < G * (D + 2); e += blockDim.x) {
-        const int gg = e / (D + 2), k = e % (D + 2);
+    // the CTA's state, one float4 of o per thread (head g, columns 4j .. 4j+3),
+    // written straight to its workspace row; j = 0 also writes m and l
+    for (int e = threadIdx.x; e < G * (D / 4); e += blockDim.x) {
+        const int g = e / (D / 4), j = e % (D / 4);
         float mw[NW], M = -INFINITY;
 #pragma unroll
         for (int w = 0; w < NW; ++w) {
-            mw[w] = comb[(w * 8 + gg) * (D + 2)];
+            mw[w] = comb[(w * 8 + g) * (D + 4)];
             M = fmaxf(M, mw[w]);
         }
-        float acc = 0.f;
-        if (k == 0) {
-            acc = M;
-        } else {
+        float L = 0.f;
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll
-            for (int w = 0; w < NW; ++w)
-                acc += (mw[w] == -INFINITY ? 0.f : exp2f(mw[w] - M)) * comb[(w * 8 + gg) * (D + 2) + k];
+        for (int w = 0; w < NW; ++w) {
+            const float *row = comb + (w * 8 + g) * (D + 4);
+            const float c = mw[w] == -INFINITY ? 0.f : ex2_approx(mw[w] - M);
+            const float4 v = reinterpret_cast<const float4 *>(row + 4)[j];
+            L = fmaf(c, row[1], L);
+            acc.x = fmaf(c, v.x, acc.x);
+            acc.y = fmaf(c, v.y, acc.y);
+            acc.z = fmaf(c, v.z, acc.z);
+            acc.w = fmaf(c, v.w, acc.w);
         }
-        prm.partials[y.partial_index(b, h * G + gg, split) * S + (k < 2 ? k : k + 2)] = acc;
+        float *prow = prm.partials + y.partial_index(b, h * G + g, split) * S;
+        reinterpret_cast<float4 *>(prow + 4)[j] = acc;
+        if (j == 0) reinterpret_cast<float4 *>(prow)[0] = make_float4(M, L, 0.f, 0.f);
     }
     // rows of head g are contiguous: partial_index(b, h G + g, 0 .. ns-1)
     const bool staged = merge_bar != nullptr && stage_buf != nullptr && (size_t)G * ns * S * 4 <= stage_cap;
@@ -159,33 +169,38 @@ __device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_i
     }
     __syncthreads();
     if (!*last) return false;
-    float *wt = scratch;  // weights [g][split]
+    float *wt = scratch, *iL = scratch + MAX_SPLITS * 8;  // weights [g][split], 1 / normaliser [g]
     auto merge = [&](auto ld1, auto ld4) {
-        // weight of split sp for head g: 2^(m_sp - M_g), M_g the max over the splits
-        for (int t = threadIdx.x; t < G * ns; t += blockDim.x) {
-            const int g = t / ns, sp = t - g * ns;
+        const int nwarps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+        for (int g = warp; g < G; g += nwarps) {  // per head: max, weights and normaliser over the splits
             float M = -INFINITY;
-            for (int s2 = 0; s2 < ns; ++s2) M = fmaxf(M, ld1(g, s2, 0));
-            const float m = ld1(g, sp, 0);
-            wt[g * MAX_SPLITS + sp] = m == -INFINITY ? 0.f : ex2_approx(m - M);
+            for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, ld1(g, sp, 0));
+            M = warp_max(M);
+            float L = 0.f;
+            for (int sp = lane; sp < ns; sp += 32) {
+                const float m = ld1(g, sp, 0);
+                const float c = m == -INFINITY ? 0.f : ex2_approx(m - M);
+                wt[g * MAX_SPLITS + sp] = c;
+                L = fmaf(c, ld1(g, sp, 1), L);
+            }
+            L = warp_sum(L);
+            if (lane == 0) iL[g] = 1.f / L;
         }
         __syncthreads();
         // o: one float4 of one head per thread, summed in split order
         for (int e = threadIdx.x; e < G * (D / 4); e += blockDim.x) {
             const int g = e / (D / 4), j = e % (D / 4);
-            float L = 0.f;
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll 4
             for (int sp = 0; sp < ns; ++sp) {
                 const float c = wt[g * MAX_SPLITS + sp];
                 const float4 v = ld4(g, sp, 4 + 4 * j);
-                L = fmaf(c, ld1(g, sp, 1), L);
                 acc.x = fmaf(c, v.x, acc.x);
                 acc.y = fmaf(c, v.y, acc.y);
                 acc.z = fmaf(c, v.z, acc.z);
                 acc.w = fmaf(c, v.w, acc.w);
             }
-            const float il = 1.f / L;
+            const float il = iL[g];
             reinterpret_cast<float4 *>(prm.out + ((size_t)b_idx * y.Hq + h * G + g) * D)[j] =
                 make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
         }
@@ -660,17 +675,17 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
         float l = w.l;
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
-        float *comb = reinterpret_cast<float *>(stages) + FIN_COMB + (size_t)warp * 8 * (D + 2);
+        float *comb = reinterpret_cast<float *>(stages) + FIN_COMB + (size_t)warp * 8 * (D + 4);
         if (g < y.G) {
-            float *row = comb + g * (D + 2);
+            float *row = comb + g * (D + 4);
             if (c2 == 0) {
                 row[0] = w.m;
                 row[1] = l;
             }
 #pragma unroll
             for (int nt = 0; nt < D / 8; ++nt) {
-                row[2 + 8 * nt + c2] = w.o[nt][0] + w.o[nt][2];
-                row[2 + 8 * nt + c2 + 1] = w.o[nt][1] + w.o[nt][3];
+                row[4 + 8 * nt + c2] = w.o[nt][0] + w.o[nt][2];
+                row[4 + 8 * nt + c2 + 1] = w.o[nt][1] + w.o[nt][3];
             }
         }
     }
@@ -731,7 +746,7 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
             LaunchSetup &c = cache[dev][slot];
             c = LaunchSetup{};
             constexpr int NS = NWC_BF16 * SLOTS_PER_WARP;
-            const size_t tail_bytes = (size_t)fin_comb<D>() * 4 + (size_t)NWC_BF16 * 8 * (D + 2) * 4;
+            const size_t tail_bytes = (size_t)fin_comb<D>() * 4 + (size_t)NWC_BF16 * 8 * (D + 4) * 4;
             if ((size_t)NS * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
             c.stages = NS;
             c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared);
