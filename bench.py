@@ -35,6 +35,11 @@ WORKLOADS = {
                      k=12, n_out=4,
                      desc="Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query heads, d=128, bf16, "
                           "T=32768, batch 1, P=64, rK=16, rV=24, sink 4, recent 128"),
+    "incremental8": dict(layers=32, H=8, Hq=32, d=128, P=64, rk=16, rv=24, sink=4, W=128, B=8, T=4096, rope=5e5,
+                         k=12, n_out=4, steps=4096,
+                         desc="Incremental compression during generation: Llama-3.1-8B-shaped attention, 32 layers, "
+                              "8 KV / 32 query heads, d=128, bf16, batch 8, 4096-token prompts then 4096 decode steps, "
+                              "P=64, rK=16, rV=24, sink 4, recent 128"),
     "qwen128k": dict(layers=64, H=8, Hq=64, d=128, P=64, rk=24, rv=24, sink=4, W=128, B=1, T=131072, rope=None,
                      k=12, n_out=4,
                      desc="Qwen3-32B-shaped attention, 64 layers, 8 KV / 64 query heads, d=128, bf16, "
@@ -45,14 +50,50 @@ WORKLOADS = {
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=64)
+    ap.add_argument("--steps", type=int, default=None, help="timed steps (default: 64, or the workload's own count)")
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", default="gpu", choices=["gpu", "reference"])
     ap.add_argument("--workload", default="llama32k", choices=sorted(WORKLOADS))
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--layers", type=int, default=0, help="override the layer count (small profiling runs)")
-    return ap.parse_args()
+    args = ap.parse_args()
+    if args.steps is None:
+        args.steps = WORKLOADS[args.workload].get("steps", 64)
+    return args
+
+
+def measured_peak_bf16():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return 1900.0, "fallback"
+
+
+def factorization_roofline(wl, jobs, sweeps, ms, sms, sm_mhz):
+    """Rates of the prefill factorization against the two peaks that bound it.
+    FLOP conventions per page job (P x d page, P x P Gram):
+      Gram 2 P^2 d; projection 2 r P d (r the mean of r_K and r_V);
+      Jacobi per sweep (P - 1) rounds x P/2 rotations x 18 P (a rotation
+      updates two rows and two columns of G and two eigenvector rows, 6 flops
+      per updated pair)."""
+    P, d = wl["P"], wl["d"]
+    r = (wl["rk"] + wl["rv"]) / 2.0
+    sec = ms * 1e-3
+    gram = jobs * 2.0 * P * P * d
+    proj = jobs * 2.0 * r * P * d
+    jac = sweeps * (P - 1) * (P / 2.0) * 18.0 * P
+    bf16_peak, bf16_kind = measured_peak_bf16()
+    fp32_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # CUDA-core fp32 FMA lanes x 2 flops
+    return {"page_jobs": int(jobs), "jacobi_sweeps_per_job": round(sweeps / max(jobs, 1), 2),
+            "gram_tflops": round(gram / sec / 1e12, 3),
+            "gram_frac_of_bf16_peak": round(gram / sec / 1e12 / bf16_peak, 6), "bf16_peak_tflops": bf16_peak,
+            "bf16_peak_source": bf16_kind,
+            "jacobi_plus_projection_tflops": round((jac + proj) / sec / 1e12, 3),
+            "jacobi_frac_of_fp32_peak": round((jac + proj) / sec / 1e12 / fp32_peak, 4),
+            "fp32_peak_tflops": round(fp32_peak, 1), "fp32_peak_basis": f"{sms} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz"}
 
 
 def measured_peak_hbm():
@@ -149,10 +190,12 @@ def dist_init(n):
 
 
 def barrier_max(x, world):
+    """Max of x over the ranks (the slowest replica sets the job's time)."""
     if world <= 1:
         return x
     import torch.distributed as dist
-    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
     dist.all_reduce(t, op=dist.ReduceOp.MAX)
     return float(t.item())
 
@@ -205,10 +248,12 @@ def gpu_arm(args, rank, world, local):
         stream.synchronize()
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
+        store.factorize_counters(stream)  # start from zero
         store.factorize_pages(0, K, V, stream=stream)
         e1.record(stream)
         st = store.check_device_status(stream)
         prefill_ms = e0.elapsed_time(e1)
+        fact_jobs, fact_sweeps = store.factorize_counters(stream)
         if st != 0:
             raise RuntimeError(f"prefill factorization status {st}: {pkv.last_error()}")
         del K, V
@@ -364,7 +409,10 @@ def gpu_arm(args, rank, world, local):
         "decode_step_us_per_layer_isolated": round(1000.0 * statistics.mean(iso_ms), 3),
         "batched_conversion_us": round(1000.0 * statistics.mean(conv_ms), 1) if conv_ms else None,
         "pages_factorized_per_s": round(pages_per_s, 1),
-        "prefill_factorization": {"pages": n_fact_pages, "ms": round(prefill_ms, 3)},
+        "prefill_factorization": dict({"pages": n_fact_pages, "ms": round(prefill_ms, 3)},
+                                      **factorization_roofline(wl, fact_jobs, fact_sweeps, prefill_ms,
+                                                               torch.cuda.get_device_properties(dev).multi_processor_count,
+                                                               (clk or {}).get("sm_mhz") or 2070.0)),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "kernel": "decode_bf16_kernel: one decode_step launch per layer (append + attention + split merge), mean over the timed steps without a page conversion",
@@ -433,6 +481,119 @@ def cpu_baseline_sample(wl):
             "pages_factorized_per_s": round(pages_s, 1), "pages_cores": nthreads, "pages_sample": n_pages}
 
 
+def incremental_arm(args, rank, world, local):
+    """Generation with pages converted on the decode stream as they complete:
+    per-step latency (mean, p50, p99, the conversion-burst steps) and pages/s.
+    Steps are timed in chunks, each queued behind a GPU-side sleep, so the
+    per-step CUDA-event deltas are GPU time, not host enqueue time."""
+    import page_wise_rank_gb300 as pkv
+    import synth
+    from page_wise_rank_gb300 import build as cuda_build
+
+    wl = dict(WORKLOADS[args.workload])
+    if args.layers:
+        wl["layers"] = args.layers
+        wl["desc"] += f" (first {args.layers} layers only)"
+    cuda_build.build()
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    stream = torch.cuda.Stream(dev)
+    L, H, Hq, d, P, B, T0 = wl["layers"], wl["H"], wl["Hq"], wl["d"], wl["P"], wl["B"], wl["T"]
+    n_steps = args.warmup + args.steps
+    cfg = pkv.StoreConfig(num_layers=L, num_kv_heads=H, num_q_heads=Hq, head_dim=d, page_size=P, rank_k=wl["rk"],
+                          rank_v=wl["rv"], sink_tokens=wl["sink"], recent_tokens=wl["W"], max_batch=B,
+                          max_tokens_per_seq=T0 + n_steps + 8, kv_dtype=torch.bfloat16)
+    spec = synth.KVSpec(layers=L, kv_heads=H, head_dim=d, page_size=P, inner_rank=wl["k"], n_outliers=wl["n_out"],
+                        rope_base=wl["rope"], dtype=torch.bfloat16)
+    seqs = list(range(B))
+    with torch.cuda.stream(stream):
+        store = pkv.Store(cfg, device=dev, stream=stream)
+        prefill_ms = 0.0
+        store.factorize_counters(stream)
+        for i in seqs:  # prompts: one whole-cache factorization per sequence
+            K, V = synth.prefill_kv(spec, T0, seq=rank * B + i, device=dev)
+            stream.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            store.factorize_pages(i, K, V, stream=stream)
+            e1.record(stream)
+            stream.synchronize()
+            prefill_ms += e0.elapsed_time(e1)
+            del K, V
+        pre_jobs, pre_sweeps = store.factorize_counters(stream)
+        # decode-phase inputs of every step, on the device: [L, steps, B, H, d]
+        kdec = torch.empty(L, n_steps, B, H, d, dtype=torch.bfloat16, device=dev)
+        vdec = torch.empty_like(kdec)
+        for l in range(L):
+            for i in seqs:
+                k, v = synth.decode_rows(spec, l, rank * B + i, T0, n_steps, device=dev)
+                kdec[l, :, i] = k.transpose(0, 1)
+                vdec[l, :, i] = v.transpose(0, 1)
+        qs = [[synth.queries(B, Hq, d, step=s, layer=l).to(dev) for l in range(L)] for s in range(8)]
+        out = torch.empty(L, B, Hq, d, dtype=torch.float32, device=dev)
+        T = [T0]
+
+        def step(s):
+            conv = (T[0] + 1) % P == 0  # this step completes a page: batched conversion
+            for l in range(L):
+                store.decode_step(l, qs[s % 8][l], kdec[l, s], vdec[l, s], out[l], seqs, stream=stream)
+            store.convert_ready_pages(stream=stream)
+            T[0] += 1
+            return conv
+
+        for s in range(args.warmup):
+            step(s)
+        stream.synchronize()
+        store.factorize_counters(stream)
+        clocks = ClockSampler(torch.cuda.current_device())
+        clocks.start()
+        barrier(world)
+        step_ms, burst = [], []
+        chunk = 16
+        for c0 in range(args.warmup, n_steps, chunk):
+            torch.cuda._sleep(20_000_000)  # lets the host queue the chunk before the GPU reaches it
+            evs = [torch.cuda.Event(enable_timing=True)]
+            evs[0].record(stream)
+            for s in range(c0, min(c0 + chunk, n_steps)):
+                burst.append(step(s))
+                e = torch.cuda.Event(enable_timing=True)
+                e.record(stream)
+                evs.append(e)
+            stream.synchronize()
+            step_ms += [evs[i].elapsed_time(evs[i + 1]) for i in range(len(evs) - 1)]
+        barrier(world)
+        clk = clocks.stop()
+        conv_jobs, conv_sweeps = store.factorize_counters(stream)
+        st = store.check_device_status(stream)
+        if st != 0:
+            raise RuntimeError(f"device status {st}: {pkv.last_error()}")
+    us = sorted(1000.0 * x for x in step_ms)
+    q = lambda f: us[min(len(us) - 1, int(round(f * (len(us) - 1))))]
+    burst_us = [1000.0 * step_ms[i] for i in range(len(step_ms)) if burst[i]]
+    plain_us = [1000.0 * step_ms[i] for i in range(len(step_ms)) if not burst[i]]
+    mean_us = barrier_max(statistics.mean(us), world)
+    extra_burst_ms = sum(burst_us) / 1000.0 - len(burst_us) * (statistics.mean(plain_us) if plain_us else 0) / 1000.0
+    return {
+        "metric": "mixed decode attention us/step (all layers, conversion included) & pages factorized/s",
+        "value": round(mean_us, 3), "unit": "us/step", "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": round(mean_us / 1000.0, 6), "higher_is_better": False,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded low-rank-plus-noise pages, RoPE keys; decode rows from the same model)",
+        "config": {"workload": wl["desc"], "global_batch": B * world, "seq_len": T0 + n_steps,
+                   "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
+                   "timing": "chunks of 16 steps behind a GPU-side sleep; per-step CUDA events"},
+        "step_latency_us": {"mean": round(statistics.mean(us), 2), "p50": round(q(0.5), 2), "p99": round(q(0.99), 2),
+                            "max": round(us[-1], 2), "burst_steps": len(burst_us),
+                            "burst_mean": round(statistics.mean(burst_us), 2) if burst_us else None,
+                            "non_burst_mean": round(statistics.mean(plain_us), 2) if plain_us else None},
+        "conversion": {"page_jobs": conv_jobs, "jacobi_sweeps_per_job": round(conv_sweeps / max(conv_jobs, 1), 2),
+                       "page_jobs_per_s_in_bursts": round(conv_jobs / extra_burst_ms * 1e3, 1) if extra_burst_ms > 0 else None},
+        "prefill_factorization": {"pages": pre_jobs, "ms": round(prefill_ms, 3),
+                                  "pages_per_s": round(pre_jobs / (prefill_ms * 1e-3), 1)},
+        "clocks": clk,
+    }
+
+
 def reference_arm(args, rank, world):
     if rank != 0:
         return None
@@ -488,6 +649,8 @@ def main():
     rank, world, local = dist_init(args.gpus)
     if args.impl == "reference":
         res = reference_arm(args, rank, world)
+    elif WORKLOADS[args.workload].get("steps"):
+        res = incremental_arm(args, rank, world, local)
     else:
         res = gpu_arm(args, rank, world, local)
     if rank == 0 and res is not None:

@@ -242,6 +242,18 @@ puzzlekv_status puzzlekv_store_stats(const puzzlekv_store *store, int32_t seq, i
 puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *store, void *stream);
 
 /*
+ * Synchronise `stream`, then read and clear the store's factorization
+ * counters: page jobs factorized (one K or one V page each) and the Jacobi
+ * sweeps they ran, summed over every factorization launch of the store
+ * (prefill, per-step and batched conversion) since the last call.  For
+ * throughput accounting (the page has no counterpart).  page_jobs and
+ * jacobi_sweeps: host pointers, both required.  The status flags read by
+ * puzzlekv_check_device_status are left untouched.
+ */
+puzzlekv_status puzzlekv_factorize_counters(puzzlekv_store *store, void *stream, int64_t *page_jobs,
+                                            int64_t *jacobi_sweeps);
+
+/*
  * Host-only page classification, the rule the store and its kernels apply
  * [PuzzleKV §3.3 ①②③, ⑤]: writes PUZZLEKV_PAGE_DENSE or
  * PUZZLEKV_PAGE_FACTORED for each of the ceil(T/P) pages of a T-token

@@ -220,3 +220,10 @@ class Store:
     def check_device_status(self, stream=None) -> int:
         """Synchronise and return the status code (raises nothing; OK = 0)."""
         return lib().puzzlekv_check_device_status(self._h, _stream(stream))
+
+    def factorize_counters(self, stream=None) -> tuple:
+        """(page jobs, Jacobi sweeps) of the store's factorization launches since
+        the last call; the counters are cleared."""
+        jobs, sweeps = ctypes.c_int64(0), ctypes.c_int64(0)
+        check(lib().puzzlekv_factorize_counters(self._h, _stream(stream), ctypes.byref(jobs), ctypes.byref(sweeps)))
+        return jobs.value, sweeps.value

@@ -30,6 +30,7 @@ EXPORTED = (
     "puzzlekv_decode_attention_static_scratch",
     "puzzlekv_store_stats",
     "puzzlekv_check_device_status",
+    "puzzlekv_factorize_counters",
     "puzzlekv_classify_pages",
     "puzzlekv_page_storage_ratio",
     "puzzlekv_last_error",
@@ -76,6 +77,7 @@ def lib() -> ctypes.CDLL:
         "puzzlekv_convert_ready_pages": ([vp, vp], i32),
         "puzzlekv_store_stats": ([vp, i32, i32, i32p, i64p, i64p, i64p], i32),
         "puzzlekv_check_device_status": ([vp, vp], i32),
+        "puzzlekv_factorize_counters": ([vp, vp, i64p, i64p], i32),
         "puzzlekv_classify_pages": ([i32, i32, i32, i32, i32p, i32], i32),
         "puzzlekv_page_storage_ratio": ([i32, i32, i32, i32], ctypes.c_double),
         "puzzlekv_last_error": ([], ctypes.c_char_p),

@@ -538,13 +538,27 @@ puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *s, void *stream) {
     int words[STATUS_WORDS] = {0};
     cudaError_t e = cudaStreamSynchronize(strm);
     if (e == cudaSuccess) e = cudaMemcpy(words, status_ptr(s), sizeof(words), cudaMemcpyDeviceToHost);
-    if (e == cudaSuccess) e = cudaMemset(status_ptr(s), 0, sizeof(words));
+    if (e == cudaSuccess) e = cudaMemset(status_ptr(s), 0, sizeof(int) * STATUS_JOBS);  // flags only
     if (e == cudaSuccess && words[STATUS_TIMEOUT])  // a CTA that gave up never took its split ticket
         e = cudaMemset(s->workspace + s->y.ticket_offset, 0, s->y.jobs_offset - s->y.ticket_offset);
     if (e != cudaSuccess) return cuda_fail(e, "status read");
     if (words[STATUS_TIMEOUT]) return fail(PUZZLEKV_ERR_DEVICE_TIMEOUT, "a kernel's bounded wait ran out");
     if (words[STATUS_NOT_CONVERGED])
         return fail(PUZZLEKV_ERR_NOT_CONVERGED, "%d page eigensolves hit the sweep cap", words[STATUS_NOT_CONVERGED]);
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_factorize_counters(puzzlekv_store *s, void *stream, int64_t *page_jobs,
+                                            int64_t *jacobi_sweeps) {
+    if (!s || !page_jobs || !jacobi_sweeps) return fail(PUZZLEKV_ERR_INVALID_ARG, "NULL argument");
+    unsigned long long c[2] = {0, 0};  // status words 2-3 and 4-5
+    static_assert(STATUS_SWEEPS == STATUS_JOBS + 2, "counter words are adjacent");
+    cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess) e = cudaMemcpy(c, status_ptr(s) + STATUS_JOBS, sizeof(c), cudaMemcpyDeviceToHost);
+    if (e == cudaSuccess) e = cudaMemset(status_ptr(s) + STATUS_JOBS, 0, sizeof(c));
+    if (e != cudaSuccess) return cuda_fail(e, "counter read");
+    *page_jobs = (int64_t)c[0];
+    *jacobi_sweeps = (int64_t)c[1];
     return PUZZLEKV_OK;
 }
 

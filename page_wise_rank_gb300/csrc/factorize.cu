@@ -275,8 +275,9 @@ __device__ __forceinline__ void store_elem(char *base, size_t idx, float v) {
     reinterpret_cast<TO *>(base)[idx] = Elem<TO>::from_f32(v);
 }
 
+// Returns the Jacobi sweeps the page took (the cap if it did not converge).
 template <typename T, int P, int D, int NT>
-__device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, long job) {
+__device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, long job) {
     const int tid = threadIdx.x;
     const JobView v = job_view(fp, job);
     load_page<T, P, D, NT>(s, v);
@@ -289,7 +290,7 @@ __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lo
         if (j > i) s.G[j][i] = s.G[i][j];
     }
     __syncthreads();
-    int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps);
+    const int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps);
     if (sweeps < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
     if (tid < P) s.lam[tid] = s.G[tid][tid];
     __syncthreads();
@@ -378,15 +379,22 @@ __device__ void factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lo
             }
         }
     }
+    return sweeps < 0 ? fp.max_sweeps : sweeps;
 }
 
 template <typename T, int P, int D, int NT>
 __global__ void __launch_bounds__(NT) factorize_kernel(const FactorParams fp) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto &s = *reinterpret_cast<FactorSmem<T, P, D> *>(smem_raw);
+    unsigned long long jobs = 0, sweeps = 0;
     for (long job = blockIdx.x; job < fp.n_jobs; job += gridDim.x) {
-        factorize_one<T, P, D, NT>(s, fp, job);
+        sweeps += (unsigned long long)factorize_one<T, P, D, NT>(s, fp, job);
+        ++jobs;
         __syncthreads();
+    }
+    if (threadIdx.x == 0 && fp.status && jobs) {  // throughput accounting, once per CTA
+        atomicAdd(reinterpret_cast<unsigned long long *>(fp.status + STATUS_JOBS), jobs);
+        atomicAdd(reinterpret_cast<unsigned long long *>(fp.status + STATUS_SWEEPS), sweeps);
     }
 }
 

@@ -110,6 +110,23 @@ def test_bf16_llama_shape_prefill_decode(pkv, T):
     run_decode_check(pkv, store, cfg, host, [1], 1, step=3, tol=TOL[torch.bfloat16])
 
 
+def test_factorize_counters_count_every_page_job(pkv):
+    """The store's factorization counters: one job per factorized K or V page
+    of every (layer, KV head), between one and the cap of sweeps each;
+    reading clears them."""
+    T = 4097
+    cfg = make_cfg(pkv, num_layers=2, num_kv_heads=4, num_q_heads=16)
+    store = pkv.Store(cfg)
+    assert store.factorize_counters() == (0, 0)
+    prefill(pkv, store, cfg, HostCache(), 0, T, rope=5e5)
+    jobs, sweeps = store.factorize_counters()
+    n_fac = int((oracle.page_kinds(T, cfg.page_size, cfg.sink_tokens, cfg.recent_tokens) == oracle.FACTORED).sum())
+    assert jobs == n_fac * cfg.num_layers * cfg.num_kv_heads * 2
+    assert jobs <= sweeps <= 24 * jobs
+    assert store.factorize_counters() == (0, 0)
+    assert store.check_device_status() == 0
+
+
 def test_bf16_gqa8_ranks_24(pkv):
     cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=16, rank_k=24, rank_v=24)
     store = pkv.Store(cfg)
