@@ -181,6 +181,17 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *store, int32_t layer, 
  * calling it once per decode step, after the last layer, is the intended use.
  * Pages whose dense slot might be reused are never listed: a page reaches
  * the window's end before its slot comes round again.
+ *   Ordering: the batch runs on a low-priority stream internal to the store,
+ *   after everything already queued on `stream`, and on at most one CTA per
+ *   SM, so that it overlaps the decode steps that follow instead of stalling
+ *   them.  A batch's factors are first read when one of its pages becomes
+ *   factorized; the first decode call (puzzlekv_decode_attention,
+ *   puzzlekv_decode_step, the static-scratch variant) that reaches that
+ *   length, and any puzzlekv_factorize_pages call, makes its own stream wait
+ *   for the batch.  puzzlekv_check_device_status and
+ *   puzzlekv_factorize_counters synchronise the internal stream as well; the
+ *   store must not be destroyed while its caller's streams still hold work
+ *   that waits on a batch.
  */
 puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *store, void *stream);
 

@@ -8,6 +8,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <climits>
 #include <cstdarg>
 #include <cstdio>
 #include <cstring>
@@ -100,7 +101,49 @@ struct puzzlekv_store {
     std::vector<int2> job_host;  // staging of the batched-conversion job list
     bool after_decode = false;   // the store's latest launch was a decode launch
     int num_sms;
+    // Batched conversions run on an internal low-priority stream.  A batch's
+    // factor records are first read when one of its pages becomes
+    // factorized, i.e. when its sequence reaches deadline[seq] tokens; the
+    // first call that attends at or past that length makes the caller's
+    // stream wait for the batch.
+    struct ConvBatch {
+        cudaEvent_t done = nullptr;
+        bool pending = false;
+        std::vector<int> deadline;  // [seq]: length at which the batch's first page is factorized
+    };
+    cudaStream_t conv_stream = nullptr;
+    cudaEvent_t conv_ready = nullptr;  // caller's stream position a batch starts after
+    std::vector<ConvBatch> batches;    // ring
+    int next_batch = 0;
+    ~puzzlekv_store() {
+        if (conv_stream) cudaStreamSynchronize(conv_stream);
+        for (auto &cb : batches)
+            if (cb.done) cudaEventDestroy(cb.done);
+        if (conv_ready) cudaEventDestroy(conv_ready);
+        if (conv_stream) cudaStreamDestroy(conv_stream);
+    }
 };
+
+constexpr int kConvBatches = 8;
+
+// Make `strm` wait for every pending background conversion batch that the
+// listed sequences (at the given lengths) reach, or for all of them when
+// `all` is set.  Returns true if a wait was inserted.
+static bool wait_conversions(puzzlekv_store *s, cudaStream_t strm, const int32_t *seq_ids, const int *lens, int B,
+                             bool all = false) {
+    bool waited = false;
+    for (auto &cb : s->batches) {
+        if (!cb.pending) continue;
+        bool due = all;
+        for (int i = 0; i < B && !due; ++i) due = lens[i] >= cb.deadline[seq_ids[i]];
+        if (due) {
+            cudaStreamWaitEvent(strm, cb.done, 0);
+            cb.pending = false;
+            waited = true;
+        }
+    }
+    return waited;
+}
 
 static int *lengths_ptr(puzzlekv_store *s) { return reinterpret_cast<int *>(s->page_table); }
 static int *desc_ptr(puzzlekv_store *s) { return reinterpret_cast<int *>(s->page_table + s->y.desc_offset); }
@@ -184,6 +227,7 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const v
     if (!k || !v || !aligned16(k) || !aligned16(v))
         return fail(PUZZLEKV_ERR_INVALID_ARG, "k and v must be non-NULL and 16-byte aligned");
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    wait_conversions(s, strm, nullptr, nullptr, 0, true);  // the slot's pages may still be read by one
     const int n_pages = (T + y.P - 1) / y.P;
     SeqInitParams ip{};
     ip.y = y;
@@ -396,6 +440,7 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *s, int32_t layer, cons
     long total;
     int max_pages;
     fill_decode_params(s, layer, q, out, seq_ids, B, 0, dp, total, max_pages);
+    if (wait_conversions(s, static_cast<cudaStream_t>(stream), seq_ids, dp.lens, B)) dp.wait_first = 1;
     cudaError_t e = launch_decode(dp, total, max_pages, s->num_sms, static_cast<cudaStream_t>(stream));
     if (e != cudaSuccess) return cuda_fail(e, "decode launch");
     s->after_decode = true;
@@ -456,6 +501,7 @@ puzzlekv_status puzzlekv_decode_step(puzzlekv_store *s, int32_t layer, const voi
         if (e != cudaSuccess) return cuda_fail(e, "conversion launch");
     }
     if (fp.n_conv > 0) dp.wait_first = 1;
+    if (wait_conversions(s, strm, seq_ids, dp.lens, B)) dp.wait_first = 1;
     e = launch_decode(dp, total, max_pages, s->num_sms, strm);
     if (e != cudaSuccess) return cuda_fail(e, "decode step launch");
     s->after_decode = true;
@@ -483,10 +529,39 @@ puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
     }
     if (s->job_host.empty()) return PUZZLEKV_OK;
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    cudaError_t e = cudaSuccess;
+    if (!s->conv_stream) {  // first batch: the internal stream (lowest priority) and its events
+        int least = 0, greatest = 0;
+        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s->conv_stream, cudaStreamNonBlocking, least);
+        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->conv_ready, cudaEventDisableTiming);
+        s->batches.resize(kConvBatches);
+        for (auto &cb : s->batches) {
+            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&cb.done, cudaEventDisableTiming);
+            cb.deadline.assign(y.Bmax, INT_MAX);
+        }
+        if (e != cudaSuccess) return cuda_fail(e, "conversion stream setup");
+    }
+    puzzlekv_store::ConvBatch &cb = s->batches[s->next_batch];
+    s->next_batch = (s->next_batch + 1) % kConvBatches;
+    if (cb.pending) {  // its event is about to be reused: order the caller's stream after it now
+        cudaStreamWaitEvent(strm, cb.done, 0);
+        cb.pending = false;
+    }
+    std::fill(cb.deadline.begin(), cb.deadline.end(), INT_MAX);
+    for (const int2 &j : s->job_host) {  // page p is factorized from length (p + 1) P + W on
+        const int b = j.x >> 8;
+        cb.deadline[b] = std::min(cb.deadline[b], (j.y + 1) * y.P + y.W);
+    }
+    // the batch reads pages the caller's stream has written: start after them
+    e = cudaEventRecord(s->conv_ready, strm);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s->conv_stream, s->conv_ready, 0);
     int2 *dev_jobs = reinterpret_cast<int2 *>(s->workspace + y.jobs_offset);
-    // pageable source: the copy has consumed job_host when cudaMemcpyAsync returns
-    cudaError_t e = cudaMemcpyAsync(dev_jobs, s->job_host.data(), s->job_host.size() * sizeof(int2),
-                                    cudaMemcpyHostToDevice, strm);
+    // the list region is reused only in the internal stream's order; pageable
+    // source: the copy has consumed job_host when cudaMemcpyAsync returns
+    if (e == cudaSuccess)
+        e = cudaMemcpyAsync(dev_jobs, s->job_host.data(), s->job_host.size() * sizeof(int2), cudaMemcpyHostToDevice,
+                            s->conv_stream);
     if (e != cudaSuccess) return cuda_fail(e, "conversion list upload");
     FactorParams fp{};
     fp.mode = FACT_MODE_CONVERT_LIST;
@@ -500,9 +575,11 @@ puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
     fp.dense_pool = s->dense_pool;
     fp.conv_list = dev_jobs;
     fp.n_jobs = (long)s->job_host.size() * y.H * 2;
-    e = launch_factorize(fp, s->num_sms, strm);
-    s->after_decode = false;
+    fp.max_ctas = s->num_sms;  // one CTA per SM: it runs beside the decode CTAs
+    e = launch_factorize(fp, s->num_sms, s->conv_stream);
+    if (e == cudaSuccess) e = cudaEventRecord(cb.done, s->conv_stream);
     if (e != cudaSuccess) return cuda_fail(e, "batched conversion launch");
+    cb.pending = true;
     return PUZZLEKV_OK;
 }
 
@@ -537,6 +614,7 @@ puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *s, void *stream) {
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     int words[STATUS_WORDS] = {0};
     cudaError_t e = cudaStreamSynchronize(strm);
+    if (e == cudaSuccess && s->conv_stream) e = cudaStreamSynchronize(s->conv_stream);
     if (e == cudaSuccess) e = cudaMemcpy(words, status_ptr(s), sizeof(words), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemset(status_ptr(s), 0, sizeof(int) * STATUS_JOBS);  // flags only
     if (e == cudaSuccess && words[STATUS_TIMEOUT])  // a CTA that gave up never took its split ticket
@@ -554,6 +632,7 @@ puzzlekv_status puzzlekv_factorize_counters(puzzlekv_store *s, void *stream, int
     unsigned long long c[2] = {0, 0};  // status words 2-3 and 4-5
     static_assert(STATUS_SWEEPS == STATUS_JOBS + 2, "counter words are adjacent");
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
+    if (e == cudaSuccess && s->conv_stream) e = cudaStreamSynchronize(s->conv_stream);
     if (e == cudaSuccess) e = cudaMemcpy(c, status_ptr(s) + STATUS_JOBS, sizeof(c), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemset(status_ptr(s) + STATUS_JOBS, 0, sizeof(c));
     if (e != cudaSuccess) return cuda_fail(e, "counter read");
@@ -629,6 +708,7 @@ extern "C" puzzlekv_status puzzlekv_decode_attention_static_scratch(puzzlekv_sto
     fill_decode_params(s, layer, q, out, seq_ids, B, 0, dp, total, max_pages);
     dp.tickets = static_cast<int *>(base);
     dp.wait_first = 1;
+    wait_conversions(s, strm, seq_ids, dp.lens, B);
     dp.partials = reinterpret_cast<float *>(static_cast<char *>(base) + ticket_bytes);
     e = launch_decode(dp, total, max_pages, s->num_sms, strm);
     if (e != cudaSuccess) return cuda_fail(e, "decode launch (static scratch)");

@@ -418,6 +418,7 @@ static cudaError_t launch_t(const FactorParams &fp, int num_sms, cudaStream_t st
     if (state != 1) return (cudaError_t)(state - 2);
     long blocks = fp.n_jobs;
     long cap = (long)num_sms * (NT >= 1024 ? 2 : 8);
+    if (fp.max_ctas > 0 && fp.max_ctas < cap) cap = fp.max_ctas;
     if (blocks > cap) blocks = cap;
     if (blocks < 1) return cudaSuccess;
     k<<<(unsigned)blocks, NT, smem, st>>>(fp);
