@@ -40,6 +40,11 @@ WORKLOADS = {
                          desc="Incremental compression during generation: Llama-3.1-8B-shaped attention, 32 layers, "
                               "8 KV / 32 query heads, d=128, bf16, batch 8, 4096-token prompts then 4096 decode steps, "
                               "P=64, rK=16, rV=24, sink 4, recent 128"),
+    "batched16": dict(layers=32, H=8, Hq=32, d=128, P=64, rk=16, rv=24, sink=4, W=128, B=16, T=32768, rope=5e5,
+                      k=12, n_out=4, steps=32, lens=(8192, 32768, 7),
+                      desc="Batched serving decode, Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query heads, "
+                           "d=128, bf16, 16 requests of U[8192, 32768] tokens (seed 7), P=64, rK=16, rV=24, sink 4, "
+                           "recent 128"),
     "qwen128k": dict(layers=64, H=8, Hq=64, d=128, P=64, rk=24, rv=24, sink=4, W=128, B=1, T=131072, rope=None,
                      k=12, n_out=4,
                      desc="Qwen3-32B-shaped attention, 64 layers, 8 KV / 64 query heads, d=128, bf16, "
@@ -482,9 +487,11 @@ def cpu_baseline_sample(wl):
             "pages_factorized_per_s": round(pages_s, 1), "pages_cores": nthreads, "pages_sample": n_pages}
 
 
-def incremental_arm(args, rank, world, local):
-    """Generation with pages converted on the decode stream as they complete:
-    per-step latency (mean, p50, p99, the conversion-burst steps) and pages/s.
+def multi_seq_arm(args, rank, world, local):
+    """Several sequences per decode call (batch 8 incremental generation, or
+    16 ragged requests): per-step latency (mean, p50, p99, the steps that
+    completed pages), the decode kernel's HBM roofline, and pages/s; pages
+    are converted on the store's internal stream as they complete.
     Steps are timed in chunks, each queued behind a GPU-side sleep, so the
     per-step CUDA-event deltas are GPU time, not host enqueue time."""
     import page_wise_rank_gb300 as pkv
@@ -499,11 +506,12 @@ def incremental_arm(args, rank, world, local):
     dev = torch.device("cuda", local)
     torch.cuda.set_device(dev)
     stream = torch.cuda.Stream(dev)
-    L, H, Hq, d, P, B, T0 = wl["layers"], wl["H"], wl["Hq"], wl["d"], wl["P"], wl["B"], wl["T"]
+    L, H, Hq, d, P, B = wl["layers"], wl["H"], wl["Hq"], wl["d"], wl["P"], wl["B"]
+    lens0 = synth.batch_lengths(B, *wl["lens"][:2], seed=wl["lens"][2]) if "lens" in wl else [wl["T"]] * B
     n_steps = args.warmup + args.steps
     cfg = pkv.StoreConfig(num_layers=L, num_kv_heads=H, num_q_heads=Hq, head_dim=d, page_size=P, rank_k=wl["rk"],
                           rank_v=wl["rv"], sink_tokens=wl["sink"], recent_tokens=wl["W"], max_batch=B,
-                          max_tokens_per_seq=T0 + n_steps + 8, kv_dtype=torch.bfloat16)
+                          max_tokens_per_seq=max(lens0) + n_steps + 8, kv_dtype=torch.bfloat16)
     spec = synth.KVSpec(layers=L, kv_heads=H, head_dim=d, page_size=P, inner_rank=wl["k"], n_outliers=wl["n_out"],
                         rope_base=wl["rope"], dtype=torch.bfloat16)
     seqs = list(range(B))
@@ -512,7 +520,7 @@ def incremental_arm(args, rank, world, local):
         prefill_ms = 0.0
         store.factorize_counters(stream)
         for i in seqs:  # prompts: one whole-cache factorization per sequence
-            K, V = synth.prefill_kv(spec, T0, seq=rank * B + i, device=dev)
+            K, V = synth.prefill_kv(spec, lens0[i], seq=rank * B + i, device=dev)
             stream.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
@@ -527,19 +535,20 @@ def incremental_arm(args, rank, world, local):
         vdec = torch.empty_like(kdec)
         for l in range(L):
             for i in seqs:
-                k, v = synth.decode_rows(spec, l, rank * B + i, T0, n_steps, device=dev)
+                k, v = synth.decode_rows(spec, l, rank * B + i, lens0[i], n_steps, device=dev)
                 kdec[l, :, i] = k.transpose(0, 1)
                 vdec[l, :, i] = v.transpose(0, 1)
         qs = [[synth.queries(B, Hq, d, step=s, layer=l).to(dev) for l in range(L)] for s in range(8)]
         out = torch.empty(L, B, Hq, d, dtype=torch.float32, device=dev)
-        T = [T0]
+        T = list(lens0)
 
         def step(s):
-            conv = (T[0] + 1) % P == 0  # this step completes a page: batched conversion
+            conv = any((t + 1) % P == 0 for t in T)  # this step completes a page: batched conversion
             for l in range(L):
                 store.decode_step(l, qs[s % 8][l], kdec[l, s], vdec[l, s], out[l], seqs, stream=stream)
             store.convert_ready_pages(stream=stream)
-            T[0] += 1
+            for i in seqs:
+                T[i] += 1
             return conv
 
         for s in range(args.warmup):
@@ -549,13 +558,14 @@ def incremental_arm(args, rank, world, local):
         clocks = ClockSampler(torch.cuda.current_device())
         clocks.start()
         barrier(world)
-        step_ms, burst = [], []
+        step_ms, burst, step_bytes = [], [], []
         chunk = 16
         for c0 in range(args.warmup, n_steps, chunk):
             torch.cuda._sleep(20_000_000)  # lets the host queue the chunk before the GPU reaches it
             evs = [torch.cuda.Event(enable_timing=True)]
             evs[0].record(stream)
             for s in range(c0, min(c0 + chunk, n_steps)):
+                step_bytes.append(sum(alg_bytes(dict(wl, B=1), t + 1) for t in T) * L)
                 burst.append(step(s))
                 e = torch.cuda.Event(enable_timing=True)
                 e.record(stream)
@@ -573,6 +583,8 @@ def incremental_arm(args, rank, world, local):
     burst_us = [1000.0 * step_ms[i] for i in range(len(step_ms)) if burst[i]]
     plain_us = [1000.0 * step_ms[i] for i in range(len(step_ms)) if not burst[i]]
     mean_us = barrier_max(statistics.mean(us), world)
+    peak, peak_kind = measured_peak_hbm()
+    achieved = sum(step_bytes) / (sum(step_ms) * 1e-3) / 1e9
     extra_burst_ms = sum(burst_us) / 1000.0 - len(burst_us) * (statistics.mean(plain_us) if plain_us else 0) / 1000.0
     return {
         "metric": "mixed decode attention us/step (all layers, conversion included) & pages factorized/s",
@@ -580,7 +592,8 @@ def incremental_arm(args, rank, world, local):
         "warmup": args.warmup, "ms_per_step": round(mean_us / 1000.0, 6), "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
         "data": "synthetic (seeded low-rank-plus-noise pages, RoPE keys; decode rows from the same model)",
-        "config": {"workload": wl["desc"], "global_batch": B * world, "seq_len": T0 + n_steps,
+        "config": {"workload": wl["desc"], "global_batch": B * world, "seq_len": max(lens0) + n_steps,
+                   "prompt_lengths": lens0,
                    "parallelism": f"replicas x{world}" if world > 1 else "single GPU",
                    "timing": "chunks of 16 steps behind a GPU-side sleep; per-step CUDA events"},
         "step_latency_us": {"mean": round(statistics.mean(us), 2), "p50": round(q(0.5), 2), "p99": round(q(0.99), 2),
@@ -593,6 +606,11 @@ def incremental_arm(args, rank, world, local):
                        "burst_step_excess_us": round(1000.0 * extra_burst_ms / max(len(burst_us), 1), 2)},
         "prefill_factorization": {"pages": pre_jobs, "ms": round(prefill_ms, 3),
                                   "pages_per_s": round(pre_jobs / (prefill_ms * 1e-3), 1)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "kernel": "decode_bf16_kernel over all layers of a step (conversion overlapped), "
+                               "algorithmic bytes of every sequence",
+                     "algorithmic_bytes_per_step": int(statistics.mean(step_bytes))},
         "clocks": clk,
     }
 
@@ -653,7 +671,7 @@ def main():
     if args.impl == "reference":
         res = reference_arm(args, rank, world)
     elif WORKLOADS[args.workload].get("steps"):
-        res = incremental_arm(args, rank, world, local)
+        res = multi_seq_arm(args, rank, world, local)
     else:
         res = gpu_arm(args, rank, world, local)
     if rank == 0 and res is not None:

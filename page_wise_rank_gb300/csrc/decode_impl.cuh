@@ -529,9 +529,8 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
     const Layout &y = prm.y;
     const int b_idx = blockIdx.z, b = prm.seqs[b_idx], h = blockIdx.y, rank = blockIdx.x;
     const int T = prm.lens[b_idx];
-    const int n_pages = (T + P - 1) / P;
-    const int ns = min((int)gridDim.x, n_pages);  // CTAs taking part for this sequence
-    if (rank >= ns) return;                       // uniform over the CTA
+    const int ns = prm.nsplit[b_idx];  // CTAs taking part for this sequence (<= its pages)
+    if (rank >= ns) return;            // uniform over the CTA
 
     const size_t stage_bytes = decode_stage_bytes<P, D>(y);
     unsigned char *stages = smem;
@@ -762,29 +761,65 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
     }
     if (setup.err != cudaSuccess) return setup.err;
     p.stages = setup.stages;
-    // one CTA per SM: a group of CTAs per (sequence, KV head), each streaming
-    // one byte-balanced range of pages; the SM's other CTA slot is left to
-    // the next launch
-    const long pairs = (long)p.nseq * y.H;
-    int group = (int)((num_sms + pairs / 2) / pairs);
-    group = group < 1 ? 1 : (group > MAX_SPLITS ? MAX_SPLITS : group);
-    group = group > max_pages ? max_pages : group;
+    // The CTAs of each KV head are shared out among the sequences in
+    // proportion to their pages (largest remainder, at least one each, at most
+    // one per page), each CTA streaming one byte-balanced range: about one CTA
+    // per SM, or two waves when the sequences' lengths are so uneven that one
+    // wave would leave a CTA with more than 1.3 times the mean load.
+    int n[MAX_CALL_BATCH];
+    {
+        long tot = 0;
+        for (int i = 0; i < p.nseq; ++i) tot += (p.lens[i] + P - 1) / P;
+        auto share_out = [&](int target) {
+            double rem[MAX_CALL_BATCH];
+            int given = 0;
+            for (int i = 0; i < p.nseq; ++i) {
+                const int pages = (p.lens[i] + P - 1) / P;
+                const double share = (double)target * pages / (double)tot;
+                n[i] = std::max(1, std::min((int)share, std::min(MAX_SPLITS, pages)));
+                rem[i] = share - (double)n[i];
+                given += n[i];
+            }
+            while (given < target) {  // the rest by largest remainder
+                int best = -1;
+                for (int i = 0; i < p.nseq; ++i)
+                    if (n[i] < std::min(MAX_SPLITS, (p.lens[i] + P - 1) / P) && (best < 0 || rem[i] > rem[best]))
+                        best = i;
+                if (best < 0) break;
+                ++n[best];
+                rem[best] -= 1.0;
+                ++given;
+            }
+            double worst = 0.0;
+            for (int i = 0; i < p.nseq; ++i) worst = std::max(worst, (double)((p.lens[i] + P - 1) / P) / n[i]);
+            return worst / ((double)tot / std::max(given, 1));  // largest load over the mean
+        };
+        const int wave = std::max(p.nseq, num_sms / y.H);
+        if (share_out(wave) > 1.3) share_out(2 * wave);
+    }
     // page bounds of every CTA, ns + 1 per call entry (fewer CTAs if they do not fit)
     for (;;) {
         int need = 0;
-        for (int i = 0; i < p.nseq; ++i) need += std::min(group, (p.lens[i] + P - 1) / P) + 1;
-        if (need <= MAX_BOUNDS || group == 1) break;
-        --group;
+        for (int i = 0; i < p.nseq; ++i) need += n[i] + 1;
+        if (need <= MAX_BOUNDS) break;
+        int big = 0;
+        for (int i = 1; i < p.nseq; ++i)
+            if (n[i] > n[big]) big = i;
+        if (n[big] == 1) return cudaErrorInvalidValue;  // cannot happen: MAX_BOUNDS >= 2 MAX_CALL_BATCH
+        --n[big];
     }
+    int group = 1;
     for (int i = 0, off = 0; i < p.nseq; ++i) {
-        const int T = p.lens[i], n = std::min(group, (T + P - 1) / P);
+        const int T = p.lens[i];
         const PageSplit split(T, P, y.sink_pages, y.sink_tokens, y.W, (long long)y.rec_bytes,
-                              (long long)P * D * 2, n);
+                              (long long)P * D * 2, n[i]);
+        p.nsplit[i] = n[i];
         p.boff[i] = off;
         p.fs[i] = split.fs;
         p.fw[i] = split.fw;
-        for (int r = 0; r <= n; ++r) p.bounds[off + r] = split.begin(r);
-        off += n + 1;
+        for (int r = 0; r <= n[i]; ++r) p.bounds[off + r] = split.begin(r);
+        off += n[i] + 1;
+        group = std::max(group, n[i]);
     }
     const int splits = group;
     cudaLaunchConfig_t cfg = {};

@@ -60,6 +60,7 @@ struct DecodeParams {
     // [bounds[boff[i] + r], bounds[boff[i] + r + 1]) (PageSplit), of which
     // [fs[i], fw[i]) are the sequence's factorized pages
     int boff[MAX_CALL_BATCH], fs[MAX_CALL_BATCH], fw[MAX_CALL_BATCH];
+    int nsplit[MAX_CALL_BATCH];     // CTAs per (sequence, KV head) of call entry i
     int bounds[MAX_BOUNDS];
     int *lengths_out, *desc_out;    // device page table (written when append)
 };

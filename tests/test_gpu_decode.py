@@ -289,3 +289,40 @@ def test_decode_step_fused_append(pkv, dtype):
         for l in range(cfg.num_layers):
             check_page_table(a, cfg, s, l, T0 + 150)
             check_page_table(c, cfg, s, l, T0 + 150)
+
+
+def test_conversion_batch_waited_at_deadline(pkv):
+    """convert_ready_pages launched on the step right before one of its pages
+    becomes factorized: the next decode_step must wait for that batch on the
+    store's internal stream.  Outputs equal, bit for bit, those of a store that
+    converts the page synchronously, and match the oracle on the stored factors."""
+    cfg = make_cfg(pkv, num_layers=1, num_kv_heads=2, num_q_heads=8, max_tokens_per_seq=1200)
+    a, b = pkv.Store(cfg), pkv.Store(cfg)
+    host = HostCache()
+    T0 = 1000  # pages 13 and 14 are complete but inside the window, not yet converted
+    spec = prefill(pkv, a, cfg, host, 0, T0)
+    K, V = synth.prefill_kv(spec, T0, seq=0)
+    b.factorize_pages(0, K.cuda(), V.cuda())
+    cache = {}
+    G = cfg.num_q_heads // cfg.num_kv_heads
+    P, W = cfg.page_size, cfg.recent_tokens
+    deadline = (13 + 1) * P + W  # length at which page 13 becomes factorized
+    for T in range(T0, deadline + 3):
+        k, v = synth.decode_tokens(spec, 0, [0], [T], cache=cache)
+        q = synth.queries(1, cfg.num_q_heads, cfg.head_dim, step=T, layer=0)
+        if T + 1 == deadline:
+            a.convert_ready_pages()  # the batch is still running when the next step needs it
+        out_a = torch.empty(1, cfg.num_q_heads, cfg.head_dim, device="cuda")
+        out_b = torch.empty_like(out_a)
+        a.decode_step(0, q.cuda(), k.cuda(), v.cuda(), out_a, [0])
+        b.decode_step(0, q.cuda(), k.cuda(), v.cuda(), out_b, [0])
+        host.append(0, 0, k[0], v[0])
+        assert torch.equal(out_a, out_b), T
+        if T + 1 >= deadline:
+            got = out_a.cpu().double().numpy()
+            for h in range(cfg.num_kv_heads):
+                ref = oracle_decode_on_store(a, cfg, host, 0, 0, h, q[0, h * G:(h + 1) * G].double().numpy())
+                assert rel_err_rows(got[0, h * G:(h + 1) * G], ref) <= TOL[torch.bfloat16]
+    assert a.check_device_status() == 0 and b.check_device_status() == 0
+    check_page_table(a, cfg, 0, 0, deadline + 3)
+
