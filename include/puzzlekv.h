@@ -129,8 +129,12 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *store, int32_t seq, con
 /*
  * Stateless batched page factorization [PuzzleKV §3.3 ③ and eq. (2)]:
  * for each of n independent pages X_i (P x d), G_i = X_i X_i^T in fp32, its
- * eigenvectors by cyclic Jacobi, L_i = top-r eigenvectors (P x r),
- * R_i = L_i^T X_i (r x d).
+ * eigenvectors by cyclic Jacobi, L_i = an orthonormal basis of the top-r
+ * eigenvector subspace (P x r), R_i = L_i^T X_i (r x d).  The eigensolve stops
+ * once no rotation could add more than 1e-5 of the energy the kept subspace
+ * leaves out (L_i R_i is then the rank-r optimum up to rounding), unless sigma
+ * is requested, in which case every eigenpair is converged and the columns
+ * of L_i are the top-r eigenvectors themselves.
  *   X:      device, [n][P][d] in x_dtype (row = token).
  *   L, R:   device, [n][P][r] and [n][r][d] in out_dtype.
  *   sigma:  device fp32 [n][P] or NULL: sqrt of the eigenvalues (clamped at

@@ -22,6 +22,9 @@
 namespace pkv {
 
 constexpr float JACOBI_TOL = 1e-6f;
+// Stop the eigensolve once the kept subspace could gain at most this fraction
+// of the energy it leaves out (reconstruction error excess about half of it).
+constexpr float SUBSPACE_TOL = 1e-5f;
 
 template <typename T, int P, int D>
 struct FactorSmem {
@@ -32,6 +35,7 @@ struct FactorSmem {
     float tn[P / 2];                 // tan of the pair's angle (0: no rotation)
     float lam[P];
     int order[P];
+    float red[64];                   // per-warp partial sums (up to 32 warps, two sums)
 };
 
 // Source page and destination of CTA `job` (mode chosen by the host).
@@ -166,8 +170,55 @@ __device__ void gram_f32(FactorSmem<float, P, D> &s) {
 // blocks of the upper triangle (each thread keeps its blocks for the whole
 // solve) and rotates pairs of eigenvector rows with 16-byte vectors.  Blocks
 // and rows of pairs that did not rotate are left alone.
+// Energy the top-r subspace of the current diagonal can still gain, over the
+// energy it leaves out: for every pair (i among the r largest diagonal
+// entries, j among the rest) the exact gain of the 2 x 2 rotation,
+// sqrt(h^2 + g_ij^2) - |h| with h = (g_ii - g_jj) / 2, summed, over the sum of
+// the left-out diagonal.  Uses s.order (free during the solve) and s.red;
+// every thread gets the result.
 template <typename T, int P, int D, int NT>
-__device__ int jacobi(FactorSmem<T, P, D> &s, int max_sweeps) {
+__device__ float subspace_gain(FactorSmem<T, P, D> &s, int r) {
+    const int tid = threadIdx.x;
+    if (tid < P) {  // rank of each diagonal entry, descending (ties: lower index first)
+        const float di = s.G[tid][tid];
+        int rk = 0;
+        for (int j = 0; j < P; ++j) {
+            const float dj = s.G[j][j];
+            rk += (dj > di) || (dj == di && j < tid);
+        }
+        s.order[rk] = tid;
+    }
+    __syncthreads();
+    float gain = 0.f, left = 0.f;
+    for (int e = tid; e < r * (P - r); e += NT) {
+        const int i = s.order[e / (P - r)], j = s.order[r + e % (P - r)];
+        const float h = 0.5f * (s.G[i][i] - s.G[j][j]);
+        const float g = i < j ? s.G[i][j] : s.G[j][i];
+        const float rad = sqrtf(fmaf(h, h, g * g));
+        gain += rad > 0.f ? g * g / (rad + fabsf(h)) : 0.f;
+    }
+    for (int k = r + tid; k < P; k += NT) left += s.G[s.order[k]][s.order[k]];
+    // block sums: warp shuffles, then one value per warp in s.lam
+    gain = warp_sum(gain);
+    left = warp_sum(left);
+    const int warp = tid >> 5, lane = tid & 31;
+    static_assert(NT / 32 <= 32, "two partial sums per warp in s.red");
+    if (lane == 0) {
+        s.red[warp] = gain;
+        s.red[32 + warp] = left;
+    }
+    __syncthreads();
+    float gs = 0.f, ls = 0.f;  // every thread sums the same values in the same order
+    for (int w = 0; w < NT / 32; ++w) {
+        gs += s.red[w];
+        ls += s.red[32 + w];
+    }
+    __syncthreads();
+    return ls > 0.f ? gs / ls : (gs > 0.f ? INFINITY : 0.f);
+}
+
+template <typename T, int P, int D, int NT>
+__device__ int jacobi(FactorSmem<T, P, D> &s, int max_sweeps, int r) {
     constexpr int NP = P / 2;
     constexpr int NBLK = NP * (NP + 1) / 2;
     constexpr int BPT = (NBLK + NT - 1) / NT;  // blocks per thread
@@ -266,6 +317,10 @@ __device__ int jacobi(FactorSmem<T, P, D> &s, int max_sweeps) {
             __syncthreads();
         }
         if (!rotated_any) return sweep + 1;
+        // only the top-r subspace is kept: stop once no rotation could add
+        // more than SUBSPACE_TOL of the energy it leaves out (rotations inside
+        // the nearly degenerate noise bulk converge slowly and change nothing)
+        if (r < P && subspace_gain<T, P, D, NT>(s, r) <= SUBSPACE_TOL) return sweep + 1;
     }
     return -1;
 }
@@ -290,7 +345,9 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
         if (j > i) s.G[j][i] = s.G[i][j];
     }
     __syncthreads();
-    const int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps);
+    // with singular values requested every eigenpair must converge; otherwise
+    // only the kept subspace has to
+    const int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps, v.sigma ? P : v.r);
     if (sweeps < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
     if (tid < P) s.lam[tid] = s.G[tid][tid];
     __syncthreads();
