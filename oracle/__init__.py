@@ -52,6 +52,13 @@ def lib() -> ctypes.CDLL:
         L.oracle_decode_head.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, ip,
                                          dp, dp, dp, dp, ctypes.c_int, dp, dp, ctypes.c_int, dp]
         L.oracle_decode_head.restype = None
+        cp = ctypes.POINTER(ctypes.c_byte)
+        L.oracle_absorb_sigma.argtypes = [dp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp, dp]
+        L.oracle_absorb_sigma.restype = None
+        L.oracle_quantize_int4.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, cp, dp]
+        L.oracle_quantize_int4.restype = None
+        L.oracle_dequantize_int4.argtypes = [cp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp]
+        L.oracle_dequantize_int4.restype = None
         _lib = L
     return _lib
 
@@ -149,6 +156,54 @@ def decode_head(q, kinds, Kd, Vd, LK, RK, LV, RV, T: int, P: int) -> np.ndarray:
     lib().oracle_decode_head(_p(q), G, d, T, P, kinds.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
                              _p(Kd), _p(Vd), _p(LK), _p(RK), rk, _p(LV), _p(RV), rv, _p(out))
     return out
+
+
+def absorb_sigma(L, R):
+    """(Lt, Rt) = (U_r Sigma^{1/2}, Sigma^{1/2} W_r^T) from the eq. (2) factors
+    L = U_r, R = Sigma_r W_r^T [PuzzleKV §4.3]."""
+    L, R = _f64(L), _f64(R)
+    P, r = L.shape
+    d = R.shape[1]
+    Lt, Rt = np.empty_like(L), np.empty_like(R)
+    lib().oracle_absorb_sigma(_p(L), _p(R), P, d, r, _p(Lt), _p(Rt))
+    return Lt, Rt
+
+
+def quantize_int4(x, per_row: bool):
+    """Symmetric INT4 codes (int8 array, values in [-7, 7]) and fp64 scales,
+    one per row (per_row) or per column [PuzzleKV §4.3]."""
+    x = _f64(x)
+    rows, cols = x.shape
+    codes = np.empty((rows, cols), dtype=np.int8)
+    scales = np.empty(rows if per_row else cols, dtype=np.float64)
+    lib().oracle_quantize_int4(_p(x), rows, cols, int(per_row), codes.ctypes.data_as(ctypes.POINTER(ctypes.c_byte)),
+                               _p(scales))
+    return codes, scales
+
+
+def dequantize_int4(codes, scales, per_row: bool) -> np.ndarray:
+    codes = np.ascontiguousarray(codes, dtype=np.int8)
+    scales = _f64(scales)
+    rows, cols = codes.shape
+    x = np.empty((rows, cols), dtype=np.float64)
+    lib().oracle_dequantize_int4(codes.ctypes.data_as(ctypes.POINTER(ctypes.c_byte)), _p(scales), rows, cols,
+                                 int(per_row), _p(x))
+    return x
+
+
+# which factor is quantized per row [PuzzleKV §4.3]: column-wise for L_K, R_K
+# and R_V, row-wise for L_V (factors in the eq. (2) orientation: L is P x r,
+# R is r x d)
+INT4_PER_ROW = {"LK": False, "RK": False, "LV": True, "RV": False}
+
+
+def int4_page_storage_ratio(P: int, d: int, rk: int, rv: int, scale_bytes: int = 2) -> float:
+    """Bytes of one page's INT4 key and value factors (4-bit codes plus one
+    scale per quantization group: r_K + d for the key, P + d for the value)
+    over the dense page pair's bf16 bytes [PuzzleKV §4.3]."""
+    codes = ((P + d) * rk + (P + d) * rv) / 2.0
+    scales = scale_bytes * ((rk + d) + (P + d))
+    return (codes + scales) / (2.0 * P * d * 2)
 
 
 def page_storage_ratio(P: int, d: int, rk: int, rv: int) -> float:

@@ -19,6 +19,9 @@
  *     every factorized page replaced by its reconstruction L R; eqs. (4)-(5)
  *     are an exact regrouping of this, so no online softmax appears here.
  *                                                   [PuzzleKV §3.2 eq. (1), §3.3 ④]
+ *   - INT4 factors: singular values absorbed into both factors, symmetric
+ *     INT4 codes with one scale per column (L_K, R_K, R_V) or per row (L_V),
+ *     and their dequantization                     [PuzzleKV §4.3]
  */
 #include <math.h>
 #include <stdlib.h>
@@ -283,4 +286,59 @@ void oracle_decode_head(const double *q, int G, int d, int T, int P,
     oracle_attention(q, K, V, G, T, d, out);
     free(K);
     free(V);
+}
+
+/*
+ * Singular values absorbed into both factors [PuzzleKV §4.3]: from
+ * L = U_r and R = Sigma_r W_r^T (the eq. (2) form), Lt = U_r Sigma_r^{1/2} and
+ * Rt = Sigma_r^{1/2} W_r^T, so that Lt Rt = L R.  Sigma_r is read off R as the
+ * norms of its rows (L has orthonormal columns); a zero row leaves both
+ * factors' j-th column / row zero.
+ *   L: [P][r], R: [r][d] in; Lt: [P][r], Rt: [r][d] out (may alias L, R).
+ */
+void oracle_absorb_sigma(const double *L, const double *R, int P, int d, int r, double *Lt, double *Rt)
+{
+    for (int j = 0; j < r; ++j) {
+        const double s = sqrt(dot(R + (size_t)j * d, R + (size_t)j * d, d));
+        const double rs = sqrt(s);
+        for (int i = 0; i < P; ++i) Lt[(size_t)i * r + j] = rs > 0.0 ? L[(size_t)i * r + j] * rs : 0.0;
+        for (int k = 0; k < d; ++k) Rt[(size_t)j * d + k] = rs > 0.0 ? R[(size_t)j * d + k] / rs : 0.0;
+    }
+}
+
+/*
+ * Symmetric INT4 quantization of one matrix [PuzzleKV §4.3]: each group (a
+ * row when per_row, else a column) gets one scale s = max|x| / 7 and codes
+ * c = round(x / s) in [-7, 7] (no zero point; the 15 symmetric levels),
+ * so that |x - c s| <= s / 2.  An all-zero group gets s = 0 and zero codes.
+ *   x: [rows][cols] in; codes: [rows][cols] out; scales: [rows] or [cols] out.
+ */
+void oracle_quantize_int4(const double *x, int rows, int cols, int per_row, signed char *codes, double *scales)
+{
+    const int ng = per_row ? rows : cols, glen = per_row ? cols : rows;
+    for (int g = 0; g < ng; ++g) {
+        double amax = 0.0;
+        for (int t = 0; t < glen; ++t) {
+            const double v = per_row ? x[(size_t)g * cols + t] : x[(size_t)t * cols + g];
+            if (fabs(v) > amax) amax = fabs(v);
+        }
+        const double s = amax / 7.0;
+        scales[g] = s;
+        for (int t = 0; t < glen; ++t) {
+            const size_t idx = per_row ? (size_t)g * cols + t : (size_t)t * cols + g;
+            double c = s > 0.0 ? nearbyint(x[idx] / s) : 0.0;
+            if (c > 7.0) c = 7.0;
+            if (c < -7.0) c = -7.0;
+            codes[idx] = (signed char)c;
+        }
+    }
+}
+
+/* x = c s, the dequantized matrix of oracle_quantize_int4's output. */
+void oracle_dequantize_int4(const signed char *codes, const double *scales, int rows, int cols, int per_row,
+                            double *x)
+{
+    for (int i = 0; i < rows; ++i)
+        for (int k = 0; k < cols; ++k)
+            x[(size_t)i * cols + k] = codes[(size_t)i * cols + k] * scales[per_row ? i : k];
 }

@@ -303,3 +303,73 @@ def test_exactly_rank_deficient_pages_converge():
             assert np.abs(L.T @ L - np.eye(r)).max() < 1e-12
             ref = np.linalg.svd(X, compute_uv=False)
             assert np.abs(S - ref).max() <= 1e-12 * ref[0]
+
+
+# ---------------------------------------------------- INT4 factors [PuzzleKV §4.3]
+
+def test_int4_quantization_bounds_and_levels():
+    """Every element within half a scale of its level; codes in [-7, 7]; the
+    largest magnitude of each group lands on +-7 exactly; zero groups stay zero;
+    brute force: each code is the nearest of the 15 symmetric levels."""
+    rng = np.random.default_rng(11)
+    for per_row in (True, False):
+        x = rng.standard_normal((9, 13)) * rng.uniform(0.1, 10.0, size=(9, 1))
+        x[3] = 0.0 if per_row else x[3]
+        if not per_row:
+            x[:, 4] = 0.0
+        c, s = oracle.quantize_int4(x, per_row)
+        xd = oracle.dequantize_int4(c, s, per_row)
+        sc = s[:, None] if per_row else s[None, :]
+        assert np.all(np.abs(x - xd) <= sc / 2 * (1 + 1e-12) + 1e-300)
+        assert c.min() >= -7 and c.max() <= 7
+        groups = x if per_row else x.T
+        codes = c if per_row else c.T
+        for g, cg, sg in zip(groups, codes, s):
+            if np.all(g == 0):
+                assert sg == 0 and np.all(cg == 0)
+                continue
+            assert sg == pytest.approx(np.abs(g).max() / 7, rel=1e-15)
+            k = np.argmax(np.abs(g))
+            assert abs(int(cg[k])) == 7 and np.sign(cg[k]) == np.sign(g[k])
+            levels = np.arange(-7, 8) * sg
+            nearest = np.abs(g[:, None] - levels[None, :]).argmin(axis=1) - 7
+            assert np.array_equal(nearest, cg)
+
+
+def test_int4_symmetric_and_scale_invariant():
+    rng = np.random.default_rng(12)
+    x = rng.standard_normal((16, 24))
+    for per_row in (True, False):
+        c, s = oracle.quantize_int4(x, per_row)
+        cn, sn = oracle.quantize_int4(-x, per_row)
+        assert np.array_equal(cn, -c) and np.array_equal(sn, s)  # symmetric: no zero point
+        c2, s2 = oracle.quantize_int4(4.0 * x, per_row)          # exact power-of-two scaling
+        assert np.array_equal(c2, c) and np.allclose(s2, 4.0 * s, rtol=0, atol=0)
+
+
+def test_int4_absorption_keeps_the_product():
+    """Lt Rt = L R; the j-th column of Lt and row of Rt both have norm
+    sqrt(sigma_j) (from the fp64 SVD); absorbing sigma instead of sigma^{1/2}
+    into L would break the column norms."""
+    X = _page(64, 128, seed=13, k=12, n_out=4)
+    r = 16
+    L, R, S = oracle.factorize(X, r)
+    Lt, Rt = oracle.absorb_sigma(L, R)
+    assert np.abs(Lt @ Rt - L @ R).max() <= 1e-12 * np.abs(L @ R).max()
+    assert np.allclose(np.linalg.norm(Lt, axis=0), np.sqrt(S[:r]), rtol=1e-12)
+    assert np.allclose(np.linalg.norm(Rt, axis=1), np.sqrt(S[:r]), rtol=1e-12)
+    wrong = L * S[:r]  # planted mistake: the whole of Sigma on L
+    assert not np.allclose(np.linalg.norm(wrong, axis=0), np.sqrt(S[:r]), rtol=1e-6)
+
+
+def test_printed_int4_storage_ratio():
+    """0.187 printed for PuzzleKV + INT4 at 16K (Table 3 setting): the whole
+    cache, with the two dense pages of the §4.1 region, at fp16 scales."""
+    g = json.load(open(GOLDEN))["storage_ratio_int4"]
+    n_pages = g["T"] // g["P"]
+    rho4 = oracle.int4_page_storage_ratio(g["P"], g["d"], g["rk"], g["rv"])
+    whole = ((n_pages - g["dense_pages"]) * rho4 + g["dense_pages"]) / n_pages
+    assert round(whole, g["printed_digits"]) == g["printed"]
+    # fp32 scales would not reproduce the printed value
+    rho32 = oracle.int4_page_storage_ratio(g["P"], g["d"], g["rk"], g["rv"], scale_bytes=4)
+    assert round(((n_pages - g["dense_pages"]) * rho32 + g["dense_pages"]) / n_pages, 3) != g["printed"]
