@@ -65,6 +65,11 @@ enum { PUZZLEKV_PAGE_FACTORED = 0, PUZZLEKV_PAGE_DENSE = 1 };
  * local window; every page holding one of the last W tokens stays dense, and
  * so does the incomplete last page [PuzzleKV §3.3 ①②③].  max_batch: number
  * of sequence slots.  max_tokens_per_seq: capacity per sequence.
+ * factor_int4: 0 = factors stored in kv_dtype; 1 = INT4 factors
+ * [PuzzleKV §4.3]: singular values absorbed into both factors
+ * (L = U Sigma^{1/2}, R = Sigma^{1/2} W^T), symmetric 4-bit codes in [-7, 7]
+ * with one fp16 scale per column of L_K, R_K, R_V and per row of L_V.
+ * Requires kv_dtype = PUZZLEKV_BF16 and rank_k, rank_v <= page_size / 2.
  */
 typedef struct {
     int32_t num_layers;
@@ -79,6 +84,7 @@ typedef struct {
     int32_t max_batch;
     int32_t max_tokens_per_seq;
     int32_t kv_dtype; /* puzzlekv_dtype */
+    int32_t factor_int4;
 } puzzlekv_config;
 
 typedef struct puzzlekv_store puzzlekv_store; /* opaque host handle */

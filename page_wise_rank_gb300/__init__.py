@@ -36,12 +36,13 @@ class StoreConfig:
     max_batch: int
     max_tokens_per_seq: int
     kv_dtype: torch.dtype = torch.bfloat16
+    factor_int4: bool = False
 
     def c(self) -> _lib.Config:
         c = _lib.Config()
         for f in _lib.Config._fields_:
             name = f[0]
-            setattr(c, name, _DT[self.kv_dtype] if name == "kv_dtype" else getattr(self, name))
+            setattr(c, name, _DT[self.kv_dtype] if name == "kv_dtype" else int(getattr(self, name)))
         return c
 
 

@@ -72,6 +72,11 @@ puzzlekv_status validate_config(const puzzlekv_config *c) {
         return fail(PUZZLEKV_ERR_INVALID_ARG, "sink_tokens and recent_tokens must be >= 0");
     if (c->kv_dtype != PUZZLEKV_F32 && c->kv_dtype != PUZZLEKV_BF16)
         return fail(PUZZLEKV_ERR_INVALID_ARG, "kv_dtype must be PUZZLEKV_F32 or PUZZLEKV_BF16");
+    if (c->factor_int4 != 0 && c->factor_int4 != 1) return fail(PUZZLEKV_ERR_INVALID_ARG, "factor_int4 must be 0 or 1");
+    if (c->factor_int4 && c->kv_dtype != PUZZLEKV_BF16)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "INT4 factors need kv_dtype = PUZZLEKV_BF16");
+    if (c->factor_int4 && (c->rank_k > c->page_size / 2 || c->rank_v > c->page_size / 2))
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "INT4 factors need rank_k, rank_v <= page_size / 2");
     if (c->max_batch > (1 << 16) || c->max_tokens_per_seq > (1 << 24) || c->num_layers > 255)
         return fail(PUZZLEKV_ERR_UNSUPPORTED, "max_batch, max_tokens_per_seq or num_layers too large");
     int P = c->page_size;
@@ -87,7 +92,8 @@ puzzlekv_status validate_config(const puzzlekv_config *c) {
 
 void layout_from(Layout &y, const puzzlekv_config *c) {
     make_layout(y, c->num_layers, c->num_kv_heads, c->num_q_heads, c->head_dim, c->page_size, c->rank_k,
-                c->rank_v, c->sink_tokens, c->recent_tokens, c->max_batch, c->max_tokens_per_seq, c->kv_dtype);
+                c->rank_v, c->sink_tokens, c->recent_tokens, c->max_batch, c->max_tokens_per_seq, c->kv_dtype,
+                c->factor_int4);
 }
 
 }  // namespace

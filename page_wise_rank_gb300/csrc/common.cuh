@@ -2,6 +2,7 @@
 // ldmatrix / mma.sync fragments, bf16 splitting, bounded waits.
 #pragma once
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -158,6 +159,28 @@ __device__ __forceinline__ void mma1688(float *d, uint32_t a0, uint32_t a1, uint
         : "r"(a0), "r"(a1), "r"(b0));
 }
 
+// The same two shapes with fp16 operands (fp32 accumulate).
+__device__ __forceinline__ void mma16816_f16(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                             uint32_t b0, uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void mma1688_f16(float *d, uint32_t a0, uint32_t a1, uint32_t b0) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k8.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5}, {%6}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(a1), "r"(b0));
+}
+
+// Pack two floats into fp16x2 (round to nearest even); `lo` goes to the low half.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
+}
+
 // Pack two floats into bf16x2 (round to nearest even); `lo` goes to the low half.
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
@@ -173,6 +196,45 @@ __device__ __forceinline__ void split_bf16(float x0, float x1, uint32_t &hi, uin
     hi = pack_bf16(x0, x1);
     lo = pack_bf16(x0 - bf16_lo_to_f32(hi), x1 - bf16_hi_to_f32(hi));
 }
+
+// fp16 counterpart of split_bf16 (about 22 bits carried by hi + lo).
+__device__ __forceinline__ void split_f16(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+    hi = pack_f16(x0, x1);
+    const float2 h = __half22float2(*reinterpret_cast<const __half2 *>(&hi));
+    lo = pack_f16(x0 - h.x, x1 - h.y);
+}
+
+// Operand traits of the tensor-core path: bf16 (stored factors and dense
+// rows) or fp16 (factors expanded from INT4 codes: code x scale keeps 14 bits,
+// of which fp16 holds 11 and bf16 only 8).
+template <bool H16>
+struct Ops;
+template <>
+struct Ops<false> {
+    static __device__ __forceinline__ void mma(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+        mma16816(d, a0, a1, a2, a3, b0, b1);
+    }
+    static __device__ __forceinline__ void mma8(float *d, uint32_t a0, uint32_t a1, uint32_t b0) {
+        mma1688(d, a0, a1, b0);
+    }
+    static __device__ __forceinline__ void split(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+        split_bf16(x0, x1, hi, lo);
+    }
+};
+template <>
+struct Ops<true> {
+    static __device__ __forceinline__ void mma(float *d, uint32_t a0, uint32_t a1, uint32_t a2, uint32_t a3,
+                                               uint32_t b0, uint32_t b1) {
+        mma16816_f16(d, a0, a1, a2, a3, b0, b1);
+    }
+    static __device__ __forceinline__ void mma8(float *d, uint32_t a0, uint32_t a1, uint32_t b0) {
+        mma1688_f16(d, a0, a1, b0);
+    }
+    static __device__ __forceinline__ void split(float x0, float x1, uint32_t &hi, uint32_t &lo) {
+        split_f16(x0, x1, hi, lo);
+    }
+};
 
 __device__ __forceinline__ float warp_max(float v) {
 #pragma unroll

@@ -25,6 +25,7 @@
 // mantissa bits and the two row halves are summed afterwards.
 // fp32 storage: CUDA-core fp32 arithmetic throughout.
 #pragma once
+#include <cuda_fp16.h>
 #include <math.h>
 
 #include <algorithm>
@@ -237,6 +238,7 @@ __device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_i
 template <int P, int D>
 struct WarpState {
     uint32_t qf[D / 16][2];  // A fragments of q (rows 0-7), k-steps of 16
+    uint32_t qh[D / 16][2];  // the same in fp16 (INT4 stores' factor contractions)
     float o[D / 8][4];       // rows 0-7: high-part products, rows 8-15: residual products
     float m, l;              // running max (log2 units) and this thread's partial sum
 };
@@ -279,7 +281,7 @@ __device__ __forceinline__ void online_softmax(WarpState<P, D> &w, float (*sv)[2
 // o += A (16 x rk, split rows) * B where B^T rows live in `rows_base`
 // (row = output column n, chunks = k in 8s), rk = 8 * nkt.
 // A fragments: av[j] = per 8-wide k tile j, (hi, lo) packed pairs.
-template <int NT_OUT, int MAXRT>
+template <int NT_OUT, int MAXRT, bool H16 = false>
 __device__ __forceinline__ void mma_rows(float (*acc)[4], const uint32_t (*ahi)[1], const uint32_t (*alo)[1],
                                          int nkt, uint32_t rows_base, int pitch, int lane) {
     const int ks_full = nkt >> 1;
@@ -294,8 +296,8 @@ __device__ __forceinline__ void mma_rows(float (*acc)[4], const uint32_t (*ahi)[
                 int ch = 2 * ks + (m & 1);
                 uint32_t r0, r1, r2, r3;
                 ldsm_x4(rows_base + swz_offset(row, ch * 16, pitch), r0, r1, r2, r3);
-                mma16816(acc[nt], a0, a1, a2, a3, r0, r1);
-                mma16816(acc[nt + 1], a0, a1, a2, a3, r2, r3);
+                Ops<H16>::mma(acc[nt], a0, a1, a2, a3, r0, r1);
+                Ops<H16>::mma(acc[nt + 1], a0, a1, a2, a3, r2, r3);
             }
         }
     }
@@ -315,15 +317,15 @@ __device__ __forceinline__ void mma_rows(float (*acc)[4], const uint32_t (*ahi)[
             uint32_t r0, r1, r2, r3;
             if (NT_OUT - nt >= 4) {
                 ldsm_x4(rows_base + swz_offset(row, j * 16, pitch), r0, r1, r2, r3);
-                mma1688(acc[nt], a0, a1, r0);
-                mma1688(acc[nt + 1], a0, a1, r1);
-                mma1688(acc[nt + 2], a0, a1, r2);
-                mma1688(acc[nt + 3], a0, a1, r3);
+                Ops<H16>::mma8(acc[nt], a0, a1, r0);
+                Ops<H16>::mma8(acc[nt + 1], a0, a1, r1);
+                Ops<H16>::mma8(acc[nt + 2], a0, a1, r2);
+                Ops<H16>::mma8(acc[nt + 3], a0, a1, r3);
             } else {
                 int row2 = 8 * (nt + (m & 1)) + (lane & 7);
                 ldsm_x2(rows_base + swz_offset(row2, j * 16, pitch), r0, r1);
-                mma1688(acc[nt], a0, a1, r0);
-                mma1688(acc[nt + 1], a0, a1, r1);
+                Ops<H16>::mma8(acc[nt], a0, a1, r0);
+                Ops<H16>::mma8(acc[nt + 1], a0, a1, r1);
             }
         }
     }
@@ -331,9 +333,13 @@ __device__ __forceinline__ void mma_rows(float (*acc)[4], const uint32_t (*ahi)[
 
 // RKT / RVT: rank tiles (ranks / 8) when fixed at compile time, 0 = read
 // from the layout (up to 8 tiles).
-template <int P, int D, int RKT, int RVT>
+// H16: the factors in shared memory are fp16 (expanded INT4 records), so
+// every contraction of the unit runs on fp16 operands.
+template <int P, int D, int RKT, int RVT, bool H16 = false>
 __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, const Layout &y, int lane,
                                               float scale_log2) {
+    using O = Ops<H16>;
+    const uint32_t(&qa)[D / 16][2] = H16 ? w.qh : w.qf;
     constexpr int MAXK = RKT ? RKT : 8, MAXV = RVT ? RVT : 8;
     const int nkt = RKT ? RKT : (y.rkp >> 3), nvt = RVT ? RVT : (y.rvp >> 3);
     const uint32_t off_RK = (uint32_t)P * nkt * 16, off_LV = off_RK + (uint32_t)nkt * 8 * D * 2;
@@ -350,19 +356,19 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
                 int row = 8 * j + (lane & 7), ch = 4 * k2 + (lane >> 3);
                 uint32_t r0, r1, r2, r3;
                 ldsm_x4(RK + swz_offset(row, ch * 16, D * 2), r0, r1, r2, r3);
-                mma16816(t[j], w.qf[2 * k2][0], 0u, w.qf[2 * k2][1], 0u, r0, r1);
-                mma16816(t[j], w.qf[2 * k2 + 1][0], 0u, w.qf[2 * k2 + 1][1], 0u, r2, r3);
+                O::mma(t[j], qa[2 * k2][0], 0u, qa[2 * k2][1], 0u, r0, r1);
+                O::mma(t[j], qa[2 * k2 + 1][0], 0u, qa[2 * k2 + 1][1], 0u, r2, r3);
             }
         }
     }
     // 2. s = t L_K^T  (16 x P), t split into high (rows 0-7) and residual (rows 8-15)
     uint32_t thi[MAXK][1], tlo[MAXK][1];
 #pragma unroll
-    for (int j = 0; j < MAXK; ++j) split_bf16(t[j][0], t[j][1], thi[j][0], tlo[j][0]);
+    for (int j = 0; j < MAXK; ++j) O::split(t[j][0], t[j][1], thi[j][0], tlo[j][0]);
     float s[P / 8][4];
 #pragma unroll
     for (int nt = 0; nt < P / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    mma_rows<P / 8, MAXK>(s, thi, tlo, nkt, LK, nkt * 16, lane);
+    mma_rows<P / 8, MAXK, H16>(s, thi, tlo, nkt, LK, nkt * 16, lane);
     float sv[P / 8][2];
 #pragma unroll
     for (int nt = 0; nt < P / 8; ++nt) {
@@ -378,23 +384,23 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
 #pragma unroll
     for (int kt = 0; kt < P / 16; ++kt) {
         uint32_t h0, l0, h1, l1;
-        split_bf16(sv[2 * kt][0], sv[2 * kt][1], h0, l0);
-        split_bf16(sv[2 * kt + 1][0], sv[2 * kt + 1][1], h1, l1);
+        O::split(sv[2 * kt][0], sv[2 * kt][1], h0, l0);
+        O::split(sv[2 * kt + 1][0], sv[2 * kt + 1][1], h1, l1);
 #pragma unroll
         for (int j = 0; j < MAXV; ++j) {
             if (j < nvt) {
                 int row = 8 * j + (lane & 7), ch = 2 * kt + ((lane >> 3) & 1);
                 uint32_t r0, r1;
                 ldsm_x2(LV + swz_offset(row, ch * 16, P * 2), r0, r1);
-                mma16816(u[j], h0, l0, h1, l1, r0, r1);
+                O::mma(u[j], h0, l0, h1, l1, r0, r1);
             }
         }
     }
     // 5. o += u R_V: A = u split by rank tiles, B = RVt rows (head dim)
     uint32_t uhi[MAXV][1], ulo[MAXV][1];
 #pragma unroll
-    for (int j = 0; j < MAXV; ++j) split_bf16(u[j][0] + u[j][2], u[j][1] + u[j][3], uhi[j][0], ulo[j][0]);
-    mma_rows<D / 8, MAXV>(w.o, uhi, ulo, nvt, RV, nvt * 16, lane);
+    for (int j = 0; j < MAXV; ++j) O::split(u[j][0] + u[j][2], u[j][1] + u[j][3], uhi[j][0], ulo[j][0]);
+    mma_rows<D / 8, MAXV, H16>(w.o, uhi, ulo, nvt, RV, nvt * 16, lane);
 }
 
 template <int P, int D>
@@ -516,12 +522,55 @@ __device__ __forceinline__ void patch_new_row(const DecodeParams &prm, unsigned 
 // rows below T - 2 (the rows the preceding launch may append are T - 2 and
 // T - 1).  L2 prefetches need no such care: L2 is the point of coherence, so
 // a row written after its prefetch is still copied fresh.
+// Expand an INT4 factor record [PuzzleKV §4.3] (4-bit codes + fp16 scales in
+// the Layout's q_off_* blocks) into the record layout at `dst` (swizzled
+// rows, the layout factored_unit reads) with fp16 elements: code x scale has
+// 14 significant bits, of which fp16 keeps 11.  One warp; each lane turns 8
+// codes of a row into one 16-byte chunk.
+template <int P, int D>
+__device__ __forceinline__ void dequant_q4(const Layout &y, const unsigned char *src, unsigned char *dst, int lane) {
+    auto expand = [&](const unsigned char *c, const __half *sc, bool per_row, int rows, int cols, unsigned char *out) {
+        const int cpr = cols >> 3, n = rows * cpr;
+        for (int e = lane; e < n; e += 32) {
+            const int row = e / cpr, cc = e - row * cpr;
+            const uint32_t wv = *reinterpret_cast<const uint32_t *>(c + ((size_t)row * cols + cc * 8) / 2);
+            float s8[8];
+            if (per_row) {
+                const float sr = __half2float(sc[row]);
+#pragma unroll
+                for (int t = 0; t < 8; ++t) s8[t] = sr;
+            } else {
+                const uint4 raw = *reinterpret_cast<const uint4 *>(sc + cc * 8);
+                const __half2 *hp = reinterpret_cast<const __half2 *>(&raw);
+#pragma unroll
+                for (int t = 0; t < 4; ++t) {
+                    const float2 f = __half22float2(hp[t]);
+                    s8[2 * t] = f.x;
+                    s8[2 * t + 1] = f.y;
+                }
+            }
+            uint32_t o[4];
+#pragma unroll
+            for (int t = 0; t < 4; ++t) {
+                const float a = (float)((int)((wv >> (8 * t)) & 15u) - 8) * s8[2 * t];
+                const float b = (float)((int)((wv >> (8 * t + 4)) & 15u) - 8) * s8[2 * t + 1];
+                o[t] = pack_f16(a, b);
+            }
+            *reinterpret_cast<uint4 *>(out + swz_offset(row, cc * 16, cols * 2)) = make_uint4(o[0], o[1], o[2], o[3]);
+        }
+    };
+    expand(src, reinterpret_cast<const __half *>(src + y.q_off_sLK), false, P, y.rkp, dst);
+    expand(src + y.q_off_RK, reinterpret_cast<const __half *>(src + y.q_off_sRK), false, y.rkp, D, dst + y.off_RK);
+    expand(src + y.q_off_LV, reinterpret_cast<const __half *>(src + y.q_off_sLV), false, y.rvp, P, dst + y.off_LV);
+    expand(src + y.q_off_RV, reinterpret_cast<const __half *>(src + y.q_off_sRV), true, D, y.rvp, dst + y.off_RV);
+}
+
 // float offset of the warp states in the ring once streaming is over (after
 // the merge scratch; a multiple of 4 floats)
 template <int D>
 __host__ __device__ constexpr int fin_comb() { return MAX_SPLITS * 8 + 8; }
 
-template <int P, int D, int RKT, int RVT>
+template <int P, int D, int RKT, int RVT, bool Q4>
 __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel(const DecodeParams prm) {
     constexpr int NWC = NWC_BF16, SPW = SLOTS_PER_WARP, NS = NWC * SPW;
     constexpr int FIN_COMB = fin_comb<D>();
@@ -534,7 +583,10 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
 
     const size_t stage_bytes = decode_stage_bytes<P, D>(y);
     unsigned char *stages = smem;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
+    // INT4 stores: each warp expands a record into its own bf16 record first
+    const size_t q16 = Q4 ? ((y.rec16_bytes + 127) & ~(size_t)127) : 0;
+    unsigned char *qstage = smem + NS * stage_bytes + (size_t)(threadIdx.x >> 5) * q16;
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes + NWC * q16);
     DecodeShared &sh = *reinterpret_cast<DecodeShared *>(full + NS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *wfull = full + warp * SPW;
@@ -622,6 +674,10 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
         for (int kk = 0; kk < D / 16; ++kk) {
             w.qf[kk][0] = g < y.G ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16 + c2) : 0u;
             w.qf[kk][1] = g < y.G ? *reinterpret_cast<const uint32_t *>(qrow + kk * 16 + 8 + c2) : 0u;
+            if constexpr (Q4) {  // bf16 -> fp16 is exact within fp16's range
+                w.qh[kk][0] = pack_f16(bf16_lo_to_f32(w.qf[kk][0]), bf16_hi_to_f32(w.qf[kk][0]));
+                w.qh[kk][1] = pack_f16(bf16_lo_to_f32(w.qf[kk][1]), bf16_hi_to_f32(w.qf[kk][1]));
+            }
         }
     }
 #pragma unroll
@@ -637,7 +693,13 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
         const int pg = info >> 2, half = info & 1;
         const uint32_t st = smem_u32(wstage + (size_t)slot * stage_bytes);
         if (!(info & 2)) {
-            factored_unit<P, D, RKT, RVT>(w, st, y, lane, scale_log2);
+            if constexpr (Q4) {
+                dequant_q4<P, D>(y, wstage + (size_t)slot * stage_bytes, qstage, lane);
+                __syncwarp();
+                factored_unit<P, D, RKT, RVT, true>(w, smem_u32(qstage), y, lane, scale_log2);
+            } else {
+                factored_unit<P, D, RKT, RVT>(w, st, y, lane, scale_log2);
+            }
         } else {
             const int valid = dense_half_valid(T, pg, P, half);
             const int first = pg * P + half * (P / 2);
@@ -719,12 +781,13 @@ struct LaunchSetup {
     cudaError_t err = cudaSuccess;
 };
 
-template <int P, int D, int RKT, int RVT>
+template <int P, int D, int RKT, int RVT, bool Q4 = false>
 cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     const Layout &y = p.y;
     const size_t stage_bytes =
         ((y.rec_bytes > (size_t)P * D * 2 ? y.rec_bytes : (size_t)P * D * 2) + 127) & ~(size_t)127;
-    auto k = decode_bf16_kernel<P, D, RKT, RVT>;
+    const size_t q16 = Q4 ? ((y.rec16_bytes + 127) & ~(size_t)127) : 0;  // per-warp bf16 record (INT4 stores)
+    auto k = decode_bf16_kernel<P, D, RKT, RVT, Q4>;
     // one set-up per (device, record size): the ring depth depends on the record size
     static std::mutex mu;
     static LaunchSetup cache[64][4];
@@ -748,7 +811,7 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
             const size_t tail_bytes = (size_t)fin_comb<D>() * 4 + (size_t)NWC_BF16 * 8 * (D + 4) * 4;
             if ((size_t)NS * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
             c.stages = NS;
-            c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared);
+            c.smem = NS * stage_bytes + NWC_BF16 * q16 + NS * sizeof(uint64_t) + sizeof(DecodeShared);
             c.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
             if (c.err == cudaSuccess &&
                 (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, NWC_BF16 * 32, c.smem) != cudaSuccess ||
@@ -842,5 +905,7 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
 cudaError_t launch_bf16_p16(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st);
 cudaError_t launch_bf16_p32(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st);
 cudaError_t launch_bf16_p64(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st);
+// INT4 factor stores, all page sizes; defined in decode_bf16_q4.cu.
+cudaError_t launch_bf16_q4(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st);
 
 }  // namespace pkv

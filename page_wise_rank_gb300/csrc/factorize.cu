@@ -14,6 +14,8 @@
 //   4. eigenvalues ranked descending (ties: lower index first);
 //   5. L = Q_r, R = Q_r^T X in fp32, written as bf16 or fp32 into either a
 //      factor record (swizzled store layout) or plain row-major arrays.
+#include <cuda_fp16.h>
+
 #include <atomic>
 
 #include "common.cuh"
@@ -330,6 +332,128 @@ __device__ __forceinline__ void store_elem(char *base, size_t idx, float v) {
     reinterpret_cast<TO *>(base)[idx] = Elem<TO>::from_f32(v);
 }
 
+// INT4 record of one page's key or value factors [PuzzleKV §4.3], from the
+// kept eigenvectors L (the first r columns of s.G, unit length) and the page
+// X (s.X):
+//   1. R = L^T X in fp32, written over X as Rf[rp][D] (X is read first; the
+//      validated ranks keep rp <= P/2, so Rf fits in X's bf16 storage);
+//   2. sigma_j = |row j of R| (R's rows are orthogonal: L holds eigenvectors),
+//      Lt = L sigma^{1/2}, Rt = sigma^{-1/2} R (zero where sigma_j = 0);
+//   3. one fp16 scale per group, max|x| / 7 rounded to fp16: columns of L_K
+//      and of R_K / R_V (head-dim columns), rows of L_V (tokens);
+//   4. codes round(x / scale) (IEEE division, round half to even) clamped to
+//      [-7, 7], stored as code + 8, two per byte, low nibble first, in the
+//      record orientation LK [P][rkp], RK [rkp][D], LVt [rvp][P], RVt [D][rvp].
+template <typename T, int P, int D, int NT>
+__device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const Layout &y) {
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    constexpr int NW = NT / 32;
+    const int r = v.r, rp = v.kind == 0 ? y.rkp : y.rvp;
+    static_assert(NT % D == 0, "one head-dim column per thread of a group");
+    constexpr int GROUPS = NT / D, QMAX = (P / 2 + GROUPS - 1) / GROUPS;
+    constexpr int PITCH = D * (int)sizeof(T);
+    // 1. projection
+    {
+        const int k = tid % D, grp = tid / D;
+        float acc[QMAX];
+#pragma unroll
+        for (int u = 0; u < QMAX; ++u) acc[u] = 0.f;
+        for (int i = 0; i < P; ++i) {
+            const float xv = Elem<T>::load(reinterpret_cast<const T *>(s.X + swz_offset(i, k * (int)sizeof(T), PITCH)));
+#pragma unroll
+            for (int u = 0; u < QMAX; ++u) {
+                const int j = grp + u * GROUPS;
+                if (j < r) acc[u] = fmaf(s.G[i][j], xv, acc[u]);
+            }
+        }
+        __syncthreads();  // every thread is done with X
+        float *Rf = reinterpret_cast<float *>(s.X);
+#pragma unroll
+        for (int u = 0; u < QMAX; ++u) {
+            const int j = grp + u * GROUPS;
+            if (j < rp) Rf[j * D + k] = j < r ? acc[u] : 0.f;
+        }
+    }
+    __syncthreads();
+    float *Rf = reinterpret_cast<float *>(s.X);
+    // 2. sigma^{1/2} per rank (one warp per row, fixed summation order)
+    for (int j = warp; j < rp; j += NW) {
+        float a = 0.f;
+        for (int k = lane; k < D; k += 32) a = fmaf(Rf[j * D + k], Rf[j * D + k], a);
+        a = warp_sum(a);
+        if (lane == 0) s.lam[j] = sqrtf(sqrtf(a));
+    }
+    __syncthreads();
+    for (int e = tid; e < P * rp; e += NT) {
+        const int i = e / rp, j = e % rp;
+        const float rs = s.lam[j];
+        s.G[i][j] = (j < r && rs > 0.f) ? s.G[i][j] * rs : 0.f;
+    }
+    for (int e = tid; e < rp * D; e += NT) {
+        const float rs = s.lam[e / D];
+        Rf[e] = rs > 0.f ? Rf[e] / rs : 0.f;
+    }
+    __syncthreads();
+    // 3. scales: fp16 in the record, their fp32 values in s.Vt for the codes
+    float *scL = &s.Vt[0][0];  // per rank (keys) or per token (values): up to P
+    float *scR = scL + P;      // per head-dim column: D
+    unsigned char *rec = reinterpret_cast<unsigned char *>(v.rec);
+    __half *hL = reinterpret_cast<__half *>(rec + (v.kind == 0 ? y.q_off_sLK : y.q_off_sLV));
+    __half *hR = reinterpret_cast<__half *>(rec + (v.kind == 0 ? y.q_off_sRK : y.q_off_sRV));
+    if (v.kind == 0) {
+        for (int j = tid; j < rp; j += NT) {  // L_K column-wise
+            float m = 0.f;
+            for (int i = 0; i < P; ++i) m = fmaxf(m, fabsf(s.G[i][j]));
+            const __half h = __float2half_rn(m / 7.f);
+            hL[j] = h;
+            scL[j] = __half2float(h);
+        }
+    } else {
+        for (int i = tid; i < P; i += NT) {  // L_V row-wise
+            float m = 0.f;
+            for (int j = 0; j < rp; ++j) m = fmaxf(m, fabsf(s.G[i][j]));
+            const __half h = __float2half_rn(m / 7.f);
+            hL[i] = h;
+            scL[i] = __half2float(h);
+        }
+    }
+    for (int k = tid; k < D; k += NT) {  // R_K and R_V column-wise
+        float m = 0.f;
+        for (int j = 0; j < rp; ++j) m = fmaxf(m, fabsf(Rf[j * D + k]));
+        const __half h = __float2half_rn(m / 7.f);
+        hR[k] = h;
+        scR[k] = __half2float(h);
+    }
+    __syncthreads();
+    // 4. codes
+    auto q = [](float x, float sc) -> unsigned {
+        int c = sc > 0.f ? (int)rintf(x / sc) : 0;
+        c = c < -7 ? -7 : (c > 7 ? 7 : c);
+        return (unsigned)(c + 8);
+    };
+    if (v.kind == 0) {
+        for (int b = tid; b < P * rp / 2; b += NT) {  // LK [P][rkp]
+            const int i = b / (rp / 2), j = (b % (rp / 2)) * 2;
+            rec[b] = (unsigned char)(q(s.G[i][j], scL[j]) | (q(s.G[i][j + 1], scL[j + 1]) << 4));
+        }
+        for (int b = tid; b < rp * D / 2; b += NT) {  // RK [rkp][D]
+            const int j = b / (D / 2), k = (b % (D / 2)) * 2;
+            rec[y.q_off_RK + b] =
+                (unsigned char)(q(Rf[j * D + k], scR[k]) | (q(Rf[j * D + k + 1], scR[k + 1]) << 4));
+        }
+    } else {
+        for (int b = tid; b < rp * P / 2; b += NT) {  // LVt [rvp][P]
+            const int j = b / (P / 2), i = (b % (P / 2)) * 2;
+            rec[y.q_off_LV + b] = (unsigned char)(q(s.G[i][j], scL[i]) | (q(s.G[i + 1][j], scL[i + 1]) << 4));
+        }
+        for (int b = tid; b < D * rp / 2; b += NT) {  // RVt [D][rvp]
+            const int k = b / (rp / 2), j = (b % (rp / 2)) * 2;
+            rec[y.q_off_RV + b] =
+                (unsigned char)(q(Rf[j * D + k], scR[k]) | (q(Rf[(j + 1) * D + k], scR[k]) << 4));
+        }
+    }
+}
+
 // Returns the Jacobi sweeps the page took (the cap if it did not converge).
 template <typename T, int P, int D, int NT>
 __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, long job) {
@@ -345,9 +469,9 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
         if (j > i) s.G[j][i] = s.G[i][j];
     }
     __syncthreads();
-    // with singular values requested every eigenpair must converge; otherwise
-    // only the kept subspace has to
-    const int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps, v.sigma ? P : v.r);
+    // with singular values requested (or absorbed into INT4 factors) every
+    // eigenpair must converge; otherwise only the kept subspace has to
+    const int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps, (v.sigma || (v.rec && fp.y.q4)) ? P : v.r);
     if (sweeps < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
     if (tid < P) s.lam[tid] = s.G[tid][tid];
     __syncthreads();
@@ -386,6 +510,10 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
 
     const Layout &y = fp.y;
     const bool rec = v.rec != nullptr;
+    if (rec && y.q4) {
+        write_q4_record<T, P, D, NT>(s, v, y);
+        return sweeps < 0 ? fp.max_sweeps : sweeps;
+    }
     const int rp = rec ? (v.kind == 0 ? y.rkp : y.rvp) : r;
     // L = Q_r  (record: keys LK[token][rank], values LVt[rank][token])
     for (int e = tid; e < P * rp; e += NT) {

@@ -153,6 +153,14 @@ struct Layout {
     int L, H, Hq, G, d, P, rk, rv, rkp, rvp, sink_tokens, W, Bmax, Tmax, esz, dtype;
     int n_pg_max, sink_pages, ring, dslots;
     size_t rec_bytes, off_RK, off_LV, off_RV;
+    // INT4 factor records [PuzzleKV §4.3] (q4 = 1): 4-bit codes (code + 8, low
+    // nibble first) of LK [P][rkp], RK [rkp][d], LVt [rvp][P], RVt [d][rvp]
+    // row-major, then fp16 scales: one per column of LK, RK and LVt (rank,
+    // head dim, token) and one per row of RVt (head dim).  rec16_bytes and
+    // off_RK / off_LV / off_RV then describe the bf16 record a decode expands
+    // an INT4 record into.
+    int q4;
+    size_t rec16_bytes, q_off_RK, q_off_LV, q_off_RV, q_off_sLK, q_off_sRK, q_off_sLV, q_off_sRV;
     size_t dense_half_bytes;  // one K or V page: P * d * esz
     size_t factor_pool_bytes, dense_pool_bytes, page_table_bytes, workspace_bytes;
     size_t desc_offset;       // byte offset of desc[] in the page table
@@ -180,7 +188,7 @@ struct Layout {
 
 // Fill a Layout from a validated configuration.
 inline void make_layout(Layout &y, int L, int H, int Hq, int d, int P, int rk, int rv, int sink, int W,
-                        int Bmax, int Tmax, int dtype) {
+                        int Bmax, int Tmax, int dtype, int q4 = 0) {
     y.L = L; y.H = H; y.Hq = Hq; y.G = Hq / H; y.d = d; y.P = P; y.rk = rk; y.rv = rv;
     y.rkp = round_up8(rk); y.rvp = round_up8(rv);
     y.sink_tokens = sink; y.W = W; y.Bmax = Bmax; y.Tmax = Tmax; y.dtype = dtype;
@@ -194,6 +202,26 @@ inline void make_layout(Layout &y, int L, int H, int Hq, int d, int P, int rk, i
     y.off_LV = y.off_RK + (size_t)y.rkp * d * e;
     y.off_RV = y.off_LV + (size_t)y.rvp * P * e;
     y.rec_bytes = y.off_RV + (size_t)d * y.rvp * e;
+    y.rec16_bytes = y.rec_bytes;
+    y.q4 = q4;
+    {  // INT4 record: code blocks, then scale blocks, each a multiple of 16 bytes
+        size_t o = (size_t)P * y.rkp / 2;
+        y.q_off_RK = o;
+        o += (size_t)y.rkp * d / 2;
+        y.q_off_LV = o;
+        o += (size_t)y.rvp * P / 2;
+        y.q_off_RV = o;
+        o += (size_t)d * y.rvp / 2;
+        y.q_off_sLK = o;
+        o += (size_t)y.rkp * 2;
+        y.q_off_sRK = o;
+        o += (size_t)d * 2;
+        y.q_off_sLV = o;
+        o += (size_t)P * 2;
+        y.q_off_sRV = o;
+        o += (size_t)d * 2;
+        if (q4) y.rec_bytes = o;
+    }
     y.dense_half_bytes = (size_t)P * d * e;
     y.factor_pool_bytes = (size_t)L * Bmax * H * y.n_pg_max * y.rec_bytes;
     y.dense_pool_bytes = (size_t)L * Bmax * y.dslots * H * 2 * y.dense_half_bytes;

@@ -34,6 +34,17 @@ class Layout:
         self.off_LV = self.off_RK + self.rkp * self.d * e
         self.off_RV = self.off_LV + self.rvp * self.P * e
         self.rec_bytes = self.off_RV + self.d * self.rvp * e
+        self.q4 = bool(getattr(cfg, "factor_int4", False))
+        if self.q4:  # INT4 record: code blocks, then fp16 scale blocks
+            P, d, rkp, rvp = self.P, self.d, self.rkp, self.rvp
+            self.q_off_RK = P * rkp // 2
+            self.q_off_LV = self.q_off_RK + rkp * d // 2
+            self.q_off_RV = self.q_off_LV + rvp * P // 2
+            self.q_off_sLK = self.q_off_RV + d * rvp // 2
+            self.q_off_sRK = self.q_off_sLK + 2 * rkp
+            self.q_off_sLV = self.q_off_sRK + 2 * d
+            self.q_off_sRV = self.q_off_sLV + 2 * P
+            self.rec_bytes = self.q_off_sRV + 2 * d
         self.desc_offset = (self.Bmax * self.L * 4 + 255) // 256 * 256
 
     def record_offset(self, l, b, h, p):
@@ -84,8 +95,33 @@ def read_factors(fp_bytes: np.ndarray, lay: Layout, l: int, b: int, h: int, p: i
     return read_record(fp_bytes[o:o + lay.rec_bytes], lay)
 
 
+def q4_codes(raw: np.ndarray, rows: int, cols: int) -> np.ndarray:
+    """Signed INT4 codes of a row-major [rows][cols] block (code + 8, low nibble first)."""
+    b = np.asarray(raw, dtype=np.uint8)[: rows * cols // 2]
+    n = np.empty(rows * cols, dtype=np.int16)
+    n[0::2] = b & 15
+    n[1::2] = b >> 4
+    return (n - 8).reshape(rows, cols).astype(np.int8)
+
+
+def read_record_q4(rec: np.ndarray, lay: Layout):
+    """INT4 record -> codes and fp16 scales of each factor, as a dict
+    {name: (codes [rows][cols] int8, scales fp64, per_row)} in the record orientation."""
+    P, d, rkp, rvp = lay.P, lay.d, lay.rkp, lay.rvp
+    sc = lambda off, n: np.frombuffer(rec[off:off + 2 * n].tobytes(), dtype=np.float16).astype(np.float64)
+    return {"LK": (q4_codes(rec[:], P, rkp), sc(lay.q_off_sLK, rkp), False),
+            "RK": (q4_codes(rec[lay.q_off_RK:], rkp, d), sc(lay.q_off_sRK, d), False),
+            "LVt": (q4_codes(rec[lay.q_off_LV:], rvp, P), sc(lay.q_off_sLV, P), False),
+            "RVt": (q4_codes(rec[lay.q_off_RV:], d, rvp), sc(lay.q_off_sRV, d), True)}
+
+
 def read_record(rec: np.ndarray, lay: Layout):
-    """Factors of one record given its rec_bytes bytes, fp64."""
+    """Factors of one record given its rec_bytes bytes, fp64 (INT4 records dequantized exactly)."""
+    if lay.q4:
+        q = read_record_q4(rec, lay)
+        deq = {k: c.astype(np.float64) * (s[:, None] if per_row else s[None, :]) for k, (c, s, per_row) in q.items()}
+        return (deq["LK"][:, : lay.rk], deq["RK"][: lay.rk], deq["LVt"][: lay.rv].T.copy(),
+                deq["RVt"][:, : lay.rv].T.copy())
     e, P, d = lay.esz, lay.P, lay.d
     LK = unswizzle(rec[: lay.off_RK], P, lay.rkp, e, lay.dtype)[:, : lay.rk]
     RK = unswizzle(rec[lay.off_RK: lay.off_LV], lay.rkp, d, e, lay.dtype)[: lay.rk]

@@ -70,10 +70,26 @@ def test_query_sizes(pkv):
     assert s["workspace"] >= 256 + 32 * 128 * 130 * 4
 
 
+def test_query_sizes_int4(pkv):
+    """INT4 records: 4-bit codes of the four factors plus fp16 scales (r_K + d
+    for the key, P + d for the value) -- the Python layout mirror agrees."""
+    import oracle
+    from store_layout import Layout
+    cfg = _cfg(pkv, factor_int4=True)
+    s = pkv.query_sizes(cfg)
+    n_pg = (cfg.max_tokens_per_seq + 63) // 64
+    rec = (16 + 24) * (64 + 128) // 2 + 2 * ((16 + 128) + (64 + 128))
+    assert Layout(cfg).rec_bytes == rec
+    assert s["factor_pool"] == 32 * 1 * 8 * n_pg * rec
+    # the same bytes as the page's storage-ratio accounting (fp16 scales)
+    assert rec / (2 * 64 * 128 * 2) == pytest.approx(oracle.int4_page_storage_ratio(64, 128, 16, 24))
+
+
 @pytest.mark.parametrize("bad,status", [
     (dict(head_dim=96), 2), (dict(page_size=128), 2), (dict(num_q_heads=33), 1),
     (dict(num_q_heads=8 * 16), 2), (dict(rank_k=0), 1), (dict(rank_v=65), 1),
     (dict(sink_tokens=-1), 1), (dict(max_batch=0), 1),
+    (dict(factor_int4=True, kv_dtype=torch.float32), 2), (dict(factor_int4=True, rank_v=40), 2),
 ])
 def test_config_validation(pkv, bad, status):
     with pytest.raises(pkv.PuzzleKVError) as e:
