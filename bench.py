@@ -45,6 +45,10 @@ WORKLOADS = {
                       desc="Batched serving decode, Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query heads, "
                            "d=128, bf16, 16 requests of U[8192, 32768] tokens (seed 7), P=64, rK=16, rV=24, sink 4, "
                            "recent 128"),
+    "llama32k-int4": dict(layers=32, H=8, Hq=32, d=128, P=64, rk=16, rv=24, sink=4, W=128, B=1, T=32768, rope=5e5,
+                          k=12, n_out=4, int4=True,
+                          desc="Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query heads, d=128, bf16, "
+                               "T=32768, batch 1, P=64, rK=16, rV=24, sink 4, recent 128, INT4 factors"),
     "qwen128k": dict(layers=64, H=8, Hq=64, d=128, P=64, rk=24, rv=24, sink=4, W=128, B=1, T=131072, rope=None,
                      k=12, n_out=4,
                      desc="Qwen3-32B-shaped attention, 64 layers, 8 KV / 64 query heads, d=128, bf16, "
@@ -112,7 +116,7 @@ def measured_peak_hbm():
 
 # the sources the bf16 decode kernel is built from (a recorded ncu traffic
 # figure is reported only while they are unchanged)
-DECODE_SOURCES = ("decode_impl.cuh", "decode_bf16_p64.cu", "common.cuh", "layout.h", "kernels.h")
+DECODE_SOURCES = ("decode_impl.cuh", "decode_bf16_p64.cu", "decode_bf16_q4.cu", "common.cuh", "layout.h", "kernels.h")
 
 
 def source_hash(names):
@@ -218,7 +222,11 @@ def alg_bytes(wl, T, esz=2):
     kinds = pkv.classify_pages(T, wl["P"], wl["sink"], wl["W"])
     n_fac = int((kinds == pkv.PAGE_FACTORED).sum())
     n_dense_tok = T - n_fac * wl["P"]
-    per_head = n_fac * (wl["rk"] + wl["rv"]) * (wl["P"] + wl["d"]) * esz + n_dense_tok * 2 * wl["d"] * esz
+    if wl.get("int4"):  # 4-bit codes of both factors plus fp16 scales (r_K + d for K, P + d for V)
+        fac = (wl["rk"] + wl["rv"]) * (wl["P"] + wl["d"]) / 2 + 2 * ((wl["rk"] + wl["d"]) + (wl["P"] + wl["d"]))
+    else:
+        fac = (wl["rk"] + wl["rv"]) * (wl["P"] + wl["d"]) * esz
+    per_head = n_fac * fac + n_dense_tok * 2 * wl["d"] * esz
     return wl["B"] * (wl["H"] * per_head + wl["Hq"] * wl["d"] * (esz + 4))
 
 
@@ -239,7 +247,8 @@ def gpu_arm(args, rank, world, local):
     n_steps_total = args.warmup + args.steps * (1 if args.no_e2e else 2) + min(args.steps, 8)
     cfg = pkv.StoreConfig(num_layers=L, num_kv_heads=H, num_q_heads=Hq, head_dim=d, page_size=P, rank_k=wl["rk"],
                           rank_v=wl["rv"], sink_tokens=wl["sink"], recent_tokens=wl["W"], max_batch=B,
-                          max_tokens_per_seq=T0 + n_steps_total + 8, kv_dtype=torch.bfloat16)
+                          max_tokens_per_seq=T0 + n_steps_total + 8, kv_dtype=torch.bfloat16,
+                          factor_int4=bool(wl.get("int4")))
     spec = synth.KVSpec(layers=L, kv_heads=H, head_dim=d, page_size=P, inner_rank=wl["k"], n_outliers=wl["n_out"],
                         rope_base=wl["rope"], dtype=torch.bfloat16)
     with torch.cuda.stream(stream):
