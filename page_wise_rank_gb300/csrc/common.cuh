@@ -204,9 +204,40 @@ __device__ __forceinline__ void split_f16(float x0, float x1, uint32_t &hi, uint
     lo = pack_f16(x0 - h.x, x1 - h.y);
 }
 
+// INT4 codes -> fp16x2 tensor-core operands.  An fp16 with biased exponent
+// 25 (bit pattern 0x6400 = 1024) has a unit-spaced mantissa, so OR-ing a
+// nibble n into mantissa bits 0-3 gives exactly 1024 + n and into bits 4-7
+// exactly 1024 + 16 n; subtracting 1032, or multiplying by 1/16 and adding
+// -72, leaves the code n - 8 exactly.  Each form converts two nibbles, one per
+// 16-bit half of the word.
+__device__ __forceinline__ uint32_t q4_pair_lo(uint32_t x) {  // nibbles at bits 0-3 and 16-19
+    const uint32_t t = (x & 0x000F000Fu) | 0x64006400u, bias = 0x64086408u;  // 1032, 1032
+    uint32_t h;
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(h) : "r"(t), "r"(bias));
+    return h;
+}
+__device__ __forceinline__ uint32_t q4_pair_hi(uint32_t x) {  // nibbles at bits 4-7 and 20-23
+    const uint32_t t = (x & 0x00F000F0u) | 0x64006400u, k = 0x2C002C00u, b = 0xD480D480u;  // 1/16, -72
+    uint32_t h;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(h) : "r"(t), "r"(k), "r"(b));
+    return h;
+}
+// Register r (0..3) of a word of an INT4 operand stream: nibbles r and r + 4.
+__device__ __forceinline__ uint32_t q4_reg(uint32_t w, int r) {
+    const uint32_t x = w >> ((r & 2) << 2);
+    return (r & 1) ? q4_pair_hi(x) : q4_pair_lo(x);
+}
+
+// a * b as an fp16x2 high part and its exact residual (the fused multiply-add
+// of a, b and -hi; exact unless the residual is subnormal).
+__device__ __forceinline__ void mul_split_f16(uint32_t a, uint32_t b, uint32_t &hi, uint32_t &lo) {
+    asm("mul.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(a), "r"(b));
+    const uint32_t nhi = hi ^ 0x80008000u;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(lo) : "r"(a), "r"(b), "r"(nhi));
+}
+
 // Operand traits of the tensor-core path: bf16 (stored factors and dense
-// rows) or fp16 (factors expanded from INT4 codes: code x scale keeps 14 bits,
-// of which fp16 holds 11 and bf16 only 8).
+// rows) or fp16 (INT4 codes, exact in fp16, against fp16 split operands).
 template <bool H16>
 struct Ops;
 template <>

@@ -238,7 +238,7 @@ __device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_i
 template <int P, int D>
 struct WarpState {
     uint32_t qf[D / 16][2];  // A fragments of q (rows 0-7), k-steps of 16
-    uint32_t qh[D / 16][2];  // the same in fp16 (INT4 stores' factor contractions)
+    uint32_t qh[D / 16][2];  // the same in fp16 (INT4 stores)
     float o[D / 8][4];       // rows 0-7: high-part products, rows 8-15: residual products
     float m, l;              // running max (log2 units) and this thread's partial sum
 };
@@ -281,7 +281,7 @@ __device__ __forceinline__ void online_softmax(WarpState<P, D> &w, float (*sv)[2
 // o += A (16 x rk, split rows) * B where B^T rows live in `rows_base`
 // (row = output column n, chunks = k in 8s), rk = 8 * nkt.
 // A fragments: av[j] = per 8-wide k tile j, (hi, lo) packed pairs.
-template <int NT_OUT, int MAXRT, bool H16 = false>
+template <int NT_OUT, int MAXRT>
 __device__ __forceinline__ void mma_rows(float (*acc)[4], const uint32_t (*ahi)[1], const uint32_t (*alo)[1],
                                          int nkt, uint32_t rows_base, int pitch, int lane) {
     const int ks_full = nkt >> 1;
@@ -296,8 +296,8 @@ __device__ __forceinline__ void mma_rows(float (*acc)[4], const uint32_t (*ahi)[
                 int ch = 2 * ks + (m & 1);
                 uint32_t r0, r1, r2, r3;
                 ldsm_x4(rows_base + swz_offset(row, ch * 16, pitch), r0, r1, r2, r3);
-                Ops<H16>::mma(acc[nt], a0, a1, a2, a3, r0, r1);
-                Ops<H16>::mma(acc[nt + 1], a0, a1, a2, a3, r2, r3);
+                Ops<false>::mma(acc[nt], a0, a1, a2, a3, r0, r1);
+                Ops<false>::mma(acc[nt + 1], a0, a1, a2, a3, r2, r3);
             }
         }
     }
@@ -317,15 +317,15 @@ __device__ __forceinline__ void mma_rows(float (*acc)[4], const uint32_t (*ahi)[
             uint32_t r0, r1, r2, r3;
             if (NT_OUT - nt >= 4) {
                 ldsm_x4(rows_base + swz_offset(row, j * 16, pitch), r0, r1, r2, r3);
-                Ops<H16>::mma8(acc[nt], a0, a1, r0);
-                Ops<H16>::mma8(acc[nt + 1], a0, a1, r1);
-                Ops<H16>::mma8(acc[nt + 2], a0, a1, r2);
-                Ops<H16>::mma8(acc[nt + 3], a0, a1, r3);
+                Ops<false>::mma8(acc[nt], a0, a1, r0);
+                Ops<false>::mma8(acc[nt + 1], a0, a1, r1);
+                Ops<false>::mma8(acc[nt + 2], a0, a1, r2);
+                Ops<false>::mma8(acc[nt + 3], a0, a1, r3);
             } else {
                 int row2 = 8 * (nt + (m & 1)) + (lane & 7);
                 ldsm_x2(rows_base + swz_offset(row2, j * 16, pitch), r0, r1);
-                Ops<H16>::mma8(acc[nt], a0, a1, r0);
-                Ops<H16>::mma8(acc[nt + 1], a0, a1, r1);
+                Ops<false>::mma8(acc[nt], a0, a1, r0);
+                Ops<false>::mma8(acc[nt + 1], a0, a1, r1);
             }
         }
     }
@@ -333,13 +333,11 @@ __device__ __forceinline__ void mma_rows(float (*acc)[4], const uint32_t (*ahi)[
 
 // RKT / RVT: rank tiles (ranks / 8) when fixed at compile time, 0 = read
 // from the layout (up to 8 tiles).
-// H16: the factors in shared memory are fp16 (expanded INT4 records), so
-// every contraction of the unit runs on fp16 operands.
-template <int P, int D, int RKT, int RVT, bool H16 = false>
+template <int P, int D, int RKT, int RVT>
 __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, const Layout &y, int lane,
                                               float scale_log2) {
-    using O = Ops<H16>;
-    const uint32_t(&qa)[D / 16][2] = H16 ? w.qh : w.qf;
+    using O = Ops<false>;
+    const uint32_t(&qa)[D / 16][2] = w.qf;
     constexpr int MAXK = RKT ? RKT : 8, MAXV = RVT ? RVT : 8;
     const int nkt = RKT ? RKT : (y.rkp >> 3), nvt = RVT ? RVT : (y.rvp >> 3);
     const uint32_t off_RK = (uint32_t)P * nkt * 16, off_LV = off_RK + (uint32_t)nkt * 8 * D * 2;
@@ -368,7 +366,7 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
     float s[P / 8][4];
 #pragma unroll
     for (int nt = 0; nt < P / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
-    mma_rows<P / 8, MAXK, H16>(s, thi, tlo, nkt, LK, nkt * 16, lane);
+    mma_rows<P / 8, MAXK>(s, thi, tlo, nkt, LK, nkt * 16, lane);
     float sv[P / 8][2];
 #pragma unroll
     for (int nt = 0; nt < P / 8; ++nt) {
@@ -400,7 +398,7 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
     uint32_t uhi[MAXV][1], ulo[MAXV][1];
 #pragma unroll
     for (int j = 0; j < MAXV; ++j) O::split(u[j][0] + u[j][2], u[j][1] + u[j][3], uhi[j][0], ulo[j][0]);
-    mma_rows<D / 8, MAXV, H16>(w.o, uhi, ulo, nvt, RV, nvt * 16, lane);
+    mma_rows<D / 8, MAXV>(w.o, uhi, ulo, nvt, RV, nvt * 16, lane);
 }
 
 template <int P, int D>
@@ -467,6 +465,156 @@ __device__ __forceinline__ void dense_unit(WarpState<P, D> &w, uint32_t st, int 
 }
 
 
+// One factorized page from an INT4 record [PuzzleKV §4.3] in shared memory.
+// The codes enter the fp16 tensor-core products as exact small integers
+// (layout.h: tensor-core operand order) and every scale is folded into the
+// small operand beside it:
+//   t = (q o s_RK) C_RK^T,  s = (t o s_LK) C_LK^T,
+//   u = (p o s_LV) C_LV,    o += (u C_RV) o s_RV
+// (o: elementwise; C: the code matrices), each scaled operand carried as an
+// fp16 high part (rows 0-7) and residual (rows 8-15) of its m16 tile, so the
+// products keep about 22 bits.  RKT / RVT: rank tiles when fixed at compile
+// time, 0 = from the layout (INT4 ranks are at most P / 2).
+template <int P, int D, int RKT, int RVT>
+__device__ __forceinline__ void factored_unit_q4(WarpState<P, D> &w, const unsigned char *rec, const Layout &y,
+                                                 int lane, float scale_log2) {
+    using O = Ops<true>;
+    constexpr int MAXK = RKT ? RKT : P / 16, MAXV = RVT ? RVT : P / 16;
+    const int nkt = RKT ? RKT : (y.rkp >> 3), nvt = RVT ? RVT : (y.rvp >> 3);
+    const int c = lane & 3;
+    // word wd of this lane's part of a stream: slab wd / 2, word wd % 2
+    const uint32_t *ks_ = reinterpret_cast<const uint32_t *>(rec) + 2 * lane;
+    const uint32_t *vs_ = reinterpret_cast<const uint32_t *>(rec + y.q_off_V) + 2 * lane;
+    auto breg = [](const uint32_t *st, int m) -> uint32_t {
+        const int wd = m >> 2;
+        return q4_reg(st[(wd >> 1) * 64 + (wd & 1)], m & 3);
+    };
+    // 1. t = (q o s_RK) C_RK^T: A = q o s_RK over the head dim (k-step ks holds
+    // columns 16 ks + 2c, +1 and 16 ks + 8 + 2c, +1: one uint2 of lane c's scales)
+    const uint2 *sRK = reinterpret_cast<const uint2 *>(rec + y.q_off_sRK) + c * (D / 16);
+    float t[MAXK][4];
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) t[j][0] = t[j][1] = t[j][2] = t[j][3] = 0.f;
+#pragma unroll
+    for (int ks = 0; ks < D / 16; ++ks) {
+        const uint2 sc = sRK[ks];
+        uint32_t h0, l0, h1, l1;
+        mul_split_f16(w.qh[ks][0], sc.x, h0, l0);
+        mul_split_f16(w.qh[ks][1], sc.y, h1, l1);
+#pragma unroll
+        for (int j = 0; j < MAXK; ++j)
+            if (j < nkt) {
+                const int m = 2 * (ks * nkt + j);
+                O::mma(t[j], h0, l0, h1, l1, breg(ks_, m), breg(ks_, m + 1));
+            }
+    }
+    // 2. s = (t o s_LK) C_LK^T: this lane holds rank columns 8j + 2c, +1
+    const __half2 *sLK = reinterpret_cast<const __half2 *>(rec + y.q_off_sLK) + c * nkt;
+    uint32_t thi[MAXK][1], tlo[MAXK][1];
+#pragma unroll
+    for (int j = 0; j < MAXK; ++j) {
+        thi[j][0] = tlo[j][0] = 0u;
+        if (j < nkt) {
+            const float2 sc = __half22float2(sLK[j]);
+            O::split((t[j][0] + t[j][2]) * sc.x, (t[j][1] + t[j][3]) * sc.y, thi[j][0], tlo[j][0]);
+        }
+    }
+    float s[P / 8][4];
+#pragma unroll
+    for (int nt = 0; nt < P / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+    {
+        const int m0 = nkt * (D / 8), kf = nkt >> 1;  // L_K's first register; full k-steps
+#pragma unroll
+        for (int ks = 0; ks < MAXK / 2; ++ks)
+            if (ks < kf) {
+#pragma unroll
+                for (int nt = 0; nt < P / 8; ++nt) {
+                    const int m = m0 + ks * (P / 4) + 2 * nt;
+                    O::mma(s[nt], thi[2 * ks][0], tlo[2 * ks][0], thi[2 * ks + 1][0], tlo[2 * ks + 1][0],
+                           breg(ks_, m), breg(ks_, m + 1));
+                }
+            }
+        if (nkt & 1) {
+            uint32_t a0 = 0u, a1 = 0u;
+#pragma unroll
+            for (int jj = 0; jj < MAXK; ++jj)  // static register indices only
+                if (jj == nkt - 1) {
+                    a0 = thi[jj][0];
+                    a1 = tlo[jj][0];
+                }
+#pragma unroll
+            for (int nt = 0; nt < P / 8; ++nt) O::mma8(s[nt], a0, a1, breg(ks_, m0 + kf * (P / 4) + nt));
+        }
+    }
+    float sv[P / 8][2];
+#pragma unroll
+    for (int nt = 0; nt < P / 8; ++nt) {
+        sv[nt][0] = (s[nt][0] + s[nt][2]) * scale_log2;
+        sv[nt][1] = (s[nt][1] + s[nt][3]) * scale_log2;
+    }
+    // 3. page-local softmax state merged into the running one
+    online_softmax<P, D>(w, sv, P / 8);
+    // 4. u = (p o s_LV) C_LV: this lane holds tokens 8nt + 2c, +1
+    const __half2 *sLV = reinterpret_cast<const __half2 *>(rec + y.q_off_sLV) + c * (P / 8);
+    float u[MAXV][4];
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) u[j][0] = u[j][1] = u[j][2] = u[j][3] = 0.f;
+#pragma unroll
+    for (int kt = 0; kt < P / 16; ++kt) {
+        const float2 s0 = __half22float2(sLV[2 * kt]), s1 = __half22float2(sLV[2 * kt + 1]);
+        uint32_t h0, l0, h1, l1;
+        O::split(sv[2 * kt][0] * s0.x, sv[2 * kt][1] * s0.y, h0, l0);
+        O::split(sv[2 * kt + 1][0] * s1.x, sv[2 * kt + 1][1] * s1.y, h1, l1);
+#pragma unroll
+        for (int j = 0; j < MAXV; ++j)
+            if (j < nvt) {
+                const int m = 2 * (kt * nvt + j);
+                O::mma(u[j], h0, l0, h1, l1, breg(vs_, m), breg(vs_, m + 1));
+            }
+    }
+    // 5. o += (u C_RV) o s_RV, four head-dim tiles at a time
+    uint32_t uhi[MAXV][1], ulo[MAXV][1];
+#pragma unroll
+    for (int j = 0; j < MAXV; ++j) O::split(u[j][0] + u[j][2], u[j][1] + u[j][3], uhi[j][0], ulo[j][0]);
+    const __half2 *sRV = reinterpret_cast<const __half2 *>(rec + y.q_off_sRV) + c * (D / 8);
+    const int m0 = nvt * (P / 8), kf = nvt >> 1;  // R_V's first register; full k-steps
+    uint32_t a0 = 0u, a1 = 0u;                    // the 8-wide last k-step's operand
+#pragma unroll
+    for (int jj = 0; jj < MAXV; ++jj)
+        if (jj == nvt - 1) {
+            a0 = uhi[jj][0];
+            a1 = ulo[jj][0];
+        }
+#pragma unroll
+    for (int n0 = 0; n0 < D / 8; n0 += 4) {
+        float acc[4][4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < MAXV / 2; ++ks)
+            if (ks < kf) {
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int m = m0 + ks * (D / 4) + 2 * (n0 + i);
+                    O::mma(acc[i], uhi[2 * ks][0], ulo[2 * ks][0], uhi[2 * ks + 1][0], ulo[2 * ks + 1][0],
+                           breg(vs_, m), breg(vs_, m + 1));
+                }
+            }
+        if (nvt & 1) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) O::mma8(acc[i], a0, a1, breg(vs_, m0 + kf * (D / 4) + n0 + i));
+        }
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float2 sc = __half22float2(sRV[n0 + i]);
+            w.o[n0 + i][0] = fmaf(acc[i][0], sc.x, w.o[n0 + i][0]);
+            w.o[n0 + i][1] = fmaf(acc[i][1], sc.y, w.o[n0 + i][1]);
+            w.o[n0 + i][2] = fmaf(acc[i][2], sc.x, w.o[n0 + i][2]);
+            w.o[n0 + i][3] = fmaf(acc[i][3], sc.y, w.o[n0 + i][3]);
+        }
+    }
+}
+
 // Fused append: page-table record of the call's new token (position T - 1),
 // written by one thread per sequence.  Nothing in this launch reads it.
 __device__ inline void append_page_table(const DecodeParams &prm, int b_idx, int b, int T) {
@@ -522,49 +670,6 @@ __device__ __forceinline__ void patch_new_row(const DecodeParams &prm, unsigned 
 // rows below T - 2 (the rows the preceding launch may append are T - 2 and
 // T - 1).  L2 prefetches need no such care: L2 is the point of coherence, so
 // a row written after its prefetch is still copied fresh.
-// Expand an INT4 factor record [PuzzleKV §4.3] (4-bit codes + fp16 scales in
-// the Layout's q_off_* blocks) into the record layout at `dst` (swizzled
-// rows, the layout factored_unit reads) with fp16 elements: code x scale has
-// 14 significant bits, of which fp16 keeps 11.  One warp; each lane turns 8
-// codes of a row into one 16-byte chunk.
-template <int P, int D>
-__device__ __forceinline__ void dequant_q4(const Layout &y, const unsigned char *src, unsigned char *dst, int lane) {
-    auto expand = [&](const unsigned char *c, const __half *sc, bool per_row, int rows, int cols, unsigned char *out) {
-        const int cpr = cols >> 3, n = rows * cpr;
-        for (int e = lane; e < n; e += 32) {
-            const int row = e / cpr, cc = e - row * cpr;
-            const uint32_t wv = *reinterpret_cast<const uint32_t *>(c + ((size_t)row * cols + cc * 8) / 2);
-            float s8[8];
-            if (per_row) {
-                const float sr = __half2float(sc[row]);
-#pragma unroll
-                for (int t = 0; t < 8; ++t) s8[t] = sr;
-            } else {
-                const uint4 raw = *reinterpret_cast<const uint4 *>(sc + cc * 8);
-                const __half2 *hp = reinterpret_cast<const __half2 *>(&raw);
-#pragma unroll
-                for (int t = 0; t < 4; ++t) {
-                    const float2 f = __half22float2(hp[t]);
-                    s8[2 * t] = f.x;
-                    s8[2 * t + 1] = f.y;
-                }
-            }
-            uint32_t o[4];
-#pragma unroll
-            for (int t = 0; t < 4; ++t) {
-                const float a = (float)((int)((wv >> (8 * t)) & 15u) - 8) * s8[2 * t];
-                const float b = (float)((int)((wv >> (8 * t + 4)) & 15u) - 8) * s8[2 * t + 1];
-                o[t] = pack_f16(a, b);
-            }
-            *reinterpret_cast<uint4 *>(out + swz_offset(row, cc * 16, cols * 2)) = make_uint4(o[0], o[1], o[2], o[3]);
-        }
-    };
-    expand(src, reinterpret_cast<const __half *>(src + y.q_off_sLK), false, P, y.rkp, dst);
-    expand(src + y.q_off_RK, reinterpret_cast<const __half *>(src + y.q_off_sRK), false, y.rkp, D, dst + y.off_RK);
-    expand(src + y.q_off_LV, reinterpret_cast<const __half *>(src + y.q_off_sLV), false, y.rvp, P, dst + y.off_LV);
-    expand(src + y.q_off_RV, reinterpret_cast<const __half *>(src + y.q_off_sRV), true, D, y.rvp, dst + y.off_RV);
-}
-
 // float offset of the warp states in the ring once streaming is over (after
 // the merge scratch; a multiple of 4 floats)
 template <int D>
@@ -583,10 +688,7 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
 
     const size_t stage_bytes = decode_stage_bytes<P, D>(y);
     unsigned char *stages = smem;
-    // INT4 stores: each warp expands a record into its own bf16 record first
-    const size_t q16 = Q4 ? ((y.rec16_bytes + 127) & ~(size_t)127) : 0;
-    unsigned char *qstage = smem + NS * stage_bytes + (size_t)(threadIdx.x >> 5) * q16;
-    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes + NWC * q16);
+    uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
     DecodeShared &sh = *reinterpret_cast<DecodeShared *>(full + NS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *wfull = full + warp * SPW;
@@ -694,9 +796,7 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
         const uint32_t st = smem_u32(wstage + (size_t)slot * stage_bytes);
         if (!(info & 2)) {
             if constexpr (Q4) {
-                dequant_q4<P, D>(y, wstage + (size_t)slot * stage_bytes, qstage, lane);
-                __syncwarp();
-                factored_unit<P, D, RKT, RVT, true>(w, smem_u32(qstage), y, lane, scale_log2);
+                factored_unit_q4<P, D, RKT, RVT>(w, wstage + (size_t)slot * stage_bytes, y, lane, scale_log2);
             } else {
                 factored_unit<P, D, RKT, RVT>(w, st, y, lane, scale_log2);
             }
@@ -786,7 +886,6 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
     const Layout &y = p.y;
     const size_t stage_bytes =
         ((y.rec_bytes > (size_t)P * D * 2 ? y.rec_bytes : (size_t)P * D * 2) + 127) & ~(size_t)127;
-    const size_t q16 = Q4 ? ((y.rec16_bytes + 127) & ~(size_t)127) : 0;  // per-warp bf16 record (INT4 stores)
     auto k = decode_bf16_kernel<P, D, RKT, RVT, Q4>;
     // one set-up per (device, record size): the ring depth depends on the record size
     static std::mutex mu;
@@ -811,7 +910,7 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
             const size_t tail_bytes = (size_t)fin_comb<D>() * 4 + (size_t)NWC_BF16 * 8 * (D + 4) * 4;
             if ((size_t)NS * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
             c.stages = NS;
-            c.smem = NS * stage_bytes + NWC_BF16 * q16 + NS * sizeof(uint64_t) + sizeof(DecodeShared);
+            c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared);
             c.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
             if (c.err == cudaSuccess &&
                 (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, NWC_BF16 * 32, c.smem) != cudaSuccess ||

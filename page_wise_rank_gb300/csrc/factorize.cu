@@ -340,10 +340,11 @@ __device__ __forceinline__ void store_elem(char *base, size_t idx, float v) {
 //   2. sigma_j = |row j of R| (R's rows are orthogonal: L holds eigenvectors),
 //      Lt = L sigma^{1/2}, Rt = sigma^{-1/2} R (zero where sigma_j = 0);
 //   3. one fp16 scale per group, max|x| / 7 rounded to fp16: columns of L_K
-//      and of R_K / R_V (head-dim columns), rows of L_V (tokens);
+//      and of R_K / R_V (head-dim columns), rows of L_V (tokens), stored in
+//      accumulator-column order (q4_scale_index);
 //   4. codes round(x / scale) (IEEE division, round half to even) clamped to
-//      [-7, 7], stored as code + 8, two per byte, low nibble first, in the
-//      record orientation LK [P][rkp], RK [rkp][D], LVt [rvp][P], RVt [D][rvp].
+//      [-7, 7], stored as code + 8 in the key or value stream's tensor-core
+//      operand order (q4_operand_elem), one 32-bit word per thread step.
 template <typename T, int P, int D, int NT>
 __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const Layout &y) {
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -394,7 +395,8 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
         Rf[e] = rs > 0.f ? Rf[e] / rs : 0.f;
     }
     __syncthreads();
-    // 3. scales: fp16 in the record, their fp32 values in s.Vt for the codes
+    // 3. scales: fp16 in the record (accumulator-column order), their fp32
+    // values in s.Vt for the codes
     float *scL = &s.Vt[0][0];  // per rank (keys) or per token (values): up to P
     float *scR = scL + P;      // per head-dim column: D
     unsigned char *rec = reinterpret_cast<unsigned char *>(v.rec);
@@ -405,7 +407,7 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
             float m = 0.f;
             for (int i = 0; i < P; ++i) m = fmaxf(m, fabsf(s.G[i][j]));
             const __half h = __float2half_rn(m / 7.f);
-            hL[j] = h;
+            hL[q4_scale_index(rp, j)] = h;
             scL[j] = __half2float(h);
         }
     } else {
@@ -413,7 +415,7 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
             float m = 0.f;
             for (int j = 0; j < rp; ++j) m = fmaxf(m, fabsf(s.G[i][j]));
             const __half h = __float2half_rn(m / 7.f);
-            hL[i] = h;
+            hL[q4_scale_index(P, i)] = h;
             scL[i] = __half2float(h);
         }
     }
@@ -421,36 +423,38 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
         float m = 0.f;
         for (int j = 0; j < rp; ++j) m = fmaxf(m, fabsf(Rf[j * D + k]));
         const __half h = __float2half_rn(m / 7.f);
-        hR[k] = h;
+        hR[q4_scale_index(D, k)] = h;
         scR[k] = __half2float(h);
     }
     __syncthreads();
-    // 4. codes
-    auto q = [](float x, float sc) -> unsigned {
+    // 4. codes: the key stream holds R_K as B[head dim][rank] then L_K as
+    // B[rank][token]; the value stream L_V as B[token][rank] then R_V as
+    // B[rank][head dim] (tensor-core operand order, see layout.h)
+    auto q = [](float x, float sc) -> uint32_t {
         int c = sc > 0.f ? (int)rintf(x / sc) : 0;
         c = c < -7 ? -7 : (c > 7 ? 7 : c);
-        return (unsigned)(c + 8);
+        return (uint32_t)(c + 8);
     };
-    if (v.kind == 0) {
-        for (int b = tid; b < P * rp / 2; b += NT) {  // LK [P][rkp]
-            const int i = b / (rp / 2), j = (b % (rp / 2)) * 2;
-            rec[b] = (unsigned char)(q(s.G[i][j], scL[j]) | (q(s.G[i][j + 1], scL[j + 1]) << 4));
+    const int K0 = v.kind == 0 ? D : P, K1 = v.kind == 0 ? P : D;
+    const int regs1 = q4_operand_regs(K0, rp), regs = regs1 + q4_operand_regs(rp, K1);
+    auto code_of = [&](int m, int ln, int e) -> uint32_t {
+        int k, n;
+        if (m >= regs) return 8u;
+        if (m < regs1) {
+            q4_operand_elem(K0, rp, m, ln, e, k, n);
+            return v.kind == 0 ? q(Rf[n * D + k], scR[k]) : q(s.G[k][n], scL[k]);
         }
-        for (int b = tid; b < rp * D / 2; b += NT) {  // RK [rkp][D]
-            const int j = b / (D / 2), k = (b % (D / 2)) * 2;
-            rec[y.q_off_RK + b] =
-                (unsigned char)(q(Rf[j * D + k], scR[k]) | (q(Rf[j * D + k + 1], scR[k + 1]) << 4));
-        }
-    } else {
-        for (int b = tid; b < rp * P / 2; b += NT) {  // LVt [rvp][P]
-            const int j = b / (P / 2), i = (b % (P / 2)) * 2;
-            rec[y.q_off_LV + b] = (unsigned char)(q(s.G[i][j], scL[i]) | (q(s.G[i + 1][j], scL[i + 1]) << 4));
-        }
-        for (int b = tid; b < D * rp / 2; b += NT) {  // RVt [D][rvp]
-            const int k = b / (rp / 2), j = (b % (rp / 2)) * 2;
-            rec[y.q_off_RV + b] =
-                (unsigned char)(q(Rf[j * D + k], scR[k]) | (q(Rf[(j + 1) * D + k], scR[k]) << 4));
-        }
+        q4_operand_elem(rp, K1, m - regs1, ln, e, k, n);
+        return v.kind == 0 ? q(s.G[n][k], scL[k]) : q(Rf[k * D + n], scR[n]);
+    };
+    uint32_t *words = reinterpret_cast<uint32_t *>(rec + (v.kind == 0 ? 0 : y.q_off_V));
+    const int nwords = (v.kind == 0 ? y.q_kslabs : y.q_vslabs) * 64;
+    for (int wi = tid; wi < nwords; wi += NT) {  // word wi: slab wi / 64, lane (wi % 64) / 2
+        const int ln = (wi & 63) >> 1, w = 2 * (wi >> 6) + (wi & 1);
+        uint32_t word = 0;
+#pragma unroll
+        for (int nu = 0; nu < 8; ++nu) word |= code_of(4 * w + (nu & 3), ln, nu >> 2) << (4 * nu);
+        words[wi] = word;
     }
 }
 

@@ -149,18 +149,54 @@ struct PageSplit {
     }
 };
 
+// INT4 code streams [PuzzleKV §4.3].  Each factor enters the decode as the B
+// operand (K x N, K the contraction) of m16n8k16 / m16n8k8 fp16 tensor-core
+// products: R_K as B[k = head dim][n = rank], L_K as B[rank][token], L_V as
+// B[token][rank], R_V as B[rank][head dim].  A factor's B operand is cut into
+// k-steps (16-wide, then one 8-wide step if K is an odd multiple of 8), each
+// k-step into n-tiles of 8, k-step outer; a 16-wide tile gives every lane
+// (lane = 4 g + c) two registers b0 = (k0 + 2c, k0 + 2c + 1; n0 + g) and
+// b1 = (k0 + 8 + 2c, k0 + 9 + 2c; n0 + g), an 8-wide tile one register b0.
+// The key stream is R_K's registers then L_K's, the value stream L_V's then
+// R_V's.  Register m of a lane sits in word m / 4 of the lane, nibbles
+// (m % 4) and (m % 4) + 4 (the register's first and second element); words
+// are laid out in 256-byte slabs of two words per lane: word w of lane l at
+// byte ((w / 2) * 32 + l) * 8 + (w % 2) * 4.  Unused nibbles hold 8 (code 0).
+PKV_HD int q4_operand_regs(int K, int N) { return K * N / 64; }  // registers per lane
+PKV_HD int q4_stream_regs(int K0, int r, int K1) {  // B1 = K0 x r, then B2 = r x K1
+    return q4_operand_regs(K0, r) + q4_operand_regs(r, K1);
+}
+// Element (k, n) of a K x N B operand held by register m (relative to the
+// operand's first register) of lane `lane`, element `e` (0 or 1).
+PKV_HD void q4_operand_elem(int K, int N, int m, int lane, int e, int &k, int &n) {
+    const int g = lane >> 2, c = lane & 3, nt = N / 8, k16 = K / 16;
+    if (m < k16 * 2 * nt) {
+        const int ks = m / (2 * nt), rem = m % (2 * nt);
+        k = 16 * ks + 8 * (rem & 1) + 2 * c + e;
+        n = 8 * (rem >> 1) + g;
+    } else {
+        k = 16 * k16 + 2 * c + e;
+        n = 8 * (m - k16 * 2 * nt) + g;
+    }
+}
+// Position of element i of a scale vector of length K (a multiple of 8) in
+// accumulator-column order: lane c's elements (8 t + 2c, 8 t + 2c + 1) for
+// t = 0 .. K/8 - 1 are contiguous, lanes c = 0..3 one after another.
+PKV_HD int q4_scale_index(int K, int i) { return ((i & 7) >> 1) * (K / 4) + (i >> 3) * 2 + (i & 1); }
+
 struct Layout {
     int L, H, Hq, G, d, P, rk, rv, rkp, rvp, sink_tokens, W, Bmax, Tmax, esz, dtype;
     int n_pg_max, sink_pages, ring, dslots;
     size_t rec_bytes, off_RK, off_LV, off_RV;
-    // INT4 factor records [PuzzleKV §4.3] (q4 = 1): 4-bit codes (code + 8, low
-    // nibble first) of LK [P][rkp], RK [rkp][d], LVt [rvp][P], RVt [d][rvp]
-    // row-major, then fp16 scales: one per column of LK, RK and LVt (rank,
-    // head dim, token) and one per row of RVt (head dim).  rec16_bytes and
-    // off_RK / off_LV / off_RV then describe the bf16 record a decode expands
-    // an INT4 record into.
+    // INT4 factor records [PuzzleKV §4.3] (q4 = 1): a key stream and a value
+    // stream of 4-bit codes (code + 8) in tensor-core operand order (Q4Stream
+    // below), each a whole number of 256-byte slabs, then fp16 scales in
+    // accumulator-column order (q4_scale_index): s_RK [d] (per head-dim column
+    // of R_K), s_RV [d] (per head-dim column of R_V), s_LV [P] (per token row
+    // of L_V), s_LK [rkp] (per rank column of L_K).
     int q4;
-    size_t rec16_bytes, q_off_RK, q_off_LV, q_off_RV, q_off_sLK, q_off_sRK, q_off_sLV, q_off_sRV;
+    int q_kslabs, q_vslabs;  // 256-byte slabs of the key / value code streams
+    size_t q_off_V, q_off_sRK, q_off_sRV, q_off_sLV, q_off_sLK;
     size_t dense_half_bytes;  // one K or V page: P * d * esz
     size_t factor_pool_bytes, dense_pool_bytes, page_table_bytes, workspace_bytes;
     size_t desc_offset;       // byte offset of desc[] in the page table
@@ -202,24 +238,21 @@ inline void make_layout(Layout &y, int L, int H, int Hq, int d, int P, int rk, i
     y.off_LV = y.off_RK + (size_t)y.rkp * d * e;
     y.off_RV = y.off_LV + (size_t)y.rvp * P * e;
     y.rec_bytes = y.off_RV + (size_t)d * y.rvp * e;
-    y.rec16_bytes = y.rec_bytes;
     y.q4 = q4;
-    {  // INT4 record: code blocks, then scale blocks, each a multiple of 16 bytes
-        size_t o = (size_t)P * y.rkp / 2;
-        y.q_off_RK = o;
-        o += (size_t)y.rkp * d / 2;
-        y.q_off_LV = o;
-        o += (size_t)y.rvp * P / 2;
-        y.q_off_RV = o;
-        o += (size_t)d * y.rvp / 2;
-        y.q_off_sLK = o;
-        o += (size_t)y.rkp * 2;
+    {  // INT4 record: code streams, then scale vectors, each a multiple of 16 bytes
+        y.q_kslabs = (q4_stream_regs(d, y.rkp, P) + 7) / 8;
+        y.q_vslabs = (q4_stream_regs(P, y.rvp, d) + 7) / 8;
+        size_t o = (size_t)y.q_kslabs * 256;
+        y.q_off_V = o;
+        o += (size_t)y.q_vslabs * 256;
         y.q_off_sRK = o;
+        o += (size_t)d * 2;
+        y.q_off_sRV = o;
         o += (size_t)d * 2;
         y.q_off_sLV = o;
         o += (size_t)P * 2;
-        y.q_off_sRV = o;
-        o += (size_t)d * 2;
+        y.q_off_sLK = o;
+        o += (size_t)y.rkp * 2;
         if (q4) y.rec_bytes = o;
     }
     y.dense_half_bytes = (size_t)P * d * e;

@@ -75,7 +75,7 @@ def test_int4_store_decode_parity(pkv, P, d, rk, rv):
     out = torch.empty(2, cfg.num_q_heads, d, device="cuda")
     store.decode_attention(1, q.cuda(), out, [0, 1])
     assert store.check_device_status() == 0
-    check_decode(store, cfg, host, [0, 1], 1, q, out)
+    print(f"int4 P={P} d={d} ranks=({rk},{rv}) worst {check_decode(store, cfg, host, [0, 1], 1, q, out):.3g}")
 
 
 def test_int4_decode_steps_with_conversion(pkv):
@@ -116,6 +116,7 @@ def test_int4_records_quantize_absorbed_factors(pkv):
             o = lay.record_offset(0, 0, h, int(p))
             rec = fpool[o:o + lay.rec_bytes]
             q = read_record_q4(rec, lay)
+            assert np.all(q.pop("pad") == 0)  # the streams' unused registers hold code 0
             for name, (codes, scales, per_row) in q.items():
                 assert codes.min() >= -7 and codes.max() <= 7
                 groups = codes if per_row else codes.T

@@ -85,6 +85,18 @@ def test_query_sizes_int4(pkv):
     assert rec / (2 * 64 * 128 * 2) == pytest.approx(oracle.int4_page_storage_ratio(64, 128, 16, 24))
 
 
+@pytest.mark.parametrize("K,N", [(128, 16), (64, 24), (24, 128), (16, 64), (8, 16), (64, 8)])
+def test_int4_operand_order_covers_each_element_once(K, N):
+    """The INT4 stream order gives every element of a K x N operand exactly one
+    (lane, register, element) and fills registers 0 .. K N / 64 - 1 of every lane."""
+    from store_layout import _operand_index
+    lane, m, e, k, n = _operand_index(K, N)
+    assert len(lane) == K * N
+    assert len(set(zip(k.tolist(), n.tolist()))) == K * N and k.max() == K - 1 and n.max() == N - 1
+    assert len(set(zip(lane.tolist(), m.tolist(), e.tolist()))) == K * N
+    assert m.max() == K * N // 64 - 1
+
+
 @pytest.mark.parametrize("bad,status", [
     (dict(head_dim=96), 2), (dict(page_size=128), 2), (dict(num_q_heads=33), 1),
     (dict(num_q_heads=8 * 16), 2), (dict(rank_k=0), 1), (dict(rank_v=65), 1),
