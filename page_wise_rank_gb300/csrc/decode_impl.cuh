@@ -37,8 +37,6 @@
 namespace pkv {
 
 constexpr int NWC = 4;            // consumer warps of the fp32 kernel
-constexpr int NWC_BF16 = 4;       // warps of the bf16 kernel
-constexpr int SLOTS_PER_WARP = 2; // shared-memory slots each warp streams its units through
 constexpr int CTAS_PER_SM = 1;    // resident bf16 decode CTAs per SM
 constexpr int NS_MAX = 16;        // shared-memory stages (bf16 kernel), chosen at launch
 constexpr int MAX_CHUNK = MAX_CHUNK_PAGES;
@@ -52,10 +50,31 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// One shared-memory slot: a factor record or half a dense page (K and V rows).
-template <int P, int D>
+// Shape of the tensor-core decode kernel: warps (NWC), shared-memory slots
+// each warp streams its units through (SPW) and units per dense page (DU).
+// A bf16 record (15 KB at P = 64, d = 128) fills a half-page slot, and two
+// slots per warp keep its copies ahead of its arithmetic.  An INT4 record
+// (4.5 KB) fits a quarter-page slot, so twice the warps fit in the same shared
+// memory; the per-page code expansion is the part that needs them.  A unit
+// keeps a multiple of 8 rows (the period of the dense pages' swizzle).
+template <bool Q4, int P>
+struct DecodeShape {
+    static constexpr int NWC = Q4 ? 8 : 4, SPW = 2, DU = Q4 && P >= 32 ? 4 : 2;
+};
+
+// One shared-memory slot: a factor record or one unit of a dense page (P / DU
+// K rows and P / DU V rows).
+template <int P, int D, int DU>
 __host__ __device__ inline size_t decode_stage_bytes(const Layout &y) {
-    return ((y.rec_bytes > (size_t)P * D * 2 ? y.rec_bytes : (size_t)P * D * 2) + 127) & ~(size_t)127;
+    const size_t unit = (size_t)(P / DU) * D * 2 * 2;
+    return ((y.rec_bytes > unit ? y.rec_bytes : unit) + 127) & ~(size_t)127;
+}
+
+// Rows of the dense-page unit starting at token `first` (units of PU rows)
+// that a length-T sequence holds.
+__device__ __forceinline__ int unit_valid(int T, int first, int PU) {
+    const int v = T - first;
+    return v < 0 ? 0 : (v > PU ? PU : v);
 }
 
 struct DecodeShared {
@@ -67,7 +86,7 @@ struct DecodeShared {
 
 
 // Walk over the units of a page range [p, pe): one per factorized page, one
-// per non-empty half of a dense page.  The range is cut into three segments
+// per non-empty DU-th of a dense page.  The range is cut into three segments
 // by the classification rule -- dense sink pages, factorized pages [a1, a2)
 // (their records are contiguous in the factor pool), dense window pages --
 // so a step costs a few integer operations.  Page kinds follow page_kind()
@@ -75,7 +94,7 @@ struct DecodeShared {
 // global memory before the first bulk copy).
 struct UnitCursor {
     int p, half, a1, a2, pe, T;
-    template <int P>
+    template <int P, int DU>
     __device__ __forceinline__ bool next(int &pg, int &hf, bool &dense) {
         while (p < pe) {
             if (p >= a1 && p < a2) {
@@ -85,13 +104,11 @@ struct UnitCursor {
                 return true;
             }
             const int pp = p, hh = half;
-            if (half == 0) {
-                half = 1;
-            } else {
+            if (++half == DU) {
                 half = 0;
                 ++p;
             }
-            if (T > pp * P + hh * (P / 2)) {
+            if (T > pp * P + hh * (P / DU)) {
                 pg = pp;
                 hf = hh;
                 dense = true;
@@ -401,10 +418,9 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
     mma_rows<D / 8, MAXV>(w.o, uhi, ulo, nvt, RV, nvt * 16, lane);
 }
 
-template <int P, int D>
+template <int P, int D, int PH>  // PH: tokens in the unit (a multiple of 8, at most P / 2)
 __device__ __forceinline__ void dense_unit(WarpState<P, D> &w, uint32_t st, int valid, int lane,
                                            float scale_log2) {
-    constexpr int PH = P / 2;  // tokens in the unit
     constexpr int NT = PH / 8;
     const uint32_t K = st, V = st + PH * D * 2;
     float s[NT][4];
@@ -626,18 +642,18 @@ __device__ inline void append_page_table(const DecodeParams &prm, int b_idx, int
     if (cp >= 0) prm.desc_out[y.desc_index(b, prm.layer, cp)] = (KIND_FACTORED << KIND_SHIFT) | cp;
 }
 
-// Fused append, bf16 path: the staged half page was copied before the new
-// token reached the pool; write the token's key and value rows into the
-// staged copy (row `srow` of the unit) and into the dense pool (row `prow`
-// of the page in `slot`).  One warp.
-template <int D>
+// Fused append, bf16 path: the staged dense unit (PU key rows, then PU
+// value rows) was copied before the new token reached the pool; write the
+// token's key and value rows into the staged copy (row `srow` of the unit)
+// and into the dense pool (row `prow` of the page in `slot`).  One warp.
+template <int D, int PU>
 __device__ __forceinline__ void patch_new_row(const DecodeParams &prm, unsigned char *stage, int b_idx, int b, int h,
                                               int slot, int prow, int srow, int lane) {
     const Layout &y = prm.y;
     const size_t in_off = ((size_t)b_idx * y.H + h) * D;
     const uint32_t *kin = reinterpret_cast<const uint32_t *>(reinterpret_cast<const __nv_bfloat16 *>(prm.k_new) + in_off);
     const uint32_t *vin = reinterpret_cast<const uint32_t *>(reinterpret_cast<const __nv_bfloat16 *>(prm.v_new) + in_off);
-    unsigned char *kst = stage, *vst = stage + (size_t)(y.P / 2) * D * 2;
+    unsigned char *kst = stage, *vst = stage + (size_t)PU * D * 2;
     char *kpool = const_cast<char *>(prm.dense_pool) + y.dense_offset(prm.layer, b, slot, h, 0);
     char *vpool = const_cast<char *>(prm.dense_pool) + y.dense_offset(prm.layer, b, slot, h, 1);
     for (int c2 = lane; c2 < D / 2; c2 += 32) {  // two bf16 per lane step
@@ -676,8 +692,11 @@ template <int D>
 __host__ __device__ constexpr int fin_comb() { return MAX_SPLITS * 8 + 8; }
 
 template <int P, int D, int RKT, int RVT, bool Q4>
-__global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel(const DecodeParams prm) {
-    constexpr int NWC = NWC_BF16, SPW = SLOTS_PER_WARP, NS = NWC * SPW;
+__global__ void __launch_bounds__(DecodeShape<Q4, P>::NWC * 32, CTAS_PER_SM)
+    decode_bf16_kernel(const DecodeParams prm) {
+    using Shape = DecodeShape<Q4, P>;
+    constexpr int NWC = Shape::NWC, SPW = Shape::SPW, NS = NWC * SPW;
+    constexpr int DU = Shape::DU, PU = P / DU;  // dense units per page, rows per unit
     constexpr int FIN_COMB = fin_comb<D>();
     extern __shared__ __align__(128) unsigned char smem[];
     const Layout &y = prm.y;
@@ -686,14 +705,14 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
     const int ns = prm.nsplit[b_idx];  // CTAs taking part for this sequence (<= its pages)
     if (rank >= ns) return;            // uniform over the CTA
 
-    const size_t stage_bytes = decode_stage_bytes<P, D>(y);
+    const size_t stage_bytes = decode_stage_bytes<P, D, DU>(y);
     unsigned char *stages = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
     DecodeShared &sh = *reinterpret_cast<DecodeShared *>(full + NS);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *wfull = full + warp * SPW;
     unsigned char *wstage = stages + (size_t)warp * SPW * stage_bytes;
-    int *winfo = sh.unit_info + warp * SPW;  // per slot: page << 2 | dense << 1 | half
+    int *winfo = sh.unit_info + warp * SPW;  // per slot: page << 3 | dense << 2 | unit
 
     // lane 0: this warp's cursor and next unit
     UnitCursor cur{};
@@ -706,23 +725,23 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
         int pg, hf;
         bool dn;
         for (int i = 0; i < skip; ++i)
-            if (!cur.next<P>(pg, hf, dn)) return false;
-        return cur.next<P>(n_pg, n_hf, n_dense);
+            if (!cur.next<P, DU>(pg, hf, dn)) return false;
+        return cur.next<P, DU>(n_pg, n_hf, n_dense);
     };
     auto issue = [&](int slot) {
-        winfo[slot] = (n_pg << 2) | (n_dense ? 2 : 0) | n_hf;
+        winfo[slot] = (n_pg << 3) | (n_dense ? 4 : 0) | n_hf;
         unsigned char *dst = wstage + (size_t)slot * stage_bytes;
         if (!n_dense) {
             mbar_arrive_expect_tx(&wfull[slot], (uint32_t)y.rec_bytes);
             bulk_g2s_hint(dst, fact + (size_t)n_pg * y.rec_bytes, (uint32_t)y.rec_bytes, &wfull[slot], policy);
         } else {
-            const int first = n_pg * P + n_hf * (P / 2);
-            if (!waited && first + dense_half_valid(T, n_pg, P, n_hf) >= T - 1) {
+            const int first = n_pg * P + n_hf * PU;
+            if (!waited && first + unit_valid(T, first, PU) >= T - 1) {
                 grid_dependency_wait();
                 waited = true;
             }
             const int slot_d = y.dense_slot(n_pg);
-            const uint32_t hb = (uint32_t)(P / 2) * D * 2;
+            const uint32_t hb = (uint32_t)PU * D * 2;
             mbar_arrive_expect_tx(&wfull[slot], 2 * hb);
             bulk_g2s_hint(dst, prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 0) + n_hf * hb, hb,
                           &wfull[slot], policy);
@@ -792,21 +811,21 @@ __global__ void __launch_bounds__(NWC_BF16 * 32, CTAS_PER_SM) decode_bf16_kernel
     for (; k < issued; ++k) {
         if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wfull[slot], ph, prm.status))) break;
         const int info = winfo[slot];
-        const int pg = info >> 2, half = info & 1;
+        const int pg = info >> 3, part = info & 3;
         const uint32_t st = smem_u32(wstage + (size_t)slot * stage_bytes);
-        if (!(info & 2)) {
+        if (!(info & 4)) {
             if constexpr (Q4) {
                 factored_unit_q4<P, D, RKT, RVT>(w, wstage + (size_t)slot * stage_bytes, y, lane, scale_log2);
             } else {
                 factored_unit<P, D, RKT, RVT>(w, st, y, lane, scale_log2);
             }
         } else {
-            const int valid = dense_half_valid(T, pg, P, half);
-            const int first = pg * P + half * (P / 2);
+            const int first = pg * P + part * PU;
+            const int valid = unit_valid(T, first, PU);
             if (prm.append && first + valid == T)  // this unit ends with the appended token
-                patch_new_row<D>(prm, wstage + (size_t)slot * stage_bytes, b_idx, b, h, y.dense_slot(pg),
+                patch_new_row<D, PU>(prm, wstage + (size_t)slot * stage_bytes, b_idx, b, h, y.dense_slot(pg),
                                  T - 1 - pg * P, valid - 1, lane);
-            dense_unit<P, D>(w, st, valid, lane, scale_log2);
+            dense_unit<P, D, PU>(w, st, valid, lane, scale_log2);
         }
         __syncwarp();
         int more = 0;
@@ -884,8 +903,8 @@ struct LaunchSetup {
 template <int P, int D, int RKT, int RVT, bool Q4 = false>
 cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     const Layout &y = p.y;
-    const size_t stage_bytes =
-        ((y.rec_bytes > (size_t)P * D * 2 ? y.rec_bytes : (size_t)P * D * 2) + 127) & ~(size_t)127;
+    using Shape = DecodeShape<Q4, P>;
+    const size_t stage_bytes = decode_stage_bytes<P, D, Shape::DU>(y);
     auto k = decode_bf16_kernel<P, D, RKT, RVT, Q4>;
     // one set-up per (device, record size): the ring depth depends on the record size
     static std::mutex mu;
@@ -906,14 +925,14 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
             if (slot < 0) slot = 0;
             LaunchSetup &c = cache[dev][slot];
             c = LaunchSetup{};
-            constexpr int NS = NWC_BF16 * SLOTS_PER_WARP;
-            const size_t tail_bytes = (size_t)fin_comb<D>() * 4 + (size_t)NWC_BF16 * 8 * (D + 4) * 4;
+            constexpr int NS = Shape::NWC * Shape::SPW;
+            const size_t tail_bytes = (size_t)fin_comb<D>() * 4 + (size_t)Shape::NWC * 8 * (D + 4) * 4;
             if ((size_t)NS * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
             c.stages = NS;
             c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared);
             c.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
             if (c.err == cudaSuccess &&
-                (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, NWC_BF16 * 32, c.smem) != cudaSuccess ||
+                (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, Shape::NWC * 32, c.smem) != cudaSuccess ||
                  c.occ < 1))
                 c.occ = 1;
             c.ready = 1;
@@ -986,7 +1005,7 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
     const int splits = group;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)splits, (unsigned)y.H, (unsigned)p.nseq);
-    cfg.blockDim = dim3(NWC_BF16 * 32, 1, 1);
+    cfg.blockDim = dim3(Shape::NWC * 32, 1, 1);
     cfg.dynamicSmemBytes = setup.smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];
