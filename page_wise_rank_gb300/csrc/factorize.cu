@@ -571,8 +571,10 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
     return sweeps < 0 ? fp.max_sweeps : sweeps;
 }
 
+// The 256-thread variant keeps four CTAs per SM (64 registers), which its
+// shared memory also allows: the Jacobi rounds are latency-bound.
 template <typename T, int P, int D, int NT>
-__global__ void __launch_bounds__(NT) factorize_kernel(const FactorParams fp) {
+__global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1) factorize_kernel(const FactorParams fp) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto &s = *reinterpret_cast<FactorSmem<T, P, D> *>(smem_raw);
     unsigned long long jobs = 0, sweeps = 0;
