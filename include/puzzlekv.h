@@ -133,6 +133,35 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *store, int32_t seq, con
                                          const void *v, int32_t T, void *stream);
 
 /*
+ * Prefill compression of one layer of one sequence, for prompt processing
+ * that produces the cache layer by layer [PuzzleKV §3.3 ①②③, §4.5 time to
+ * first token]: as puzzlekv_factorize_pages restricted to `layer`.  The dense
+ * pages and the page table are written on `stream`.  With async = 0 the
+ * factorization also runs on `stream`.  With async = 1 it runs on the
+ * store's internal low-priority stream, after the work already queued on
+ * `stream`, so that the caller's next layers (their dense attention) overlap
+ * it; the sequence's next attention call waits for it.
+ *   k, v: device, [num_kv_heads][T][head_dim] in kv_dtype.  With async = 0
+ *         they may be freed once the stream passes this call; with async = 1
+ *         they are read on the internal stream (puzzlekv_background_stream),
+ *         so they must stay unchanged until work queued there completes --
+ *         order their reuse after puzzlekv_wait_background, or tell the
+ *         allocator that owns them about that stream.
+ *   seq, T: as puzzlekv_factorize_pages; every layer of a sequence must be
+ *         given the same T before it is decoded.
+ */
+puzzlekv_status puzzlekv_factorize_layer(puzzlekv_store *store, int32_t seq, int32_t layer, const void *k,
+                                         const void *v, int32_t T, int32_t async, void *stream);
+
+/* Make `stream` wait for all background work of the store (batched
+ * conversions and asynchronous layer prefills) queued so far. */
+puzzlekv_status puzzlekv_wait_background(puzzlekv_store *store, void *stream);
+
+/* The store's internal low-priority stream (created on first use); owned by
+ * the store and destroyed with it. */
+puzzlekv_status puzzlekv_background_stream(puzzlekv_store *store, void **stream);
+
+/*
  * Stateless batched page factorization [PuzzleKV §3.3 ③ and eq. (2)]:
  * for each of n independent pages X_i (P x d), G_i = X_i X_i^T in fp32, its
  * eigenvectors by cyclic Jacobi, L_i = an orthonormal basis of the top-r
@@ -197,8 +226,9 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *store, int32_t layer, 
  *   them.  A batch's factors are first read when one of its pages becomes
  *   factorized; the first decode call (puzzlekv_decode_attention,
  *   puzzlekv_decode_step, the static-scratch variant) that reaches that
- *   length, and any puzzlekv_factorize_pages call, makes its own stream wait
- *   for the batch.  puzzlekv_check_device_status and
+ *   length, and any prefill call (puzzlekv_factorize_pages,
+ *   puzzlekv_factorize_layer) that rewrites one of the batch's layers, makes
+ *   its own stream wait for the batch.  puzzlekv_check_device_status and
  *   puzzlekv_factorize_counters synchronise the internal stream as well; the
  *   store must not be destroyed while its caller's streams still hold work
  *   that waits on a batch.

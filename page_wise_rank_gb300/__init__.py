@@ -140,8 +140,9 @@ class Store:
 
     def close(self) -> None:
         if getattr(self, "_h", None):
-            lib().puzzlekv_store_destroy(self._h)
+            lib().puzzlekv_store_destroy(self._h)  # waits for the background stream
             self._h = None
+            self._inputs = []
 
     def __del__(self):
         try:
@@ -161,6 +162,47 @@ class Store:
         _need(k, shape, c.kv_dtype, "k")
         _need(v, shape, c.kv_dtype, "v")
         check(lib().puzzlekv_factorize_pages(self._h, seq, _ptr(k), _ptr(v), T, _stream(stream)))
+
+    def factorize_layer(self, seq: int, layer: int, k: torch.Tensor, v: torch.Tensor, background: bool = True,
+                        stream=None) -> None:
+        """Prefill compression of one layer from dense k, v [H, T, d] (§3.3 ①②③).  With
+        `background`, the factorization runs on the store's internal stream so that the
+        caller's later layers overlap it; the store then keeps k and v referenced until
+        that stream is past the call (or until wait_background / close)."""
+        c = self.cfg
+        T = k.shape[1]
+        shape = (c.num_kv_heads, T, c.head_dim)
+        _need(k, shape, c.kv_dtype, "k")
+        _need(v, shape, c.kv_dtype, "v")
+        self._release_inputs()
+        check(lib().puzzlekv_factorize_layer(self._h, seq, layer, _ptr(k), _ptr(v), T, int(background),
+                                             _stream(stream)))
+        if background:  # k and v stay referenced until the background stream is past this call
+            ev = torch.cuda.Event()
+            ev.record(self.background_stream())
+            self._inputs.append((ev, k, v))
+
+    def _release_inputs(self) -> None:
+        """Drop the references to background prefill inputs the internal stream is done with."""
+        inputs = getattr(self, "_inputs", None)
+        if inputs is None:
+            self._inputs = []
+            return
+        while inputs and inputs[0][0].query():
+            inputs.pop(0)
+
+    def wait_background(self, stream=None) -> None:
+        """Order `stream` after all background work queued so far (conversions, layer prefills)."""
+        check(lib().puzzlekv_wait_background(self._h, _stream(stream)))
+        self._release_inputs()
+
+    def background_stream(self) -> torch.cuda.ExternalStream:
+        """The store's internal low-priority stream, as a torch stream object."""
+        if getattr(self, "_bg", None) is None:
+            h = ctypes.c_void_p()
+            check(lib().puzzlekv_background_stream(self._h, ctypes.byref(h)))
+            self._bg = torch.cuda.ExternalStream(h.value, device=self.dense_pool.device)
+        return self._bg
 
     def append_token(self, layer: int, k: torch.Tensor, v: torch.Tensor, seq_ids: Sequence[int], stream=None) -> None:
         """Append one token per sequence to `layer`; converts pages leaving the window (§3.3 ⑤)."""
@@ -220,7 +262,9 @@ class Store:
 
     def check_device_status(self, stream=None) -> int:
         """Synchronise and return the status code (raises nothing; OK = 0)."""
-        return lib().puzzlekv_check_device_status(self._h, _stream(stream))
+        st = lib().puzzlekv_check_device_status(self._h, _stream(stream))
+        self._release_inputs()
+        return st
 
     def factorize_counters(self, stream=None) -> tuple:
         """(page jobs, Jacobi sweeps) of the store's factorization launches since

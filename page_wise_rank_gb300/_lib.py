@@ -22,6 +22,9 @@ EXPORTED = (
     "puzzlekv_store_create",
     "puzzlekv_store_destroy",
     "puzzlekv_factorize_pages",
+    "puzzlekv_factorize_layer",
+    "puzzlekv_wait_background",
+    "puzzlekv_background_stream",
     "puzzlekv_factorize_batch",
     "puzzlekv_append_token",
     "puzzlekv_decode_attention",
@@ -69,6 +72,9 @@ def lib() -> ctypes.CDLL:
         "puzzlekv_store_create": ([cfgp, vp, vp, vp, vp, vp, ctypes.POINTER(vp)], i32),
         "puzzlekv_store_destroy": ([vp], i32),
         "puzzlekv_factorize_pages": ([vp, i32, vp, vp, i32, vp], i32),
+        "puzzlekv_factorize_layer": ([vp, i32, i32, vp, vp, i32, i32, vp], i32),
+        "puzzlekv_wait_background": ([vp, vp], i32),
+        "puzzlekv_background_stream": ([vp, ctypes.POINTER(vp)], i32),
         "puzzlekv_factorize_batch": ([vp, i32, i64, i32, i32, i32, vp, vp, i32, vp, vp, vp], i32),
         "puzzlekv_append_token": ([vp, i32, vp, vp, i32p, i32, vp], i32),
         "puzzlekv_decode_attention": ([vp, i32, vp, vp, i32p, i32, vp], i32),

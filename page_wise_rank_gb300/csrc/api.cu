@@ -116,6 +116,7 @@ struct puzzlekv_store {
         cudaEvent_t done = nullptr;
         bool pending = false;
         std::vector<int> deadline;  // [seq]: length at which the batch's first page is factorized
+        std::vector<char> uses;     // [seq][layer]: the batch writes factor records of that layer
     };
     cudaStream_t conv_stream = nullptr;
     cudaEvent_t conv_ready = nullptr;  // caller's stream position a batch starts after
@@ -149,6 +150,50 @@ static bool wait_conversions(puzzlekv_store *s, cudaStream_t strm, const int32_t
         }
     }
     return waited;
+}
+
+// Background batches run on the store's internal lowest-priority stream,
+// created on first use.  begin_batch takes the next ring entry (ordering the
+// caller's stream after the entry's previous batch if that is still
+// pending), clears its deadlines and orders the internal stream after the
+// work already queued on `strm`; end_batch marks the batch's end.
+static cudaError_t ensure_background(puzzlekv_store *s) {
+    if (s->conv_stream) return cudaSuccess;
+    int least = 0, greatest = 0;
+    cudaError_t e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
+    if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s->conv_stream, cudaStreamNonBlocking, least);
+    if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->conv_ready, cudaEventDisableTiming);
+    s->batches.resize(kConvBatches);
+    for (auto &cb : s->batches) {
+        if (e == cudaSuccess && !cb.done) e = cudaEventCreateWithFlags(&cb.done, cudaEventDisableTiming);
+        cb.deadline.assign(s->y.Bmax, INT_MAX);
+        cb.uses.assign((size_t)s->y.Bmax * s->y.L, 0);
+    }
+    return e;
+}
+
+static cudaError_t begin_batch(puzzlekv_store *s, cudaStream_t strm, puzzlekv_store::ConvBatch *&out) {
+    cudaError_t e = ensure_background(s);
+    if (e != cudaSuccess) return e;
+    puzzlekv_store::ConvBatch &cb = s->batches[s->next_batch];
+    s->next_batch = (s->next_batch + 1) % kConvBatches;
+    if (cb.pending) {  // its event is about to be reused: order the caller's stream after it now
+        e = cudaStreamWaitEvent(strm, cb.done, 0);
+        cb.pending = false;
+    }
+    std::fill(cb.deadline.begin(), cb.deadline.end(), INT_MAX);
+    std::fill(cb.uses.begin(), cb.uses.end(), 0);
+    // the batch reads what the caller's stream has written: start after it
+    if (e == cudaSuccess) e = cudaEventRecord(s->conv_ready, strm);
+    if (e == cudaSuccess) e = cudaStreamWaitEvent(s->conv_stream, s->conv_ready, 0);
+    out = &cb;
+    return e;
+}
+
+static cudaError_t end_batch(puzzlekv_store *s, puzzlekv_store::ConvBatch &cb) {
+    cudaError_t e = cudaEventRecord(cb.done, s->conv_stream);
+    if (e == cudaSuccess) cb.pending = true;
+    return e;
 }
 
 static int *lengths_ptr(puzzlekv_store *s) { return reinterpret_cast<int *>(s->page_table); }
@@ -223,17 +268,20 @@ puzzlekv_status puzzlekv_store_destroy(puzzlekv_store *store) {
     return PUZZLEKV_OK;
 }
 
-puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const void *k, const void *v, int32_t T,
-                                         void *stream) {
-    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+}  // extern "C"
+
+// Prefill of layers [layer0, layer0 + n_layers) of sequence `seq` from
+// k / v ([n_layers][H][T][d]): the dense pages and page table on `strm`, the
+// eligible pages' factorization on `strm` or, with `async`, as a background
+// batch that every later attention call on `seq` waits for.
+static puzzlekv_status prefill(puzzlekv_store *s, int32_t seq, int32_t layer0, int32_t n_layers, const void *k,
+                               const void *v, int32_t T, bool async, cudaStream_t strm) {
     const Layout &y = s->y;
     if (seq < 0 || seq >= y.Bmax) return fail(PUZZLEKV_ERR_INVALID_ARG, "seq %d out of range", seq);
     if (T < 1) return fail(PUZZLEKV_ERR_INVALID_ARG, "T must be >= 1");
     if (T > y.Tmax) return fail(PUZZLEKV_ERR_CAPACITY, "T=%d exceeds max_tokens_per_seq=%d", T, y.Tmax);
     if (!k || !v || !aligned16(k) || !aligned16(v))
         return fail(PUZZLEKV_ERR_INVALID_ARG, "k and v must be non-NULL and 16-byte aligned");
-    cudaStream_t strm = static_cast<cudaStream_t>(stream);
-    wait_conversions(s, strm, nullptr, nullptr, 0, true);  // the slot's pages may still be read by one
     const int n_pages = (T + y.P - 1) / y.P;
     SeqInitParams ip{};
     ip.y = y;
@@ -244,6 +292,8 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const v
     ip.v_src = static_cast<const char *>(v);
     ip.seq = seq;
     ip.T = T;
+    ip.layer0 = layer0;
+    ip.n_layers = n_layers;
     int f_lo = -1, f_hi = -1;
     for (int p = 0; p < n_pages; ++p) {
         if (host_page_kind(p, T, y.P, y.sink_tokens, y.W) == KIND_DENSE) {
@@ -253,6 +303,16 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const v
             if (f_lo < 0) f_lo = p;
             if (f_hi >= 0 && f_hi != p) return fail(PUZZLEKV_ERR_INVALID_ARG, "factorized pages not contiguous");
             f_hi = p + 1;
+        }
+    }
+    // background work of an earlier use of these layers may still write
+    // their records: order the new writes after it
+    for (auto &cb : s->batches) {
+        bool uses = false;
+        for (int l = layer0; cb.pending && l < layer0 + n_layers && !uses; ++l) uses = cb.uses[(size_t)seq * y.L + l];
+        if (uses) {
+            cudaStreamWaitEvent(strm, cb.done, 0);
+            cb.pending = false;
         }
     }
     cudaError_t e = launch_seq_init(ip, strm);
@@ -274,15 +334,57 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const v
         fp.T = T;
         fp.p_lo = f_lo;
         fp.p_hi = f_hi;
-        fp.n_jobs = (long)y.L * y.H * 2 * (f_hi - f_lo);
-        e = launch_factorize(fp, s->num_sms, strm);
+        fp.layer0 = layer0;
+        fp.n_layers = n_layers;
+        fp.n_jobs = (long)n_layers * y.H * 2 * (f_hi - f_lo);
+        if (async) {
+            puzzlekv_store::ConvBatch *cb = nullptr;
+            e = begin_batch(s, strm, cb);
+            if (e == cudaSuccess) {
+                cb->deadline[seq] = 0;  // the sequence's next attention call waits for it
+                for (int l = layer0; l < layer0 + n_layers; ++l) cb->uses[(size_t)seq * y.L + l] = 1;
+                e = launch_factorize(fp, s->num_sms, s->conv_stream);
+            }
+            if (e == cudaSuccess) e = end_batch(s, *cb);
+        } else {
+            e = launch_factorize(fp, s->num_sms, strm);
+        }
         s->after_decode = false;
         if (e != cudaSuccess) return cuda_fail(e, "factorize launch");
     }
-    for (int l = 0; l < y.L; ++l) {
+    for (int l = layer0; l < layer0 + n_layers; ++l) {
         s->len[(size_t)seq * y.L + l] = T;
         s->conv_upto[(size_t)seq * y.L + l] = f_lo >= 0 ? f_hi : y.sink_pages;
     }
+    return PUZZLEKV_OK;
+}
+
+extern "C" {
+
+puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const void *k, const void *v, int32_t T,
+                                         void *stream) {
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    return prefill(s, seq, 0, s->y.L, k, v, T, false, static_cast<cudaStream_t>(stream));
+}
+
+puzzlekv_status puzzlekv_factorize_layer(puzzlekv_store *s, int32_t seq, int32_t layer, const void *k, const void *v,
+                                         int32_t T, int32_t async, void *stream) {
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    if (layer < 0 || layer >= s->y.L) return fail(PUZZLEKV_ERR_INVALID_ARG, "layer %d out of range", layer);
+    return prefill(s, seq, layer, 1, k, v, T, async != 0, static_cast<cudaStream_t>(stream));
+}
+
+puzzlekv_status puzzlekv_wait_background(puzzlekv_store *s, void *stream) {
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    wait_conversions(s, static_cast<cudaStream_t>(stream), nullptr, nullptr, 0, true);
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_background_stream(puzzlekv_store *s, void **stream) {
+    if (!s || !stream) return fail(PUZZLEKV_ERR_INVALID_ARG, "store and stream must be non-NULL");
+    cudaError_t e = ensure_background(s);
+    if (e != cudaSuccess) return cuda_fail(e, "background stream setup");
+    *stream = s->conv_stream;
     return PUZZLEKV_OK;
 }
 
@@ -535,33 +637,15 @@ puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
     }
     if (s->job_host.empty()) return PUZZLEKV_OK;
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
-    cudaError_t e = cudaSuccess;
-    if (!s->conv_stream) {  // first batch: the internal stream (lowest priority) and its events
-        int least = 0, greatest = 0;
-        e = cudaDeviceGetStreamPriorityRange(&least, &greatest);
-        if (e == cudaSuccess) e = cudaStreamCreateWithPriority(&s->conv_stream, cudaStreamNonBlocking, least);
-        if (e == cudaSuccess) e = cudaEventCreateWithFlags(&s->conv_ready, cudaEventDisableTiming);
-        s->batches.resize(kConvBatches);
-        for (auto &cb : s->batches) {
-            if (e == cudaSuccess) e = cudaEventCreateWithFlags(&cb.done, cudaEventDisableTiming);
-            cb.deadline.assign(y.Bmax, INT_MAX);
-        }
-        if (e != cudaSuccess) return cuda_fail(e, "conversion stream setup");
-    }
-    puzzlekv_store::ConvBatch &cb = s->batches[s->next_batch];
-    s->next_batch = (s->next_batch + 1) % kConvBatches;
-    if (cb.pending) {  // its event is about to be reused: order the caller's stream after it now
-        cudaStreamWaitEvent(strm, cb.done, 0);
-        cb.pending = false;
-    }
-    std::fill(cb.deadline.begin(), cb.deadline.end(), INT_MAX);
+    puzzlekv_store::ConvBatch *cbp = nullptr;
+    cudaError_t e = begin_batch(s, strm, cbp);
+    if (e != cudaSuccess) return cuda_fail(e, "conversion stream setup");
+    puzzlekv_store::ConvBatch &cb = *cbp;
     for (const int2 &j : s->job_host) {  // page p is factorized from length (p + 1) P + W on
         const int b = j.x >> 8;
         cb.deadline[b] = std::min(cb.deadline[b], (j.y + 1) * y.P + y.W);
+        cb.uses[(size_t)b * y.L + (j.x & 255)] = 1;
     }
-    // the batch reads pages the caller's stream has written: start after them
-    e = cudaEventRecord(s->conv_ready, strm);
-    if (e == cudaSuccess) e = cudaStreamWaitEvent(s->conv_stream, s->conv_ready, 0);
     int2 *dev_jobs = reinterpret_cast<int2 *>(s->workspace + y.jobs_offset);
     // the list region is reused only in the internal stream's order; pageable
     // source: the copy has consumed job_host when cudaMemcpyAsync returns
@@ -583,9 +667,8 @@ puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
     fp.n_jobs = (long)s->job_host.size() * y.H * 2;
     fp.max_ctas = s->num_sms;  // one CTA per SM: it runs beside the decode CTAs
     e = launch_factorize(fp, s->num_sms, s->conv_stream);
-    if (e == cudaSuccess) e = cudaEventRecord(cb.done, s->conv_stream);
+    if (e == cudaSuccess) e = end_batch(s, cb);
     if (e != cudaSuccess) return cuda_fail(e, "batched conversion launch");
-    cb.pending = true;
     return PUZZLEKV_OK;
 }
 

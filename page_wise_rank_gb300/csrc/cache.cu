@@ -13,7 +13,7 @@ namespace pkv {
 template <typename T>
 __global__ void seq_init_kernel(const SeqInitParams p) {
     const Layout &y = p.y;
-    const int layer = blockIdx.z;
+    const int lrel = blockIdx.z, layer = p.layer0 + lrel;
     const int n_pages = (p.T + y.P - 1) / y.P;
     if (blockIdx.x == 0 && blockIdx.y == 0) {
         if (threadIdx.x == 0) p.lengths[y.len_index(p.seq, layer)] = p.T;
@@ -31,7 +31,7 @@ __global__ void seq_init_kernel(const SeqInitParams p) {
     if (k >= p.n_dense) return;
     const int pg = p.dense_pages[k];
     const T *src = reinterpret_cast<const T *>(kv == 0 ? p.k_src : p.v_src) +
-                   (((size_t)layer * y.H + h) * p.T + (size_t)pg * y.P) * y.d;
+                   (((size_t)lrel * y.H + h) * p.T + (size_t)pg * y.P) * y.d;
     char *dst = p.dense_pool + y.dense_offset(layer, p.seq, y.dense_slot(pg), h, kv);
     const int valid = min(y.P, p.T - pg * y.P);
     for (int e = threadIdx.x; e < y.P * y.d; e += blockDim.x) {
@@ -71,7 +71,7 @@ __global__ void append_kernel(const AppendParams p) {
 }
 
 cudaError_t launch_seq_init(const SeqInitParams &p, cudaStream_t st) {
-    dim3 grid((unsigned)(p.n_dense > 0 ? p.n_dense : 1), (unsigned)(p.y.H * 2), (unsigned)p.y.L);
+    dim3 grid((unsigned)(p.n_dense > 0 ? p.n_dense : 1), (unsigned)(p.y.H * 2), (unsigned)p.n_layers);
     if (p.y.dtype == 1)
         seq_init_kernel<__nv_bfloat16><<<grid, 256, 0, st>>>(p);
     else

@@ -71,13 +71,13 @@ __device__ __forceinline__ JobView job_view(const FactorParams &fp, long job) {
         int pg = fp.p_lo + (int)(t % np); t /= np;
         int kind = (int)(t % 2); t /= 2;
         int h = (int)(t % y.H); t /= y.H;
-        int l = (int)t;
+        int lrel = (int)t;  // layer fp.layer0 + lrel, block lrel of the sources
         const char *src = kind == 0 ? fp.k_src : fp.v_src;
-        v.x = src + (((size_t)l * y.H + h) * fp.T + (size_t)pg * y.P) * y.d * y.esz;
+        v.x = src + (((size_t)lrel * y.H + h) * fp.T + (size_t)pg * y.P) * y.d * y.esz;
         v.x_pool = 0;
         v.kind = kind;
         v.r = kind == 0 ? y.rk : y.rv;
-        v.rec = fp.factor_pool + y.record_offset(l, fp.seq, h, pg);
+        v.rec = fp.factor_pool + y.record_offset(fp.layer0 + lrel, fp.seq, h, pg);
     } else if (fp.mode == FACT_MODE_CONVERT_LIST) {  // job -> (list entry, head, kind)
         int kind = (int)(job % 2);
         long t = job / 2;

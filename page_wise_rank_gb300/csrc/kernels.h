@@ -24,9 +24,10 @@ struct FactorParams {
     Layout y;
     char *factor_pool;
     const char *dense_pool;
-    // prefill: pages [p_lo, p_hi) of sequence `seq` from k_src / v_src ([L][H][T][d])
+    // prefill: pages [p_lo, p_hi) of sequence `seq`, layers layer0 ..
+    // layer0 + n_layers - 1, from k_src / v_src ([n_layers][H][T][d])
     const char *k_src, *v_src;
-    int seq, T, p_lo, p_hi;
+    int seq, T, p_lo, p_hi, layer0, n_layers;
     // convert: one page per call entry of `layer`
     int layer, n_conv;
     int conv_seq[MAX_CALL_BATCH], conv_page[MAX_CALL_BATCH];
@@ -71,8 +72,8 @@ struct SeqInitParams {
     Layout y;
     int *lengths, *desc;
     char *dense_pool;
-    const char *k_src, *v_src;  // [L][H][T][d]
-    int seq, T, n_dense;
+    const char *k_src, *v_src;  // [n_layers][H][T][d]: layers layer0 .. layer0 + n_layers - 1
+    int seq, T, n_dense, layer0, n_layers;
     int dense_pages[MAX_DENSE_PAGES];
 };
 
