@@ -14,7 +14,8 @@ Pins (see tests/test_oracle_pins.py): Eckart-Young energy identity,
 orthonormal factors, singular values against LAPACK, 2x2 closed form,
 brute force over the unit sphere on 4x4 pages, full-rank factorized
 attention equal to dense attention, closed-form attention special cases,
-token-level reclassification, and the page's printed storage ratios.
+token-level reclassification, the page's printed storage ratios, and RoPE
+against complex multiplication and its relative-position property.
 """
 from __future__ import annotations
 
@@ -58,6 +59,8 @@ def lib() -> ctypes.CDLL:
         L.oracle_quantize_int4.argtypes = [dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, cp, dp]
         L.oracle_quantize_int4.restype = None
         L.oracle_dequantize_int4.argtypes = [cp, dp, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp]
+        L.oracle_rope.argtypes = [dp, ctypes.POINTER(ctypes.c_long), ctypes.c_long, ctypes.c_int, ctypes.c_double, dp]
+        L.oracle_rope.restype = None
         L.oracle_dequantize_int4.restype = None
         _lib = L
     return _lib
@@ -156,6 +159,34 @@ def decode_head(q, kinds, Kd, Vd, LK, RK, LV, RV, T: int, P: int) -> np.ndarray:
     lib().oracle_decode_head(_p(q), G, d, T, P, kinds.ctypes.data_as(ctypes.POINTER(ctypes.c_int)),
                              _p(Kd), _p(Vd), _p(LK), _p(RK), rk, _p(LV), _p(RV), rv, _p(out))
     return out
+
+
+def rope(X, positions, theta: float) -> np.ndarray:
+    """Rotary position embedding of the rows of X [n, d] at `positions` (rotate-half
+    pairing (i, i + d/2), angle position * theta^(-2i/d)) [PuzzleKV §4.1, Appendix D.3]."""
+    X = np.ascontiguousarray(_f64(X))
+    n, d = X.shape
+    pos = np.ascontiguousarray(np.asarray(positions, dtype=np.int64))
+    assert pos.shape == (n,) and d % 2 == 0
+    out = np.zeros_like(X)
+    lib().oracle_rope(_p(X), pos.ctypes.data_as(ctypes.POINTER(ctypes.c_long)), n, d, float(theta), _p(out))
+    return out
+
+
+def decode_head_rope(q, kinds, Kd, Vd, LK, RK, LV, RV, T: int, P: int, theta: float) -> np.ndarray:
+    """decode_head for keys stored before RoPE: every key is reconstructed as
+    stored (dense rows, or L_K R_K of its page), turned by RoPE at its absolute
+    position, and the query rows (already rotated at their own position)
+    attend with plain softmax [PuzzleKV §3.3 ④, §4.1, Appendix D.3]."""
+    kinds = np.asarray(kinds)
+    Kd, Vd, LK, RK, LV, RV = (_f64(a) for a in (Kd, Vd, LK, RK, LV, RV))
+    K = Kd[:T].copy()
+    V = Vd[:T].copy()
+    for p in range((T + P - 1) // P):
+        if kinds[p] == FACTORED:
+            K[p * P:(p + 1) * P] = LK[p] @ RK[p]
+            V[p * P:(p + 1) * P] = LV[p] @ RV[p]
+    return attention(q, rope(K, np.arange(T), theta), V)
 
 
 def absorb_sigma(L, R):

@@ -22,6 +22,8 @@
  *   - INT4 factors: singular values absorbed into both factors, symmetric
  *     INT4 codes with one scale per column (L_K, R_K, R_V) or per row (L_V),
  *     and their dequantization                     [PuzzleKV §4.3]
+ *   - the rotary position embedding applied to keys at cache access when
+ *     keys are factorized before it          [PuzzleKV §4.1, Appendix D.3]
  */
 #include <math.h>
 #include <stdlib.h>
@@ -341,4 +343,28 @@ void oracle_dequantize_int4(const signed char *codes, const double *scales, int 
     for (int i = 0; i < rows; ++i)
         for (int k = 0; k < cols; ++k)
             x[(size_t)i * cols + k] = codes[(size_t)i * cols + k] * scales[per_row ? i : k];
+}
+
+/*
+ * Rotary position embedding of n rows of X (n x d) [PuzzleKV §4.1 and
+ * Appendix D.3: keys factorized before RoPE are rotated at cache access].
+ * Rotate-half pairing: row t sits at position pos[t]; for each i < d/2 the
+ * pair (x_i, x_{i+d/2}) turns by the angle pos[t] * theta^(-2i/d):
+ *     x'_i       = x_i cos(a) - x_{i+d/2} sin(a)
+ *     x'_{i+d/2} = x_{i+d/2} cos(a) + x_i sin(a)
+ * out may not alias X.
+ */
+void oracle_rope(const double *X, const long *pos, long n, int d, double theta, double *out)
+{
+    int h = d / 2;
+    for (long t = 0; t < n; ++t) {
+        const double *x = X + t * (long)d;
+        double *y = out + t * (long)d;
+        for (int i = 0; i < h; ++i) {
+            double a = (double)pos[t] * pow(theta, -2.0 * (double)i / (double)d);
+            double c = cos(a), s = sin(a);
+            y[i] = x[i] * c - x[i + h] * s;
+            y[i + h] = x[i + h] * c + x[i] * s;
+        }
+    }
 }

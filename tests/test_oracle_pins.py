@@ -373,3 +373,68 @@ def test_printed_int4_storage_ratio():
     # fp32 scales would not reproduce the printed value
     rho32 = oracle.int4_page_storage_ratio(g["P"], g["d"], g["rk"], g["rv"], scale_bytes=4)
     assert round(((n_pages - g["dense_pages"]) * rho32 + g["dense_pages"]) / n_pages, 3) != g["printed"]
+
+
+# --- RoPE at cache access for keys factorized before it [PuzzleKV §4.1, Appendix D.3] ---
+
+def _rope_complex(X, pos, theta):
+    """Rotate-half RoPE as complex multiplication: z_i = x_i + i x_{i+d/2} turns by pos theta^(-2i/d)."""
+    d = X.shape[1]
+    h = d // 2
+    z = (X[:, :h] + 1j * X[:, h:]) * np.exp(1j * np.outer(pos, theta ** (-2.0 * np.arange(h) / d)))
+    return np.concatenate([z.real, z.imag], axis=1)
+
+
+def test_rope_is_complex_multiplication():
+    rng = np.random.default_rng(3)
+    X = rng.standard_normal((7, 16))
+    pos = np.array([0, 1, 5, 17, 1000, 32767, 131071])
+    for theta in (1e4, 5e5):
+        got = oracle.rope(X, pos, theta)
+        assert np.allclose(got, _rope_complex(X, pos, theta), rtol=0, atol=1e-9)
+    assert np.array_equal(oracle.rope(X[:1], [0], 1e4), X[:1])  # position 0 is the identity
+
+
+def test_rope_relative_position_and_norm():
+    """<R(m) q, R(n) k> = <q, R(n - m) k>, and every rotation keeps norms."""
+    rng = np.random.default_rng(4)
+    q, k = rng.standard_normal((1, 128)), rng.standard_normal((1, 128))
+    for m, n in ((0, 9), (300, 1000), (40000, 40063)):
+        lhs = (oracle.rope(q, [m], 5e5) @ oracle.rope(k, [n], 5e5).T).item()
+        rhs = (q @ oracle.rope(k, [n - m], 5e5).T).item()
+        assert abs(lhs - rhs) <= 1e-9 * max(1.0, abs(rhs))
+        assert np.isclose(np.linalg.norm(oracle.rope(k, [n], 5e5)), np.linalg.norm(k), rtol=1e-13)
+
+
+def test_prerope_decode_full_rank_is_dense_rope_attention():
+    """With keys kept exactly (rank = P), the pre-RoPE hybrid decode is softmax
+    attention over the RoPE-rotated keys, stated here independently (complex
+    rotation, numpy softmax); at a lower rank it is not."""
+    rng = np.random.default_rng(5)
+    T, P, d, G, theta = 230, 32, 64, 3, 1e4
+    K, V = rng.standard_normal((T, d)), rng.standard_normal((T, d))
+    q = rng.standard_normal((G, d)) / np.sqrt(d)
+    kinds = oracle.page_kinds(T, P, 4, 64)
+    n = len(kinds)
+
+    def factors(X, r):
+        L, R = np.zeros((n, P, r)), np.zeros((n, r, d))
+        for p in np.nonzero(kinds == oracle.FACTORED)[0]:
+            L[p], R[p], _ = oracle.factorize(X[p * P:(p + 1) * P], r)
+        return L, R
+
+    Kr = _rope_complex(K, np.arange(T), theta)
+    s = q @ Kr.T / np.sqrt(d)
+    w = np.exp(s - s.max(axis=1, keepdims=True))
+    want = (w / w.sum(axis=1, keepdims=True)) @ V
+    LK, RK = factors(K, P)
+    LV, RV = factors(V, P)
+    got = oracle.decode_head_rope(q, kinds, K, V, LK, RK, LV, RV, T, P, theta)
+    assert np.max(np.abs(got - want)) <= 1e-10
+    LK, RK = factors(K, 8)
+    low = oracle.decode_head_rope(q, kinds, K, V, LK, RK, LV, RV, T, P, theta)
+    assert np.max(np.abs(low - want)) > 1e-3
+    # keys rotated after their reconstruction, not before the factorization
+    # (a reading error this path must not make)
+    post = oracle.decode_head(q, kinds, Kr, V, *factors(Kr, 8), LV, RV, T, P)
+    assert np.max(np.abs(post - low)) > 1e-4
