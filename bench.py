@@ -58,6 +58,12 @@ WORKLOADS = {
                               rope=5e5, k=12, n_out=4, int4=True,
                               desc="Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query heads, d=128, bf16, "
                                    "T=32768, batch 1, P=32, rK=16, rV=14, sink 4, recent 64, INT4 factors"),
+    # keys given before RoPE: factorized unrotated, turned at attention (theta 5e5)
+    "llama32k-prerope": dict(layers=32, H=8, Hq=32, d=128, P=64, rk=16, rv=24, sink=4, W=128, B=1, T=32768,
+                             rope=None, rope_theta=5e5, k=12, n_out=4,
+                             desc="Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query heads, d=128, bf16, "
+                                  "T=32768, batch 1, P=64, rK=16, rV=24, sink 4, recent 128, keys stored before "
+                                  "RoPE (theta 5e5) and turned at attention"),
     # prompt processing: per-layer dense attention (PyTorch's fused causal attention
     # as the model's stand-in) followed by that layer's page factorization
     "prefill-llama32k": dict(layers=32, H=8, Hq=32, d=128, P=64, rk=16, rv=24, sink=4, W=128, B=1, T=32768,
@@ -265,7 +271,7 @@ def gpu_arm(args, rank, world, local):
     cfg = pkv.StoreConfig(num_layers=L, num_kv_heads=H, num_q_heads=Hq, head_dim=d, page_size=P, rank_k=wl["rk"],
                           rank_v=wl["rv"], sink_tokens=wl["sink"], recent_tokens=wl["W"], max_batch=B,
                           max_tokens_per_seq=T0 + n_steps_total + 8, kv_dtype=torch.bfloat16,
-                          factor_int4=bool(wl.get("int4")))
+                          factor_int4=bool(wl.get("int4")), rope_theta=float(wl.get("rope_theta", 0.0)))
     spec = synth.KVSpec(layers=L, kv_heads=H, head_dim=d, page_size=P, inner_rank=wl["k"], n_outliers=wl["n_out"],
                         rope_base=wl["rope"], dtype=torch.bfloat16)
     with torch.cuda.stream(stream):

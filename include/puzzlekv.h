@@ -70,6 +70,14 @@ enum { PUZZLEKV_PAGE_FACTORED = 0, PUZZLEKV_PAGE_DENSE = 1 };
  * (L = U Sigma^{1/2}, R = Sigma^{1/2} W^T), symmetric 4-bit codes in [-7, 7]
  * with one fp16 scale per column of L_K, R_K, R_V and per row of L_V.
  * Requires kv_dtype = PUZZLEKV_BF16 and rank_k, rank_v <= page_size / 2.
+ * rope_theta: 0 = keys are stored as given (already rotated by the model's
+ * RoPE, or without one) [PuzzleKV §4.1: post-RoPE keys].  > 0 = keys are
+ * given before RoPE (prefill, append, decode step); pages are factorized
+ * unrotated and every key is turned at attention by its absolute position n
+ * with the rotate-half pairing (i, i + head_dim/2) and angles
+ * n * rope_theta^(-2i/head_dim) [PuzzleKV Appendix D.3]; queries are given
+ * already rotated at their own position.  Requires kv_dtype = PUZZLEKV_BF16,
+ * factor_int4 = 0 and page_size 32 or 64.
  */
 typedef struct {
     int32_t num_layers;
@@ -85,6 +93,7 @@ typedef struct {
     int32_t max_tokens_per_seq;
     int32_t kv_dtype; /* puzzlekv_dtype */
     int32_t factor_int4;
+    float rope_theta;
 } puzzlekv_config;
 
 typedef struct puzzlekv_store puzzlekv_store; /* opaque host handle */

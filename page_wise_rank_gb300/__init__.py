@@ -37,12 +37,17 @@ class StoreConfig:
     max_tokens_per_seq: int
     kv_dtype: torch.dtype = torch.bfloat16
     factor_int4: bool = False
+    rope_theta: float = 0.0  # > 0: keys are given before RoPE with this base and turned at attention
 
     def c(self) -> _lib.Config:
         c = _lib.Config()
-        for f in _lib.Config._fields_:
-            name = f[0]
-            setattr(c, name, _DT[self.kv_dtype] if name == "kv_dtype" else int(getattr(self, name)))
+        for name, ctype in _lib.Config._fields_:
+            if name == "kv_dtype":
+                setattr(c, name, _DT[self.kv_dtype])
+            elif ctype is ctypes.c_float:
+                setattr(c, name, float(getattr(self, name)))
+            else:
+                setattr(c, name, int(getattr(self, name)))
         return c
 
 

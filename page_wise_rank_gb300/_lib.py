@@ -49,7 +49,8 @@ class PuzzleKVError(RuntimeError):
 class Config(ctypes.Structure):
     _fields_ = [(n, ctypes.c_int32) for n in (
         "num_layers", "num_kv_heads", "num_q_heads", "head_dim", "page_size", "rank_k", "rank_v",
-        "sink_tokens", "recent_tokens", "max_batch", "max_tokens_per_seq", "kv_dtype", "factor_int4")]
+        "sink_tokens", "recent_tokens", "max_batch", "max_tokens_per_seq", "kv_dtype", "factor_int4")] + [
+        ("rope_theta", ctypes.c_float)]
 
 
 _lib = None

@@ -14,6 +14,7 @@
 #include <cstring>
 #include <mutex>
 #include <string>
+#include <cmath>
 #include <vector>
 
 #include "../../include/puzzlekv.h"
@@ -77,6 +78,11 @@ puzzlekv_status validate_config(const puzzlekv_config *c) {
         return fail(PUZZLEKV_ERR_UNSUPPORTED, "INT4 factors need kv_dtype = PUZZLEKV_BF16");
     if (c->factor_int4 && (c->rank_k > c->page_size / 2 || c->rank_v > c->page_size / 2))
         return fail(PUZZLEKV_ERR_UNSUPPORTED, "INT4 factors need rank_k, rank_v <= page_size / 2");
+    if (!(c->rope_theta >= 0.f) || c->rope_theta > 1e30f)
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "rope_theta must be 0 (keys stored as given) or a positive base");
+    if (c->rope_theta > 0.f && (c->kv_dtype != PUZZLEKV_BF16 || c->factor_int4 || c->page_size < 32))
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "keys before RoPE need kv_dtype = PUZZLEKV_BF16, factor_int4 = 0 "
+                                              "and page_size 32 or 64");
     if (c->max_batch > (1 << 16) || c->max_tokens_per_seq > (1 << 24) || c->num_layers > 255)
         return fail(PUZZLEKV_ERR_UNSUPPORTED, "max_batch, max_tokens_per_seq or num_layers too large");
     int P = c->page_size;
@@ -93,7 +99,7 @@ puzzlekv_status validate_config(const puzzlekv_config *c) {
 void layout_from(Layout &y, const puzzlekv_config *c) {
     make_layout(y, c->num_layers, c->num_kv_heads, c->num_q_heads, c->head_dim, c->page_size, c->rank_k,
                 c->rank_v, c->sink_tokens, c->recent_tokens, c->max_batch, c->max_tokens_per_seq, c->kv_dtype,
-                c->factor_int4);
+                c->factor_int4, c->rope_theta);
 }
 
 }  // namespace
@@ -255,6 +261,26 @@ puzzlekv_status puzzlekv_store_create(const puzzlekv_config *cfg, void *dense_po
     cudaError_t e = cudaMemsetAsync(dense_pool, 0, s->y.dense_pool_bytes, strm);
     if (e == cudaSuccess) e = cudaMemsetAsync(page_table, 0, s->y.page_table_bytes, strm);
     if (e == cudaSuccess) e = cudaMemsetAsync(workspace, 0, s->y.workspace_bytes, strm);
+    if (e == cudaSuccess && s->y.rope) {  // (cos, sin) tables of the RoPE angles, from fp64
+        const Layout &y = s->y;
+        const int h = y.d / 2;
+        std::vector<float2> base((size_t)y.n_pg_max * h), delta((size_t)y.P * h);
+        for (int i = 0; i < h; ++i) {
+            const double th = std::pow((double)y.rope_theta, -2.0 * i / y.d);
+            for (int p = 0; p < y.n_pg_max; ++p) {
+                const double a = (double)p * y.P * th;
+                base[(size_t)p * h + i] = make_float2((float)std::cos(a), (float)std::sin(a));
+            }
+            for (int t = 0; t < y.P; ++t)
+                delta[(size_t)t * h + i] = make_float2((float)std::cos(t * th), (float)std::sin(t * th));
+        }
+        // pageable sources: consumed when cudaMemcpyAsync returns
+        e = cudaMemcpyAsync(s->workspace + y.rope_base_offset, base.data(), base.size() * sizeof(float2),
+                            cudaMemcpyHostToDevice, strm);
+        if (e == cudaSuccess)
+            e = cudaMemcpyAsync(s->workspace + y.rope_delta_offset, delta.data(), delta.size() * sizeof(float2),
+                                cudaMemcpyHostToDevice, strm);
+    }
     if (e != cudaSuccess) {
         delete s;
         return cuda_fail(e, "store_create memset");
@@ -442,6 +468,8 @@ static void fill_decode_params(puzzlekv_store *s, int32_t layer, const void *q, 
     dp.desc = reinterpret_cast<const int *>(s->page_table + y.desc_offset);
     dp.q = static_cast<const char *>(q);
     dp.partials = reinterpret_cast<float *>(s->workspace + y.partial_offset);
+    dp.rope_base = reinterpret_cast<const float2 *>(s->workspace + y.rope_base_offset);
+    dp.rope_delta = reinterpret_cast<const float2 *>(s->workspace + y.rope_delta_offset);
     dp.tickets = reinterpret_cast<int *>(s->workspace + y.ticket_offset);
     dp.wait_first = s->after_decode ? 0 : 1;
     dp.out = out;

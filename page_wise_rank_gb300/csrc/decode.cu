@@ -182,6 +182,7 @@ static cudaError_t launch_f32(DecodeParams &p, long total_pages, int max_pages, 
 cudaError_t launch_decode(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     if (p.y.dtype == 1) {
         if (p.y.q4) return launch_bf16_q4(p, total_pages, max_pages, num_sms, st);
+        if (p.y.rope) return launch_bf16_rope(p, total_pages, max_pages, num_sms, st);
         if (p.y.P == 64) return launch_bf16_p64(p, total_pages, max_pages, num_sms, st);
         if (p.y.P == 32) return launch_bf16_p32(p, total_pages, max_pages, num_sms, st);
         if (p.y.P == 16) return launch_bf16_p16(p, total_pages, max_pages, num_sms, st);

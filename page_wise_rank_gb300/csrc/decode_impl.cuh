@@ -65,9 +65,15 @@ struct DecodeShape {
 // One shared-memory slot: a factor record or one unit of a dense page (P / DU
 // K rows and P / DU V rows).
 template <int P, int D, int DU>
-__host__ __device__ inline size_t decode_stage_bytes(const Layout &y) {
+__host__ __device__ inline size_t decode_unit_bytes(const Layout &y) {
     const size_t unit = (size_t)(P / DU) * D * 2 * 2;
-    return ((y.rec_bytes > unit ? y.rec_bytes : unit) + 127) & ~(size_t)127;
+    return ((y.rec_bytes > unit ? y.rec_bytes : unit) + 15) & ~(size_t)15;
+}
+// ... followed, when keys precede RoPE, by the (cos, sin) row of the unit's
+// page start (D / 2 float2).
+template <int P, int D, int DU, bool ROPE>
+__host__ __device__ inline size_t decode_stage_bytes(const Layout &y) {
+    return (decode_unit_bytes<P, D, DU>(y) + (ROPE ? (size_t)D * 4 : 0) + 127) & ~(size_t)127;
 }
 
 // Rows of the dense-page unit starting at token `first` (units of PU rows)
@@ -348,6 +354,13 @@ __device__ __forceinline__ void mma_rows(float (*acc)[4], const uint32_t (*ahi)[
     }
 }
 
+template <int P, int D, int RKT, int RVT>
+__device__ __forceinline__ void factored_values(WarpState<P, D> &w, const float (*s)[4], uint32_t st,
+                                                const Layout &y, int lane, float scale_log2);
+template <int P, int D, int RKT, int RVT>
+__device__ __forceinline__ void factored_values_sv(WarpState<P, D> &w, float (*sv)[2], uint32_t st,
+                                                   const Layout &y, int lane);
+
 // RKT / RVT: rank tiles (ranks / 8) when fixed at compile time, 0 = read
 // from the layout (up to 8 tiles).
 template <int P, int D, int RKT, int RVT>
@@ -355,11 +368,9 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
                                               float scale_log2) {
     using O = Ops<false>;
     const uint32_t(&qa)[D / 16][2] = w.qf;
-    constexpr int MAXK = RKT ? RKT : 8, MAXV = RVT ? RVT : 8;
-    const int nkt = RKT ? RKT : (y.rkp >> 3), nvt = RVT ? RVT : (y.rvp >> 3);
-    const uint32_t off_RK = (uint32_t)P * nkt * 16, off_LV = off_RK + (uint32_t)nkt * 8 * D * 2;
-    const uint32_t off_RV = off_LV + (uint32_t)nvt * 8 * P * 2;
-    const uint32_t LK = st, RK = st + off_RK, LV = st + off_LV, RV = st + off_RV;
+    constexpr int MAXK = RKT ? RKT : 8;
+    const int nkt = RKT ? RKT : (y.rkp >> 3);
+    const uint32_t LK = st, RK = st + (uint32_t)P * nkt * 16;
     // 1. t = q R_K^T  (16 x rkp; rows 8-15 stay zero)
     float t[MAXK][4];
 #pragma unroll
@@ -384,12 +395,34 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
 #pragma unroll
     for (int nt = 0; nt < P / 8; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
     mma_rows<P / 8, MAXK>(s, thi, tlo, nkt, LK, nkt * 16, lane);
+    factored_values<P, D, RKT, RVT>(w, s, st, y, lane, scale_log2);
+}
+
+// Stages 3-5 of a factorized page from its raw scores s (rows 0-7 and 8-15
+// of each tile summed): the page-local softmax state merged into the running
+// one, u = p L_V and o += u R_V, from the bf16 record at `st`.
+template <int P, int D, int RKT, int RVT>
+__device__ __forceinline__ void factored_values(WarpState<P, D> &w, const float (*s)[4], uint32_t st,
+                                                const Layout &y, int lane, float scale_log2) {
     float sv[P / 8][2];
 #pragma unroll
     for (int nt = 0; nt < P / 8; ++nt) {
         sv[nt][0] = (s[nt][0] + s[nt][2]) * scale_log2;
         sv[nt][1] = (s[nt][1] + s[nt][3]) * scale_log2;
     }
+    factored_values_sv<P, D, RKT, RVT>(w, sv, st, y, lane);
+}
+
+// The same from the scaled scores sv (log2 units; head g, tokens 8 nt + 2c, +1).
+template <int P, int D, int RKT, int RVT>
+__device__ __forceinline__ void factored_values_sv(WarpState<P, D> &w, float (*sv)[2], uint32_t st,
+                                                   const Layout &y, int lane) {
+    using O = Ops<false>;
+    constexpr int MAXV = RVT ? RVT : 8;
+    const int nkt = RKT ? RKT : (y.rkp >> 3), nvt = RVT ? RVT : (y.rvp >> 3);
+    const uint32_t off_RK = (uint32_t)P * nkt * 16, off_LV = off_RK + (uint32_t)nkt * 8 * D * 2;
+    const uint32_t off_RV = off_LV + (uint32_t)nvt * 8 * P * 2;
+    const uint32_t LV = st + off_LV, RV = st + off_RV;
     // 3. page-local softmax state merged into the running one
     online_softmax<P, D>(w, sv, P / 8);
     // 4. u = p L_V  (16 x rvp): A = p split by token k-steps, B = LVt rows (rank)
@@ -418,6 +451,10 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
     mma_rows<D / 8, MAXV>(w.o, uhi, ulo, nvt, RV, nvt * 16, lane);
 }
 
+template <int P, int D, int PH>
+__device__ __forceinline__ void dense_values(WarpState<P, D> &w, const float (*s)[4], uint32_t V, int valid,
+                                             int lane, float scale_log2);
+
 template <int P, int D, int PH>  // PH: tokens in the unit (a multiple of 8, at most P / 2)
 __device__ __forceinline__ void dense_unit(WarpState<P, D> &w, uint32_t st, int valid, int lane,
                                            float scale_log2) {
@@ -436,13 +473,23 @@ __device__ __forceinline__ void dense_unit(WarpState<P, D> &w, uint32_t st, int 
             mma16816(s[nt], w.qf[2 * k2 + 1][0], 0u, w.qf[2 * k2 + 1][1], 0u, r2, r3);
         }
     }
+    dense_values<P, D, PH>(w, s, V, valid, lane, scale_log2);
+}
+
+// The rest of a dense unit from its raw scores s (rows 0-7 and 8-15 of each
+// tile summed): rows at or past `valid` masked, the softmax state merged into
+// the running one, o += p V from the unit's V rows at `V`.
+template <int P, int D, int PH>
+__device__ __forceinline__ void dense_values(WarpState<P, D> &w, const float (*s)[4], uint32_t V, int valid,
+                                             int lane, float scale_log2) {
+    constexpr int NT = PH / 8;
     float sv[P / 8][2];
     const int c2 = 2 * (lane & 3);
 #pragma unroll
     for (int nt = 0; nt < NT; ++nt) {
         int tok = 8 * nt + c2;
-        sv[nt][0] = tok < valid ? s[nt][0] * scale_log2 : -INFINITY;
-        sv[nt][1] = tok + 1 < valid ? s[nt][1] * scale_log2 : -INFINITY;
+        sv[nt][0] = tok < valid ? (s[nt][0] + s[nt][2]) * scale_log2 : -INFINITY;
+        sv[nt][1] = tok + 1 < valid ? (s[nt][1] + s[nt][3]) * scale_log2 : -INFINITY;
     }
     online_softmax<P, D>(w, sv, NT);
     // o += p V: V rows are tokens (k); transposed ldmatrix gives the col-major B
@@ -631,6 +678,192 @@ __device__ __forceinline__ void factored_unit_q4(WarpState<P, D> &w, const unsig
     }
 }
 
+// ---------------------------------------------------------------- keys stored before RoPE
+//
+// Keys given before RoPE [PuzzleKV §4.1, Appendix D.3] are factorized as
+// they are and turned at attention: the key at absolute position n meets the
+// (already rotated) query as q . R(n) k.  A page starting at n0 splits the
+// rotation as R(n0 + delta) = R(n0) R(delta), so each unit turns the query
+// back once by the page start, q_p = R(n0)^T q, and each key only by its
+// offset delta < P inside the page.  R pairs dims (i, i + D/2) with angle
+// n theta_i; `base` holds (cos, sin) of n0 theta_i (D/2 entries, copied with
+// the unit) and `delta` the (cos, sin) of delta theta_i ([P][D/2], shared).
+
+// q_p as fp16 high parts (A rows 0-7) and residuals (rows 8-15): this lane's
+// q elements (head g, dims 16 ks + 8 b + 2c, +1) pair dim i < D/2 (k-step
+// ks < D/32) with i + D/2 (k-step ks + D/32, same b and lane position).
+template <int D>
+__device__ __forceinline__ void rope_query(const uint32_t (&qf)[D / 16][2], const float2 *base, int lane,
+                                           uint32_t (&qhi)[D / 16][2], uint32_t (&qlo)[D / 16][2]) {
+    const int c2 = 2 * (lane & 3);
+#pragma unroll
+    for (int ks = 0; ks < D / 32; ++ks)
+#pragma unroll
+        for (int b = 0; b < 2; ++b) {
+            const int i = 16 * ks + 8 * b + c2;
+            const float4 cs = *reinterpret_cast<const float4 *>(base + i);  // (cos, sin) of dims i, i + 1
+            const float x0 = bf16_lo_to_f32(qf[ks][b]), x1 = bf16_hi_to_f32(qf[ks][b]);
+            const float y0 = bf16_lo_to_f32(qf[ks + D / 32][b]), y1 = bf16_hi_to_f32(qf[ks + D / 32][b]);
+            // R^T turns (x, y) by minus the angle: x' = x c + y s, y' = y c - x s
+            split_f16(fmaf(x0, cs.x, y0 * cs.y), fmaf(x1, cs.z, y1 * cs.w), qhi[ks][b], qlo[ks][b]);
+            split_f16(fmaf(y0, cs.x, -x0 * cs.y), fmaf(y1, cs.z, -x1 * cs.w), qhi[ks + D / 32][b],
+                      qlo[ks + D / 32][b]);
+        }
+}
+
+// Turn the pair (x, y) = (k_i, k_{i + D/2}) by the angle whose (cos, sin) is cs.
+__device__ __forceinline__ void rope_turn(float &x, float &y, float c, float s) {
+    const float xr = fmaf(x, c, -y * s), yr = fmaf(y, c, x * s);
+    x = xr;
+    y = yr;
+}
+
+// acc (rows g: high parts of q_p, rows g + 8: residuals) += q_p . k over one
+// k-step (q_p fragments qh0, ql0 for dims 2c, +1 and qh1, ql1 for 8 + 2c, +1
+// of the step) for the 8 tokens of an n-tile, whose rotated keys this lane
+// holds as fp32 pairs (x0, x1) (dims 2c, +1 of the step, token g) and
+// (y0, y1) (dims 8 + 2c, +1); each key pair goes in as an fp16 high part and a
+// residual (two products).
+__device__ __forceinline__ void rope_score_step(float *acc, uint32_t qh0, uint32_t ql0, uint32_t qh1, uint32_t ql1,
+                                                float x0, float x1, float y0, float y1) {
+    uint32_t h0, l0, h1, l1;
+    split_f16(x0, x1, h0, l0);
+    split_f16(y0, y1, h1, l1);
+    mma16816_f16(acc, qh0, ql0, qh1, ql1, h0, h1);
+    mma16816_f16(acc, qh0, ql0, qh1, ql1, l0, l1);
+}
+
+// A factorized page of a store whose keys precede RoPE: K = L_K R_K rebuilt
+// 16 tokens at a time on the tensor cores (bf16 x bf16 products are exact in
+// fp32), each row turned by its offset, scored against q_p; then the value
+// stages as for any factorized page.
+template <int P, int D, int RKT, int RVT>
+__device__ __forceinline__ void factored_unit_rope(WarpState<P, D> &w, uint32_t st, const float2 *base,
+                                                   const float2 *delta, const Layout &y, int lane,
+                                                   float scale_log2) {
+    constexpr int MAXK = RKT ? RKT : P / 8;
+    const int nkt = RKT ? RKT : (y.rkp >> 3);
+    const uint32_t LK = st, RK = st + (uint32_t)P * nkt * 16;
+    const int g = lane >> 2, c2 = 2 * (lane & 3), m = lane >> 3;
+    uint32_t qhi[D / 16][2], qlo[D / 16][2];
+    rope_query<D>(w.qf, base, lane, qhi, qlo);
+    float sv[P / 8][2];
+#pragma unroll
+    for (int mt = 0; mt < P / 16; ++mt) {
+        // kh[nt]: tokens 16 mt + g (elements 0, 1) and + 8 (2, 3), dims 8 nt + 2c, +1
+        float kh[D / 8][4];
+#pragma unroll
+        for (int nt = 0; nt < D / 8; ++nt) kh[nt][0] = kh[nt][1] = kh[nt][2] = kh[nt][3] = 0.f;
+        const int arow = 16 * mt + 8 * (m & 1) + (lane & 7);
+#pragma unroll
+        for (int kr = 0; kr < MAXK / 2; ++kr)
+            if (kr < (nkt >> 1)) {
+                uint32_t a0, a1, a2, a3;
+                ldsm_x4(LK + swz_offset(arow, (2 * kr + (m >> 1)) * 16, nkt * 16), a0, a1, a2, a3);
+#pragma unroll
+                for (int nt = 0; nt < D / 8; nt += 2) {
+                    uint32_t r0, r1, r2, r3;
+                    ldsm_x4_t(RK + swz_offset(16 * kr + 8 * (m & 1) + (lane & 7), (nt + (m >> 1)) * 16, D * 2), r0,
+                              r1, r2, r3);
+                    mma16816(kh[nt], a0, a1, a2, a3, r0, r1);
+                    mma16816(kh[nt + 1], a0, a1, a2, a3, r2, r3);
+                }
+            }
+        if (nkt & 1) {  // an 8-wide last rank step
+            const int kr = nkt - 1;
+            uint32_t a0, a1;
+            ldsm_x2(LK + swz_offset(arow, kr * 16, nkt * 16), a0, a1);
+#pragma unroll
+            for (int nt = 0; nt < D / 8; nt += 4) {
+                uint32_t r0, r1, r2, r3;
+                ldsm_x4_t(RK + swz_offset(8 * kr + (lane & 7), (nt + m) * 16, D * 2), r0, r1, r2, r3);
+                mma1688(kh[nt], a0, a1, r0);
+                mma1688(kh[nt + 1], a0, a1, r1);
+                mma1688(kh[nt + 2], a0, a1, r2);
+                mma1688(kh[nt + 3], a0, a1, r3);
+            }
+        }
+        // turn each row by its offset (dims 8 nt + 2c + e, nt < D/16, pair with
+        // nt + D/16) and score it: k-steps ks and ks + D/32 share their turns
+        const float2 *d0 = delta + (16 * mt + g) * (D / 2), *d1 = d0 + 8 * (D / 2);
+        float sa[4] = {0.f, 0.f, 0.f, 0.f}, sb[4] = {0.f, 0.f, 0.f, 0.f};  // tokens 16 mt + 0..7, + 8..15
+#pragma unroll
+        for (int ks = 0; ks < D / 32; ++ks) {
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const int nt = 2 * ks + b;
+                const float4 ca = *reinterpret_cast<const float4 *>(d0 + 8 * nt + c2);
+                const float4 cb = *reinterpret_cast<const float4 *>(d1 + 8 * nt + c2);
+                rope_turn(kh[nt][0], kh[nt + D / 16][0], ca.x, ca.y);
+                rope_turn(kh[nt][1], kh[nt + D / 16][1], ca.z, ca.w);
+                rope_turn(kh[nt][2], kh[nt + D / 16][2], cb.x, cb.y);
+                rope_turn(kh[nt][3], kh[nt + D / 16][3], cb.z, cb.w);
+            }
+            const int lo = 2 * ks, hi = 2 * ks + D / 16, kq = ks + D / 32;
+            rope_score_step(sa, qhi[ks][0], qlo[ks][0], qhi[ks][1], qlo[ks][1], kh[lo][0], kh[lo][1], kh[lo + 1][0],
+                            kh[lo + 1][1]);
+            rope_score_step(sb, qhi[ks][0], qlo[ks][0], qhi[ks][1], qlo[ks][1], kh[lo][2], kh[lo][3], kh[lo + 1][2],
+                            kh[lo + 1][3]);
+            rope_score_step(sa, qhi[kq][0], qlo[kq][0], qhi[kq][1], qlo[kq][1], kh[hi][0], kh[hi][1], kh[hi + 1][0],
+                            kh[hi + 1][1]);
+            rope_score_step(sb, qhi[kq][0], qlo[kq][0], qhi[kq][1], qlo[kq][1], kh[hi][2], kh[hi][3], kh[hi + 1][2],
+                            kh[hi + 1][3]);
+        }
+        sv[2 * mt][0] = (sa[0] + sa[2]) * scale_log2;
+        sv[2 * mt][1] = (sa[1] + sa[3]) * scale_log2;
+        sv[2 * mt + 1][0] = (sb[0] + sb[2]) * scale_log2;
+        sv[2 * mt + 1][1] = (sb[1] + sb[3]) * scale_log2;
+    }
+    factored_values_sv<P, D, RKT, RVT>(w, sv, st, y, lane);
+}
+
+// A dense unit (PH rows from page offset `off`) of a store whose keys precede
+// RoPE: each key row is turned by its offset inside the page and scored
+// against q_p, then the value stages as for any dense unit.
+template <int P, int D, int PH>
+__device__ __forceinline__ void dense_unit_rope(WarpState<P, D> &w, uint32_t st, const float2 *base,
+                                                const float2 *delta, int off, int valid, int lane,
+                                                float scale_log2) {
+    constexpr int NT = PH / 8;
+    const uint32_t K = st, V = st + PH * D * 2;
+    const int g = lane >> 2, c2 = 2 * (lane & 3);
+    uint32_t qhi[D / 16][2], qlo[D / 16][2];
+    rope_query<D>(w.qf, base, lane, qhi, qlo);
+    float s[NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+        s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+        uint32_t kr[D / 16][2];  // token 8 nt + g, dims 16 ks + 8 b + 2c, +1 (bf16 pairs)
+#pragma unroll
+        for (int k2 = 0; k2 < D / 32; ++k2) {
+            int row = 8 * nt + (lane & 7), ch = 4 * k2 + (lane >> 3);
+            ldsm_x4(K + swz_offset(row, ch * 16, D * 2), kr[2 * k2][0], kr[2 * k2][1], kr[2 * k2 + 1][0],
+                    kr[2 * k2 + 1][1]);
+        }
+        const float2 *dr = delta + (off + 8 * nt + g) * (D / 2);
+#pragma unroll
+        for (int ks = 0; ks < D / 32; ++ks) {  // k-steps ks and ks + D/32 share their turns
+            float x[2][2], yv[2][2];
+#pragma unroll
+            for (int b = 0; b < 2; ++b) {
+                const float4 cs = *reinterpret_cast<const float4 *>(dr + 16 * ks + 8 * b + c2);
+                x[b][0] = bf16_lo_to_f32(kr[ks][b]);
+                x[b][1] = bf16_hi_to_f32(kr[ks][b]);
+                yv[b][0] = bf16_lo_to_f32(kr[ks + D / 32][b]);
+                yv[b][1] = bf16_hi_to_f32(kr[ks + D / 32][b]);
+                rope_turn(x[b][0], yv[b][0], cs.x, cs.y);
+                rope_turn(x[b][1], yv[b][1], cs.z, cs.w);
+            }
+            const int kq = ks + D / 32;
+            rope_score_step(s[nt], qhi[ks][0], qlo[ks][0], qhi[ks][1], qlo[ks][1], x[0][0], x[0][1], x[1][0],
+                            x[1][1]);
+            rope_score_step(s[nt], qhi[kq][0], qlo[kq][0], qhi[kq][1], qlo[kq][1], yv[0][0], yv[0][1], yv[1][0],
+                            yv[1][1]);
+        }
+    }
+    dense_values<P, D, PH>(w, s, V, valid, lane, scale_log2);
+}
+
 // Fused append: page-table record of the call's new token (position T - 1),
 // written by one thread per sequence.  Nothing in this launch reads it.
 __device__ inline void append_page_table(const DecodeParams &prm, int b_idx, int b, int T) {
@@ -691,7 +924,7 @@ __device__ __forceinline__ void patch_new_row(const DecodeParams &prm, unsigned 
 template <int D>
 __host__ __device__ constexpr int fin_comb() { return MAX_SPLITS * 8 + 8; }
 
-template <int P, int D, int RKT, int RVT, bool Q4>
+template <int P, int D, int RKT, int RVT, bool Q4, bool ROPE>
 __global__ void __launch_bounds__(DecodeShape<Q4, P>::NWC * 32, CTAS_PER_SM)
     decode_bf16_kernel(const DecodeParams prm) {
     using Shape = DecodeShape<Q4, P>;
@@ -705,10 +938,14 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P>::NWC * 32, CTAS_PER_SM)
     const int ns = prm.nsplit[b_idx];  // CTAs taking part for this sequence (<= its pages)
     if (rank >= ns) return;            // uniform over the CTA
 
-    const size_t stage_bytes = decode_stage_bytes<P, D, DU>(y);
+    const size_t stage_bytes = decode_stage_bytes<P, D, DU, ROPE>(y);
+    const size_t base_off = decode_unit_bytes<P, D, DU>(y);  // RoPE: the page-start row in a slot
     unsigned char *stages = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
     DecodeShared &sh = *reinterpret_cast<DecodeShared *>(full + NS);
+    // RoPE: the in-page offsets' (cos, sin) table [P][D/2], after the shared state
+    float2 *rope_delta = reinterpret_cast<float2 *>(
+        (reinterpret_cast<uintptr_t>(&sh + 1) + 15) & ~static_cast<uintptr_t>(15));
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *wfull = full + warp * SPW;
     unsigned char *wstage = stages + (size_t)warp * SPW * stage_bytes;
@@ -731,8 +968,9 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P>::NWC * 32, CTAS_PER_SM)
     auto issue = [&](int slot) {
         winfo[slot] = (n_pg << 3) | (n_dense ? 4 : 0) | n_hf;
         unsigned char *dst = wstage + (size_t)slot * stage_bytes;
+        const uint32_t extra = ROPE ? (uint32_t)D * 4 : 0u;  // the page start's (cos, sin) row
         if (!n_dense) {
-            mbar_arrive_expect_tx(&wfull[slot], (uint32_t)y.rec_bytes);
+            mbar_arrive_expect_tx(&wfull[slot], (uint32_t)y.rec_bytes + extra);
             bulk_g2s_hint(dst, fact + (size_t)n_pg * y.rec_bytes, (uint32_t)y.rec_bytes, &wfull[slot], policy);
         } else {
             const int first = n_pg * P + n_hf * PU;
@@ -742,16 +980,23 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P>::NWC * 32, CTAS_PER_SM)
             }
             const int slot_d = y.dense_slot(n_pg);
             const uint32_t hb = (uint32_t)PU * D * 2;
-            mbar_arrive_expect_tx(&wfull[slot], 2 * hb);
+            mbar_arrive_expect_tx(&wfull[slot], 2 * hb + extra);
             bulk_g2s_hint(dst, prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 0) + n_hf * hb, hb,
                           &wfull[slot], policy);
             bulk_g2s_hint(dst + hb, prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 1) + n_hf * hb, hb,
                           &wfull[slot], policy);
         }
+        if (ROPE)  // constant table: no launch writes it
+            bulk_g2s(dst + base_off, prm.rope_base + (size_t)n_pg * (D / 2), extra, &wfull[slot]);
     };
     // this CTA's pages and their factorized stretch (split on the host)
     const int pb = prm.bounds[prm.boff[b_idx] + rank], pe = prm.bounds[prm.boff[b_idx] + rank + 1];
     const int a1 = min(max(pb, prm.fs[b_idx]), pe), a2 = max(a1, min(pe, prm.fw[b_idx]));
+    if (ROPE) {  // constant table: read before any dependency wait
+        const float4 *src = reinterpret_cast<const float4 *>(prm.rope_delta);
+        float4 *dstt = reinterpret_cast<float4 *>(rope_delta);
+        for (int i = threadIdx.x; i < P * D / 4; i += blockDim.x) dstt[i] = __ldg(src + i);
+    }
     if (threadIdx.x == 0) {
         sh.failed = 0;
         for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
@@ -816,6 +1061,10 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P>::NWC * 32, CTAS_PER_SM)
         if (!(info & 4)) {
             if constexpr (Q4) {
                 factored_unit_q4<P, D, RKT, RVT>(w, wstage + (size_t)slot * stage_bytes, y, lane, scale_log2);
+            } else if constexpr (ROPE) {
+                factored_unit_rope<P, D, RKT, RVT>(
+                    w, st, reinterpret_cast<const float2 *>(wstage + (size_t)slot * stage_bytes + base_off),
+                    rope_delta, y, lane, scale_log2);
             } else {
                 factored_unit<P, D, RKT, RVT>(w, st, y, lane, scale_log2);
             }
@@ -825,7 +1074,12 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P>::NWC * 32, CTAS_PER_SM)
             if (prm.append && first + valid == T)  // this unit ends with the appended token
                 patch_new_row<D, PU>(prm, wstage + (size_t)slot * stage_bytes, b_idx, b, h, y.dense_slot(pg),
                                  T - 1 - pg * P, valid - 1, lane);
-            dense_unit<P, D, PU>(w, st, valid, lane, scale_log2);
+            if constexpr (ROPE)
+                dense_unit_rope<P, D, PU>(
+                    w, st, reinterpret_cast<const float2 *>(wstage + (size_t)slot * stage_bytes + base_off),
+                    rope_delta, part * PU, valid, lane, scale_log2);
+            else
+                dense_unit<P, D, PU>(w, st, valid, lane, scale_log2);
         }
         __syncwarp();
         int more = 0;
@@ -900,12 +1154,12 @@ struct LaunchSetup {
     cudaError_t err = cudaSuccess;
 };
 
-template <int P, int D, int RKT, int RVT, bool Q4 = false>
+template <int P, int D, int RKT, int RVT, bool Q4 = false, bool ROPE = false>
 cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     const Layout &y = p.y;
     using Shape = DecodeShape<Q4, P>;
-    const size_t stage_bytes = decode_stage_bytes<P, D, Shape::DU>(y);
-    auto k = decode_bf16_kernel<P, D, RKT, RVT, Q4>;
+    const size_t stage_bytes = decode_stage_bytes<P, D, Shape::DU, ROPE>(y);
+    auto k = decode_bf16_kernel<P, D, RKT, RVT, Q4, ROPE>;
     // one set-up per (device, record size): the ring depth depends on the record size
     static std::mutex mu;
     static LaunchSetup cache[64][4];
@@ -929,7 +1183,8 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
             const size_t tail_bytes = (size_t)fin_comb<D>() * 4 + (size_t)Shape::NWC * 8 * (D + 4) * 4;
             if ((size_t)NS * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
             c.stages = NS;
-            c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared);
+            c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared) +
+                     (ROPE ? 16 + (size_t)P * D * 4 : 0);  // RoPE: the aligned in-page angle table
             c.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
             if (c.err == cudaSuccess &&
                 (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, Shape::NWC * 32, c.smem) != cudaSuccess ||
@@ -1025,5 +1280,7 @@ cudaError_t launch_bf16_p32(DecodeParams &p, long total_pages, int max_pages, in
 cudaError_t launch_bf16_p64(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st);
 // INT4 factor stores, all page sizes; defined in decode_bf16_q4.cu.
 cudaError_t launch_bf16_q4(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st);
+// Stores whose keys precede RoPE, P = 32 and 64; defined in decode_bf16_rope.cu.
+cudaError_t launch_bf16_rope(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st);
 
 }  // namespace pkv

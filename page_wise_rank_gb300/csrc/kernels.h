@@ -64,6 +64,7 @@ struct DecodeParams {
     int nsplit[MAX_CALL_BATCH];     // CTAs per (sequence, KV head) of call entry i
     int bounds[MAX_BOUNDS];
     int *lengths_out, *desc_out;    // device page table (written when append)
+    const float2 *rope_base, *rope_delta;  // keys stored before RoPE: (cos, sin) tables (Layout)
 };
 
 constexpr int MAX_DENSE_PAGES = 64;  // dense pages of one sequence (sink + window + filling)

@@ -196,6 +196,14 @@ struct Layout {
     // of L_V), s_LK [rkp] (per rank column of L_K).
     int q4;
     int q_kslabs, q_vslabs;  // 256-byte slabs of the key / value code streams
+    // Keys stored before RoPE (rope = 1), turned at attention by
+    // theta_i = rope_theta^(-2i/d): the workspace holds (cos, sin) float2
+    // tables of the angles p P theta_i of every page's first position
+    // ([n_pg_max][d/2] at rope_base_offset) and of the offsets delta theta_i
+    // inside a page ([P][d/2] at rope_delta_offset).
+    int rope;
+    float rope_theta;
+    size_t rope_base_offset, rope_delta_offset;
     size_t q_off_V, q_off_sRK, q_off_sRV, q_off_sLV, q_off_sLK;
     size_t dense_half_bytes;  // one K or V page: P * d * esz
     size_t factor_pool_bytes, dense_pool_bytes, page_table_bytes, workspace_bytes;
@@ -224,7 +232,7 @@ struct Layout {
 
 // Fill a Layout from a validated configuration.
 inline void make_layout(Layout &y, int L, int H, int Hq, int d, int P, int rk, int rv, int sink, int W,
-                        int Bmax, int Tmax, int dtype, int q4 = 0) {
+                        int Bmax, int Tmax, int dtype, int q4 = 0, float rope_theta = 0.f) {
     y.L = L; y.H = H; y.Hq = Hq; y.G = Hq / H; y.d = d; y.P = P; y.rk = rk; y.rv = rv;
     y.rkp = round_up8(rk); y.rvp = round_up8(rv);
     y.sink_tokens = sink; y.W = W; y.Bmax = Bmax; y.Tmax = Tmax; y.dtype = dtype;
@@ -267,6 +275,14 @@ inline void make_layout(Layout &y, int L, int H, int Hq, int d, int P, int rk, i
     y.partial_offset = y.jobs_offset + (((size_t)y.max_conv_jobs * 8 + 255) & ~(size_t)255);
     y.part_stride = d + 4;
     y.workspace_bytes = y.partial_offset + (size_t)Bmax * Hq * MAX_SPLITS * y.part_stride * 4;
+    y.rope = rope_theta > 0.f;
+    y.rope_theta = rope_theta;
+    y.rope_base_offset = y.rope_delta_offset = 0;
+    if (y.rope) {
+        y.rope_base_offset = (y.workspace_bytes + 255) & ~(size_t)255;
+        y.rope_delta_offset = y.rope_base_offset + (((size_t)y.n_pg_max * (d / 2) * 8 + 255) & ~(size_t)255);
+        y.workspace_bytes = y.rope_delta_offset + (size_t)P * (d / 2) * 8;
+    }
 }
 
 }  // namespace pkv

@@ -62,6 +62,9 @@ def oracle_decode_on_store(store, cfg, host: HostCache, seq: int, layer: int, h:
     LV, RV = np.zeros((n, P, cfg.rank_v)), np.zeros((n, cfg.rank_v, cfg.head_dim))
     for p in np.nonzero(kinds == oracle.FACTORED)[0]:
         LK[p], RK[p], LV[p], RV[p] = read_factors(fpool, lay, layer, seq, h, int(p))
+    theta = float(getattr(cfg, "rope_theta", 0.0))
+    if theta > 0:  # keys stored before RoPE: turned at their positions in the oracle too
+        return oracle.decode_head_rope(q_rows, kinds, K, V, LK, RK, LV, RV, T, P, theta)
     return oracle.decode_head(q_rows, kinds, K, V, LK, RK, LV, RV, T, P)
 
 

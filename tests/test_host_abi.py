@@ -102,6 +102,8 @@ def test_int4_operand_order_covers_each_element_once(K, N):
     (dict(num_q_heads=8 * 16), 2), (dict(rank_k=0), 1), (dict(rank_v=65), 1),
     (dict(sink_tokens=-1), 1), (dict(max_batch=0), 1),
     (dict(factor_int4=True, kv_dtype=torch.float32), 2), (dict(factor_int4=True, rank_v=40), 2),
+    (dict(rope_theta=-1.0), 1), (dict(rope_theta=float("nan")), 1), (dict(rope_theta=1e4, kv_dtype=torch.float32), 2),
+    (dict(rope_theta=1e4, factor_int4=True), 2), (dict(rope_theta=1e4, page_size=16, rank_k=8, rank_v=8), 2),
 ])
 def test_config_validation(pkv, bad, status):
     with pytest.raises(pkv.PuzzleKVError) as e:
@@ -131,3 +133,17 @@ def test_binding_has_no_cpu_fallback(tmp_path, monkeypatch):
     monkeypatch.setattr(_lib, "_lib", None)
     with pytest.raises(RuntimeError, match="no CPU fallback"):
         _lib.lib()
+
+
+def test_query_sizes_rope(pkv):
+    """Keys before RoPE: the workspace grows by the two fp32 (cos, sin) tables
+    (page starts [n_pages][d/2], in-page offsets [P][d/2]); nothing else changes."""
+    plain = pkv.query_sizes(_cfg(pkv))
+    cfg = _cfg(pkv, rope_theta=5e5)
+    rope = pkv.query_sizes(cfg)
+    n_pg = (cfg.max_tokens_per_seq + 63) // 64
+    assert {k: rope[k] for k in ("dense_pool", "factor_pool", "page_table")} == \
+        {k: plain[k] for k in ("dense_pool", "factor_pool", "page_table")}
+    extra = rope["workspace"] - plain["workspace"]
+    tables = n_pg * 64 * 8 + 64 * 64 * 8
+    assert tables <= extra < tables + 512
