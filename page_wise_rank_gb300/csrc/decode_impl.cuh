@@ -55,11 +55,14 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // A bf16 record (15 KB at P = 64, d = 128) fills a half-page slot, and two
 // slots per warp keep its copies ahead of its arithmetic.  An INT4 record
 // (4.5 KB) fits a quarter-page slot, so twice the warps fit in the same shared
-// memory; the per-page code expansion is the part that needs them.  A unit
-// keeps a multiple of 8 rows (the period of the dense pages' swizzle).
-template <bool Q4, int P>
+// memory; the per-page code expansion is the part that needs them.  Keys
+// stored before RoPE make a factorized page several times the arithmetic of a
+// bf16 one (rebuilding and turning its keys), so that path also runs 8 warps,
+// with one slot each.  A unit keeps a multiple of 8 rows (the period of the
+// dense pages' swizzle).
+template <bool Q4, int P, bool ROPE = false>
 struct DecodeShape {
-    static constexpr int NWC = Q4 ? 8 : 4, SPW = 2, DU = Q4 && P >= 32 ? 4 : 2;
+    static constexpr int NWC = Q4 || ROPE ? 8 : 4, SPW = ROPE ? 1 : 2, DU = Q4 && P >= 32 ? 4 : 2;
 };
 
 // One shared-memory slot: a factor record or one unit of a dense page (P / DU
@@ -925,9 +928,9 @@ template <int D>
 __host__ __device__ constexpr int fin_comb() { return MAX_SPLITS * 8 + 8; }
 
 template <int P, int D, int RKT, int RVT, bool Q4, bool ROPE>
-__global__ void __launch_bounds__(DecodeShape<Q4, P>::NWC * 32, CTAS_PER_SM)
+__global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE>::NWC * 32, CTAS_PER_SM)
     decode_bf16_kernel(const DecodeParams prm) {
-    using Shape = DecodeShape<Q4, P>;
+    using Shape = DecodeShape<Q4, P, ROPE>;
     constexpr int NWC = Shape::NWC, SPW = Shape::SPW, NS = NWC * SPW;
     constexpr int DU = Shape::DU, PU = P / DU;  // dense units per page, rows per unit
     constexpr int FIN_COMB = fin_comb<D>();
@@ -1157,7 +1160,7 @@ struct LaunchSetup {
 template <int P, int D, int RKT, int RVT, bool Q4 = false, bool ROPE = false>
 cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     const Layout &y = p.y;
-    using Shape = DecodeShape<Q4, P>;
+    using Shape = DecodeShape<Q4, P, ROPE>;
     const size_t stage_bytes = decode_stage_bytes<P, D, Shape::DU, ROPE>(y);
     auto k = decode_bf16_kernel<P, D, RKT, RVT, Q4, ROPE>;
     // one set-up per (device, record size): the ring depth depends on the record size
