@@ -116,6 +116,16 @@ __device__ __forceinline__ void fence_proxy_async_global() {
 
 // Order this thread's earlier generic-proxy accesses to shared memory before
 // its later async-proxy (bulk copy) writes there.
+// Atomic add with release and acquire semantics at GPU scope: writes that
+// happen before it (a CTA barrier included) are visible to whoever later
+// acquires the location, and writes released to the location before it are
+// visible after it.
+__device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
+    int old;
+    asm volatile("atom.acq_rel.gpu.global.add.s32 %0, [%1], %2;" : "=r"(old) : "l"(p), "r"(v) : "memory");
+    return old;
+}
+
 __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Programmatic dependent launch: wait until the preceding grid in the stream

@@ -178,11 +178,11 @@ __device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_i
     const bool staged = merge_bar != nullptr && stage_buf != nullptr && (size_t)G * ns * S * 4 <= stage_cap;
     __syncthreads();
     if (threadIdx.x == 0) {
-        __threadfence();  // this CTA's state is visible before its ticket
-        const bool is_last = atomicAdd(arrivals, 1) == ns - 1;
+        // release: the CTA's state (ordered before this by the barrier) is
+        // visible before its ticket; acquire: the last CTA sees every state
+        const bool is_last = atom_add_acq_rel_gpu(arrivals, 1) == ns - 1;
         *last = is_last;
         if (is_last) {
-            __threadfence();
             if (staged) {  // the states were written through the generic proxy
                 fence_proxy_async_global();
                 fence_proxy_async_shared();  // the warp states in stage_buf have been read
