@@ -139,7 +139,8 @@ def measured_peak_hbm():
 
 # the sources the bf16 decode kernel is built from (a recorded ncu traffic
 # figure is reported only while they are unchanged)
-DECODE_SOURCES = ("decode_impl.cuh", "decode_bf16_p64.cu", "decode_bf16_q4.cu", "common.cuh", "layout.h", "kernels.h")
+DECODE_SOURCES = ("decode_impl.cuh", "decode_bf16_p64.cu", "decode_bf16_q4.cu", "decode_bf16_rope.cu", "common.cuh",
+                  "layout.h", "kernels.h")
 
 
 def source_hash(names):
