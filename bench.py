@@ -128,6 +128,9 @@ def factorization_roofline(wl, jobs, sweeps, ms, sms, sm_mhz):
             "fp32_peak_tflops": round(fp32_peak, 1), "fp32_peak_basis": f"{sms} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz"}
 
 
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal (the measured copy peak is the primary denominator)
+
+
 def measured_peak_hbm():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -454,6 +457,7 @@ def gpu_arm(args, rank, world, local):
                                                                (clk or {}).get("sm_mhz") or 2070.0)),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "kernel": "decode_bf16_kernel: one decode_step launch per layer (append + attention + split merge), mean over the timed steps",
                      "traffic": (traffic["bytes_per_launch"] if traffic else None),
                      "algorithmic_bytes_per_launch": int(statistics.mean(dec_bytes))},
@@ -641,6 +645,7 @@ def multi_seq_arm(args, rank, world, local):
                                   "pages_per_s": round(pre_jobs / (prefill_ms * 1e-3), 1)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "nominal_peak": NOMINAL_HBM_GBS, "frac_of_nominal": round(achieved / NOMINAL_HBM_GBS, 4),
                      "kernel": "decode_bf16_kernel over all layers of a step (conversion overlapped), "
                                "algorithmic bytes of every sequence",
                      "algorithmic_bytes_per_step": int(statistics.mean(step_bytes))},
