@@ -106,7 +106,9 @@ typedef struct puzzlekv_store puzzlekv_store; /* opaque host handle */
  *               head, page) [PuzzleKV §3.3 ⑤ "preallocated storage"];
  *   page_table: per (sequence, layer): current length and one descriptor
  *               per page (kind, slot);
- *   workspace:  split-K partial softmax states and the device status word.
+ *   workspace:  split-K partial softmax states and the device status word
+ *               (for rope_theta > 0 also the fp32 (cos, sin) tables of the
+ *               RoPE angles, filled by puzzlekv_store_create).
  * Host-only; needs no GPU.
  */
 puzzlekv_status puzzlekv_query_sizes(const puzzlekv_config *cfg, size_t *dense_pool_bytes,
