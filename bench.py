@@ -45,6 +45,11 @@ WORKLOADS = {
                       desc="Batched serving decode, Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query heads, "
                            "d=128, bf16, 16 requests of U[8192, 32768] tokens (seed 7), P=64, rK=16, rV=24, sink 4, "
                            "recent 128"),
+    "batched16-int4": dict(layers=32, H=8, Hq=32, d=128, P=64, rk=16, rv=24, sink=4, W=128, B=16, T=32768, rope=5e5,
+                           k=12, n_out=4, steps=32, lens=(8192, 32768, 7), int4=True,
+                           desc="Batched serving decode, Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query "
+                                "heads, d=128, bf16, 16 requests of U[8192, 32768] tokens (seed 7), P=64, rK=16, "
+                                "rV=24, sink 4, recent 128, INT4 factors"),
     "llama32k-int4": dict(layers=32, H=8, Hq=32, d=128, P=64, rk=16, rv=24, sink=4, W=128, B=1, T=32768, rope=5e5,
                           k=12, n_out=4, int4=True,
                           desc="Llama-3.1-8B-shaped attention, 32 layers, 8 KV / 32 query heads, d=128, bf16, "
@@ -548,7 +553,8 @@ def multi_seq_arm(args, rank, world, local):
     n_steps = args.warmup + args.steps
     cfg = pkv.StoreConfig(num_layers=L, num_kv_heads=H, num_q_heads=Hq, head_dim=d, page_size=P, rank_k=wl["rk"],
                           rank_v=wl["rv"], sink_tokens=wl["sink"], recent_tokens=wl["W"], max_batch=B,
-                          max_tokens_per_seq=max(lens0) + n_steps + 8, kv_dtype=torch.bfloat16)
+                          max_tokens_per_seq=max(lens0) + n_steps + 8, kv_dtype=torch.bfloat16,
+                          factor_int4=bool(wl.get("int4")))
     spec = synth.KVSpec(layers=L, kv_heads=H, head_dim=d, page_size=P, inner_rank=wl["k"], n_outliers=wl["n_out"],
                         rope_base=wl["rope"], dtype=torch.bfloat16)
     seqs = list(range(B))

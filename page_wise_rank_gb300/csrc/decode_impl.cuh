@@ -63,6 +63,10 @@ __device__ __forceinline__ float ex2_approx(float x) {
 template <bool Q4, int P, bool ROPE = false>
 struct DecodeShape {
     static constexpr int NWC = Q4 || ROPE ? 8 : 4, SPW = ROPE ? 1 : 2, DU = Q4 && P >= 32 ? 4 : 2;
+    // INT4: 256 threads x 192 registers leave room for a 256-thread,
+    // 64-register background conversion CTA on the same SM (the INT4 kernel
+    // needs no more; at 209 it locked conversions out of SMs it held)
+    static constexpr int MAXREG = Q4 ? 192 : 255;
 };
 
 // One shared-memory slot: a factor record or one unit of a dense page (P / DU
@@ -929,7 +933,7 @@ __host__ __device__ constexpr int fin_comb() { return MAX_SPLITS * 8 + 8; }
 
 template <int P, int D, int RKT, int RVT, bool Q4, bool ROPE>
 __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE>::NWC * 32, CTAS_PER_SM)
-    decode_bf16_kernel(const DecodeParams prm) {
+    __maxnreg__((DecodeShape<Q4, P, ROPE>::MAXREG)) decode_bf16_kernel(const DecodeParams prm) {
     using Shape = DecodeShape<Q4, P, ROPE>;
     constexpr int NWC = Shape::NWC, SPW = Shape::SPW, NS = NWC * SPW;
     constexpr int DU = Shape::DU, PU = P / DU;  // dense units per page, rows per unit
