@@ -618,10 +618,12 @@ static cudaError_t launch_t(const FactorParams &fp, int num_sms, cudaStream_t st
 
 // A few pages (conversions during decoding) are latency-bound: 1024 threads
 // per page.  Many pages (prefill, batches) are throughput-bound: 256 threads,
-// several pages per SM.
+// several pages per SM.  Work capped to run beside decode launches (max_ctas,
+// the background batches) always takes 256 threads: a 1024-thread CTA holds
+// all of an SM's registers, so no decode CTA could share the SM with it.
 template <typename T, int P, int D>
 static cudaError_t launch_nt(const FactorParams &fp, int num_sms, cudaStream_t st) {
-    if (fp.n_jobs <= 2L * num_sms) return launch_t<T, P, D, 1024>(fp, num_sms, st);
+    if (fp.n_jobs <= 2L * num_sms && fp.max_ctas <= 0) return launch_t<T, P, D, 1024>(fp, num_sms, st);
     return launch_t<T, P, D, 256>(fp, num_sms, st);
 }
 
