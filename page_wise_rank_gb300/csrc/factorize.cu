@@ -327,6 +327,134 @@ __device__ int jacobi(FactorSmem<T, P, D> &s, int max_sweeps, int r) {
     return -1;
 }
 
+// INT4 records need the kept vectors to be eigenvectors (their sigma^{1/2}
+// scaling), not just a basis of the kept subspace.  After the subspace stop
+// the subspace is settled, so cyclic Jacobi restricted to the block of the r
+// largest diagonal entries finishes the job: round-robin pairs among the
+// block's indices (a dummy index when r is odd), each rotation applied to the
+// block's entries of G and to the whole eigenvector rows.  Entries between
+// the block and the rest are left alone: nothing reads them afterwards.
+// Leaves s.order as the final ranking -- the block's indices by their
+// polished eigenvalue (ties: lower index first), then the others in index
+// order -- and returns the block sweeps taken (-1 at the cap).
+template <typename T, int P, int D, int NT>
+__device__ int polish_block(FactorSmem<T, P, D> &s, int r, int max_sweeps) {
+    constexpr int V4 = P / 4;
+    const int tid = threadIdx.x;
+    const int n = (r + 1) & ~1, np = n / 2;
+    if (tid < P) {
+        const float li = s.G[tid][tid];
+        int rank = 0;
+        for (int j = 0; j < P; ++j) {
+            const float lj = s.G[j][j];
+            rank += (lj > li) || (lj == li && j < tid);
+        }
+        s.red[tid] = rank < r ? 1.f : 0.f;  // block membership
+        if (rank < r) s.order[rank] = tid;
+    }
+    __syncthreads();
+    const float tol2 = JACOBI_TOL * JACOBI_TOL;
+    int done = -1;
+    for (int sweep = 0; sweep < max_sweeps && done < 0; ++sweep) {
+        int rotated_any = 0;
+        for (int round = 0; round < n - 1; ++round) {
+            int rot = 0;
+            if (tid < np) {
+                const int k = tid;
+                const int a = k == 0 ? 0 : 1 + ((k - 1 - round + 2 * (n - 1)) % (n - 1));
+                const int kb = n - 1 - k;
+                const int b = 1 + ((kb - 1 - round + 2 * (n - 1)) % (n - 1));
+                int p = -1, q = -1;
+                float c = 1.f, sn = 0.f, t = 0.f;
+                if (a < r && b < r) {
+                    const int ia = s.order[a], ib = s.order[b];
+                    p = ia < ib ? ia : ib;
+                    q = ia < ib ? ib : ia;
+                    const float gpp = s.G[p][p], gqq = s.G[q][q], gpq = s.G[p][q];
+                    if (gpq * gpq > tol2 * fabsf(gpp * gqq) && gpq != 0.f) {
+                        float zeta = __fdividef(gqq - gpp, 2.f * gpq);
+                        float z2 = fmaf(zeta, zeta, 1.f);
+                        t = copysignf(__fdividef(1.f, fabsf(zeta) + z2 * rsqrtf(z2)), zeta);
+                        if (fabsf(zeta) > 1e18f) t = __fdividef(0.5f, zeta);
+                        c = rsqrtf(fmaf(t, t, 1.f));
+                        sn = t * c;
+                        rot = 1;
+                    }
+                }
+                s.pair[k] = make_float4(__int_as_float(p), __int_as_float(q), c, sn);  // p < 0: the dummy
+                s.tn[k] = t;
+            }
+            rotated_any |= __syncthreads_or(rot);
+            const int nblk = np * (np + 1) / 2;
+            for (int e = tid; e < nblk; e += NT) {  // 2x2 blocks (al <= be) of this round's pairs
+                int be = 0;
+                while ((be + 1) * (be + 2) / 2 <= e) ++be;
+                const int al = e - be * (be + 1) / 2;
+                const float4 A = s.pair[al], B = s.pair[be];
+                const int pa = __float_as_int(A.x), qa = __float_as_int(A.y);
+                const int pb = __float_as_int(B.x), qb = __float_as_int(B.y);
+                if (pa < 0 || pb < 0) continue;
+                if (al == be) {
+                    const float t = s.tn[al];
+                    if (t != 0.f) {
+                        const float g00 = s.G[pa][pa], g01 = s.G[pa][qa], g11 = s.G[qa][qa];
+                        s.G[pa][pa] = g00 - t * g01;
+                        s.G[qa][qa] = g11 + t * g01;
+                        s.G[pa][qa] = 0.f;
+                    }
+                    continue;
+                }
+                if (A.w == 0.f && B.w == 0.f) continue;
+                float *e00 = pa < pb ? &s.G[pa][pb] : &s.G[pb][pa];
+                float *e01 = pa < qb ? &s.G[pa][qb] : &s.G[qb][pa];
+                float *e10 = qa < pb ? &s.G[qa][pb] : &s.G[pb][qa];
+                float *e11 = qa < qb ? &s.G[qa][qb] : &s.G[qb][qa];
+                const float ca = A.z, sa = A.w, cb = B.z, sb = B.w;
+                const float g00 = *e00, g01 = *e01, g10 = *e10, g11 = *e11;
+                const float h00 = ca * g00 - sa * g10, h01 = ca * g01 - sa * g11;
+                const float h10 = sa * g00 + ca * g10, h11 = sa * g01 + ca * g11;
+                *e00 = cb * h00 - sb * h01;
+                *e01 = sb * h00 + cb * h01;
+                *e10 = cb * h10 - sb * h11;
+                *e11 = sb * h10 + cb * h11;
+            }
+            for (int e = tid; e < np * V4; e += NT) {  // eigenvector rows p, q of each rotating pair
+                const int k = e / V4, c4 = e % V4;
+                const float4 A = s.pair[k];
+                if (A.w == 0.f) continue;
+                const int p = __float_as_int(A.x), q = __float_as_int(A.y);
+                float4 *vp = reinterpret_cast<float4 *>(&s.Vt[p][0]) + c4;
+                float4 *vq = reinterpret_cast<float4 *>(&s.Vt[q][0]) + c4;
+                const float4 a = *vp, b = *vq;
+                const float c = A.z, sn = A.w;
+                *vp = make_float4(c * a.x - sn * b.x, c * a.y - sn * b.y, c * a.z - sn * b.z, c * a.w - sn * b.w);
+                *vq = make_float4(sn * a.x + c * b.x, sn * a.y + c * b.y, sn * a.z + c * b.z, sn * a.w + c * b.w);
+            }
+            __syncthreads();
+        }
+        if (!rotated_any) done = sweep + 1;
+    }
+    // final ranking: the block by polished eigenvalue, then the rest by index
+    if (tid < P) {
+        const bool member = s.red[tid] != 0.f;
+        const float li = s.G[tid][tid];
+        int pos = member ? 0 : r;
+        for (int j = 0; j < P; ++j) {
+            const bool mj = s.red[j] != 0.f;
+            if (member && mj) {
+                const float lj = s.G[j][j];
+                pos += (lj > li) || (lj == li && j < tid);
+            } else if (!member && !mj) {
+                pos += j < tid;
+            }
+        }
+        s.lam[tid] = li;
+        s.order[pos] = tid;
+    }
+    __syncthreads();
+    return done;
+}
+
 template <typename TO>
 __device__ __forceinline__ void store_elem(char *base, size_t idx, float v) {
     reinterpret_cast<TO *>(base)[idx] = Elem<TO>::from_f32(v);
@@ -473,22 +601,27 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
         if (j > i) s.G[j][i] = s.G[i][j];
     }
     __syncthreads();
-    // with singular values requested (or absorbed into INT4 factors) every
-    // eigenpair must converge; otherwise only the kept subspace has to
-    const int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps, (v.sigma || (v.rec && fp.y.q4)) ? P : v.r);
+    // with singular values requested every eigenpair must converge; otherwise
+    // only the kept subspace has to, and INT4 records (whose kept vectors
+    // must be eigenvectors) then finish the kept block on its own
+    const bool polish = !v.sigma && v.r < P && v.rec && fp.y.q4;
+    int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps, v.sigma ? P : v.r);
+    if (polish && sweeps >= 0 && polish_block<T, P, D, NT>(s, v.r, fp.max_sweeps) < 0) sweeps = -1;
     if (sweeps < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
-    if (tid < P) s.lam[tid] = s.G[tid][tid];
-    __syncthreads();
-    if (tid < P) {
-        float li = s.lam[tid];
-        int rank = 0;
-        for (int j = 0; j < P; ++j) {
-            float lj = s.lam[j];
-            rank += (lj > li) || (lj == li && j < tid);
+    if (!polish) {
+        if (tid < P) s.lam[tid] = s.G[tid][tid];
+        __syncthreads();
+        if (tid < P) {
+            float li = s.lam[tid];
+            int rank = 0;
+            for (int j = 0; j < P; ++j) {
+                float lj = s.lam[j];
+                rank += (lj > li) || (lj == li && j < tid);
+            }
+            s.order[rank] = tid;
         }
-        s.order[rank] = tid;
+        __syncthreads();
     }
-    __syncthreads();
     const int r = v.r;
     if (v.sigma && tid < P) v.sigma[tid] = sqrtf(fmaxf(s.lam[s.order[tid]], 0.f));
     __syncthreads();
