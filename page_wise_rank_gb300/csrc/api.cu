@@ -53,6 +53,8 @@ int sm_count() {
 
 int host_page_kind(int p, int T, int P, int sink, int W) { return page_kind(p, T, P, sink, W); }
 
+void layout_from(Layout &y, const puzzlekv_config *c);
+
 puzzlekv_status validate_config(const puzzlekv_config *c) {
     if (!c) return fail(PUZZLEKV_ERR_INVALID_ARG, "config is NULL");
     if (c->num_layers < 1 || c->num_kv_heads < 1 || c->num_q_heads < 1 || c->max_batch < 1 ||
@@ -93,6 +95,13 @@ puzzlekv_status validate_config(const puzzlekv_config *c) {
     int n_pg = (c->max_tokens_per_seq + P - 1) / P;
     if ((long)(n_pg + MAX_CHUNK_PAGES - 1) / MAX_CHUNK_PAGES > MAX_SPLITS)
         return fail(PUZZLEKV_ERR_UNSUPPORTED, "max_tokens_per_seq too large for the split-K workspace");
+    Layout y;
+    layout_from(y, c);
+    const size_t smem = decode_smem_bytes(y);
+    if (smem > MAX_DECODE_SMEM)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "factor records of %zu bytes need %zu bytes of decode shared memory "
+                                              "(at most %zu): lower rank_k + rank_v", y.rec_bytes, smem,
+                    MAX_DECODE_SMEM);
     return PUZZLEKV_OK;
 }
 

@@ -179,6 +179,19 @@ static cudaError_t launch_f32(DecodeParams &p, long total_pages, int max_pages, 
     return cudaGetLastError();
 }
 
+size_t decode_smem_bytes(const Layout &y) {
+    if (y.dtype != 1) return 0;  // the fp32 kernel's shared memory is static and small
+    const bool q4 = y.q4 != 0, rope = y.rope != 0;
+    // the shape of the runtime-rank kernel of this path (DecodeShape): warps x slots, units per dense page
+    const int nwc = q4 || rope ? 8 : 4, spw = rope ? 1 : 2, du = q4 && y.P >= 32 ? 4 : 2;
+    const size_t unit = (size_t)(y.P / du) * y.d * 2 * 2;
+    size_t stage = ((y.rec_bytes > unit ? y.rec_bytes : unit) + 15) & ~(size_t)15;
+    if (rope) stage += (size_t)y.d * 4;
+    stage = (stage + 127) & ~(size_t)127;
+    const size_t ns = (size_t)nwc * spw;
+    return ns * stage + ns * sizeof(uint64_t) + sizeof(DecodeShared) + (rope ? 16 + (size_t)y.P * y.d * 4 : 0);
+}
+
 cudaError_t launch_decode(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     if (p.y.dtype == 1) {
         if (p.y.q4) return launch_bf16_q4(p, total_pages, max_pages, num_sms, st);

@@ -58,15 +58,18 @@ __device__ __forceinline__ float ex2_approx(float x) {
 // memory; the per-page code expansion is the part that needs them.  Keys
 // stored before RoPE make a factorized page several times the arithmetic of a
 // bf16 one (rebuilding and turning its keys), so that path also runs 8 warps,
-// with one slot each.  A unit keeps a multiple of 8 rows (the period of the
-// dense pages' swizzle).
-template <bool Q4, int P, bool ROPE = false>
+// with one slot each.  Pages of 32 or fewer tokens carry half the bytes (or
+// less) for the same work per unit; with ranks fixed at compile time and a
+// record of at most 12 KB they run 8 warps x 2 slots as well.  A unit keeps a
+// multiple of 8 rows (the period of the dense pages' swizzle).
+template <bool Q4, int P, bool ROPE = false, int D = 128, int RKT = 0, int RVT = 0>
 struct DecodeShape {
-    static constexpr int NWC = Q4 || ROPE ? 8 : 4, SPW = ROPE ? 1 : 2, DU = Q4 && P >= 32 ? 4 : 2;
-    // INT4: 256 threads x 192 registers leave room for a 256-thread,
-    // 64-register background conversion CTA on the same SM (the INT4 kernel
-    // needs no more; at 209 it locked conversions out of SMs it held)
-    static constexpr int MAXREG = Q4 ? 192 : 255;
+    static constexpr bool WIDE = !Q4 && !ROPE && P <= 32 && RKT > 0 && RVT > 0 && 16 * (RKT + RVT) * (P + D) <= 12288;
+    static constexpr int NWC = Q4 || ROPE || WIDE ? 8 : 4, SPW = ROPE ? 1 : 2, DU = Q4 && P >= 32 ? 4 : 2;
+    // 256 threads x 192 registers leave room for a 256-thread, 64-register
+    // background conversion CTA on the same SM (at 209 the INT4 kernel locked
+    // conversions out of the SMs it held); the pre-RoPE kernel needs all 255
+    static constexpr int MAXREG = NWC == 8 && !ROPE ? 192 : 255;
 };
 
 // One shared-memory slot: a factor record or one unit of a dense page (P / DU
@@ -932,9 +935,9 @@ template <int D>
 __host__ __device__ constexpr int fin_comb() { return MAX_SPLITS * 8 + 8; }
 
 template <int P, int D, int RKT, int RVT, bool Q4, bool ROPE>
-__global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE>::NWC * 32, CTAS_PER_SM)
-    __maxnreg__((DecodeShape<Q4, P, ROPE>::MAXREG)) decode_bf16_kernel(const DecodeParams prm) {
-    using Shape = DecodeShape<Q4, P, ROPE>;
+__global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 32, CTAS_PER_SM)
+    __maxnreg__((DecodeShape<Q4, P, ROPE, D, RKT, RVT>::MAXREG)) decode_bf16_kernel(const DecodeParams prm) {
+    using Shape = DecodeShape<Q4, P, ROPE, D, RKT, RVT>;
     constexpr int NWC = Shape::NWC, SPW = Shape::SPW, NS = NWC * SPW;
     constexpr int DU = Shape::DU, PU = P / DU;  // dense units per page, rows per unit
     constexpr int FIN_COMB = fin_comb<D>();
@@ -1164,7 +1167,7 @@ struct LaunchSetup {
 template <int P, int D, int RKT, int RVT, bool Q4 = false, bool ROPE = false>
 cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {
     const Layout &y = p.y;
-    using Shape = DecodeShape<Q4, P, ROPE>;
+    using Shape = DecodeShape<Q4, P, ROPE, D, RKT, RVT>;
     const size_t stage_bytes = decode_stage_bytes<P, D, Shape::DU, ROPE>(y);
     auto k = decode_bf16_kernel<P, D, RKT, RVT, Q4, ROPE>;
     // one set-up per (device, record size): the ring depth depends on the record size

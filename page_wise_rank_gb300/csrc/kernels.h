@@ -95,5 +95,9 @@ cudaError_t launch_append(const AppendParams &p, cudaStream_t st);
 // Chooses pages per CTA (p.chunk) for one wave over total_pages pages
 // (all listed sequences and KV heads), then launches.
 cudaError_t launch_decode(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st);
+// Dynamic shared memory the tensor-core decode kernel of this layout's path
+// needs in its runtime-rank form (0 for fp32 stores).
+size_t decode_smem_bytes(const Layout &y);
+constexpr size_t MAX_DECODE_SMEM = 227 * 1024;  // opt-in shared memory per CTA on sm_103a
 
 }  // namespace pkv

@@ -104,6 +104,7 @@ def test_int4_operand_order_covers_each_element_once(K, N):
     (dict(factor_int4=True, kv_dtype=torch.float32), 2), (dict(factor_int4=True, rank_v=40), 2),
     (dict(rope_theta=-1.0), 1), (dict(rope_theta=float("nan")), 1), (dict(rope_theta=1e4, kv_dtype=torch.float32), 2),
     (dict(rope_theta=1e4, factor_int4=True), 2), (dict(rope_theta=1e4, page_size=16, rank_k=8, rank_v=8), 2),
+    (dict(rank_k=40, rank_v=40), 2), (dict(rank_k=64, rank_v=64), 2),
 ])
 def test_config_validation(pkv, bad, status):
     with pytest.raises(pkv.PuzzleKVError) as e:
@@ -147,3 +148,12 @@ def test_query_sizes_rope(pkv):
     extra = rope["workspace"] - plain["workspace"]
     tables = n_pg * 64 * 8 + 64 * 64 * 8
     assert tables <= extra < tables + 512
+
+
+def test_largest_records_that_fit_decode_shared_memory(pkv):
+    """bf16 records of up to 72 padded ranks (K + V) fit the decode kernel's
+    8 shared-memory slots at P = 64, d = 128 (28.3 KB each); 80 do not."""
+    for rk, rv in ((32, 40), (8, 64), (64, 8)):
+        pkv.query_sizes(_cfg(pkv, rank_k=rk, rank_v=rv))
+    with pytest.raises(pkv.PuzzleKVError):
+        pkv.query_sizes(_cfg(pkv, rank_k=33, rank_v=40))
