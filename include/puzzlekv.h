@@ -64,7 +64,10 @@ enum { PUZZLEKV_PAGE_FACTORED = 0, PUZZLEKV_PAGE_DENSE = 1 };
  * is every page holding one of them.  recent_tokens: width W of the dense
  * local window; every page holding one of the last W tokens stays dense, and
  * so does the incomplete last page [PuzzleKV §3.3 ①②③].  max_batch: number
- * of sequence slots.  max_tokens_per_seq: capacity per sequence.
+ * of sequence slots.  max_tokens_per_seq: capacity per sequence.  A bf16
+ * store's factor records must fit the decode kernel's shared-memory slots:
+ * at page_size 64 and head_dim 128, rank_k + rank_v (each rounded up to a
+ * multiple of 8) may be at most 72 (PUZZLEKV_ERR_UNSUPPORTED otherwise).
  * factor_int4: 0 = factors stored in kv_dtype; 1 = INT4 factors
  * [PuzzleKV §4.3]: singular values absorbed into both factors
  * (L = U Sigma^{1/2}, R = Sigma^{1/2} W^T), symmetric 4-bit codes in [-7, 7]
