@@ -791,12 +791,22 @@ def reference_arm(args, rank, world):
     LK[fac], RK[fac] = a, b
     a, b, _ = oracle.factorize_pages(np.stack([Vh[p * P:(p + 1) * P] for p in fac]), wl["rv"], nthreads)
     LV[fac], RV[fac] = a, b
+    if wl.get("int4"):  # the oracle's INT4 factors: sigma^{1/2} absorbed, quantized, dequantized exactly
+        for p in fac:
+            for L_, R_, per_row in ((LK, RK, False), (LV, RV, True)):
+                Lt, Rt = oracle.absorb_sigma(L_[p], R_[p])
+                L_[p] = oracle.dequantize_int4(*oracle.quantize_int4(Lt, per_row), per_row)
+                R_[p] = oracle.dequantize_int4(*oracle.quantize_int4(Rt, False), False)
+    theta = float(wl.get("rope_theta", 0.0))
     G = wl["Hq"] // H
     times = []
     for s in range(args.warmup + args.steps):
         q = synth.queries(1, wl["Hq"], d, step=s, layer=0)[0, :G].double().numpy()
         t0 = time.perf_counter()
-        oracle.decode_head(q, kinds, Kh, Vh, LK, RK, LV, RV, T, P)
+        if theta > 0:  # keys stored before RoPE: turned at their positions
+            oracle.decode_head_rope(q, kinds, Kh, Vh, LK, RK, LV, RV, T, P, theta)
+        else:
+            oracle.decode_head(q, kinds, Kh, Vh, LK, RK, LV, RV, T, P)
         if s >= args.warmup:
             times.append(time.perf_counter() - t0)
     heads = layers * H * wl["B"]
