@@ -152,10 +152,15 @@ DECODE_SOURCES = ("decode_impl.cuh", "decode_bf16_p64.cu", "decode_bf16_q4.cu", 
 
 
 def source_hash(names):
+    """Hash of the sources' code: comments and whitespace do not change a kernel."""
+    import re
     h = hashlib.sha256()
     for n in names:
-        with open(os.path.join(ROOT, "page_wise_rank_gb300", "csrc", n), "rb") as f:
-            h.update(f.read())
+        with open(os.path.join(ROOT, "page_wise_rank_gb300", "csrc", n), encoding="utf-8") as f:
+            text = f.read()
+        text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+        text = re.sub(r"//[^\n]*", " ", text)
+        h.update(" ".join(text.split()).encode())
     return h.hexdigest()[:16]
 
 

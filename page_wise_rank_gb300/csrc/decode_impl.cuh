@@ -8,8 +8,8 @@
 // the online-softmax reduction of eq. (5).
 //
 // One CTA handles one (sequence, KV head, page range).  Its pages are cut
-// into units -- a factorized page, or half of a dense page (keys and values of
-// P/2 tokens) -- each of which fits one shared-memory slot.  The CTA's warps
+// into units -- a factorized page, or a half (a quarter for INT4 stores) of a
+// dense page, keys and values -- each of which fits one shared-memory slot.  The CTA's warps
 // take its units round-robin and stream them through private slots with one
 // or two bulk copies per unit (mbarrier transaction counts), each keeping its
 // own running (m, l, o) for the G query heads of the KV head.  At the end the
@@ -23,6 +23,11 @@
 // weights, and their product with L_V) are split into a bf16 high part in rows
 // 0-7 and a bf16 residual in rows 8-15, so a single mma carries about 16
 // mantissa bits and the two row halves are summed afterwards.
+// INT4 factor records [PuzzleKV §4.3]: the 4-bit codes enter fp16 products
+// as exact integers and the scales are folded into the small operands
+// (factored_unit_q4).  Keys stored before RoPE [PuzzleKV §4.1, Appendix D.3]:
+// each page's keys are rebuilt and turned at their positions
+// (factored_unit_rope, dense_unit_rope).
 // fp32 storage: CUDA-core fp32 arithmetic throughout.
 #pragma once
 #include <cuda_fp16.h>
