@@ -17,6 +17,8 @@
 #include <cmath>
 #include <vector>
 
+#include <nvtx3/nvToolsExt.h>
+
 #include "../../include/puzzlekv.h"
 #include "kernels.h"
 #include "layout.h"
@@ -110,6 +112,15 @@ void layout_from(Layout &y, const puzzlekv_config *c) {
                 c->rank_v, c->sink_tokens, c->recent_tokens, c->max_batch, c->max_tokens_per_seq, c->kv_dtype,
                 c->factor_int4, c->rope_theta);
 }
+
+// An NVTX range around a call of the C ABI, seen by profilers (free when
+// none is attached).
+struct NvtxRange {
+    explicit NvtxRange(const char *name) { nvtxRangePushA(name); }
+    ~NvtxRange() { nvtxRangePop(); }
+    NvtxRange(const NvtxRange &) = delete;
+    NvtxRange &operator=(const NvtxRange &) = delete;
+};
 
 }  // namespace
 
@@ -248,6 +259,7 @@ puzzlekv_status puzzlekv_query_sizes(const puzzlekv_config *cfg, size_t *dense_p
 
 puzzlekv_status puzzlekv_store_create(const puzzlekv_config *cfg, void *dense_pool, void *factor_pool,
                                       void *page_table, void *workspace, void *stream, puzzlekv_store **out) {
+    NvtxRange nvtx_range("puzzlekv_store_create");
     if (!out) return fail(PUZZLEKV_ERR_INVALID_ARG, "out is NULL");
     *out = nullptr;
     puzzlekv_status st = validate_config(cfg);
@@ -398,12 +410,14 @@ extern "C" {
 
 puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const void *k, const void *v, int32_t T,
                                          void *stream) {
+    NvtxRange nvtx_range("puzzlekv_factorize_pages");
     if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
     return prefill(s, seq, 0, s->y.L, k, v, T, false, static_cast<cudaStream_t>(stream));
 }
 
 puzzlekv_status puzzlekv_factorize_layer(puzzlekv_store *s, int32_t seq, int32_t layer, const void *k, const void *v,
                                          int32_t T, int32_t async, void *stream) {
+    NvtxRange nvtx_range("puzzlekv_factorize_layer");
     if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
     if (layer < 0 || layer >= s->y.L) return fail(PUZZLEKV_ERR_INVALID_ARG, "layer %d out of range", layer);
     return prefill(s, seq, layer, 1, k, v, T, async != 0, static_cast<cudaStream_t>(stream));
@@ -426,6 +440,7 @@ puzzlekv_status puzzlekv_background_stream(puzzlekv_store *s, void **stream) {
 puzzlekv_status puzzlekv_factorize_batch(const void *X, int32_t x_dtype, int64_t n, int32_t P, int32_t d, int32_t r,
                                          void *L, void *R, int32_t out_dtype, float *sigma, int32_t *status,
                                          void *stream) {
+    NvtxRange nvtx_range("puzzlekv_factorize_batch");
     if (n < 0) return fail(PUZZLEKV_ERR_INVALID_ARG, "n must be >= 0");
     if ((x_dtype != PUZZLEKV_F32 && x_dtype != PUZZLEKV_BF16) || (out_dtype != PUZZLEKV_F32 && out_dtype != PUZZLEKV_BF16))
         return fail(PUZZLEKV_ERR_INVALID_ARG, "dtype must be PUZZLEKV_F32 or PUZZLEKV_BF16");
@@ -516,6 +531,7 @@ static puzzlekv_status check_call(puzzlekv_store *s, int32_t layer, const int32_
 
 puzzlekv_status puzzlekv_append_token(puzzlekv_store *s, int32_t layer, const void *k, const void *v,
                                       const int32_t *seq_ids, int32_t B, void *stream) {
+    NvtxRange nvtx_range("puzzlekv_append_token");
     puzzlekv_status st = check_call(s, layer, seq_ids, B);
     if (st != PUZZLEKV_OK) return st;
     if (!k || !v || !aligned16(k) || !aligned16(v))
@@ -577,6 +593,7 @@ puzzlekv_status puzzlekv_append_token(puzzlekv_store *s, int32_t layer, const vo
 
 puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *s, int32_t layer, const void *q, float *out,
                                           const int32_t *seq_ids, int32_t B, void *stream) {
+    NvtxRange nvtx_range("puzzlekv_decode_attention");
     puzzlekv_status st = check_call(s, layer, seq_ids, B);
     if (st != PUZZLEKV_OK) return st;
     if (!q || !out || !aligned16(q) || !aligned16(out))
@@ -594,6 +611,7 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *s, int32_t layer, cons
 
 puzzlekv_status puzzlekv_decode_step(puzzlekv_store *s, int32_t layer, const void *q, const void *k, const void *v,
                                      float *out, const int32_t *seq_ids, int32_t B, void *stream) {
+    NvtxRange nvtx_range("puzzlekv_decode_step");
     puzzlekv_status st = check_call(s, layer, seq_ids, B);
     if (st != PUZZLEKV_OK) return st;
     if (!q || !out || !k || !v || !aligned16(q) || !aligned16(out) || !aligned16(k) || !aligned16(v))
@@ -655,6 +673,7 @@ puzzlekv_status puzzlekv_decode_step(puzzlekv_store *s, int32_t layer, const voi
 }
 
 puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
+    NvtxRange nvtx_range("puzzlekv_convert_ready_pages");
     if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
     const Layout &y = s->y;
     s->job_host.clear();
@@ -797,6 +816,7 @@ void *g_scratch_addr[kMaxDevices] = {nullptr};
 extern "C" puzzlekv_status puzzlekv_decode_attention_static_scratch(puzzlekv_store *s, int32_t layer, const void *q,
                                                                     float *out, const int32_t *seq_ids, int32_t B,
                                                                     void *stream) {
+    NvtxRange nvtx_range("puzzlekv_decode_attention_static_scratch");
     puzzlekv_status st = check_call(s, layer, seq_ids, B);
     if (st != PUZZLEKV_OK) return st;
     if (!q || !out || !aligned16(q) || !aligned16(out))
