@@ -180,7 +180,7 @@ puzzlekv_status puzzlekv_background_stream(puzzlekv_store *store, void **stream)
  * for each of n independent pages X_i (P x d), G_i = X_i X_i^T in fp32, its
  * eigenvectors by cyclic Jacobi, L_i = an orthonormal basis of the top-r
  * eigenvector subspace (P x r), R_i = L_i^T X_i (r x d).  The eigensolve stops
- * once no rotation could add more than 1e-5 of the energy the kept subspace
+ * once no rotation could add more than 1e-4 of the energy the kept subspace
  * leaves out (L_i R_i is then the rank-r optimum up to rounding), unless sigma
  * is requested, in which case every eigenpair is converged and the columns
  * of L_i are the top-r eigenvectors themselves.
