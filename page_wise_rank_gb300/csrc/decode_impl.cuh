@@ -974,6 +974,10 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     uint64_t policy = 0;
     const char *fact = prm.factor_pool + y.record_offset(prm.layer, b, h, 0);
     auto take = [&](int skip) -> bool {  // skip units dealt to the other warps, then take one
+        if (cur.half == 0 && cur.p >= cur.a1 && cur.p + skip < cur.a2) {
+            cur.p += skip;  // inside the factorized stretch a unit is a page
+            return cur.next<P, DU>(n_pg, n_hf, n_dense);
+        }
         int pg, hf;
         bool dn;
         for (int i = 0; i < skip; ++i)
