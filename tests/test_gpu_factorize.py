@@ -47,7 +47,7 @@ def check_c5(X, L, R, S, r, tol=1e-3):
         nx = np.linalg.norm(Xd[i])
         if e_star > 1e-6 * nx:
             worst = max(worst, (e - e_star) / e_star)
-        else:  # (near) exact rank <= r: judge against the page norm
+        else:  # (near) exact rank <= r: measure against the page norm
             worst = max(worst, e / nx)
         # singular values from the fp32 Gram eigenvalues (when requested)
         if Sg is not None:
