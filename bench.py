@@ -836,7 +836,8 @@ def reference_arm(args, rank, world):
             "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
             "config": {"workload": wl["desc"], "global_batch": wl["B"], "seq_len": T, "parallelism": "cpu oracle"},
             "cpu_baseline": {"value": round(us_step, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
-                             "sample": sample, "pages_factorized_per_s": round(pages_s, 1)},
+                             "sample": sample, "pages_factorized_per_s": round(pages_s, 1),
+                             "pages_cores": nthreads},
             "e2e": {"value": round(us_step, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 
