@@ -33,6 +33,8 @@
  *     with P <= d; 1 <= rank <= P; query heads per KV head G = Hq / H in
  *     1..8.  Key/value ranks are stored padded to a multiple of 8 (the
  *     padding is zero and never changes a result).
+ *   - Calls that take a list of sequences (seq_ids, B) take 1 <= B <= 64
+ *     distinct slots in [0, max_batch); an empty list is an invalid argument.
  */
 #ifndef PUZZLEKV_H
 #define PUZZLEKV_H
