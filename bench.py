@@ -528,6 +528,30 @@ def _oracle_sample(wl, layer_heads, nthreads):
     return n_pages / t_fact, statistics.mean(t_dec), n_pages
 
 
+def cpu_model():
+    """The host CPU's model name (lscpu, else /proc/cpuinfo), with the machine type."""
+    name = ""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.startswith("Model name:"):
+                name = line.split(":", 1)[1].strip()
+                break
+    except Exception:
+        pass
+    if not name:
+        try:
+            with open("/proc/cpuinfo") as f:
+                for line in f:
+                    if line.lower().startswith("model name"):
+                        name = line.split(":", 1)[1].strip()
+                        break
+        except OSError:
+            pass
+    import platform
+    return f"{name or 'unknown'} ({platform.machine()})"
+
+
 def cpu_baseline_sample(wl):
     nthreads = os.cpu_count() or 1
     pairs = [(0, 0), (wl["layers"] - 1, wl["H"] - 1)]
@@ -540,7 +564,8 @@ def cpu_baseline_sample(wl):
             "sample": f"oracle decode of {len(pairs)} (layer, KV head) pairs at T={wl['T']} on 1 thread, "
                       f"scaled to {heads} pairs per step, plus {conv_per_step:.0f} page conversions per step "
                       f"at the oracle's factorization rate",
-            "pages_factorized_per_s": round(pages_s, 1), "pages_cores": nthreads, "pages_sample": n_pages}
+            "pages_factorized_per_s": round(pages_s, 1), "pages_cores": nthreads, "pages_sample": n_pages,
+            "cpu_model": cpu_model()}
 
 
 def multi_seq_arm(args, rank, world, local):
@@ -837,7 +862,7 @@ def reference_arm(args, rank, world):
             "config": {"workload": wl["desc"], "global_batch": wl["B"], "seq_len": T, "parallelism": "cpu oracle"},
             "cpu_baseline": {"value": round(us_step, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
                              "sample": sample, "pages_factorized_per_s": round(pages_s, 1),
-                             "pages_cores": nthreads},
+                             "pages_cores": nthreads, "cpu_model": cpu_model()},
             "e2e": {"value": round(us_step, 1), "unit": "us/step", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
             "gpu_launches": 0}
 

@@ -30,7 +30,7 @@ def test_reference_arm_line(monkeypatch, extra):
     assert line["config"]["workload"] == wl["desc"] and line["config"]["seq_len"] == wl["T"]
     cb = line["cpu_baseline"]
     assert cb["kind"] == "oracle" and cb["value"] == line["value"] and cb["unit"] == line["unit"]
-    assert cb["cores"] >= 1 and cb["pages_cores"] >= 1 and cb["sample"]
+    assert cb["cores"] >= 1 and cb["pages_cores"] >= 1 and cb["sample"] and cb["cpu_model"]
     e2e = line["e2e"]
     assert e2e["value"] == line["value"] and e2e["unit"] == line["unit"]
     assert e2e["h2d_bytes_per_step"] == 0 and e2e["d2h_bytes_per_step"] == 0
