@@ -41,3 +41,11 @@ def test_reference_arm_other_ranks_do_no_work(monkeypatch):
     monkeypatch.setitem(bench.WORKLOADS, "small-check", SMALL)
     args = argparse.Namespace(workload="small-check", steps=1, warmup=0)
     assert bench.reference_arm(args, 1, 2) is None
+
+
+def test_gpu_arm_cpu_baseline_fields():
+    """The cpu_baseline object of the GPU arm's line (host work only)."""
+    cb = bench.cpu_baseline_sample(SMALL)
+    assert cb["kind"] == "oracle" and cb["unit"] == "us/step" and cb["value"] > 0
+    assert cb["cores"] == 1 and cb["pages_cores"] >= 1 and cb["pages_sample"] > 0
+    assert cb["pages_factorized_per_s"] > 0 and cb["sample"] and cb["cpu_model"]
