@@ -108,7 +108,8 @@ typedef struct puzzlekv_store puzzlekv_store; /* opaque host handle */
  *   dense_pool: dense pages (sink, window, page being filled) for every
  *               (layer, sequence, KV head), K and V;
  *   factor_pool: one preallocated factor record per (layer, sequence, KV
- *               head, page) [PuzzleKV §3.3 ⑤ "preallocated storage"];
+ *               head, page) [PuzzleKV §3.3 ⑤: factors go to storage
+ *               set aside in advance];
  *   page_table: per (sequence, layer): current length and one descriptor
  *               per page (kind, slot);
  *   workspace:  split-K partial softmax states and the device status word
