@@ -20,6 +20,10 @@ Workloads:
   * Incremental compression during generation: Llama shapes, batch 8,
     4096-token prompts, 4096 decode steps with pages converted on the decode
     stream as they complete.
+  * The Llama shape at T = 32768 with INT4 factor records (PuzzleKV §4.3;
+    the oracle decodes the exactly dequantized codes), with the pages' own
+    P = 32, (r_K, r_V) = (16, 14) and a 64-token window, and with keys stored
+    before RoPE (theta 5e5) and turned at attention (PuzzleKV §4.1).
 """
 import numpy as np
 import pytest
@@ -66,7 +70,11 @@ def oracle_err(store, cfg, K, V, q_rows, got_rows, seq, layer, h):
     LV, RV = np.zeros((n, P, cfg.rank_v)), np.zeros((n, cfg.rank_v, cfg.head_dim))
     for p in np.nonzero(kinds == oracle.FACTORED)[0]:
         LK[p], RK[p], LV[p], RV[p] = read_record(raw[p * lay.rec_bytes:(p + 1) * lay.rec_bytes], lay)
-    ref = oracle.decode_head(q_rows, kinds, K, V, LK, RK, LV, RV, T, P)
+    theta = float(getattr(cfg, "rope_theta", 0.0))
+    if theta > 0:  # keys stored before RoPE: the oracle turns them at their positions too
+        ref = oracle.decode_head_rope(q_rows, kinds, K, V, LK, RK, LV, RV, T, P, theta)
+    else:
+        ref = oracle.decode_head(q_rows, kinds, K, V, LK, RK, LV, RV, T, P)
     return rel_err_rows(got_rows, ref)
 
 
@@ -192,3 +200,25 @@ def test_incremental_4096_steps_batch8(pkv):
     for i, l, _ in samples:
         check_table(store, cfg, i, l, T0 + steps)
     print("incremental worst", worst)
+
+
+@pytest.mark.parametrize("variant", ["int4", "p32", "prerope"])
+def test_llama32k_variants_full_size(pkv, variant):
+    T0 = 32768
+    rope = 5e5
+    if variant == "int4":
+        kw = dict(factor_int4=True)
+    elif variant == "p32":
+        kw = dict(page_size=32, rank_k=16, rank_v=14, recent_tokens=64)
+    else:  # keys given before RoPE: the store turns them, the generator leaves them unrotated
+        kw = dict(rope_theta=5e5)
+        rope = None
+    cfg = llama_cfg(pkv, 32, 1, T0 + 64, **kw)
+    spec = spec_of(cfg, inner_rank=12, n_outliers=4, rope_base=rope)
+    store = pkv.Store(cfg)
+    samples = [(0, 0, 0), (0, 31, 7)]
+    rows = {}
+    prefill_seq(store, spec, 0, T0, [(l, h) for _, l, h in samples], rows, 0)
+    worst = run_steps(store, cfg, spec, [0], [T0], 2, samples, rows, make_q(cfg, 1), check_steps={1})
+    check_table(store, cfg, 0, 31, T0 + 2)
+    print(variant, "worst", worst)
