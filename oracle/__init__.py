@@ -11,7 +11,9 @@ Citations name sections/equations of "PuzzleKV: Page-Wise Low-Rank
 Decomposition for KV Cache Compression" ([PuzzleKV]).
 
 Pins (see tests/test_oracle_pins.py): Eckart-Young energy identity,
-orthonormal factors, singular values against LAPACK, 2x2 closed form,
+orthonormal factors, singular values against LAPACK, the Gram route
+(top-r eigenvectors of X X^T from LAPACK's symmetric eigensolver give the
+same L L^T and L R), 2x2 closed form,
 brute force over the unit sphere on 4x4 pages, full-rank factorized
 attention equal to dense attention, closed-form attention special cases,
 token-level reclassification, the page's printed storage ratios, and RoPE

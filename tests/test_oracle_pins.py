@@ -65,6 +65,27 @@ def test_singular_values_match_lapack():
         assert np.abs(S - ref).max() <= 1e-12 * ref[0]
 
 
+def test_gram_route_gives_the_same_factors():
+    """PuzzleKV §3.3: the top-r eigenvectors Q_r of the Gram matrix X X^T give
+    L = Q_r and R = Q_r^T X, the same rank-r factorization as the truncated
+    SVD.  The oracle's one-sided Jacobi on X must match LAPACK's symmetric
+    eigensolver on X X^T: the same projector L L^T, the same product L R, and
+    the eigenvalues equal to the squared singular values."""
+    rng = np.random.default_rng(11)
+    for P, d, r in [(8, 8, 3), (32, 64, 8), (64, 128, 16), (64, 128, 24)]:
+        # well-separated spectrum around the cut, so the kept subspace is unique
+        U, _ = np.linalg.qr(rng.standard_normal((P, P)))
+        W, _ = np.linalg.qr(rng.standard_normal((d, P)))
+        sig = np.sort(rng.uniform(1.0, 2.0, P))[::-1] * np.where(np.arange(P) < r, 10.0, 1.0)
+        X = (U * sig) @ W.T
+        L, R, S = oracle.factorize(X, r)
+        lam, Q = np.linalg.eigh(X @ X.T)  # ascending
+        Qr = Q[:, ::-1][:, :r]
+        assert np.allclose(L @ L.T, Qr @ Qr.T, atol=1e-10)
+        assert np.allclose(L @ R, Qr @ (Qr.T @ X), atol=1e-10 * sig[0])
+        assert np.allclose(S[:r] ** 2, lam[::-1][:r], rtol=1e-10)
+
+
 def test_two_by_two_closed_form():
     """Singular values of a 2 x d page from the closed-form eigenvalues of
     the 2 x 2 Gram X X^T: (tr +- sqrt(tr^2 - 4 det)) / 2."""
