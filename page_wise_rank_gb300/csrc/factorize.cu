@@ -706,7 +706,8 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
 }
 
 // The 256-thread variant keeps four CTAs per SM (64 registers), which its
-// shared memory also allows: the Jacobi rounds are latency-bound.
+// shared memory also allows: four pages in flight keep the shared-memory
+// pipe, which bounds the Jacobi rounds, busy through each round's barriers.
 template <typename T, int P, int D, int NT>
 __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1) factorize_kernel(const FactorParams fp) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
