@@ -459,3 +459,22 @@ def test_prerope_decode_full_rank_is_dense_rope_attention():
     # (a reading error this path must not make)
     post = oracle.decode_head(q, kinds, Kr, V, *factors(Kr, 8), LV, RV, T, P)
     assert np.max(np.abs(post - low)) > 1e-4
+
+
+def test_batched_wrapper_equals_per_page():
+    """The batched oracle wrapper (independent pages on several host threads,
+    [PuzzleKV §3.3 ③]) gives, page for page, exactly the pinned single-page
+    factorization: a stride or offset mistake in the wrapper would move some
+    page's factors onto another page's slot."""
+    P, d, r = 32, 64, 8
+    X = np.stack([_page(P, d, seed=s) for s in range(21)])
+    X[5] = 0.0                              # all-zero page (C12)
+    X[9] = np.outer(X[9][:, 0], X[9][0])    # exactly rank one
+    ref = [oracle.factorize(X[i], r) for i in range(X.shape[0])]
+    for nthreads in (1, 4):
+        L, R, S = oracle.factorize_pages(X, r, nthreads)
+        for i, (Li, Ri, Si) in enumerate(ref):
+            assert np.array_equal(L[i], Li) and np.array_equal(R[i], Ri) and np.array_equal(S[i], Si), (nthreads, i)
+    # a wrapper that paired pages with the wrong slots would fail the comparison
+    L, R, S = oracle.factorize_pages(X[::-1].copy(), r, 4)
+    assert not np.array_equal(L[0] @ R[0], ref[0][0] @ ref[0][1])
