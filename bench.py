@@ -305,7 +305,7 @@ def gpu_arm(args, rank, world, local):
         e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         e0.record(stream)
         store.factorize_counters(stream)  # start from zero
-        store.factorize_pages(0, K, V, stream=stream)
+        store.load_prefill(0, K, V, stream=stream)
         e1.record(stream)
         st = store.check_device_status(stream)
         prefill_ms = e0.elapsed_time(e1)
@@ -606,7 +606,7 @@ def multi_seq_arm(args, rank, world, local):
             stream.synchronize()
             e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
             e0.record(stream)
-            store.factorize_pages(i, K, V, stream=stream)
+            store.load_prefill(i, K, V, stream=stream)
             e1.record(stream)
             stream.synchronize()
             prefill_ms += e0.elapsed_time(e1)

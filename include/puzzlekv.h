@@ -146,13 +146,37 @@ puzzlekv_status puzzlekv_store_destroy(puzzlekv_store *store);
  *   seq:  sequence slot in [0, max_batch); any previous content is dropped.
  *   T:    prompt length, 1 <= T <= max_tokens_per_seq.
  */
-puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *store, int32_t seq, const void *k,
-                                         const void *v, int32_t T, void *stream);
+puzzlekv_status puzzlekv_load_prefill(puzzlekv_store *store, int32_t seq, const void *k, const void *v,
+                                     int32_t T, void *stream);
+
+/*
+ * Factorize a chosen list of completed pages [PuzzleKV §3.3 ③ and ⑤: every
+ * completed page is factorized independently, once]: for each listed
+ * (seq_ids[i], page_ids[i]), the key and value pages of every layer and KV
+ * head, read from the dense pool, go into their preallocated factor records
+ * in one batched launch on `stream`.  The page keeps its kind: a page inside
+ * the local window stays dense for attention until it leaves the window,
+ * which then only switches it to its factors (as puzzlekv_convert_ready_pages
+ * does in the background).  Pages that already have factors are skipped
+ * (never refactorized), and so is a page listed twice.
+ *   seq_ids, page_ids: host, n entries.  A page must be complete (all P of
+ *            its tokens present) in every layer of its sequence and must not
+ *            be a sink page; any other entry (bad slot, empty sequence,
+ *            incomplete, sink or out-of-range page) makes the call return
+ *            PUZZLEKV_ERR_INVALID_ARG with nothing launched and no state
+ *            changed.
+ *   n:       number of entries; n = -1 ignores the lists (which may be NULL)
+ *            and factorizes every eligible page (complete, not a sink page,
+ *            no factors yet) of every sequence; n = 0 does nothing.
+ * The call orders `stream` after any pending background conversion batch.
+ */
+puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *store, const int32_t *seq_ids, const int32_t *page_ids,
+                                         int32_t n, void *stream);
 
 /*
  * Prefill compression of one layer of one sequence, for prompt processing
  * that produces the cache layer by layer [PuzzleKV §3.3 ①②③, §4.5 time to
- * first token]: as puzzlekv_factorize_pages restricted to `layer`.  The dense
+ * first token]: as puzzlekv_load_prefill restricted to `layer`.  The dense
  * pages and the page table are written on `stream`.  With async = 0 the
  * factorization also runs on `stream`.  With async = 1 it runs on the
  * store's internal low-priority stream, after the work already queued on
@@ -164,7 +188,7 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *store, int32_t seq, con
  *         so they must stay unchanged until work queued there completes --
  *         order their reuse after puzzlekv_wait_background, or tell the
  *         allocator that owns them about that stream.
- *   seq, T: as puzzlekv_factorize_pages; every layer of a sequence must be
+ *   seq, T: as puzzlekv_load_prefill; every layer of a sequence must be
  *         given the same T before it is decoded.
  */
 puzzlekv_status puzzlekv_factorize_layer(puzzlekv_store *store, int32_t seq, int32_t layer, const void *k,
@@ -197,6 +221,36 @@ puzzlekv_status puzzlekv_background_stream(puzzlekv_store *store, void **stream)
 puzzlekv_status puzzlekv_factorize_batch(const void *X, int32_t x_dtype, int64_t n, int32_t P, int32_t d,
                                          int32_t r, void *L, void *R, int32_t out_dtype, float *sigma,
                                          int32_t *status, void *stream);
+
+/*
+ * Byte size of one INT4 factor record of a store with these page size, head
+ * dimension and ranks [PuzzleKV §4.3] (the `records` stride of
+ * puzzlekv_factorize_batch_int4).  Host-only.
+ */
+puzzlekv_status puzzlekv_int4_record_bytes(int32_t P, int32_t d, int32_t rank_k, int32_t rank_v, int64_t *bytes);
+
+/*
+ * Stateless INT4 factorization of independent pages [PuzzleKV §4.3], the
+ * computation an INT4 store runs on each page: the rank-r factorization of
+ * puzzlekv_factorize_batch with every kept pair converged, singular values
+ * absorbed into both factors (L~ = U Sigma^{1/2}, R~ = Sigma^{1/2} W^T), and
+ * each factor quantized symmetrically to codes in [-7, 7] with fp16 scales
+ * (max |x| / 7 per group; code = x / scale rounded to nearest even, clamped).
+ *   X:       device bf16 [n][P][d].
+ *   kind:    0 = key pages (rank rank_k; groups: columns of L~ and of R~),
+ *            1 = value pages (rank rank_v; groups: rows of L~, columns of R~).
+ *   records: device, [n][puzzlekv_int4_record_bytes(P, d, rank_k, rank_v)]:
+ *            each page's code stream and scales for `kind` in the store's
+ *            record layout; the other kind's bytes are not written.
+ *   L_absorbed, R_absorbed: device fp32 [n][P][rp] and [n][rp][d] (rp = the
+ *            rank rounded up to a multiple of 8, padding zero), or NULL: the
+ *            absorbed factors the codes quantize, for checking the codes.
+ *   status:  device int32 or NULL, nonzero if an eigensolve hit its cap.
+ * Requires rank_k, rank_v <= P / 2 and the shapes of puzzlekv_factorize_batch.
+ */
+puzzlekv_status puzzlekv_factorize_batch_int4(const void *X, int64_t n, int32_t P, int32_t d, int32_t rank_k,
+                                              int32_t rank_v, int32_t kind, void *records, float *L_absorbed,
+                                              float *R_absorbed, int32_t *status, void *stream);
 
 /*
  * Append one decoded token per listed sequence to `layer` [PuzzleKV §3.3 ⑤]:
@@ -243,7 +297,7 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *store, int32_t layer, 
  *   them.  A batch's factors are first read when one of its pages becomes
  *   factorized; the first decode call (puzzlekv_decode_attention,
  *   puzzlekv_decode_step, the static-scratch variant) that reaches that
- *   length, and any prefill call (puzzlekv_factorize_pages,
+ *   length, and any prefill call (puzzlekv_load_prefill,
  *   puzzlekv_factorize_layer) that rewrites one of the batch's layers, makes
  *   its own stream wait for the batch.  puzzlekv_check_device_status and
  *   puzzlekv_factorize_counters synchronise the internal stream as well; the
@@ -280,10 +334,16 @@ puzzlekv_status puzzlekv_decode_step(puzzlekv_store *store, int32_t layer, const
  *   - Stores needing more than 16 MiB of scratch (8 bytes x max_batch x
  *     num_kv_heads rounded up to 256 bytes, + 4 bytes x max_batch x
  *     num_q_heads x 128 x (head_dim + 4)) are rejected with
- *     PUZZLEKV_ERR_CAPACITY before anything is launched.
+ *     PUZZLEKV_ERR_CAPACITY before anything is launched.  At head_dim 128
+ *     that allows max_batch up to 7 with 32 query heads, 3 with 64 and 31
+ *     with 8; at head_dim 64, 15 with 32 query heads.
  *   - The first call on a device looks up the array's device address
- *     (cudaGetSymbolAddress) with that device current; make that first call
- *     before any stream capture begins.
+ *     (cudaGetSymbolAddress) with that device current.  Under CUDA's lazy
+ *     module loading (the default) that lookup is also what loads the
+ *     library's device code on the device, and with it the 16 MiB array, so
+ *     the first call can take device memory: make it once as a warm-up,
+ *     before serving starts and before any stream capture begins.  Later
+ *     calls take none.
  *   - Every call shares the one array and clears its counters on `stream`
  *     before launching; calls whose kernels overlap on the GPU
  *     (other streams, other threads) race on it and must be serialised by
@@ -301,6 +361,29 @@ puzzlekv_status puzzlekv_decode_attention_static_scratch(puzzlekv_store *store, 
  */
 puzzlekv_status puzzlekv_store_stats(const puzzlekv_store *store, int32_t seq, int32_t layer, int32_t *length,
                                      int64_t *dense_pages, int64_t *factored_pages, int64_t *bytes_live);
+
+/*
+ * Test hook of the failure path (the page has no counterpart).  The store's
+ * next decode launch (puzzlekv_decode_attention, puzzlekv_decode_step or the
+ * static-scratch variant; bf16 stores) makes one of its shared-memory
+ * barriers expect 16 bytes that no copy delivers, so that a bounded wait
+ * runs out after wait_ns nanoseconds instead of the library's 1 s:
+ *   where = 1: the first unit that the first CTA of the first listed
+ *              sequence's KV head 0 streams; that CTA gives up, lets its
+ *              copies land and exits without its split state, so no output
+ *              row of that KV head is written;
+ *   where = 2: the split merge of every (sequence, KV head) whose split
+ *              states are staged in shared memory (all but calls with more
+ *              splits than its room holds); those output rows are not
+ *              written;
+ *   where = 0: clears a pending request.
+ * Nothing faults and nothing hangs: the launch ends (the drain of an
+ * abandoned barrier is itself bounded by 1 s) and the next
+ * puzzlekv_check_device_status returns PUZZLEKV_ERR_DEVICE_TIMEOUT and
+ * clears the split tickets, after which the store decodes normally.  The
+ * request applies to one launch.  wait_ns in [1e3, 1e9].
+ */
+puzzlekv_status puzzlekv_debug_fail_next_wait(puzzlekv_store *store, int32_t where, int64_t wait_ns);
 
 /*
  * Synchronise `stream`, read the device status word and clear it.  Returns

@@ -124,6 +124,34 @@ def factorize_batch(X: torch.Tensor, r: int, out_dtype: torch.dtype = torch.floa
     return L, R, S, status
 
 
+def int4_record_bytes(P: int, d: int, rank_k: int, rank_v: int) -> int:
+    """Bytes of one INT4 factor record (§4.3) of a store with these shapes."""
+    b = ctypes.c_int64()
+    check(lib().puzzlekv_int4_record_bytes(P, d, rank_k, rank_v, ctypes.byref(b)))
+    return b.value
+
+
+def factorize_batch_int4(X: torch.Tensor, rank_k: int, rank_v: int, kind: int, absorbed: bool = True,
+                         stream: Optional[torch.cuda.Stream] = None):
+    """INT4 records of independent bf16 pages X[n, P, d] (§4.3): returns (records uint8
+    [n, record_bytes], L~ fp32 [n, P, rp] or None, R~ fp32 [n, rp, d] or None, status[1]);
+    kind 0 = key pages at rank_k, 1 = value pages at rank_v."""
+    if X.dim() != 3 or X.dtype != torch.bfloat16:
+        raise ValueError("X must be bf16 [n, P, d]")
+    n, P, d = X.shape
+    _need(X, (n, P, d), torch.bfloat16, "X")
+    rb = int4_record_bytes(P, d, rank_k, rank_v)
+    rp = ((rank_k if kind == 0 else rank_v) + 7) // 8 * 8
+    rec = torch.zeros(n, rb, dtype=torch.uint8, device=X.device)
+    Lq = torch.empty(n, P, rp, dtype=torch.float32, device=X.device) if absorbed else None
+    Rq = torch.empty(n, rp, d, dtype=torch.float32, device=X.device) if absorbed else None
+    status = torch.zeros(1, dtype=torch.int32, device=X.device)
+    check(lib().puzzlekv_factorize_batch_int4(_ptr(X), n, P, d, rank_k, rank_v, kind, _ptr(rec),
+                                              _ptr(Lq) if absorbed else None, _ptr(Rq) if absorbed else None,
+                                              _ptr(status), _stream(stream)))
+    return rec, Lq, Rq, status
+
+
 class Store:
     """Paged factor store over four torch-allocated device buffers."""
 
@@ -159,14 +187,25 @@ class Store:
     def handle(self) -> ctypes.c_void_p:
         return self._h
 
-    def factorize_pages(self, seq: int, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
+    def load_prefill(self, seq: int, k: torch.Tensor, v: torch.Tensor, stream=None) -> None:
         """Prefill compression of sequence `seq` from dense k, v [L, H, T, d] (§3.3 ①②③)."""
         c = self.cfg
         T = k.shape[2]
         shape = (c.num_layers, c.num_kv_heads, T, c.head_dim)
         _need(k, shape, c.kv_dtype, "k")
         _need(v, shape, c.kv_dtype, "v")
-        check(lib().puzzlekv_factorize_pages(self._h, seq, _ptr(k), _ptr(v), T, _stream(stream)))
+        check(lib().puzzlekv_load_prefill(self._h, seq, _ptr(k), _ptr(v), T, _stream(stream)))
+
+    def factorize_pages(self, pages: Optional[Sequence[tuple]] = None, stream=None) -> None:
+        """Factorize the listed completed pages [(seq, page), ...] of every layer, or
+        every eligible page when `pages` is None (§3.3 ③⑤); pages with factors are skipped."""
+        if pages is None:
+            check(lib().puzzlekv_factorize_pages(self._h, None, None, -1, _stream(stream)))
+            return
+        n = len(pages)
+        seqs = (ctypes.c_int32 * max(n, 1))(*[int(b) for b, _ in pages])
+        pgs = (ctypes.c_int32 * max(n, 1))(*[int(p) for _, p in pages])
+        check(lib().puzzlekv_factorize_pages(self._h, seqs, pgs, n, _stream(stream)))
 
     def factorize_layer(self, seq: int, layer: int, k: torch.Tensor, v: torch.Tensor, background: bool = True,
                         stream=None) -> None:
@@ -264,6 +303,11 @@ class Store:
         check(lib().puzzlekv_store_stats(self._h, seq, layer, ctypes.byref(n), ctypes.byref(nd), ctypes.byref(nf),
                                          ctypes.byref(nb)))
         return {"length": n.value, "dense_pages": nd.value, "factored_pages": nf.value, "bytes_live": nb.value}
+
+    def debug_fail_next_wait(self, where: int, wait_ns: int = 100_000) -> None:
+        """Test hook of the failure path: the next decode launch's wait at `where`
+        (1 = a unit copy, 2 = the split merge) runs out after wait_ns (see include/puzzlekv.h)."""
+        check(lib().puzzlekv_debug_fail_next_wait(self._h, int(where), int(wait_ns)))
 
     def check_device_status(self, stream=None) -> int:
         """Synchronise and return the status code (raises nothing; OK = 0)."""

@@ -21,17 +21,21 @@ EXPORTED = (
     "puzzlekv_query_sizes",
     "puzzlekv_store_create",
     "puzzlekv_store_destroy",
+    "puzzlekv_load_prefill",
     "puzzlekv_factorize_pages",
     "puzzlekv_factorize_layer",
     "puzzlekv_wait_background",
     "puzzlekv_background_stream",
     "puzzlekv_factorize_batch",
+    "puzzlekv_int4_record_bytes",
+    "puzzlekv_factorize_batch_int4",
     "puzzlekv_append_token",
     "puzzlekv_decode_attention",
     "puzzlekv_decode_step",
     "puzzlekv_convert_ready_pages",
     "puzzlekv_decode_attention_static_scratch",
     "puzzlekv_store_stats",
+    "puzzlekv_debug_fail_next_wait",
     "puzzlekv_check_device_status",
     "puzzlekv_factorize_counters",
     "puzzlekv_classify_pages",
@@ -72,17 +76,21 @@ def lib() -> ctypes.CDLL:
         "puzzlekv_query_sizes": ([cfgp, szp, szp, szp, szp], i32),
         "puzzlekv_store_create": ([cfgp, vp, vp, vp, vp, vp, ctypes.POINTER(vp)], i32),
         "puzzlekv_store_destroy": ([vp], i32),
-        "puzzlekv_factorize_pages": ([vp, i32, vp, vp, i32, vp], i32),
+        "puzzlekv_load_prefill": ([vp, i32, vp, vp, i32, vp], i32),
+        "puzzlekv_factorize_pages": ([vp, i32p, i32p, i32, vp], i32),
         "puzzlekv_factorize_layer": ([vp, i32, i32, vp, vp, i32, i32, vp], i32),
         "puzzlekv_wait_background": ([vp, vp], i32),
         "puzzlekv_background_stream": ([vp, ctypes.POINTER(vp)], i32),
         "puzzlekv_factorize_batch": ([vp, i32, i64, i32, i32, i32, vp, vp, i32, vp, vp, vp], i32),
+        "puzzlekv_int4_record_bytes": ([i32, i32, i32, i32, i64p], i32),
+        "puzzlekv_factorize_batch_int4": ([vp, i64, i32, i32, i32, i32, i32, vp, vp, vp, vp, vp], i32),
         "puzzlekv_append_token": ([vp, i32, vp, vp, i32p, i32, vp], i32),
         "puzzlekv_decode_attention": ([vp, i32, vp, vp, i32p, i32, vp], i32),
         "puzzlekv_decode_attention_static_scratch": ([vp, i32, vp, vp, i32p, i32, vp], i32),
         "puzzlekv_decode_step": ([vp, i32, vp, vp, vp, vp, i32p, i32, vp], i32),
         "puzzlekv_convert_ready_pages": ([vp, vp], i32),
         "puzzlekv_store_stats": ([vp, i32, i32, i32p, i64p, i64p, i64p], i32),
+        "puzzlekv_debug_fail_next_wait": ([vp, i32, i64], i32),
         "puzzlekv_check_device_status": ([vp, vp], i32),
         "puzzlekv_factorize_counters": ([vp, vp, i64p, i64p], i32),
         "puzzlekv_classify_pages": ([i32, i32, i32, i32, i32p, i32], i32),

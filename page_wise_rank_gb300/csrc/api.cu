@@ -129,9 +129,15 @@ struct puzzlekv_store {
     Layout y;
     char *dense_pool, *factor_pool, *page_table, *workspace;
     std::vector<int> len;    // host mirror [seq][layer]; -1 = empty slot
-    std::vector<int> conv_upto;  // [seq][layer]: pages below this index (past the sink) have factor records
+    // Which pages have factor records, per (seq, layer): every page in
+    // [sink_pages, conv_upto) and, above it, the pages marked in `marked`
+    // (factorized out of order by a page-list call).
+    std::vector<int> conv_upto;                   // [seq][layer]
+    std::vector<std::vector<uint8_t>> marked;     // [seq][layer][page], allocated on first use
     std::vector<int2> job_host;  // staging of the batched-conversion job list
     bool after_decode = false;   // the store's latest launch was a decode launch
+    int fail_next = 0;           // failure-path test hook for the next decode launch (0 = off)
+    uint64_t fail_wait_ns = 0;   // its waits' limit
     int num_sms;
     // Batched conversions run on an internal low-priority stream.  A batch's
     // factor records are first read when one of its pages becomes
@@ -226,6 +232,28 @@ static int *lengths_ptr(puzzlekv_store *s) { return reinterpret_cast<int *>(s->p
 static int *desc_ptr(puzzlekv_store *s) { return reinterpret_cast<int *>(s->page_table + s->y.desc_offset); }
 static int *status_ptr(puzzlekv_store *s) { return reinterpret_cast<int *>(s->workspace); }
 
+// Factor-record bookkeeping of (seq b, layer l).
+static bool has_factors(const puzzlekv_store *s, int b, int l, int p) {
+    const size_t i = (size_t)b * s->y.L + l;
+    if (p < s->conv_upto[i]) return p >= s->y.sink_pages;
+    const std::vector<uint8_t> &m = s->marked[i];
+    return (size_t)p < m.size() && m[p] != 0;
+}
+static void set_factors(puzzlekv_store *s, int b, int l, int p) {
+    const size_t i = (size_t)b * s->y.L + l;
+    int &upto = s->conv_upto[i];
+    std::vector<uint8_t> &m = s->marked[i];
+    if (p < upto) return;
+    if (m.size() < (size_t)s->y.n_pg_max) m.assign(s->y.n_pg_max, 0);
+    m[p] = 1;
+    while (upto < s->y.n_pg_max && m[upto]) m[upto++] = 0;  // extend the prefix over marked pages
+}
+static void reset_factors(puzzlekv_store *s, int b, int l, int upto) {
+    const size_t i = (size_t)b * s->y.L + l;
+    s->conv_upto[i] = upto;
+    std::vector<uint8_t>().swap(s->marked[i]);
+}
+
 extern "C" {
 
 const char *puzzlekv_last_error(void) { return g_last_error.c_str(); }
@@ -277,6 +305,7 @@ puzzlekv_status puzzlekv_store_create(const puzzlekv_config *cfg, void *dense_po
     s->workspace = static_cast<char *>(workspace);
     s->len.assign((size_t)cfg->max_batch * cfg->num_layers, -1);
     s->conv_upto.assign((size_t)cfg->max_batch * cfg->num_layers, 0);
+    s->marked.resize((size_t)cfg->max_batch * cfg->num_layers);
     s->num_sms = sm_count();
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     cudaError_t e = cudaMemsetAsync(dense_pool, 0, s->y.dense_pool_bytes, strm);
@@ -401,16 +430,16 @@ static puzzlekv_status prefill(puzzlekv_store *s, int32_t seq, int32_t layer0, i
     }
     for (int l = layer0; l < layer0 + n_layers; ++l) {
         s->len[(size_t)seq * y.L + l] = T;
-        s->conv_upto[(size_t)seq * y.L + l] = f_lo >= 0 ? f_hi : y.sink_pages;
+        reset_factors(s, seq, l, f_lo >= 0 ? f_hi : y.sink_pages);
     }
     return PUZZLEKV_OK;
 }
 
 extern "C" {
 
-puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, int32_t seq, const void *k, const void *v, int32_t T,
-                                         void *stream) {
-    NvtxRange nvtx_range("puzzlekv_factorize_pages");
+puzzlekv_status puzzlekv_load_prefill(puzzlekv_store *s, int32_t seq, const void *k, const void *v, int32_t T,
+                                     void *stream) {
+    NvtxRange nvtx_range("puzzlekv_load_prefill");
     if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
     return prefill(s, seq, 0, s->y.L, k, v, T, false, static_cast<cudaStream_t>(stream));
 }
@@ -468,6 +497,49 @@ puzzlekv_status puzzlekv_factorize_batch(const void *X, int32_t x_dtype, int64_t
     return PUZZLEKV_OK;
 }
 
+puzzlekv_status puzzlekv_int4_record_bytes(int32_t P, int32_t d, int32_t rank_k, int32_t rank_v, int64_t *bytes) {
+    if (!bytes) return fail(PUZZLEKV_ERR_INVALID_ARG, "bytes is NULL");
+    if ((P != 16 && P != 32 && P != 64) || (d != 64 && d != 128) || P > d)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "need P in {16,32,64}, d in {64,128}, P <= d");
+    if (rank_k < 1 || rank_v < 1 || rank_k > P / 2 || rank_v > P / 2)
+        return fail(PUZZLEKV_ERR_UNSUPPORTED, "INT4 ranks must be in [1, P/2]");
+    Layout y;
+    make_layout(y, 1, 1, 1, d, P, rank_k, rank_v, 0, 0, 1, P, 1, 1);
+    *bytes = (int64_t)y.rec_bytes;
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_factorize_batch_int4(const void *X, int64_t n, int32_t P, int32_t d, int32_t rank_k,
+                                              int32_t rank_v, int32_t kind, void *records, float *L_absorbed,
+                                              float *R_absorbed, int32_t *status, void *stream) {
+    NvtxRange nvtx_range("puzzlekv_factorize_batch_int4");
+    int64_t rec_bytes = 0;
+    puzzlekv_status st = puzzlekv_int4_record_bytes(P, d, rank_k, rank_v, &rec_bytes);
+    if (st != PUZZLEKV_OK) return st;
+    if (n < 0) return fail(PUZZLEKV_ERR_INVALID_ARG, "n must be >= 0");
+    if (kind != 0 && kind != 1) return fail(PUZZLEKV_ERR_INVALID_ARG, "kind must be 0 (key) or 1 (value)");
+    if (n == 0) return PUZZLEKV_OK;
+    if (!X || !records || !aligned16(X) || !aligned16(records) || !aligned16(L_absorbed) || !aligned16(R_absorbed))
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "X and records must be non-NULL; all pointers 16-byte aligned");
+    FactorParams fp{};
+    fp.mode = FACT_MODE_BATCH_Q4;
+    fp.n_jobs = (long)n;
+    fp.max_sweeps = 24;
+    fp.status = status;
+    make_layout(fp.y, 1, 1, 1, d, P, rank_k, rank_v, 0, 0, 1, P, 1, 1);
+    fp.P = P;
+    fp.d = d;
+    fp.x_esz = 2;
+    fp.x_base = static_cast<const char *>(X);
+    fp.q4_kind = kind;
+    fp.q4_records = static_cast<char *>(records);
+    fp.q4_L = L_absorbed;
+    fp.q4_R = R_absorbed;
+    cudaError_t e = launch_factorize(fp, sm_count(), static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail(e, "factorize_batch_int4 launch");
+    return PUZZLEKV_OK;
+}
+
 // [PuzzleKV §3.3 ⑤]: the page (if any) that growing a sequence from T to
 // T + 1 tokens moves out of the dense region; at most one per step.
 static int converted_page(const Layout &y, int T) {
@@ -496,6 +568,9 @@ static void fill_decode_params(puzzlekv_store *s, int32_t layer, const void *q, 
     dp.rope_delta = reinterpret_cast<const float2 *>(s->workspace + y.rope_delta_offset);
     dp.tickets = reinterpret_cast<int *>(s->workspace + y.ticket_offset);
     dp.wait_first = s->after_decode ? 0 : 1;
+    dp.inject = s->fail_next;  // consumed by this launch
+    dp.wait_ns = s->fail_next ? s->fail_wait_ns : 0;
+    s->fail_next = 0;
     dp.out = out;
     dp.status = reinterpret_cast<int *>(s->workspace);
     dp.layer = layer;
@@ -559,12 +634,11 @@ puzzlekv_status puzzlekv_append_token(puzzlekv_store *s, int32_t layer, const vo
         ap.pos[i] = T;
         const int conv = converted_page(y, T);
         ap.conv_page[i] = conv;  // descriptor flip
-        int &upto = s->conv_upto[(size_t)b * y.L + layer];
-        if (conv >= upto) {  // not factorized ahead of time: factorize it now, before attention
+        if (conv >= 0 && !has_factors(s, b, layer, conv)) {  // not factorized ahead of time: now, before attention
             fp.conv_seq[fp.n_conv] = b;
             fp.conv_page[fp.n_conv] = conv;
             fp.n_conv++;
-            upto = conv + 1;
+            set_factors(s, b, layer, conv);
         }
     }
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
@@ -637,12 +711,11 @@ puzzlekv_status puzzlekv_decode_step(puzzlekv_store *s, int32_t layer, const voi
         const int b = seq_ids[i];
         const int conv = converted_page(y, s->len[(size_t)b * y.L + layer]);
         dp.conv_page[i] = conv;  // descriptor flip
-        int &upto = s->conv_upto[(size_t)b * y.L + layer];
-        if (conv >= upto) {  // not factorized ahead of time: factorize it now, before attention
+        if (conv >= 0 && !has_factors(s, b, layer, conv)) {  // not factorized ahead of time: now, before attention
             fp.conv_seq[fp.n_conv] = b;
             fp.conv_page[fp.n_conv] = conv;
             fp.n_conv++;
-            upto = conv + 1;
+            set_factors(s, b, layer, conv);
         }
     }
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
@@ -672,6 +745,81 @@ puzzlekv_status puzzlekv_decode_step(puzzlekv_store *s, int32_t layer, const voi
     return PUZZLEKV_OK;
 }
 
+puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, const int32_t *seq_ids, const int32_t *page_ids,
+                                         int32_t n, void *stream) {
+    NvtxRange nvtx_range("puzzlekv_factorize_pages");
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    if (n < -1) return fail(PUZZLEKV_ERR_INVALID_ARG, "n must be -1 (all eligible pages) or >= 0 (got %d)", n);
+    if (n > 0 && (!seq_ids || !page_ids)) return fail(PUZZLEKV_ERR_INVALID_ARG, "seq_ids and page_ids must be non-NULL");
+    const Layout &y = s->y;
+    // every check first: a bad entry changes nothing
+    auto complete_pages = [&](int b) {  // pages complete in every layer of sequence b (-1: empty slot)
+        int c = INT_MAX;
+        for (int l = 0; l < y.L; ++l) {
+            const int T = s->len[(size_t)b * y.L + l];
+            if (T < 1) return -1;
+            c = std::min(c, T / y.P);
+        }
+        return c;
+    };
+    for (int i = 0; i < n; ++i) {
+        const int b = seq_ids[i], p = page_ids[i];
+        if (b < 0 || b >= y.Bmax) return fail(PUZZLEKV_ERR_INVALID_ARG, "entry %d: seq id %d out of range", i, b);
+        const int c = complete_pages(b);
+        if (c < 0) return fail(PUZZLEKV_ERR_INVALID_ARG, "entry %d: sequence %d holds no tokens", i, b);
+        if (p < y.sink_pages || p >= c)
+            return fail(PUZZLEKV_ERR_INVALID_ARG,
+                        "entry %d: page %d of sequence %d is not eligible (sink pages end at %d, complete pages at %d)",
+                        i, p, b, y.sink_pages, c);
+    }
+    // the jobs: every layer of each page without factors, marked as it is
+    // listed (so a page listed twice is factorized once)
+    s->job_host.clear();
+    auto add = [&](int b, int p) {
+        for (int l = 0; l < y.L; ++l)
+            if (!has_factors(s, b, l, p)) {
+                s->job_host.push_back(make_int2((b << 8) | l, p));
+                set_factors(s, b, l, p);
+            }
+    };
+    if (n == -1) {
+        for (int b = 0; b < y.Bmax; ++b) {
+            const int c = complete_pages(b);
+            for (int p = y.sink_pages; p < c; ++p) add(b, p);
+        }
+    } else {
+        for (int i = 0; i < n; ++i) add(seq_ids[i], page_ids[i]);
+    }
+    if (s->job_host.empty()) return PUZZLEKV_OK;
+    if ((int)s->job_host.size() > y.max_conv_jobs)
+        return fail(PUZZLEKV_ERR_CAPACITY, "internal: conversion list overflow");
+    cudaStream_t strm = static_cast<cudaStream_t>(stream);
+    // the job list region is shared with the background batches: order this
+    // call after every pending one (later batches start after this stream's work)
+    wait_conversions(s, strm, nullptr, nullptr, 0, true);
+    int2 *dev_jobs = reinterpret_cast<int2 *>(s->workspace + y.jobs_offset);
+    // pageable source: the copy has consumed job_host when cudaMemcpyAsync returns
+    cudaError_t e = cudaMemcpyAsync(dev_jobs, s->job_host.data(), s->job_host.size() * sizeof(int2),
+                                    cudaMemcpyHostToDevice, strm);
+    if (e != cudaSuccess) return cuda_fail(e, "page list upload");
+    FactorParams fp{};
+    fp.mode = FACT_MODE_CONVERT_LIST;
+    fp.max_sweeps = 24;
+    fp.status = status_ptr(s);
+    fp.y = y;
+    fp.P = y.P;
+    fp.d = y.d;
+    fp.x_esz = y.esz;
+    fp.factor_pool = s->factor_pool;
+    fp.dense_pool = s->dense_pool;
+    fp.conv_list = dev_jobs;
+    fp.n_jobs = (long)s->job_host.size() * y.H * 2;
+    e = launch_factorize(fp, s->num_sms, strm);
+    s->after_decode = false;
+    if (e != cudaSuccess) return cuda_fail(e, "page list factorization launch");
+    return PUZZLEKV_OK;
+}
+
 puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
     NvtxRange nvtx_range("puzzlekv_convert_ready_pages");
     if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
@@ -681,14 +829,15 @@ puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
         for (int l = 0; l < y.L; ++l) {
             const int T = s->len[(size_t)b * y.L + l];
             if (T < 1) continue;
-            int &upto = s->conv_upto[(size_t)b * y.L + l];
             const int complete = T / y.P;  // pages whose P tokens are all present
-            for (int p = std::max(upto, y.sink_pages); p < complete; ++p) {
+            for (int p = std::max(s->conv_upto[(size_t)b * y.L + l], y.sink_pages); p < complete; ++p) {
+                if (has_factors(s, b, l, p)) continue;
                 if ((int)s->job_host.size() >= y.max_conv_jobs)
                     return fail(PUZZLEKV_ERR_CAPACITY, "internal: conversion list overflow");
                 s->job_host.push_back(make_int2((b << 8) | l, p));
             }
-            upto = std::max(upto, complete);
+            for (int p = std::max(s->conv_upto[(size_t)b * y.L + l], y.sink_pages); p < complete; ++p)
+                set_factors(s, b, l, p);
         }
     }
     if (s->job_host.empty()) return PUZZLEKV_OK;
@@ -751,6 +900,17 @@ puzzlekv_status puzzlekv_store_stats(const puzzlekv_store *s, int32_t seq, int32
     if (dense_pages) *dense_pages = nd;
     if (factored_pages) *factored_pages = nf;
     if (bytes_live) *bytes_live = bytes;
+    return PUZZLEKV_OK;
+}
+
+puzzlekv_status puzzlekv_debug_fail_next_wait(puzzlekv_store *s, int32_t where, int64_t wait_ns) {
+    if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
+    if (where < 0 || where > 2) return fail(PUZZLEKV_ERR_INVALID_ARG, "where must be 0, 1 or 2 (got %d)", where);
+    if (wait_ns < 1000 || wait_ns > (int64_t)1000000000)
+        return fail(PUZZLEKV_ERR_INVALID_ARG, "wait_ns must be in [1e3, 1e9] (got %lld)", (long long)wait_ns);
+    if (s->y.dtype != 1) return fail(PUZZLEKV_ERR_UNSUPPORTED, "the hook exists on the bf16 decode path only");
+    s->fail_next = where;
+    s->fail_wait_ns = (uint64_t)wait_ns;
     return PUZZLEKV_OK;
 }
 

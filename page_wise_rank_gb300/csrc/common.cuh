@@ -57,17 +57,18 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Longest time any spin-wait of the library waits before it gives up.
 constexpr uint64_t WAIT_NS = 1000000000ull;
 
-// Wait for phase `parity` of `bar` to complete, giving up after WAIT_NS of
-// polling (each try_wait itself suspends for a short while).  On give-up the
-// device status word records a timeout and false is returned.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status) {
+// Wait for phase `parity` of `bar` to complete, giving up after `limit_ns`
+// of polling (each try_wait itself suspends for a short while).  On give-up
+// the device status word records a timeout and false is returned.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, uint32_t parity, int *status,
+                                                  uint64_t limit_ns = WAIT_NS) {
     if (mbar_try_wait(bar, parity)) return true;
     const uint64_t t0 = global_ns();
     for (uint32_t i = 1;; ++i) {
         if (mbar_try_wait(bar, parity)) return true;
         if (i >= 64) {
             __nanosleep(64);
-            if ((i & 63) == 0 && global_ns() - t0 > WAIT_NS) break;
+            if ((i & 63) == 0 && global_ns() - t0 > limit_ns) break;
         }
     }
     if (status) atomicOr(status + STATUS_TIMEOUT, 1);
@@ -114,8 +115,6 @@ __device__ __forceinline__ void fence_proxy_async_global() {
     asm volatile("fence.proxy.async.global;" ::: "memory");
 }
 
-// Order this thread's earlier generic-proxy accesses to shared memory before
-// its later async-proxy (bulk copy) writes there.
 // Atomic add with release and acquire semantics at GPU scope: writes that
 // happen before it (a CTA barrier included) are visible to whoever later
 // acquires the location, and writes released to the location before it are
@@ -126,6 +125,8 @@ __device__ __forceinline__ int atom_add_acq_rel_gpu(int *p, int v) {
     return old;
 }
 
+// Order this thread's earlier generic-proxy accesses to shared memory before
+// its later async-proxy (bulk copy) writes there.
 __device__ __forceinline__ void fence_proxy_async_shared() { asm volatile("fence.proxy.async.shared::cta;" ::: "memory"); }
 
 // Programmatic dependent launch: wait until the preceding grid in the stream

@@ -25,7 +25,6 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
     constexpr int DPL = D / 32;         // head dims per lane
     const float scale = rsqrtf((float)D);
     __shared__ __align__(16) float comb[NWC][8][D + 4];
-    __shared__ float scratch[MAX_SPLITS * 8 + 8];
     __shared__ int last;
 
     float q[8][DPL];  // this lane's head dims of each query row
@@ -158,7 +157,7 @@ __global__ void __launch_bounds__(NWC * 32) decode_f32_kernel(const DecodeParams
     }
     __syncthreads();
     const int ns = (n_pages + prm.chunk - 1) / prm.chunk;
-    finish_split<D, NWC>(prm, &comb[0][0][0], b_idx, b, h, split, ns, scratch, &last);
+    finish_split<D, NWC>(prm, &comb[0][0][0], b_idx, b, h, split, ns, &last);
 }
 
 // ---------------------------------------------------------------- launch

@@ -98,93 +98,139 @@ __device__ __forceinline__ int unit_valid(int T, int first, int PU) {
     return v < 0 ? 0 : (v > PU ? PU : v);
 }
 
+// Dense units of one CTA's page range at most: every dense page of a sequence
+// (sink, window, the page being filled) cut into at most four units.
+constexpr int MAX_DENSE_UNITS = MAX_DENSE_PAGES * 4;
+
 struct DecodeShared {
     uint64_t merge_bar;  // completion of the split-merge bulk copies
     int failed;
     int last;
-    int unit_info[NS_MAX];
+    int n_pre, n_dense;  // dense units before the factorized stretch, and in all
+    int slot_info[NS_MAX];                // per slot: page << 3 | dense << 2 | unit
+    int dense_units[MAX_DENSE_UNITS];     // the same code for each dense unit, in page order
 };
 
 
-// Walk over the units of a page range [p, pe): one per factorized page, one
-// per non-empty DU-th of a dense page.  The range is cut into three segments
-// by the classification rule -- dense sink pages, factorized pages [a1, a2)
-// (their records are contiguous in the factor pool), dense window pages --
-// so a step costs a few integer operations.  Page kinds follow page_kind()
-// at the call's length (the host mirror passes it, so nothing is read from
-// global memory before the first bulk copy).
-struct UnitCursor {
-    int p, half, a1, a2, pe, T;
-    template <int P, int DU>
-    __device__ __forceinline__ bool next(int &pg, int &hf, bool &dense) {
-        while (p < pe) {
-            if (p >= a1 && p < a2) {
-                pg = p++;
-                hf = 0;
-                dense = false;
-                return true;
-            }
-            const int pp = p, hh = half;
-            if (++half == DU) {
-                half = 0;
-                ++p;
-            }
-            if (T > pp * P + hh * (P / DU)) {
-                pg = pp;
-                hf = hh;
-                dense = true;
-                return true;
-            }
-        }
-        return false;
-    }
-};
-
-// Split hand-off, eq. (5).  `comb` holds the NW warp states of this CTA
+// Split hand-off, eq. (5).  `comb` holds the NW warp states of a CTA
 // ([warp][g][m, l, pad, pad, o...], D + 4 floats per row, 16-byte aligned, m
-// in log2 units); they are
-// merged into the CTA's state, which every CTA writes to the workspace and
-// makes visible before it takes its arrival
-// ticket for (b, h).  The CTA that takes the last ticket therefore sees every
-// state: it merges them in split order (the same sums whichever CTA that is)
-// and writes `out`, then resets the ticket.  `scratch` holds MAX_SPLITS * 8
-// + 8 floats.  With `merge_bar` (an mbarrier of count 1 in its first phase)
-// and room in `stage_buf` (16-byte aligned shared memory, `stage_cap` bytes,
-// may overlap `comb`), the states arrive by one bulk copy per query head;
-// otherwise they are read from global memory.
+// in log2 units).  cta_state merges them into the CTA's state for element e
+// = (head g, columns 4j .. 4j+3): o (a float4) and (m, l).
 template <int D, int NW>
-__device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_idx, int b, int h, int split, int ns,
-                             float *scratch, int *last, float *stage_buf = nullptr,
-                             size_t stage_cap = 0, uint64_t *merge_bar = nullptr) {
-    const Layout &y = prm.y;
-    const int G = y.G, S = y.part_stride;
-    int *arrivals = prm.tickets + y.ticket_index(b, h);
-    // the CTA's state, one float4 of o per thread (head g, columns 4j .. 4j+3),
-    // written straight to its workspace row; j = 0 also writes m and l
+__device__ __forceinline__ void cta_state(const float *comb, int e, float4 &acc, float2 &ml) {
+    const int g = e / (D / 4), j = e % (D / 4);
+    float mw[NW], M = -INFINITY;
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        mw[w] = comb[(w * 8 + g) * (D + 4)];
+        M = fmaxf(M, mw[w]);
+    }
+    float L = 0.f;
+    acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int w = 0; w < NW; ++w) {
+        const float *row = comb + (w * 8 + g) * (D + 4);
+        const float c = mw[w] == -INFINITY ? 0.f : ex2_approx(mw[w] - M);
+        const float4 v = reinterpret_cast<const float4 *>(row + 4)[j];
+        L = fmaf(c, row[1], L);
+        acc.x = fmaf(c, v.x, acc.x);
+        acc.y = fmaf(c, v.y, acc.y);
+        acc.z = fmaf(c, v.z, acc.z);
+        acc.w = fmaf(c, v.w, acc.w);
+    }
+    ml = make_float2(M, L);
+}
+
+// The merge of eq. (5) over the ns split states of each of the G query heads
+// of (b, h), written to `out`.  One pass per output float4: the largest m
+// over the splits, then the weights 2^(m_s - m), the normaliser and o summed
+// in split order (the same sums whichever CTA merges, so results are
+// bitwise reproducible).  ld1(g, s, k) and ld4(g, s, k) read float k (or
+// floats k .. k+3) of split s's row of head g.
+template <int D, typename LD1, typename LD4>
+__device__ __forceinline__ void merge_states(const DecodeParams &prm, int b_idx, int h, int ns, LD1 ld1, LD4 ld4) {
+    const int G = prm.y.G;
     for (int e = threadIdx.x; e < G * (D / 4); e += blockDim.x) {
         const int g = e / (D / 4), j = e % (D / 4);
-        float mw[NW], M = -INFINITY;
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            mw[w] = comb[(w * 8 + g) * (D + 4)];
-            M = fmaxf(M, mw[w]);
-        }
+        float M = -INFINITY;
+        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, ld1(g, sp, 0));
         float L = 0.f;
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-        for (int w = 0; w < NW; ++w) {
-            const float *row = comb + (w * 8 + g) * (D + 4);
-            const float c = mw[w] == -INFINITY ? 0.f : ex2_approx(mw[w] - M);
-            const float4 v = reinterpret_cast<const float4 *>(row + 4)[j];
-            L = fmaf(c, row[1], L);
+#pragma unroll 4
+        for (int sp = 0; sp < ns; ++sp) {
+            const float m = ld1(g, sp, 0);
+            const float c = m == -INFINITY ? 0.f : ex2_approx(m - M);
+            L = fmaf(c, ld1(g, sp, 1), L);
+            const float4 v = ld4(g, sp, 4 + 4 * j);
             acc.x = fmaf(c, v.x, acc.x);
             acc.y = fmaf(c, v.y, acc.y);
             acc.z = fmaf(c, v.z, acc.z);
             acc.w = fmaf(c, v.w, acc.w);
         }
+        const float il = 1.f / L;
+        reinterpret_cast<float4 *>(prm.out + ((size_t)b_idx * prm.y.Hq + h * G + g) * D)[j] =
+            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+    }
+}
+
+// Reads of split states staged in shared memory at `sb` (rows of S floats,
+// head g's ns rows contiguous).
+struct StagedRows {
+    uint32_t sb;
+    int ns, S;
+    __device__ __forceinline__ float one(int g, int sp, int k) const {
+        float v;
+        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(sb + (uint32_t)(((g * ns + sp) * S + k) * 4)));
+        return v;
+    }
+    __device__ __forceinline__ float4 four(int g, int sp, int k) const {
+        float4 v;
+        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
+                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+                     : "r"(sb + (uint32_t)(((g * ns + sp) * S + k) * 4)));
+        return v;
+    }
+};
+
+// The merge bulk copies of a staged hand-off were issued on `bar`: wait for
+// them (bounded by the launch's limit) and agree over the CTA whether they
+// landed.  If a wait gave up, the copies are given one more bounded wait so
+// that none is still writing when the CTA exits, and false is returned: the
+// caller then skips the merge, leaves `out` and the ticket as they are, and
+// the status word (set by the wait) tells the host, whose status check also
+// clears the tickets.
+__device__ __forceinline__ bool merge_copies_landed(const DecodeParams &prm, uint64_t *bar) {
+    const uint64_t lim = prm.wait_ns ? prm.wait_ns : WAIT_NS;
+    const bool ok = __syncthreads_and(mbar_wait_bounded(bar, 0, prm.status, lim) ? 1 : 0) != 0;
+    if (!ok && threadIdx.x == 0) mbar_wait_bounded(bar, 0, nullptr);
+    return ok;
+}
+
+// Publishing hand-off: the CTA's state goes to its workspace row and becomes
+// visible before the CTA takes its arrival ticket for (b, h) with one
+// acquire-release atomic; the CTA that takes the last ticket therefore sees
+// every state, merges them and writes `out`, then resets the ticket.  With
+// `merge_bar` (an mbarrier of count 1 in its first phase) and room in
+// `stage_buf` (16-byte aligned shared memory, `stage_cap` bytes, may overlap
+// `comb`) the states arrive by one bulk copy per query head; otherwise they
+// are read from global memory.  Returns true in the CTA that merged.
+template <int D, int NW>
+__device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_idx, int b, int h, int split, int ns,
+                             int *last, float *stage_buf = nullptr, size_t stage_cap = 0,
+                             uint64_t *merge_bar = nullptr) {
+    const Layout &y = prm.y;
+    const int G = y.G, S = y.part_stride;
+    int *arrivals = prm.tickets + y.ticket_index(b, h);
+    // the CTA's state, one float4 of o per thread, written straight to its
+    // workspace row; j = 0 also writes m and l
+    for (int e = threadIdx.x; e < G * (D / 4); e += blockDim.x) {
+        float4 acc;
+        float2 ml;
+        cta_state<D, NW>(comb, e, acc, ml);
+        const int g = e / (D / 4), j = e % (D / 4);
         float *prow = prm.partials + y.partial_index(b, h * G + g, split) * S;
         reinterpret_cast<float4 *>(prow + 4)[j] = acc;
-        if (j == 0) reinterpret_cast<float4 *>(prow)[0] = make_float4(M, L, 0.f, 0.f);
+        if (j == 0) reinterpret_cast<float4 *>(prow)[0] = make_float4(ml.x, ml.y, 0.f, 0.f);
     }
     // rows of head g are contiguous: partial_index(b, h G + g, 0 .. ns-1)
     const bool staged = merge_bar != nullptr && stage_buf != nullptr && (size_t)G * ns * S * 4 <= stage_cap;
@@ -194,78 +240,31 @@ __device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_i
         // visible before its ticket; acquire: the last CTA sees every state
         const bool is_last = atom_add_acq_rel_gpu(arrivals, 1) == ns - 1;
         *last = is_last;
-        if (is_last) {
-            if (staged) {  // the states were written through the generic proxy
-                fence_proxy_async_global();
-                fence_proxy_async_shared();  // the warp states in stage_buf have been read
-                const uint32_t bytes = (uint32_t)ns * S * 4;
-                mbar_arrive_expect_tx(merge_bar, (uint32_t)G * bytes);
-                for (int g = 0; g < G; ++g)
-                    bulk_g2s(stage_buf + (size_t)g * ns * S, prm.partials + y.partial_index(b, h * G + g, 0) * S,
-                             bytes, merge_bar);
-            }
+        if (is_last && staged) {  // the states were written through the generic proxy
+            fence_proxy_async_global();
+            fence_proxy_async_shared();  // the warp states in stage_buf have been read
+            const uint32_t bytes = (uint32_t)ns * S * 4;
+            mbar_arrive_expect_tx(merge_bar, (uint32_t)G * bytes + (prm.inject == 2 ? 16u : 0u));
+            for (int g = 0; g < G; ++g)
+                bulk_g2s(stage_buf + (size_t)g * ns * S, prm.partials + y.partial_index(b, h * G + g, 0) * S,
+                         bytes, merge_bar);
         }
     }
     __syncthreads();
     if (!*last) return false;
-    float *wt = scratch, *iL = scratch + MAX_SPLITS * 8;  // weights [g][split], 1 / normaliser [g]
-    auto merge = [&](auto ld1, auto ld4) {
-        const int nwarps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-        for (int g = warp; g < G; g += nwarps) {  // per head: max, weights and normaliser over the splits
-            float M = -INFINITY;
-            for (int sp = lane; sp < ns; sp += 32) M = fmaxf(M, ld1(g, sp, 0));
-            M = warp_max(M);
-            float L = 0.f;
-            for (int sp = lane; sp < ns; sp += 32) {
-                const float m = ld1(g, sp, 0);
-                const float c = m == -INFINITY ? 0.f : ex2_approx(m - M);
-                wt[g * MAX_SPLITS + sp] = c;
-                L = fmaf(c, ld1(g, sp, 1), L);
-            }
-            L = warp_sum(L);
-            if (lane == 0) iL[g] = 1.f / L;
-        }
-        __syncthreads();
-        // o: one float4 of one head per thread, summed in split order
-        for (int e = threadIdx.x; e < G * (D / 4); e += blockDim.x) {
-            const int g = e / (D / 4), j = e % (D / 4);
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-            for (int sp = 0; sp < ns; ++sp) {
-                const float c = wt[g * MAX_SPLITS + sp];
-                const float4 v = ld4(g, sp, 4 + 4 * j);
-                acc.x = fmaf(c, v.x, acc.x);
-                acc.y = fmaf(c, v.y, acc.y);
-                acc.z = fmaf(c, v.z, acc.z);
-                acc.w = fmaf(c, v.w, acc.w);
-            }
-            const float il = iL[g];
-            reinterpret_cast<float4 *>(prm.out + ((size_t)b_idx * y.Hq + h * G + g) * D)[j] =
-                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
-        }
-    };
     if (staged) {
-        mbar_wait_bounded(merge_bar, 0, prm.status);
-        const uint32_t sb = smem_u32(stage_buf);
-        merge(
-            [&](int g, int sp, int k) -> float {
-                float v;
-                asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(sb + (uint32_t)(((g * ns + sp) * S + k) * 4)));
-                return v;
-            },
-            [&](int g, int sp, int k) -> float4 {
-                float4 v;
-                asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                             : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                             : "r"(sb + (uint32_t)(((g * ns + sp) * S + k) * 4)));
-                return v;
-            });
+        if (!merge_copies_landed(prm, merge_bar)) return false;
+        const StagedRows rows{smem_u32(stage_buf), ns, S};
+        merge_states<D>(prm, b_idx, h, ns, [&](int g, int sp, int k) { return rows.one(g, sp, k); },
+                        [&](int g, int sp, int k) { return rows.four(g, sp, k); });
     } else {
         const float *rows = prm.partials + y.partial_index(b, h * G, 0) * S;  // head g at + g MAX_SPLITS S
-        merge([&](int g, int sp, int k) -> float { return __ldcg(rows + ((size_t)g * MAX_SPLITS + sp) * S + k); },
-              [&](int g, int sp, int k) -> float4 {
-                  return __ldcg(reinterpret_cast<const float4 *>(rows + ((size_t)g * MAX_SPLITS + sp) * S + k));
-              });
+        merge_states<D>(
+            prm, b_idx, h, ns,
+            [&](int g, int sp, int k) -> float { return __ldcg(rows + ((size_t)g * MAX_SPLITS + sp) * S + k); },
+            [&](int g, int sp, int k) -> float4 {
+                return __ldcg(reinterpret_cast<const float4 *>(rows + ((size_t)g * MAX_SPLITS + sp) * S + k));
+            });
     }
     if (threadIdx.x == 0) arrivals[0] = 0;
     return true;
@@ -934,10 +933,6 @@ __device__ __forceinline__ void patch_new_row(const DecodeParams &prm, unsigned 
 // rows below T - 2 (the rows the preceding launch may append are T - 2 and
 // T - 1).  L2 prefetches need no such care: L2 is the point of coherence, so
 // a row written after its prefetch is still copied fresh.
-// float offset of the warp states in the ring once streaming is over (after
-// the merge scratch; a multiple of 4 floats)
-template <int D>
-__host__ __device__ constexpr int fin_comb() { return MAX_SPLITS * 8 + 8; }
 
 template <int P, int D, int RKT, int RVT, bool Q4, bool ROPE>
 __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 32, CTAS_PER_SM)
@@ -945,7 +940,6 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     using Shape = DecodeShape<Q4, P, ROPE, D, RKT, RVT>;
     constexpr int NWC = Shape::NWC, SPW = Shape::SPW, NS = NWC * SPW;
     constexpr int DU = Shape::DU, PU = P / DU;  // dense units per page, rows per unit
-    constexpr int FIN_COMB = fin_comb<D>();
     extern __shared__ __align__(128) unsigned char smem[];
     const Layout &y = prm.y;
     const int b_idx = blockIdx.z, b = prm.seqs[b_idx], h = blockIdx.y, rank = blockIdx.x;
@@ -964,53 +958,45 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     uint64_t *wfull = full + warp * SPW;
     unsigned char *wstage = stages + (size_t)warp * SPW * stage_bytes;
-    int *winfo = sh.unit_info + warp * SPW;  // per slot: page << 3 | dense << 2 | unit
+    int *winfo = sh.slot_info + warp * SPW;  // per slot: page << 3 | dense << 2 | unit
 
-    // lane 0: this warp's cursor and next unit
-    UnitCursor cur{};
-    int n_pg = 0, n_hf = 0;
-    bool n_dense = false, have_next = false;
+    // this CTA's pages and their factorized stretch (split on the host)
+    const int pb = prm.bounds[prm.boff[b_idx] + rank], pe = prm.bounds[prm.boff[b_idx] + rank + 1];
+    const int a1 = min(max(pb, prm.fs[b_idx]), pe), a2 = max(a1, min(pe, prm.fw[b_idx]));
+    const int n_fac = a2 - a1;
     bool waited = prm.wait_first != 0;
     uint64_t policy = 0;
     const char *fact = prm.factor_pool + y.record_offset(prm.layer, b, h, 0);
-    auto take = [&](int skip) -> bool {  // skip units dealt to the other warps, then take one
-        if (cur.half == 0 && cur.p >= cur.a1 && cur.p + skip < cur.a2) {
-            cur.p += skip;  // inside the factorized stretch a unit is a page
-            return cur.next<P, DU>(n_pg, n_hf, n_dense);
-        }
-        int pg, hf;
-        bool dn;
-        for (int i = 0; i < skip; ++i)
-            if (!cur.next<P, DU>(pg, hf, dn)) return false;
-        return cur.next<P, DU>(n_pg, n_hf, n_dense);
-    };
-    auto issue = [&](int slot) {
-        winfo[slot] = (n_pg << 3) | (n_dense ? 4 : 0) | n_hf;
+    // failure-path test hook: the very first unit of CTA (0, 0, 0) expects 16
+    // bytes that no copy delivers, so its wait runs out
+    bool poison = prm.inject == 1 && blockIdx.x == 0 && blockIdx.y == 0 && blockIdx.z == 0 && warp == 0;
+    // one unit (code page << 3 | dense << 2 | unit) into this warp's slot
+    auto issue = [&](int slot, int info) {
+        winfo[slot] = info;
+        const int pg = info >> 3, hf = info & 3;
         unsigned char *dst = wstage + (size_t)slot * stage_bytes;
-        const uint32_t extra = ROPE ? (uint32_t)D * 4 : 0u;  // the page start's (cos, sin) row
-        if (!n_dense) {
+        const uint32_t extra = (ROPE ? (uint32_t)D * 4 : 0u) + (poison ? 16u : 0u);  // RoPE: the page start's (cos, sin) row
+        poison = false;
+        if (!(info & 4)) {
             mbar_arrive_expect_tx(&wfull[slot], (uint32_t)y.rec_bytes + extra);
-            bulk_g2s_hint(dst, fact + (size_t)n_pg * y.rec_bytes, (uint32_t)y.rec_bytes, &wfull[slot], policy);
+            bulk_g2s_hint(dst, fact + (size_t)pg * y.rec_bytes, (uint32_t)y.rec_bytes, &wfull[slot], policy);
         } else {
-            const int first = n_pg * P + n_hf * PU;
+            const int first = pg * P + hf * PU;
             if (!waited && first + unit_valid(T, first, PU) >= T - 1) {
                 grid_dependency_wait();
                 waited = true;
             }
-            const int slot_d = y.dense_slot(n_pg);
+            const int slot_d = y.dense_slot(pg);
             const uint32_t hb = (uint32_t)PU * D * 2;
             mbar_arrive_expect_tx(&wfull[slot], 2 * hb + extra);
-            bulk_g2s_hint(dst, prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 0) + n_hf * hb, hb,
+            bulk_g2s_hint(dst, prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 0) + hf * hb, hb,
                           &wfull[slot], policy);
-            bulk_g2s_hint(dst + hb, prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 1) + n_hf * hb, hb,
+            bulk_g2s_hint(dst + hb, prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 1) + hf * hb, hb,
                           &wfull[slot], policy);
         }
         if (ROPE)  // constant table: no launch writes it
-            bulk_g2s(dst + base_off, prm.rope_base + (size_t)n_pg * (D / 2), extra, &wfull[slot]);
+            bulk_g2s(dst + base_off, prm.rope_base + (size_t)pg * (D / 2), extra, &wfull[slot]);
     };
-    // this CTA's pages and their factorized stretch (split on the host)
-    const int pb = prm.bounds[prm.boff[b_idx] + rank], pe = prm.bounds[prm.boff[b_idx] + rank + 1];
-    const int a1 = min(max(pb, prm.fs[b_idx]), pe), a2 = max(a1, min(pe, prm.fw[b_idx]));
     if (ROPE) {  // constant table: read before any dependency wait
         const float4 *src = reinterpret_cast<const float4 *>(prm.rope_delta);
         float4 *dstt = reinterpret_cast<float4 *>(rope_delta);
@@ -1018,23 +1004,40 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     }
     if (threadIdx.x == 0) {
         sh.failed = 0;
+        // The CTA's units in page order: the dense units of [pb, a1) (sink
+        // pages), one unit per factorized page of [a1, a2), the dense units of
+        // [a2, pe) (window and incomplete pages).  The few dense ones are
+        // listed here, before any dependency wait, so that taking a unit later
+        // is a table lookup; units with no valid row are left out.
+        int n = 0;
+        for (int p = pb; p < pe; ++p) {
+            if (p == a1) {
+                sh.n_pre = n;
+                p = a2;
+                if (p >= pe) break;
+            }
+            for (int hf = 0; hf < DU; ++hf)
+                if (T > p * P + hf * PU) sh.dense_units[n++] = (p << 3) | 4 | hf;
+        }
+        if (a1 >= pe) sh.n_pre = n;
+        sh.n_dense = n;
         for (int i = 0; i < NS; ++i) mbar_init(&full[i], 1);
         mbar_init(&sh.merge_bar, 1);
         fence_barrier_init();
     }
     __syncthreads();
-    int issued = 0;
+    // unit u of the CTA goes to warp u mod NWC
+    const int n_pre = sh.n_pre, n_units = sh.n_dense + n_fac;
+    const int n_mine = n_units > warp ? (n_units - 1 - warp) / NWC + 1 : 0;
+    auto unit_of = [&](int u) -> int {
+        return u < n_pre ? sh.dense_units[u] : (u < n_pre + n_fac ? (a1 + u - n_pre) << 3 : sh.dense_units[u - n_fac]);
+    };
     if (lane == 0) {
         policy = l2_evict_first();
         if (waited) grid_dependency_wait();
-        cur = UnitCursor{pb, 0, a1, a2, pe, T};
-        have_next = take(warp);
-        while (have_next && issued < SPW) {
-            issue(issued++);
-            have_next = take(NWC - 1);
-        }
+        for (int k = 0; k < SPW && k < n_mine; ++k) issue(k, unit_of(warp + NWC * k));
         if (warp == NWC - 1) {  // the rest of the range: L2 prefetches
-            for (size_t off = 0, len = (size_t)(a2 - a1) * y.rec_bytes; off < len; off += 65536)
+            for (size_t off = 0, len = (size_t)n_fac * y.rec_bytes; off < len; off += 65536)
                 prefetch_l2(fact + (size_t)a1 * y.rec_bytes + off, (uint32_t)min(len - off, (size_t)65536));
             for (int p = pb; p < pe; ++p) {
                 if (p >= a1 && p < a2) continue;
@@ -1044,7 +1047,6 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
             }
         }
     }
-    issued = __shfl_sync(0xffffffffu, issued, 0);
 
     // q, the appended token and the page table may come from the preceding grid
     grid_dependency_wait();
@@ -1070,10 +1072,11 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     w.m = -INFINITY;
     w.l = 0.f;
     const float scale_log2 = LOG2E * rsqrtf((float)D);
+    const uint64_t wait_lim = prm.wait_ns ? prm.wait_ns : WAIT_NS;
     int slot = 0, k = 0;
     uint32_t ph = 0;
-    for (; k < issued; ++k) {
-        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wfull[slot], ph, prm.status))) break;
+    for (; k < n_mine; ++k) {
+        if (!__all_sync(0xffffffffu, mbar_wait_bounded(&wfull[slot], ph, prm.status, wait_lim))) break;
         const int info = winfo[slot];
         const int pg = info >> 3, part = info & 3;
         const uint32_t st = smem_u32(wstage + (size_t)slot * stage_bytes);
@@ -1101,34 +1104,31 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
                 dense_unit<P, D, PU>(w, st, valid, lane, scale_log2);
         }
         __syncwarp();
-        int more = 0;
-        if (lane == 0 && have_next) {  // the slot is free again: this warp's next unit goes into it
+        if (lane == 0 && k + SPW < n_mine) {  // the slot is free again: this warp's next unit goes into it
             fence_proxy_async_shared();
-            issue(slot);
-            have_next = take(NWC - 1);
-            more = 1;
+            issue(slot, unit_of(warp + NWC * (k + SPW)));
         }
-        issued += __shfl_sync(0xffffffffu, more, 0);
         if (++slot == SPW) {
             slot = 0;
             ph ^= 1;
         }
     }
-    if (k < issued) {  // a bounded wait gave up: let this warp's copies land before the CTA exits
+    if (k < n_mine) {  // a bounded wait gave up: let this warp's copies land before the CTA exits
         if (lane == 0) {
             sh.failed = 1;
+            const int issued = min(n_mine, k + SPW);  // units [0, issued) had their copies issued
             for (int kk = k; kk < issued; ++kk) mbar_wait_bounded(&wfull[kk % SPW], (kk / SPW) & 1, nullptr);
         }
         __syncwarp();
     }
-    __syncthreads();
+    __syncthreads();  // the warp states go over slots that other warps may have been filling
     if (sh.failed) return;
     {  // per-warp state -> shared memory (every copy has landed and been read)
         const int g = lane >> 2, c2 = 2 * (lane & 3);
         float l = w.l;
         l += __shfl_xor_sync(0xffffffffu, l, 1);
         l += __shfl_xor_sync(0xffffffffu, l, 2);
-        float *comb = reinterpret_cast<float *>(stages) + FIN_COMB + (size_t)warp * 8 * (D + 4);
+        float *comb = reinterpret_cast<float *>(stages) + (size_t)warp * 8 * (D + 4);
         if (g < y.G) {
             float *row = comb + g * (D + 4);
             if (c2 == 0) {
@@ -1144,12 +1144,11 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     }
     __syncthreads();
     {
-        // ring reuse: merge scratch, then the warp states, which the other
-        // CTAs' states overwrite once merged
-        float *scratch = reinterpret_cast<float *>(stages);
-        float *comb = scratch + FIN_COMB;
-        const size_t cap = (size_t)NS * stage_bytes - (size_t)FIN_COMB * 4;
-        finish_split<D, NWC>(prm, comb, b_idx, b, h, rank, ns, scratch, &sh.last, comb, cap, &sh.merge_bar);
+        // ring reuse: the warp states, over which the merging CTA stages the
+        // other CTAs' states (it has merged its warps' states by then)
+        float *comb = reinterpret_cast<float *>(stages);
+        finish_split<D, NWC>(prm, comb, b_idx, b, h, rank, ns, &sh.last, comb, (size_t)NS * stage_bytes,
+                             &sh.merge_bar);
     }
 }
 
@@ -1199,7 +1198,7 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
             LaunchSetup &c = cache[dev][slot];
             c = LaunchSetup{};
             constexpr int NS = Shape::NWC * Shape::SPW;
-            const size_t tail_bytes = (size_t)fin_comb<D>() * 4 + (size_t)Shape::NWC * 8 * (D + 4) * 4;
+            const size_t tail_bytes = (size_t)Shape::NWC * 8 * (D + 4) * 4;  // the warp states
             if ((size_t)NS * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
             c.stages = NS;
             c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared) +

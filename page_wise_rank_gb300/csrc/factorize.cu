@@ -51,6 +51,7 @@ struct JobView {
     char *L;        // plain outputs (batch mode)
     char *R;
     float *sigma;
+    float *qL, *qR;  // batch INT4 mode: the absorbed fp32 factors (or nullptr)
 };
 
 __device__ __forceinline__ JobView job_view(const FactorParams &fp, long job) {
@@ -79,6 +80,15 @@ __device__ __forceinline__ JobView job_view(const FactorParams &fp, long job) {
         v.kind = kind;
         v.r = kind == 0 ? y.rk : y.rv;
         v.rec = fp.factor_pool + y.record_offset(fp.layer0 + lrel, fp.seq, h, pg);
+    } else if (fp.mode == FACT_MODE_BATCH_Q4) {
+        const int rp = fp.q4_kind == 0 ? y.rkp : y.rvp;
+        v.x = fp.x_base + (size_t)job * y.P * y.d * 2;
+        v.x_pool = 0;
+        v.kind = fp.q4_kind;
+        v.r = fp.q4_kind == 0 ? y.rk : y.rv;
+        v.rec = fp.q4_records + (size_t)job * y.rec_bytes;
+        v.qL = fp.q4_L ? fp.q4_L + (size_t)job * y.P * rp : nullptr;
+        v.qR = fp.q4_R ? fp.q4_R + (size_t)job * rp * y.d : nullptr;
     } else if (fp.mode == FACT_MODE_CONVERT_LIST) {  // job -> (list entry, head, kind)
         int kind = (int)(job % 2);
         long t = job / 2;
@@ -524,6 +534,10 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
         Rf[e] = rs > 0.f ? Rf[e] / rs : 0.f;
     }
     __syncthreads();
+    if (v.qL)  // the absorbed factors the codes below quantize
+        for (int e = tid; e < P * rp; e += NT) v.qL[e] = s.G[e / rp][e % rp];
+    if (v.qR)
+        for (int e = tid; e < rp * D; e += NT) v.qR[e] = Rf[e];
     // 3. scales: fp16 in the record (accumulator-column order), their fp32
     // values in s.Vt for the codes
     float *scL = &s.Vt[0][0];  // per rank (keys) or per token (values): up to P

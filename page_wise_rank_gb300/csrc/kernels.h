@@ -7,7 +7,8 @@
 
 namespace pkv {
 
-enum { FACT_MODE_BATCH = 0, FACT_MODE_PREFILL = 1, FACT_MODE_CONVERT = 2, FACT_MODE_CONVERT_LIST = 3 };
+enum { FACT_MODE_BATCH = 0, FACT_MODE_PREFILL = 1, FACT_MODE_CONVERT = 2, FACT_MODE_CONVERT_LIST = 3,
+       FACT_MODE_BATCH_Q4 = 4 };
 
 struct FactorParams {
     int mode;
@@ -33,6 +34,13 @@ struct FactorParams {
     int conv_seq[MAX_CALL_BATCH], conv_page[MAX_CALL_BATCH];
     // convert list: device int2 {seq << 8 | layer, page} per page, 2 H jobs each
     const int2 *conv_list;
+    // batch INT4 mode: pages X[n][P][d] (x_base) of one kind (0 key, 1 value)
+    // -> INT4 records q4_records[n][y.rec_bytes] (that kind's code stream and
+    // scales), and optionally the absorbed fp32 factors the codes quantize,
+    // q4_L[n][P][rank padded to 8] and q4_R[n][rank padded][d]
+    int q4_kind;
+    char *q4_records;
+    float *q4_L, *q4_R;
 };
 
 constexpr int MAX_BOUNDS = 384;  // page bounds of all CTAs of one bf16 decode launch
@@ -45,6 +53,11 @@ struct DecodeParams {
     float *partials;    // workspace split partials
     int *tickets;       // workspace split tickets, zero between launches
     int wait_first;     // bf16 kernel: the preceding launch may have written factor records
+    // failure-path test hook (0 = off): 1 = the first unit of CTA (0, 0, 0)
+    // expects bytes no copy delivers, 2 = so does every split merge; the waits
+    // of this launch give up after wait_ns (0 = the library's limit)
+    int inject;
+    unsigned long long wait_ns;
     float *out;         // [B][Hq][d]
     int *status;
     int layer, chunk, nseq;

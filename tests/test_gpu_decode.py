@@ -56,7 +56,7 @@ def run_decode_check(pkv, store, cfg, host, seqs, layer, step, tol, heads=None):
 def prefill(pkv, store, cfg, host, seq, T, rope=None, k=12, n_out=4):
     spec = spec_of(cfg, inner_rank=k, n_outliers=n_out, rope_base=rope)
     K, V = synth.prefill_kv(spec, T, seq=seq)
-    store.factorize_pages(seq, K.cuda(), V.cuda())
+    store.load_prefill(seq, K.cuda(), V.cuda())
     host.set_prefill(seq, K, V)
     return spec
 
@@ -256,8 +256,8 @@ def test_decode_step_fused_append(pkv, dtype):
     prefill(pkv, a, cfg, host, 3, 1061)
     for seq, T in ((0, 1000), (3, 1061)):
         K, V = synth.prefill_kv(spec, T, seq=seq)
-        b.factorize_pages(seq, K.cuda(), V.cuda())
-        c.factorize_pages(seq, K.cuda(), V.cuda())
+        b.load_prefill(seq, K.cuda(), V.cuda())
+        c.load_prefill(seq, K.cuda(), V.cuda())
     seqs = [3, 0]
     cache = {}
     G = cfg.num_q_heads // cfg.num_kv_heads
@@ -302,7 +302,7 @@ def test_conversion_batch_waited_at_deadline(pkv):
     T0 = 1000  # pages 13 and 14 are complete but inside the window, not yet converted
     spec = prefill(pkv, a, cfg, host, 0, T0)
     K, V = synth.prefill_kv(spec, T0, seq=0)
-    b.factorize_pages(0, K.cuda(), V.cuda())
+    b.load_prefill(0, K.cuda(), V.cuda())
     cache = {}
     G = cfg.num_q_heads // cfg.num_kv_heads
     P, W = cfg.page_size, cfg.recent_tokens

@@ -127,7 +127,7 @@ def run_steps(store, cfg, spec, seqs, T0, steps, samples, prefill_rows, q_of, ch
 
 def prefill_seq(store, spec, seq, T, samples_for_seq, rows, index):
     K, V = synth.prefill_kv(spec, T, seq=seq, device="cuda")
-    store.factorize_pages(seq, K, V)
+    store.load_prefill(seq, K, V)
     for (l, h) in samples_for_seq:
         rows[(index, l, h)] = (K[l, h].double().cpu().numpy(), V[l, h].double().cpu().numpy())
     del K, V

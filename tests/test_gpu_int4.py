@@ -45,7 +45,7 @@ def cfg_q4(pkv, **kw):
 def prefill(store, cfg, host, seq, T, rope=5e5):
     spec = spec_of(cfg, rope_base=rope)
     K, V = synth.prefill_kv(spec, T, seq=seq)
-    store.factorize_pages(seq, K.cuda(), V.cuda())
+    store.load_prefill(seq, K.cuda(), V.cuda())
     host.set_prefill(seq, K, V)
     return spec
 
@@ -143,3 +143,68 @@ def test_int4_records_quantize_absorbed_factors(pkv):
                 ref = oracle.dequantize_int4(cL, sL, per_row_L) @ oracle.dequantize_int4(cR, sR, False)
                 err_o = np.linalg.norm(Xp - ref) / np.linalg.norm(Xp)
                 assert err <= 1.15 * err_o + 1e-3 and err_o <= 1.15 * err + 1e-3, (err, err_o)
+
+
+def expected_codes(x, per_row):
+    """Codes and fp16 scales of the rule the records follow [PuzzleKV §4.3,
+    readings C17-C18], in the kernel's fp32: scale = fp16(max|x| / 7) per
+    group, code = round-half-to-even(x / scale) clamped to [-7, 7] (0 where
+    the scale is 0)."""
+    x = np.asarray(x, dtype=np.float32)
+    m = np.abs(x).max(axis=1 if per_row else 0)
+    s = (m / np.float32(7)).astype(np.float32).astype(np.float16).astype(np.float32)
+    sb = s[:, None] if per_row else s[None, :]
+    with np.errstate(divide="ignore", invalid="ignore"):
+        c = np.where(sb > 0, np.rint(x / np.where(sb > 0, sb, np.float32(1))), 0)
+    return np.clip(c, -7, 7).astype(np.int64), s.astype(np.float64)
+
+
+def kind_bytes(lay, kind):
+    """Byte ranges of a record written by one kind's factorization job."""
+    if kind == 0:
+        return [(0, lay.q_off_V), (lay.q_off_sRK, lay.q_off_sRK + 2 * lay.d), (lay.q_off_sLK, lay.rec_bytes)]
+    return [(lay.q_off_V, lay.q_off_sRK), (lay.q_off_sRV, lay.q_off_sRV + 2 * lay.d),
+            (lay.q_off_sLV, lay.q_off_sLV + 2 * lay.P)]
+
+
+@pytest.mark.parametrize("P,d,rk,rv", [(64, 128, 16, 24), (32, 128, 16, 14), (16, 64, 8, 8)])
+def test_int4_codes_are_the_nearest_levels(pkv, P, d, rk, rv):
+    """Integer work, checked exactly: every stored code is the nearest level
+    x / s (ties to even, clamped to +-7) of the kernel's own absorbed fp32
+    factor x and the record's own fp16 scale s, and every scale is
+    fp16(max |x| / 7) of its group (columns of L~_K, R~_K and R~_V, rows of
+    L~_V).  The store's records of the same pages are byte for byte the
+    stateless call's."""
+    cfg = cfg_q4(pkv, page_size=P, head_dim=d, rank_k=rk, rank_v=rv, num_layers=1, recent_tokens=2 * P)
+    lay = Layout(cfg)
+    assert pkv.int4_record_bytes(P, d, rk, rv) == lay.rec_bytes
+    T = 30 * P
+    store = pkv.Store(cfg)
+    host = HostCache()
+    prefill(store, cfg, host, 0, T)
+    kinds = oracle.page_kinds(T, P, cfg.sink_tokens, cfg.recent_tokens)
+    fac = [int(p) for p in np.nonzero(kinds == oracle.FACTORED)[0]]
+    for kind, r in ((0, rk), (1, rv)):
+        X = torch.tensor(np.stack([host.rows(0, 0, h)[kind][p * P:(p + 1) * P] for h in range(cfg.num_kv_heads)
+                                   for p in fac]), dtype=torch.bfloat16, device="cuda")
+        rec, Lq, Rq, st = pkv.factorize_batch_int4(X, rk, rv, kind)
+        assert int(st.item()) == 0
+        rec, Lq, Rq = rec.cpu().numpy(), Lq.cpu().numpy(), Rq.cpu().numpy()
+        i = 0
+        for h in range(cfg.num_kv_heads):
+            fpool = factor_pool_slice(store, lay, 0, 0, h)
+            for p in fac:
+                q = read_record_q4(rec[i], lay)
+                if kind == 0:
+                    parts = ((q["LK"], Lq[i], False), (q["RK"], Rq[i], False))
+                else:  # stored transposed: L_V as [rank][token] (groups = tokens), R_V as [dim][rank]
+                    parts = ((q["LVt"], Lq[i].T, False), (q["RVt"], Rq[i].T, True))
+                for (codes, scales, per_row), x, per_row_x in parts:
+                    assert per_row == per_row_x
+                    want_c, want_s = expected_codes(x, per_row)
+                    assert np.array_equal(scales, want_s), (kind, h, p)
+                    assert np.array_equal(codes.astype(np.int64), want_c), (kind, h, p)
+                o = lay.record_offset(0, 0, h, p)
+                for a, b in kind_bytes(lay, kind):
+                    assert np.array_equal(fpool[o + a:o + b], rec[i][a:b]), (kind, h, p, a)
+                i += 1

@@ -39,7 +39,7 @@ def cfg_rope(pkv, **kw):
 
 def prefill(store, cfg, host, seq, T):
     K, V = synth.prefill_kv(spec_of(cfg), T, seq=seq)  # unrotated keys
-    store.factorize_pages(seq, K.cuda(), V.cuda())
+    store.load_prefill(seq, K.cuda(), V.cuda())
     host.set_prefill(seq, K, V)
 
 

@@ -25,7 +25,7 @@ def pkv():
 def header_functions():
     src = open(os.path.join(ROOT, "include", "puzzlekv.h")).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
-    return sorted(set(re.findall(r"\b(puzzlekv_[a-z_]+)\s*\(", src)))
+    return sorted(set(re.findall(r"\b(puzzlekv_[a-z0-9_]+)\s*\(", src)))
 
 
 def test_library_exports_every_declared_symbol(pkv):
@@ -121,7 +121,9 @@ def test_store_create_rejects_bad_pointers_without_gpu(pkv):
     assert L.puzzlekv_store_create(ctypes.byref(c), None, None, None, None, None, ctypes.byref(h)) == 1
     assert L.puzzlekv_store_create(ctypes.byref(c), 16, 256, 256, 256, None, ctypes.byref(h)) == 1  # misaligned
     assert h.value is None
-    assert L.puzzlekv_factorize_pages(None, 0, None, None, 1, None) == 1
+    assert L.puzzlekv_load_prefill(None, 0, None, None, 1, None) == 1
+    assert L.puzzlekv_factorize_pages(None, None, None, -1, None) == 1
+    assert L.puzzlekv_debug_fail_next_wait(None, 1, 10000) == 1
     assert L.puzzlekv_decode_attention(None, 0, None, None, None, 1, None) == 1
     assert L.puzzlekv_factorize_batch(None, 1, 4, 64, 96, 8, None, None, 0, None, None, None) == 2
     assert L.puzzlekv_factorize_batch(None, 1, 0, 64, 128, 8, None, None, 0, None, None, None) == 0

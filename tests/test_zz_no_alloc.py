@@ -38,16 +38,25 @@ def test_static_scratch_decode_matches_workspace_decode(pkv):
     store = pkv.Store(cfg)
     for seq, T in ((0, 4321), (2, 900)):
         K, V = synth.prefill_kv(spec, T, seq=seq)
-        store.factorize_pages(seq, K.cuda(), V.cuda())
+        store.load_prefill(seq, K.cuda(), V.cuda())
     q = synth.queries(2, 16, 128, step=9, layer=1).cuda()
     ref = torch.empty(2, 16, 128, device="cuda")
     store.decode_attention(1, q, ref, [2, 0])
     assert store.check_device_status() == 0
-    for _ in range(2):  # two calls in a row: the array keeps the last call's contents
-        out = torch.full((2, 16, 128), float("nan"), device="cuda")
+    outs = [torch.full((2, 16, 128), float("nan"), device="cuda") for _ in range(2)]
+    torch.cuda.synchronize()
+    free = []
+    for out in outs:  # two calls in a row: the array keeps the last call's contents
+        free.append(torch.cuda.mem_get_info()[0])
         store.decode_attention_static_scratch(1, q, out, [2, 0])
         assert store.check_device_status() == 0
+        # the same kernel on the same inputs, merging the splits in the same
+        # order: bitwise equal to the workspace path
         assert rel_err_rows(out.cpu().double().numpy(), ref.cpu().double().numpy()) <= 2e-3
+        assert torch.equal(out, ref)
+    # the first call may load the library's device code and its array; after
+    # that the call takes no device memory
+    assert torch.cuda.mem_get_info()[0] == free[1]
 
 
 def test_static_scratch_rejects_oversized_store(pkv):
@@ -57,7 +66,7 @@ def test_static_scratch_rejects_oversized_store(pkv):
     store = pkv.Store(cfg)
     spec = synth.KVSpec(layers=1, kv_heads=8, head_dim=128, page_size=64, dtype=torch.bfloat16)
     K, V = synth.prefill_kv(spec, 200)
-    store.factorize_pages(0, K.cuda(), V.cuda())
+    store.load_prefill(0, K.cuda(), V.cuda())
     q = torch.zeros(1, 64, 128, dtype=torch.bfloat16, device="cuda")
     out = torch.empty(1, 64, 128, device="cuda")
     with pytest.raises(pkv.PuzzleKVError) as e:
