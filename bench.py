@@ -110,27 +110,28 @@ def measured_peak_bf16():
         return 1900.0, "fallback"
 
 
-def factorization_roofline(wl, jobs, sweeps, ms, sms, sm_mhz):
+def factorization_roofline(wl, jobs, rotations, ms, sms, sm_mhz):
     """Rates of the prefill factorization against the two peaks that bound it.
     FLOP conventions per page job (P x d page, P x P Gram):
       Gram 2 P^2 d; projection 2 r P d (r the mean of r_K and r_V);
-      Jacobi per sweep (P - 1) rounds x P/2 rotations x 18 P (a rotation
-      updates two rows and two columns of G and two eigenvector rows, 6 flops
-      per updated pair)."""
+      Householder reduction 2 P^3 (per reflection a matrix-vector product and
+      a rank-2 update of the trailing block, 6 n^2 summed over n < P);
+      forming the reflections' product 4/3 P^3; QL 6 P + 20 per plane
+      rotation (two columns of the eigenvector matrix, and the recurrence)."""
     P, d = wl["P"], wl["d"]
     r = (wl["rk"] + wl["rv"]) / 2.0
     sec = ms * 1e-3
     gram = jobs * 2.0 * P * P * d
     proj = jobs * 2.0 * r * P * d
-    jac = sweeps * (P - 1) * (P / 2.0) * 18.0 * P
+    eig = jobs * (2.0 + 4.0 / 3.0) * P ** 3 + rotations * (6.0 * P + 20.0)
     bf16_peak, bf16_kind = measured_peak_bf16()
     fp32_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # CUDA-core fp32 FMA lanes x 2 flops
-    return {"page_jobs": int(jobs), "jacobi_sweeps_per_job": round(sweeps / max(jobs, 1), 2),
+    return {"page_jobs": int(jobs), "ql_rotations_per_job": round(rotations / max(jobs, 1), 1),
             "gram_tflops": round(gram / sec / 1e12, 3),
             "gram_frac_of_bf16_peak": round(gram / sec / 1e12 / bf16_peak, 6), "bf16_peak_tflops": bf16_peak,
             "bf16_peak_source": bf16_kind,
-            "jacobi_plus_projection_tflops": round((jac + proj) / sec / 1e12, 3),
-            "jacobi_frac_of_fp32_peak": round((jac + proj) / sec / 1e12 / fp32_peak, 4),
+            "eigensolve_plus_projection_tflops": round((eig + proj) / sec / 1e12, 3),
+            "eigensolve_frac_of_fp32_peak": round((eig + proj) / sec / 1e12 / fp32_peak, 4),
             "fp32_peak_tflops": round(fp32_peak, 1), "fp32_peak_basis": f"{sms} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz"}
 
 
@@ -289,7 +290,7 @@ def gpu_arm(args, rank, world, local):
     n_steps_total = args.warmup + args.steps * (1 if args.no_e2e else 2) + min(args.steps, 8)
     cfg = pkv.StoreConfig(num_layers=L, num_kv_heads=H, num_q_heads=Hq, head_dim=d, page_size=P, rank_k=wl["rk"],
                           rank_v=wl["rv"], sink_tokens=wl["sink"], recent_tokens=wl["W"], max_batch=B,
-                          max_tokens_per_seq=T0 + n_steps_total + 8, kv_dtype=torch.bfloat16,
+                          max_tokens_per_seq=T0 + n_steps_total + P + 8, kv_dtype=torch.bfloat16,
                           factor_int4=bool(wl.get("int4")), rope_theta=float(wl.get("rope_theta", 0.0)))
     spec = synth.KVSpec(layers=L, kv_heads=H, head_dim=d, page_size=P, inner_rank=wl["k"], n_outliers=wl["n_out"],
                         rope_base=wl["rope"], dtype=torch.bfloat16)
@@ -309,7 +310,7 @@ def gpu_arm(args, rank, world, local):
         e1.record(stream)
         st = store.check_device_status(stream)
         prefill_ms = e0.elapsed_time(e1)
-        fact_jobs, fact_sweeps = store.factorize_counters(stream)
+        fact_jobs, fact_rot = store.factorize_counters(stream)
         if st != 0:
             raise RuntimeError(f"prefill factorization status {st}: {pkv.last_error()}")
         del K, V
@@ -441,7 +442,30 @@ def gpu_arm(args, rank, world, local):
             e2e_ms = barrier_max(x0.elapsed_time(x1), world)
             e2e = {"value": 1000.0 * e2e_ms / args.steps, "unit": "us/step",
                    "h2d_bytes_per_step": int(din.numel() * 2),
-                   "d2h_bytes_per_step": int(out.numel() * 4)}
+                   "d2h_bytes_per_step": int(out.numel() * 4),
+                   "copies": "made by the caller on the decode stream, as a serving loop would: one "
+                             "cudaMemcpyAsync of the step's q, k and v (packed, pinned host memory) before the "
+                             "step's decode_step calls through the library's C ABI, one of the outputs after"}
+        # ---- one batched page conversion alone: decode steps (untimed, no
+        # conversion) up to the next page boundary, then the batch that the
+        # boundary makes due, timed with the caller's stream waiting for it
+        while (store_len[0] + 1) % P != 0:
+            for l in range(L):
+                store.decode_step(l, qs[-1][l], ks[-1][l], vs[-1][l], out[l], seqs, stream=stream)
+            store_len[0] += 1
+        for l in range(L):
+            store.decode_step(l, qs[-1][l], ks[-1][l], vs[-1][l], out[l], seqs, stream=stream)
+        store_len[0] += 1
+        stream.synchronize()
+        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        torch.cuda._sleep(4_000_000)
+        c0.record(stream)
+        store.convert_ready_pages(stream=stream)
+        store.wait_background(stream=stream)
+        c1.record(stream)
+        stream.synchronize()
+        conv_ms = c0.elapsed_time(c1)
+        conv_jobs = 2 * L * H * B
     us_step = 1000.0 * ms_total / args.steps
     dec_us = 1000.0 * sum(dec_ms) / len(dec_ms)
     achieved = sum(dec_bytes) / (sum(dec_ms) * 1e-3) / 1e9
@@ -467,11 +491,15 @@ def gpu_arm(args, rank, world, local):
                    "l2": f"inputs larger than L2: {alg_bytes(wl, T0) * L / 1e9:.2f} GB read per step"},
         "decode_attention_us_per_layer": round(dec_us, 3),
         "decode_step_us_per_layer_isolated": round(1000.0 * statistics.mean(iso_ms), 3),
-        "page_conversion": "batched, on the store's internal stream, overlapping the decode steps "
-                           f"({sum(conv_steps)} batch(es) started in the timed steps)",
+        "page_conversion": {
+            "how": "batched, on the store's internal stream, overlapping the decode steps",
+            "batches_started_in_timed_steps": sum(conv_steps),
+            "batch_every_steps": P, "page_jobs_per_batch": conv_jobs,
+            "batch_ms_alone": round(conv_ms, 4),
+            "amortized_us_per_step_if_serialized": round(1000.0 * conv_ms / P, 3)},
         "pages_factorized_per_s": round(pages_per_s, 1),
         "prefill_factorization": dict({"pages": n_fact_pages, "ms": round(prefill_ms, 3)},
-                                      **factorization_roofline(wl, fact_jobs, fact_sweeps, prefill_ms,
+                                      **factorization_roofline(wl, fact_jobs, fact_rot, prefill_ms,
                                                                torch.cuda.get_device_properties(dev).multi_processor_count,
                                                                (clk or {}).get("sm_mhz") or 2070.0)),
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -493,7 +521,10 @@ def gpu_arm(args, rank, world, local):
 def _oracle_sample(wl, layer_heads, nthreads):
     """Oracle factorization of every eligible page of the sampled (layer, KV head)
     pairs (timed, all host threads) and oracle decode of each pair (timed, one
-    thread).  Returns (pages/s, seconds per (layer, head) decode, pages)."""
+    thread), then the same decodes run nthreads at a time on a thread pool (the
+    oracle releases the interpreter while it computes).  Returns (pages/s,
+    seconds per (layer, head) decode on one thread, (layer, head) decodes per
+    second on nthreads threads, pages)."""
     import oracle
     import synth
 
@@ -503,7 +534,7 @@ def _oracle_sample(wl, layer_heads, nthreads):
     kinds = oracle.page_kinds(T, P, wl["sink"], wl["W"])
     fac = np.nonzero(kinds == oracle.FACTORED)[0]
     n = len(kinds)
-    t_fact, n_pages, t_dec = 0.0, 0, []
+    t_fact, n_pages, t_dec, jobs = 0.0, 0, [], []
     for (layer, h) in layer_heads:
         # layer index only selects the seed; generate that layer's cache on the host
         g = synth.KVSpec(**{**spec.__dict__, "layers": layer + 1})
@@ -525,7 +556,15 @@ def _oracle_sample(wl, layer_heads, nthreads):
         t0 = time.perf_counter()
         oracle.decode_head(q, kinds, Kh, Vh, LK, RK, LV, RV, T, P)
         t_dec.append(time.perf_counter() - t0)
-    return n_pages / t_fact, statistics.mean(t_dec), n_pages
+        jobs.append((q, kinds, Kh, Vh, LK, RK, LV, RV))
+    # all host threads: each sampled pair's decode repeated so that every thread has work
+    from concurrent.futures import ThreadPoolExecutor
+    calls = [jobs[i % len(jobs)] for i in range(max(nthreads, len(jobs)))]
+    t0 = time.perf_counter()
+    with ThreadPoolExecutor(max_workers=nthreads) as ex:
+        list(ex.map(lambda a: oracle.decode_head(*a, T, P), calls))
+    par_rate = len(calls) / (time.perf_counter() - t0)
+    return n_pages / t_fact, statistics.mean(t_dec), par_rate, n_pages
 
 
 def cpu_model():
@@ -552,20 +591,51 @@ def cpu_model():
     return f"{name or 'unknown'} ({platform.machine()})"
 
 
+def tiny_oracle_run():
+    """The oracle over the whole tiny workload (1 layer, 2 KV / 8 query heads,
+    d = 64, fp32, T = 1024, P = 32, r = 8, sink 4, recent 64): every eligible
+    page of both heads factorized (keys and values) and one decode step of all
+    query heads, on one thread.  Returns seconds."""
+    import oracle
+    import synth
+
+    T, P, d, r = 1024, 32, 64, 8
+    spec = synth.KVSpec(layers=1, kv_heads=2, head_dim=d, page_size=P, inner_rank=6, n_outliers=2,
+                        dtype=torch.float32)
+    K, V = synth.prefill_kv(spec, T)
+    q = synth.queries(1, 8, d, step=0, dtype=torch.float32)[0].double().numpy()
+    kinds = oracle.page_kinds(T, P, 4, 64)
+    fac = np.nonzero(kinds == oracle.FACTORED)[0]
+    n = len(kinds)
+    t0 = time.perf_counter()
+    for h in range(2):
+        Kh, Vh = K[0, h].double().numpy(), V[0, h].double().numpy()
+        LK, RK = np.zeros((n, P, r)), np.zeros((n, r, d))
+        LV, RV = np.zeros((n, P, r)), np.zeros((n, r, d))
+        LK[fac], RK[fac], _ = oracle.factorize_pages(np.stack([Kh[p * P:(p + 1) * P] for p in fac]), r, 1)
+        LV[fac], RV[fac], _ = oracle.factorize_pages(np.stack([Vh[p * P:(p + 1) * P] for p in fac]), r, 1)
+        oracle.decode_head(q[4 * h:4 * h + 4], kinds, Kh, Vh, LK, RK, LV, RV, T, P)
+    return time.perf_counter() - t0
+
+
 def cpu_baseline_sample(wl):
     nthreads = os.cpu_count() or 1
     pairs = [(0, 0), (wl["layers"] - 1, wl["H"] - 1)]
-    pages_s, t_head, n_pages = _oracle_sample(wl, pairs, nthreads)
+    pages_s, t_head, par_rate, n_pages = _oracle_sample(wl, pairs, nthreads)
     heads = wl["layers"] * wl["H"] * wl["B"]
     # per step: attention over every (layer, KV head), plus on average 2 H L / P page conversions
     conv_per_step = 2.0 * wl["H"] * wl["layers"] * wl["B"] / wl["P"]
-    us_step = 1e6 * (heads * t_head + conv_per_step / pages_s)
-    return {"value": round(us_step, 1), "unit": "us/step", "cores": 1, "kind": "oracle",
-            "sample": f"oracle decode of {len(pairs)} (layer, KV head) pairs at T={wl['T']} on 1 thread, "
-                      f"scaled to {heads} pairs per step, plus {conv_per_step:.0f} page conversions per step "
-                      f"at the oracle's factorization rate",
+    us_step = 1e6 * (heads / par_rate + conv_per_step / pages_s)
+    us_step_1 = 1e6 * heads * t_head
+    return {"value": round(us_step, 1), "unit": "us/step", "cores": nthreads, "kind": "oracle",
+            "sample": f"oracle decode of {len(pairs)} (layer, KV head) pairs at T={wl['T']}, run "
+                      f"{max(nthreads, len(pairs))} times on {nthreads} threads at once, scaled to {heads} pairs per "
+                      f"step, plus {conv_per_step:.0f} page conversions per step at the oracle's factorization rate",
+            "decode_us_per_step_1_core": round(us_step_1, 1),
+            "decode_pairs_per_s": {"1_core": round(1.0 / t_head, 3), f"{nthreads}_cores": round(par_rate, 3)},
             "pages_factorized_per_s": round(pages_s, 1), "pages_cores": nthreads, "pages_sample": n_pages,
-            "cpu_model": cpu_model()}
+            "nproc": nthreads, "cpu_model": cpu_model(),
+            "tiny_workload_full_oracle_s": round(tiny_oracle_run(), 4)}
 
 
 def multi_seq_arm(args, rank, world, local):
@@ -611,7 +681,7 @@ def multi_seq_arm(args, rank, world, local):
             stream.synchronize()
             prefill_ms += e0.elapsed_time(e1)
             del K, V
-        pre_jobs, pre_sweeps = store.factorize_counters(stream)
+        pre_jobs, pre_rot = store.factorize_counters(stream)
         # decode-phase inputs of every step, on the device: [L, steps, B, H, d]
         kdec = torch.empty(L, n_steps, B, H, d, dtype=torch.bfloat16, device=dev)
         vdec = torch.empty_like(kdec)
@@ -656,7 +726,7 @@ def multi_seq_arm(args, rank, world, local):
             step_ms += [evs[i].elapsed_time(evs[i + 1]) for i in range(len(evs) - 1)]
         barrier(world)
         clk = clocks.stop()
-        conv_jobs, conv_sweeps = store.factorize_counters(stream)
+        conv_jobs, conv_rot = store.factorize_counters(stream)
         st = store.check_device_status(stream)
         if st != 0:
             raise RuntimeError(f"device status {st}: {pkv.last_error()}")
@@ -682,7 +752,7 @@ def multi_seq_arm(args, rank, world, local):
                             "max": round(us[-1], 2), "burst_steps": len(burst_us),
                             "burst_mean": round(statistics.mean(burst_us), 2) if burst_us else None,
                             "non_burst_mean": round(statistics.mean(plain_us), 2) if plain_us else None},
-        "conversion": {"page_jobs": conv_jobs, "jacobi_sweeps_per_job": round(conv_sweeps / max(conv_jobs, 1), 2),
+        "conversion": {"page_jobs": conv_jobs, "ql_rotations_per_job": round(conv_rot / max(conv_jobs, 1), 1),
                        "where": "store's internal low-priority stream, overlapping the decode steps",
                        "page_jobs_per_s_sustained": round(conv_jobs / (sum(step_ms) * 1e-3), 1),
                        "burst_step_excess_us": round(1000.0 * extra_burst_ms / max(len(burst_us), 1), 2)},
@@ -749,7 +819,7 @@ def prefill_arm(args, rank, world, local):
         if mode == "background":
             store.wait_background(stream)
 
-    res, sweeps = {}, {}
+    res, counters = {}, {}
     clocks = ClockSampler(torch.cuda.current_device())
     clocks.start()
     with torch.cuda.stream(stream):
@@ -769,15 +839,15 @@ def prefill_arm(args, rank, world, local):
                 stream.synchronize()
                 ms.append(e0.elapsed_time(e1))
             res[mode] = barrier_max(statistics.mean(ms), world)
-            sweeps[mode] = store.factorize_counters(stream)
+            counters[mode] = store.factorize_counters(stream)
         st = store.check_device_status(stream)
         if st != 0:
             raise RuntimeError(f"device status {st}: {pkv.last_error()}")
     clk = clocks.stop()
     fact_ms = res["inline"] - res["attention"]
-    jobs, sw = sweeps["inline"]
+    jobs, rot = counters["inline"]
     props = torch.cuda.get_device_properties(dev)
-    fr = factorization_roofline(wl, jobs / args.steps, sw / args.steps, fact_ms, props.multi_processor_count,
+    fr = factorization_roofline(wl, jobs / args.steps, rot / args.steps, fact_ms, props.multi_processor_count,
                                 clk.get("sm_mhz") or 2070.0)
     return {
         "metric": "prompt processing ms (dense attention of every layer + page factorization), background "
@@ -796,8 +866,8 @@ def prefill_arm(args, rank, world, local):
         "overhead_vs_attention": {"inline": round(res["inline"] / res["attention"] - 1, 4),
                                   "background": round(res["background"] / res["attention"] - 1, 4)},
         "page_jobs_per_step": jobs_per_step,
-        "roofline": {"bound": "alu", "achieved": fr["jacobi_plus_projection_tflops"], "peak": fr["fp32_peak_tflops"],
-                     "unit": "TFLOP/s", "frac": fr["jacobi_frac_of_fp32_peak"], "traffic": None,
+        "roofline": {"bound": "alu", "achieved": fr["eigensolve_plus_projection_tflops"], "peak": fr["fp32_peak_tflops"],
+                     "unit": "TFLOP/s", "frac": fr["eigensolve_frac_of_fp32_peak"], "traffic": None,
                      "peak_source": "derived: " + fr["fp32_peak_basis"],
                      "kernel": "factorize_kernel (prefill mode, one launch per layer), inline timing"},
         "prefill_factorization": fr,
@@ -815,7 +885,7 @@ def reference_arm(args, rank, world):
 
     T, P, d, layers, H = wl["T"], wl["P"], wl["d"], wl["layers"], wl["H"]
     nthreads = os.cpu_count() or 1
-    pages_s, _, n_pages = _oracle_sample(wl, [(0, 0)], nthreads)
+    pages_s, _, _, n_pages = _oracle_sample(wl, [(0, 0)], nthreads)
     # per step: oracle decode of one (layer, KV head) pair, scaled to all pairs
     spec = synth.KVSpec(layers=1, kv_heads=H, head_dim=d, page_size=P, inner_rank=wl["k"], n_outliers=wl["n_out"],
                         rope_base=wl["rope"], dtype=torch.bfloat16)

@@ -51,7 +51,7 @@ typedef enum {
     PUZZLEKV_ERR_INVALID_ARG = 1,   /* null/misaligned pointer, bad index or size */
     PUZZLEKV_ERR_UNSUPPORTED = 2,   /* shape outside the supported set above */
     PUZZLEKV_ERR_CAPACITY = 3,      /* sequence would exceed max_tokens_per_seq */
-    PUZZLEKV_ERR_NOT_CONVERGED = 4, /* an eigensolve hit its sweep cap (results kept) */
+    PUZZLEKV_ERR_NOT_CONVERGED = 4, /* an eigensolve hit its iteration cap (results kept) */
     PUZZLEKV_ERR_CUDA = 5,          /* a CUDA launch or copy failed */
     PUZZLEKV_ERR_DEVICE_TIMEOUT = 6 /* a kernel's bounded wait ran out (error flag set) */
 } puzzlekv_status;
@@ -205,18 +205,16 @@ puzzlekv_status puzzlekv_background_stream(puzzlekv_store *store, void **stream)
 /*
  * Stateless batched page factorization [PuzzleKV §3.3 ③ and eq. (2)]:
  * for each of n independent pages X_i (P x d), G_i = X_i X_i^T in fp32, its
- * eigenvectors by cyclic Jacobi, L_i = an orthonormal basis of the top-r
- * eigenvector subspace (P x r), R_i = L_i^T X_i (r x d).  The eigensolve stops
- * once no rotation could add more than 1e-4 of the energy the kept subspace
- * leaves out (L_i R_i is then the rank-r optimum up to rounding), unless sigma
- * is requested, in which case every eigenpair is converged and the columns
- * of L_i are the top-r eigenvectors themselves.
+ * eigenvectors (Householder reduction to tridiagonal form, then implicit QL
+ * with Wilkinson shifts, all in fp32), L_i = the top-r eigenvectors (P x r,
+ * unit columns), R_i = L_i^T X_i (r x d).
  *   X:      device, [n][P][d] in x_dtype (row = token).
  *   L, R:   device, [n][P][r] and [n][r][d] in out_dtype.
  *   sigma:  device fp32 [n][P] or NULL: sqrt of the eigenvalues (clamped at
  *           0), descending -- the singular values of X_i.
  *   status: device int32 or NULL; on return of the stream work, nonzero if
- *           any page hit the sweep cap (its factors are still written).
+ *           an eigenvalue of any page took more than 30 QL iterations (its
+ *           factors are still written).
  */
 puzzlekv_status puzzlekv_factorize_batch(const void *X, int32_t x_dtype, int64_t n, int32_t P, int32_t d,
                                          int32_t r, void *L, void *R, int32_t out_dtype, float *sigma,
@@ -387,22 +385,23 @@ puzzlekv_status puzzlekv_debug_fail_next_wait(puzzlekv_store *store, int32_t whe
 
 /*
  * Synchronise `stream`, read the device status word and clear it.  Returns
- * PUZZLEKV_ERR_NOT_CONVERGED if an eigensolve hit its sweep cap since the last
+ * PUZZLEKV_ERR_NOT_CONVERGED if an eigensolve hit its iteration cap since the last
  * check, PUZZLEKV_ERR_DEVICE_TIMEOUT if a kernel's bounded wait ran out.
  */
 puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *store, void *stream);
 
 /*
  * Synchronise `stream`, then read and clear the store's factorization
- * counters: page jobs factorized (one K or one V page each) and the Jacobi
- * sweeps they ran, summed over every factorization launch of the store
- * (prefill, per-step and batched conversion) since the last call.  For
- * throughput accounting (the page has no counterpart).  page_jobs and
- * jacobi_sweeps: host pointers, both required.  The status flags read by
+ * counters: page jobs factorized (one K or one V page each) and the QL
+ * plane rotations their eigensolves applied, summed over every
+ * factorization launch of the store (prefill, per-step and batched
+ * conversion) since the last call.  For throughput accounting (the page has
+ * no counterpart).  page_jobs and ql_rotations: host pointers, both
+ * required.  The status flags read by
  * puzzlekv_check_device_status are left untouched.
  */
 puzzlekv_status puzzlekv_factorize_counters(puzzlekv_store *store, void *stream, int64_t *page_jobs,
-                                            int64_t *jacobi_sweeps);
+                                            int64_t *ql_rotations);
 
 /*
  * Host-only page classification, the rule the store and its kernels apply

@@ -107,7 +107,7 @@ def factorize_batch(X: torch.Tensor, r: int, out_dtype: torch.dtype = torch.floa
                     stream: Optional[torch.cuda.Stream] = None):
     """Factorize independent pages X[n, P, d] -> (L[n, P, r], R[n, r, d], sigma[n, P] or None, status[1]).
 
-    ``status`` (int32 on the device) is nonzero if an eigensolve hit its sweep cap.
+    ``status`` (int32 on the device) is nonzero if an eigensolve hit its iteration cap.
     """
     if X.dim() != 3:
         raise ValueError("X must be [n, P, d]")
@@ -316,8 +316,8 @@ class Store:
         return st
 
     def factorize_counters(self, stream=None) -> tuple:
-        """(page jobs, Jacobi sweeps) of the store's factorization launches since
+        """(page jobs, QL rotations) of the store's factorization launches since
         the last call; the counters are cleared."""
-        jobs, sweeps = ctypes.c_int64(0), ctypes.c_int64(0)
-        check(lib().puzzlekv_factorize_counters(self._h, _stream(stream), ctypes.byref(jobs), ctypes.byref(sweeps)))
-        return jobs.value, sweeps.value
+        jobs, rotations = ctypes.c_int64(0), ctypes.c_int64(0)
+        check(lib().puzzlekv_factorize_counters(self._h, _stream(stream), ctypes.byref(jobs), ctypes.byref(rotations)))
+        return jobs.value, rotations.value

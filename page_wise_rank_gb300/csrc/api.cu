@@ -397,7 +397,7 @@ static puzzlekv_status prefill(puzzlekv_store *s, int32_t seq, int32_t layer0, i
     if (f_lo >= 0) {
         FactorParams fp{};
         fp.mode = FACT_MODE_PREFILL;
-        fp.max_sweeps = 24;
+        fp.max_ql_iter = 30;
         fp.status = status_ptr(s);
         fp.y = y;
         fp.P = y.P;
@@ -481,7 +481,7 @@ puzzlekv_status puzzlekv_factorize_batch(const void *X, int32_t x_dtype, int64_t
     FactorParams fp{};
     fp.mode = FACT_MODE_BATCH;
     fp.n_jobs = (long)n;
-    fp.max_sweeps = 24;
+    fp.max_ql_iter = 30;
     fp.status = status;
     fp.x_base = static_cast<const char *>(X);
     fp.x_esz = x_dtype == PUZZLEKV_BF16 ? 2 : 4;
@@ -524,7 +524,7 @@ puzzlekv_status puzzlekv_factorize_batch_int4(const void *X, int64_t n, int32_t 
     FactorParams fp{};
     fp.mode = FACT_MODE_BATCH_Q4;
     fp.n_jobs = (long)n;
-    fp.max_sweeps = 24;
+    fp.max_ql_iter = 30;
     fp.status = status;
     make_layout(fp.y, 1, 1, 1, d, P, rank_k, rank_v, 0, 0, 1, P, 1, 1);
     fp.P = P;
@@ -647,7 +647,7 @@ puzzlekv_status puzzlekv_append_token(puzzlekv_store *s, int32_t layer, const vo
     if (e != cudaSuccess) return cuda_fail(e, "append launch");
     if (fp.n_conv > 0) {
         fp.mode = FACT_MODE_CONVERT;
-        fp.max_sweeps = 24;
+        fp.max_ql_iter = 30;
         fp.status = status_ptr(s);
         fp.y = y;
         fp.P = y.P;
@@ -722,7 +722,7 @@ puzzlekv_status puzzlekv_decode_step(puzzlekv_store *s, int32_t layer, const voi
     cudaError_t e;
     if (fp.n_conv > 0) {  // the page leaving the window is factorized before this step's attention
         fp.mode = FACT_MODE_CONVERT;
-        fp.max_sweeps = 24;
+        fp.max_ql_iter = 30;
         fp.status = status_ptr(s);
         fp.y = y;
         fp.P = y.P;
@@ -772,27 +772,31 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, const int32_t *seq_i
                         "entry %d: page %d of sequence %d is not eligible (sink pages end at %d, complete pages at %d)",
                         i, p, b, y.sink_pages, c);
     }
-    // the jobs: every layer of each page without factors, marked as it is
-    // listed (so a page listed twice is factorized once)
-    s->job_host.clear();
-    auto add = [&](int b, int p) {
-        for (int l = 0; l < y.L; ++l)
-            if (!has_factors(s, b, l, p)) {
-                s->job_host.push_back(make_int2((b << 8) | l, p));
-                set_factors(s, b, l, p);
-            }
-    };
+    // the jobs: every layer of each listed page without factors (a page
+    // listed twice counts once); the pages are marked only once the list is
+    // known to fit
+    std::vector<int2> pages;
     if (n == -1) {
         for (int b = 0; b < y.Bmax; ++b) {
             const int c = complete_pages(b);
-            for (int p = y.sink_pages; p < c; ++p) add(b, p);
+            for (int p = y.sink_pages; p < c; ++p) pages.push_back(make_int2(b, p));
         }
     } else {
-        for (int i = 0; i < n; ++i) add(seq_ids[i], page_ids[i]);
+        for (int i = 0; i < n; ++i) pages.push_back(make_int2(seq_ids[i], page_ids[i]));
+        std::sort(pages.begin(), pages.end(), [](int2 u, int2 w) { return u.x != w.x ? u.x < w.x : u.y < w.y; });
+        pages.erase(std::unique(pages.begin(), pages.end(), [](int2 u, int2 w) { return u.x == w.x && u.y == w.y; }),
+                    pages.end());
     }
+    s->job_host.clear();
+    for (const int2 &bp : pages)
+        for (int l = 0; l < y.L; ++l)
+            if (!has_factors(s, bp.x, l, bp.y)) s->job_host.push_back(make_int2((bp.x << 8) | l, bp.y));
     if (s->job_host.empty()) return PUZZLEKV_OK;
+    // cannot trigger (a page outside the window always has factors, so at
+    // most ring + 1 pages per (seq, layer) lack them)
     if ((int)s->job_host.size() > y.max_conv_jobs)
         return fail(PUZZLEKV_ERR_CAPACITY, "internal: conversion list overflow");
+    for (const int2 &j : s->job_host) set_factors(s, j.x >> 8, j.x & 255, j.y);
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
     // the job list region is shared with the background batches: order this
     // call after every pending one (later batches start after this stream's work)
@@ -804,7 +808,7 @@ puzzlekv_status puzzlekv_factorize_pages(puzzlekv_store *s, const int32_t *seq_i
     if (e != cudaSuccess) return cuda_fail(e, "page list upload");
     FactorParams fp{};
     fp.mode = FACT_MODE_CONVERT_LIST;
-    fp.max_sweeps = 24;
+    fp.max_ql_iter = 30;
     fp.status = status_ptr(s);
     fp.y = y;
     fp.P = y.P;
@@ -860,7 +864,7 @@ puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
     if (e != cudaSuccess) return cuda_fail(e, "conversion list upload");
     FactorParams fp{};
     fp.mode = FACT_MODE_CONVERT_LIST;
-    fp.max_sweeps = 24;
+    fp.max_ql_iter = 30;
     fp.status = status_ptr(s);
     fp.y = y;
     fp.P = y.P;
@@ -932,17 +936,17 @@ puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *s, void *stream) {
 }
 
 puzzlekv_status puzzlekv_factorize_counters(puzzlekv_store *s, void *stream, int64_t *page_jobs,
-                                            int64_t *jacobi_sweeps) {
-    if (!s || !page_jobs || !jacobi_sweeps) return fail(PUZZLEKV_ERR_INVALID_ARG, "NULL argument");
+                                            int64_t *ql_rotations) {
+    if (!s || !page_jobs || !ql_rotations) return fail(PUZZLEKV_ERR_INVALID_ARG, "NULL argument");
     unsigned long long c[2] = {0, 0};  // status words 2-3 and 4-5
-    static_assert(STATUS_SWEEPS == STATUS_JOBS + 2, "counter words are adjacent");
+    static_assert(STATUS_ROTATIONS == STATUS_JOBS + 2, "counter words are adjacent");
     cudaError_t e = cudaStreamSynchronize(static_cast<cudaStream_t>(stream));
     if (e == cudaSuccess && s->conv_stream) e = cudaStreamSynchronize(s->conv_stream);
     if (e == cudaSuccess) e = cudaMemcpy(c, status_ptr(s) + STATUS_JOBS, sizeof(c), cudaMemcpyDeviceToHost);
     if (e == cudaSuccess) e = cudaMemset(status_ptr(s) + STATUS_JOBS, 0, sizeof(c));
     if (e != cudaSuccess) return cuda_fail(e, "counter read");
     *page_jobs = (int64_t)c[0];
-    *jacobi_sweeps = (int64_t)c[1];
+    *ql_rotations = (int64_t)c[1];
     return PUZZLEKV_OK;
 }
 

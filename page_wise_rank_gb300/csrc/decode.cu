@@ -181,8 +181,11 @@ static cudaError_t launch_f32(DecodeParams &p, long total_pages, int max_pages, 
 size_t decode_smem_bytes(const Layout &y) {
     if (y.dtype != 1) return 0;  // the fp32 kernel's shared memory is static and small
     const bool q4 = y.q4 != 0, rope = y.rope != 0;
-    // the shape of the runtime-rank kernel of this path (DecodeShape): warps x slots, units per dense page
-    const int nwc = q4 || rope ? 8 : 4, spw = rope ? 1 : 2, du = q4 && y.P >= 32 ? 4 : 2;
+    // the shape of the runtime-rank kernel of this path (DecodeShape): warps x
+    // slots, units per dense page
+    const int nwc = q4 || rope ? DecodeShape<true, 64>::NWC : DecodeShape<false, 64>::NWC;
+    const int spw = rope ? DecodeShape<false, 64, true>::SPW : DecodeShape<false, 64>::SPW;
+    const int du = q4 && y.P >= 32 ? DecodeShape<true, 64>::DU : DecodeShape<false, 64>::DU;
     const size_t unit = (size_t)(y.P / du) * y.d * 2 * 2;
     size_t stage = ((y.rec_bytes > unit ? y.rec_bytes : unit) + 15) & ~(size_t)15;
     if (rope) stage += (size_t)y.d * 4;

@@ -57,20 +57,27 @@ __device__ __forceinline__ float ex2_approx(float x) {
 
 // Shape of the tensor-core decode kernel: warps (NWC), shared-memory slots
 // each warp streams its units through (SPW) and units per dense page (DU).
-// A bf16 record (15 KB at P = 64, d = 128) fills a half-page slot, and two
-// slots per warp keep its copies ahead of its arithmetic.  An INT4 record
-// (4.5 KB) fits a quarter-page slot, so twice the warps fit in the same shared
-// memory; the per-page code expansion is the part that needs them.  Keys
-// stored before RoPE make a factorized page several times the arithmetic of a
-// bf16 one (rebuilding and turning its keys), so that path also runs 8 warps,
-// with one slot each.  Pages of 32 or fewer tokens carry half the bytes (or
-// less) for the same work per unit; with ranks fixed at compile time and a
-// record of at most 12 KB they run 8 warps x 2 slots as well.  A unit keeps a
-// multiple of 8 rows (the period of the dense pages' swizzle).
+// Two slots per warp keep its copies ahead of its arithmetic.  A bf16 record
+// of at most 18 KB (ranks fixed at compile time) leaves room for 6 warps x 2
+// slots, which hide more of each warp's latency than 4; larger or
+// runtime-rank records keep 4 x 2.  An INT4 record (4.5 KB) fits a
+// quarter-page slot, so 8 warps fit in the same shared memory; the per-page
+// code expansion is the part that needs them.  Keys stored before RoPE make a
+// factorized page several times the arithmetic of a bf16 one (rebuilding and
+// turning its keys), so that path also runs 8 warps, with one slot each.
+// Pages of 32 or fewer tokens carry half the bytes (or less) for the same
+// work per unit; with ranks fixed at compile time and a record of at most
+// 12 KB they run 8 warps x 2 slots as well.  A unit keeps a multiple of 8
+// rows (the period of the dense pages' swizzle).
 template <bool Q4, int P, bool ROPE = false, int D = 128, int RKT = 0, int RVT = 0>
 struct DecodeShape {
-    static constexpr bool WIDE = !Q4 && !ROPE && P <= 32 && RKT > 0 && RVT > 0 && 16 * (RKT + RVT) * (P + D) <= 12288;
-    static constexpr int NWC = Q4 || ROPE || WIDE ? 8 : 4, SPW = ROPE ? 1 : 2, DU = Q4 && P >= 32 ? 4 : 2;
+    static constexpr int REC = RKT > 0 && RVT > 0 ? 16 * (RKT + RVT) * (P + D) : 0;  // bf16 record bytes
+    static constexpr bool WIDE = !Q4 && !ROPE && P <= 32 && REC > 0 && REC <= 12288;
+    static constexpr int NWC = Q4 || ROPE || WIDE ? 8 : (REC > 0 && REC <= 18432 ? 6 : 4);
+    // bf16 stores cut dense pages in halves: quarter pages would make the
+    // slots no larger than a 15 KB record, but in back-to-back fused steps
+    // they stretched each layer's split-merge tail (1.9 us more per layer)
+    static constexpr int SPW = ROPE ? 1 : 2, DU = Q4 && P >= 32 ? 4 : 2;
     // 256 threads x 192 registers leave room for a 256-thread, 64-register
     // background conversion CTA on the same SM (at 209 the INT4 kernel locked
     // conversions out of the SMs it held); the pre-RoPE kernel needs all 255
@@ -142,53 +149,76 @@ __device__ __forceinline__ void cta_state(const float *comb, int e, float4 &acc,
 }
 
 // The merge of eq. (5) over the ns split states of each of the G query heads
-// of (b, h), written to `out`.  One pass per output float4: the largest m
-// over the splits, then the weights 2^(m_s - m), the normaliser and o summed
-// in split order (the same sums whichever CTA merges, so results are
-// bitwise reproducible).  ld1(g, s, k) and ld4(g, s, k) read float k (or
-// floats k .. k+3) of split s's row of head g.
+// of (b, h), written to `out`.  One warp per head, everything in registers:
+// lane t holds the m of splits t, t + 32, ...; their largest value and the
+// weights 2^(m_s - m) and normaliser come from warp shuffles, and each lane
+// sums one float4 of o over the splits in split order (at D = 64, two lanes
+// per float4, even and odd splits, added in a fixed order).  The sums are the
+// same whichever CTA merges, so results are bitwise reproducible.  ld1(g, s,
+// k) and ld4(g, s, k) read float k (or floats k .. k+3) of split s's row of
+// head g.
 template <int D, typename LD1, typename LD4>
 __device__ __forceinline__ void merge_states(const DecodeParams &prm, int b_idx, int h, int ns, LD1 ld1, LD4 ld4) {
+    constexpr int NJ = D / 4, NSUB = 32 / NJ, NI = MAX_SPLITS / 32;
     const int G = prm.y.G;
-    for (int e = threadIdx.x; e < G * (D / 4); e += blockDim.x) {
-        const int g = e / (D / 4), j = e % (D / 4);
+    const int nwarps = blockDim.x >> 5, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int j = lane % NJ, sub = lane / NJ;
+    for (int g = warp; g < G; g += nwarps) {
+        float m[NI], c[NI];
         float M = -INFINITY;
-        for (int sp = 0; sp < ns; ++sp) M = fmaxf(M, ld1(g, sp, 0));
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int sp = lane + 32 * i;
+            m[i] = sp < ns ? ld1(g, sp, 0) : -INFINITY;
+            M = fmaxf(M, m[i]);
+        }
+        M = warp_max(M);
         float L = 0.f;
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int sp = lane + 32 * i;
+            c[i] = m[i] == -INFINITY ? 0.f : ex2_approx(m[i] - M);
+            if (sp < ns) L = fmaf(c[i], ld1(g, sp, 1), L);
+        }
+        L = warp_sum(L);
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-        for (int sp = 0; sp < ns; ++sp) {
-            const float m = ld1(g, sp, 0);
-            const float c = m == -INFINITY ? 0.f : ex2_approx(m - M);
-            L = fmaf(c, ld1(g, sp, 1), L);
-            const float4 v = ld4(g, sp, 4 + 4 * j);
-            acc.x = fmaf(c, v.x, acc.x);
-            acc.y = fmaf(c, v.y, acc.y);
-            acc.z = fmaf(c, v.z, acc.z);
-            acc.w = fmaf(c, v.w, acc.w);
+#pragma unroll
+        for (int i = 0; i < NI; ++i) {
+            const int n_here = min(32, ns - 32 * i);
+            for (int t2 = 0; NSUB * t2 < n_here; ++t2) {  // the same trip count in every lane
+                const int t = NSUB * t2 + sub;
+                const float cs = __shfl_sync(0xffffffffu, c[i], t < 32 ? t : 31);
+                if (t < n_here) {
+                    const float4 v = ld4(g, 32 * i + t, 4 + 4 * j);
+                    acc.x = fmaf(cs, v.x, acc.x);
+                    acc.y = fmaf(cs, v.y, acc.y);
+                    acc.z = fmaf(cs, v.z, acc.z);
+                    acc.w = fmaf(cs, v.w, acc.w);
+                }
+            }
+        }
+        if constexpr (NSUB == 2) {  // odd splits' partial sums into the even lanes'
+            acc.x += __shfl_down_sync(0xffffffffu, acc.x, NJ);
+            acc.y += __shfl_down_sync(0xffffffffu, acc.y, NJ);
+            acc.z += __shfl_down_sync(0xffffffffu, acc.z, NJ);
+            acc.w += __shfl_down_sync(0xffffffffu, acc.w, NJ);
         }
         const float il = 1.f / L;
-        reinterpret_cast<float4 *>(prm.out + ((size_t)b_idx * prm.y.Hq + h * G + g) * D)[j] =
-            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+        if (sub == 0)
+            reinterpret_cast<float4 *>(prm.out + ((size_t)b_idx * prm.y.Hq + h * G + g) * D)[j] =
+                make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
     }
 }
 
-// Reads of split states staged in shared memory at `sb` (rows of S floats,
-// head g's ns rows contiguous).
+// Reads of split states staged in shared memory at `rows` (rows of S
+// floats, head g's ns rows contiguous): plain loads, which the compiler may
+// batch (the staging barrier's wait orders them after the copies).
 struct StagedRows {
-    uint32_t sb;
+    const float *rows;
     int ns, S;
-    __device__ __forceinline__ float one(int g, int sp, int k) const {
-        float v;
-        asm volatile("ld.shared.f32 %0, [%1];" : "=f"(v) : "r"(sb + (uint32_t)(((g * ns + sp) * S + k) * 4)));
-        return v;
-    }
+    __device__ __forceinline__ float one(int g, int sp, int k) const { return rows[(g * ns + sp) * S + k]; }
     __device__ __forceinline__ float4 four(int g, int sp, int k) const {
-        float4 v;
-        asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];"
-                     : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
-                     : "r"(sb + (uint32_t)(((g * ns + sp) * S + k) * 4)));
-        return v;
+        return *reinterpret_cast<const float4 *>(rows + (g * ns + sp) * S + k);
     }
 };
 
@@ -254,7 +284,7 @@ __device__ bool finish_split(const DecodeParams &prm, const float *comb, int b_i
     if (!*last) return false;
     if (staged) {
         if (!merge_copies_landed(prm, merge_bar)) return false;
-        const StagedRows rows{smem_u32(stage_buf), ns, S};
+        const StagedRows rows{stage_buf, ns, S};
         merge_states<D>(prm, b_idx, h, ns, [&](int g, int sp, int k) { return rows.one(g, sp, k); },
                         [&](int g, int sp, int k) { return rows.four(g, sp, k); });
     } else {
@@ -385,11 +415,14 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
     constexpr int MAXK = RKT ? RKT : 8;
     const int nkt = RKT ? RKT : (y.rkp >> 3);
     const uint32_t LK = st, RK = st + (uint32_t)P * nkt * 16;
-    // 1. t = q R_K^T  (16 x rkp; rows 8-15 stay zero)
-    float t[MAXK][4];
+    // 1. t = q R_K^T  (16 x rkp; rows 8-15 stay zero), as two accumulator
+    // chains of half the head dim each, so the products of a rank tile do not
+    // wait on one another D / 16 deep
+    float t[MAXK][4], t2[MAXK][4];
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) {
         t[j][0] = t[j][1] = t[j][2] = t[j][3] = 0.f;
+        t2[j][0] = t2[j][1] = t2[j][2] = t2[j][3] = 0.f;
         if (j < nkt) {
 #pragma unroll
             for (int k2 = 0; k2 < D / 32; ++k2) {
@@ -397,8 +430,12 @@ __device__ __forceinline__ void factored_unit(WarpState<P, D> &w, uint32_t st, c
                 uint32_t r0, r1, r2, r3;
                 ldsm_x4(RK + swz_offset(row, ch * 16, D * 2), r0, r1, r2, r3);
                 O::mma(t[j], qa[2 * k2][0], 0u, qa[2 * k2][1], 0u, r0, r1);
-                O::mma(t[j], qa[2 * k2 + 1][0], 0u, qa[2 * k2 + 1][1], 0u, r2, r3);
+                O::mma(t2[j], qa[2 * k2 + 1][0], 0u, qa[2 * k2 + 1][1], 0u, r2, r3);
             }
+            t[j][0] += t2[j][0];
+            t[j][1] += t2[j][1];
+            t[j][2] += t2[j][2];
+            t[j][3] += t2[j][3];
         }
     }
     // 2. s = t L_K^T  (16 x P), t split into high (rows 0-7) and residual (rows 8-15)
@@ -919,9 +956,12 @@ __device__ __forceinline__ void patch_new_row(const DecodeParams &prm, unsigned 
 // through SPW private shared-memory slots, its lane 0 issuing the bulk copy of
 // the warp's next unit into the slot the warp has just finished with (one
 // mbarrier per slot, so a slot's phases are always consumed in order by the
-// warp that fills it).  Right after its first copies, lane 0 of warp 0 asks
-// L2 for the rest of the CTA's range, so the bytes in flight do not depend on
-// the slot count.
+// warp that fills it).  The slots' first fill, issued before the dependency
+// wait, holds a large part of the range (NWC x SPW units); the rest is
+// copied on demand.  Asking L2 to prefetch the rest of the range as well made
+// back-to-back launches slower (the next launch's prefetches compete with the
+// current one's last copies and its completion) and the single launch no
+// faster, so the kernel does not.
 //
 // Overlap with the neighbouring launches (programmatic dependent launch): a
 // CTA lets the next launch start as soon as its own wait for the preceding
@@ -931,8 +971,8 @@ __device__ __forceinline__ void patch_new_row(const DecodeParams &prm, unsigned 
 // (unless the preceding launch of this store was a conversion, a prefill or an
 // append, in which case prm.wait_first makes the first copy wait) and dense
 // rows below T - 2 (the rows the preceding launch may append are T - 2 and
-// T - 1).  L2 prefetches need no such care: L2 is the point of coherence, so
-// a row written after its prefetch is still copied fresh.
+// T - 1).  The query rows are prefetched into L2 before that wait: L2 is the
+// point of coherence, so a row written after its prefetch is still read fresh.
 
 template <int P, int D, int RKT, int RVT, bool Q4, bool ROPE>
 __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 32, CTAS_PER_SM)
@@ -1034,18 +1074,10 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     };
     if (lane == 0) {
         policy = l2_evict_first();
+        if (warp == 0)  // the query rows, read by every warp right after the dependency wait
+            prefetch_l2(prm.q + ((size_t)b_idx * y.Hq + (size_t)h * y.G) * D * 2, (uint32_t)(y.G * D * 2));
         if (waited) grid_dependency_wait();
         for (int k = 0; k < SPW && k < n_mine; ++k) issue(k, unit_of(warp + NWC * k));
-        if (warp == NWC - 1) {  // the rest of the range: L2 prefetches
-            for (size_t off = 0, len = (size_t)n_fac * y.rec_bytes; off < len; off += 65536)
-                prefetch_l2(fact + (size_t)a1 * y.rec_bytes + off, (uint32_t)min(len - off, (size_t)65536));
-            for (int p = pb; p < pe; ++p) {
-                if (p >= a1 && p < a2) continue;
-                const int slot_d = y.dense_slot(p);
-                prefetch_l2(prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 0), (uint32_t)y.dense_half_bytes);
-                prefetch_l2(prm.dense_pool + y.dense_offset(prm.layer, b, slot_d, h, 1), (uint32_t)y.dense_half_bytes);
-            }
-        }
     }
 
     // q, the appended token and the page table may come from the preceding grid
@@ -1204,6 +1236,12 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
             c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared) +
                      (ROPE ? 16 + (size_t)P * D * 4 : 0);  // RoPE: the aligned in-page angle table
             c.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
+            // An SM's shared/L1 split is set when it takes a CTA and holds
+            // while any CTA runs there: with the largest split a background
+            // factorization CTA still fits beside a decode CTA.
+            if (c.err == cudaSuccess)
+                c.err = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                             cudaSharedmemCarveoutMaxShared);
             if (c.err == cudaSuccess &&
                 (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&c.occ, k, Shape::NWC * 32, c.smem) != cudaSuccess ||
                  c.occ < 1))

@@ -7,10 +7,9 @@
 //   1. X -> shared memory (bf16 rows in the swizzled layout, or fp32 rows);
 //   2. G = X X^T in fp32: bf16 pages on tensor cores (mma.sync m16n8k16,
 //      bf16 products are exact in fp32), fp32 pages on CUDA cores;
-//   3. cyclic Jacobi on G with the round-robin (circle) pairing: each round
-//      rotates P/2 disjoint pairs at once (2x2 blocks of G, pairs of
-//      eigenvector rows); a sweep is P-1 rounds; stop after a sweep with no
-//      rotation (relative threshold), or at the cap;
+//   3. the eigenvectors of G: Householder reduction to tridiagonal form, the
+//      reflections' product formed explicitly, then implicit QL on the
+//      tridiagonal with every rotation applied to that product;
 //   4. eigenvalues ranked descending (ties: lower index first);
 //   5. L = Q_r, R = Q_r^T X in fp32, written as bf16 or fp32 into either a
 //      factor record (swizzled store layout) or plain row-major arrays.
@@ -23,21 +22,36 @@
 
 namespace pkv {
 
-constexpr float JACOBI_TOL = 1e-6f;
-// Stop the eigensolve once the kept subspace could gain at most this fraction
-// of the energy it leaves out (reconstruction error excess about half of it:
-// 5e-5, twenty times inside the 1e-3 bound on the excess).
-constexpr float SUBSPACE_TOL = 1e-4f;
+// An off-diagonal entry of the tridiagonal at or below this fraction of its
+// norm counts as zero (the fp32 unit roundoff, 2^-23).
+constexpr float QL_EPS = 1.1920929e-7f;
+// The eigensolve works on G scaled to a largest diagonal entry in [1, 2).
+// A column whose norm below the diagonal is at most NEGLIGIBLE gets no
+// reflection, and a QL rotation whose radius is below it counts as a split:
+// such entries change no eigenvalue by more than 1e-18, while reflecting or
+// rotating by them would square them into the subnormal range (a block of
+// repeated rows drives the trailing columns that low) and divide by that.
+constexpr float NEGLIGIBLE = 1e-18f;
 
 template <typename T, int P, int D>
 struct FactorSmem {
-    alignas(128) unsigned char X[P * D * sizeof(T)];  // swizzled rows, pitch D * sizeof(T)
-    float G[P][P + 1];  // Gram matrix; after the eigensolve reused for Q[i][j] = Vt[order[j]][i]
-    alignas(16) float Vt[P][P + 4];  // eigenvectors, one per row (rows stay 16-byte aligned)
-    float4 pair[P / 2];              // per pair of the round: (p, q as int bits, cos, sin)
-    float tn[P / 2];                 // tan of the pair's angle (0: no rotation)
-    float lam[P];
+    // The page X is needed for the Gram matrix and again for the projection,
+    // the eigenvectors only in between: they share storage, and the page is
+    // loaded a second time once the eigenvectors are taken out.  (At P = 64,
+    // d = 128, bf16, the CTA then takes 36 KB instead of 53 KB, which lets a
+    // background conversion CTA sit beside a decode CTA on one SM.)
+    union {
+        alignas(128) unsigned char X[P * D * sizeof(T)];  // swizzled rows, pitch D * sizeof(T)
+        float Z[P][P + 1];  // eigenvectors as columns: Z[i][j] = component i of vector j
+    };
+    float G[P][P + 1];  // Gram matrix; after the eigensolve reused for Q[i][j] = Z[i][order[j]]
+    float lam[P];       // diagonal of the tridiagonal, then the eigenvalues
+    float off[P];       // its off-diagonal: off[k] couples k and k + 1
+    float hb[P];        // Householder reflections: beta_k (0: none) ...
+    float hv0[P];       // ... and the first entry of v_k
+    float pv[P];        // a work vector of the reduction
     int order[P];
+    float sc[P + D];                 // INT4 scales in fp32: per rank or token, then per head-dim column
     float red[64];                   // per-warp partial sums (up to 32 warps, two sums)
 };
 
@@ -175,295 +189,204 @@ __device__ void gram_f32(FactorSmem<float, P, D> &s) {
     }
 }
 
-// Cyclic Jacobi eigensolve of the symmetric P x P matrix in s.G (upper
-// triangle, G[i][j] with i <= j, is the matrix); eigenvectors accumulate as
-// the rows of s.Vt.  Returns the number of sweeps, or -1 at the cap.  A round
-// rotates the P/2 disjoint pairs of the round-robin (circle) pairing at once:
-// phase A computes the angles, phase B applies G <- J^T G J to the 2x2
-// blocks of the upper triangle (each thread keeps its blocks for the whole
-// solve) and rotates pairs of eigenvector rows with 16-byte vectors.  Blocks
-// and rows of pairs that did not rotate are left alone.
-// Energy the top-r subspace of the current diagonal can still gain, over the
-// energy it leaves out: for every pair (i among the r largest diagonal
-// entries, j among the rest) the exact gain of the 2 x 2 rotation,
-// sqrt(h^2 + g_ij^2) - |h| with h = (g_ii - g_jj) / 2, summed, over the sum of
-// the left-out diagonal.  Uses s.order (free during the solve) and s.red;
-// every thread gets the result.
-template <typename T, int P, int D, int NT>
-__device__ float subspace_gain(FactorSmem<T, P, D> &s, int r) {
-    const int tid = threadIdx.x;
-    if (tid < P) {  // rank of each diagonal entry, descending (ties: lower index first)
-        const float di = s.G[tid][tid];
-        int rk = 0;
-        for (int j = 0; j < P; ++j) {
-            const float dj = s.G[j][j];
-            rk += (dj > di) || (dj == di && j < tid);
-        }
-        s.order[rk] = tid;
-    }
-    __syncthreads();
-    float gain = 0.f, left = 0.f;
-    for (int e = tid; e < r * (P - r); e += NT) {
-        const int i = s.order[e / (P - r)], j = s.order[r + e % (P - r)];
-        const float h = 0.5f * (s.G[i][i] - s.G[j][j]);
-        const float g = i < j ? s.G[i][j] : s.G[j][i];
-        const float rad = sqrtf(fmaf(h, h, g * g));
-        gain += rad > 0.f ? g * g / (rad + fabsf(h)) : 0.f;
-    }
-    for (int k = r + tid; k < P; k += NT) left += s.G[s.order[k]][s.order[k]];
-    // block sums: warp shuffles, then one value per warp in s.lam
-    gain = warp_sum(gain);
-    left = warp_sum(left);
-    const int warp = tid >> 5, lane = tid & 31;
-    static_assert(NT / 32 <= 32, "two partial sums per warp in s.red");
-    if (lane == 0) {
-        s.red[warp] = gain;
-        s.red[32 + warp] = left;
-    }
-    __syncthreads();
-    float gs = 0.f, ls = 0.f;  // every thread sums the same values in the same order
-    for (int w = 0; w < NT / 32; ++w) {
-        gs += s.red[w];
-        ls += s.red[32 + w];
-    }
-    __syncthreads();
-    return ls > 0.f ? gs / ls : (gs > 0.f ? INFINITY : 0.f);
+// ---------------------------------------------------------------- eigensolve
+// Eigenvectors of the symmetric P x P matrix in s.G (both triangles), by
+// three classical steps:
+//   1. Householder reduction to tridiagonal form T = Q^T G Q, with P - 2
+//      reflections H_k = I - beta_k v_k v_k^T (v_k supported on the indices
+//      k+1 .. P-1), each applied to both sides of the trailing block as one
+//      rank-2 update;
+//   2. Q = H_0 H_1 ... H_{P-3} formed explicitly in s.Z, last reflection
+//      first;
+//   3. the implicit QL algorithm with Wilkinson shifts on T, every plane
+//      rotation also applied to two columns of s.Z, whose columns so become
+//      the eigenvectors of G (the tql2 scheme of Bowdler, Martin, Reinsch and
+//      Wilkinson, "The QR and QL algorithms for symmetric matrices", 1968).
+// Every sum is taken by a fixed set of lanes in a fixed order, whatever the
+// block size, so every variant of the kernel gives the same bits.
+
+// Sum over i in [0, n) of the products a(i) b(i), four lanes per output
+// (lanes 4t .. 4t+3 of a warp; call with every lane of the warp): lane
+// quarter q takes i = 8q + m + 32t (m < 8), which keeps the eight outputs of
+// a warp on distinct banks when the products read row (or column) o + i of a
+// matrix with pitch P + 1; the four partial sums meet by shuffles in a fixed
+// order.  `active`: whether this lane's output exists (its products are
+// skipped otherwise).
+template <typename F>
+__device__ __forceinline__ float quad_dot(int n, bool active, F prod) {
+    const int q = threadIdx.x & 3;
+    float acc = 0.f;
+    if (active)
+        for (int t = 0; 32 * t < n; ++t)
+#pragma unroll
+            for (int m = 0; m < 8; ++m) {
+                const int i = 32 * t + 8 * q + m;
+                if (i < n) acc = prod(i, acc);
+            }
+    acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+    acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+    return acc;
 }
 
+// Step 1.  On return s.lam[k] = T_kk, s.off[k] = T_{k,k+1} (off[P-1] = 0);
+// v_k stays in column k of s.G from row k+2 on, its first entry in s.hv0[k],
+// beta_k in s.hb[k] (0: no reflection).
 template <typename T, int P, int D, int NT>
-__device__ int jacobi(FactorSmem<T, P, D> &s, int max_sweeps, int r) {
-    constexpr int NP = P / 2;
-    constexpr int NBLK = NP * (NP + 1) / 2;
-    constexpr int BPT = (NBLK + NT - 1) / NT;  // blocks per thread
-    constexpr int V4 = P / 4;                  // float4 per eigenvector row
-    const int tid = threadIdx.x;
-    for (int e = tid; e < P * P; e += NT) s.Vt[e / P][e % P] = (e / P == e % P) ? 1.f : 0.f;
-    int my_al[BPT], my_be[BPT];
-#pragma unroll
-    for (int i = 0; i < BPT; ++i) {  // block e = tid + i * NT of the row-major upper triangle
-        int e = tid + i * NT, be = 0;
-        if (e < NBLK) {
-            while ((be + 1) * (be + 2) / 2 <= e) ++be;
-            my_al[i] = e - be * (be + 1) / 2;
-            my_be[i] = be;
-        } else {
-            my_al[i] = my_be[i] = -1;
+__device__ void tridiagonalize(FactorSmem<T, P, D> &s) {
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int k = 0; k < P - 2; ++k) {
+        const int n = P - 1 - k;  // order of the trailing block S = G[k+1.., k+1..]
+        // every warp forms the reflection itself (the same sums in the same
+        // order, hence the same bits): x = G[k+1.., k], x0 its first entry
+        float sig = 0.f;
+        for (int i = 1 + lane; i < n; i += 32) sig = fmaf(s.G[k + 1 + i][k], s.G[k + 1 + i][k], sig);
+        sig = warp_sum(sig);
+        const float x0 = s.G[k + 1][k];
+        float alpha = x0, beta = 0.f, v0 = 0.f;
+        if (sig > NEGLIGIBLE * NEGLIGIBLE) {  // H x = alpha e_1, v = x - alpha e_1, beta = 2 / |v|^2 <= 1 / sig
+            alpha = -copysignf(sqrtf(fmaf(x0, x0, sig)), x0);
+            v0 = x0 - alpha;  // |v0| = |x0| + |alpha|: no cancellation
+            beta = -1.f / (alpha * v0);
         }
-    }
-    const float tol2 = JACOBI_TOL * JACOBI_TOL;
-    __syncthreads();
-    for (int sweep = 0; sweep < max_sweeps; ++sweep) {
-        int rotated_any = 0;
-        for (int round = 0; round < P - 1; ++round) {
-            // Phase A: slot 0 holds index 0, slot i >= 1 holds 1 + (i - 1 - round) mod (P - 1);
-            // slot k meets slot P - 1 - k.
-            int rot = 0;
-            if (tid < NP) {
-                int k = tid;
-                int a = k == 0 ? 0 : 1 + ((k - 1 - round + 2 * (P - 1)) % (P - 1));
-                int kb = P - 1 - k;
-                int b = 1 + ((kb - 1 - round + 2 * (P - 1)) % (P - 1));
-                int p = a < b ? a : b, q = a < b ? b : a;
-                float gpp = s.G[p][p], gqq = s.G[q][q], gpq = s.G[p][q];
-                float c = 1.f, sn = 0.f, t = 0.f;
-                if (gpq * gpq > tol2 * fabsf(gpp * gqq) && gpq != 0.f) {
-                    // tan of the angle that zeroes G_pq: smaller root of t^2 + 2 zeta t - 1 = 0
-                    float zeta = __fdividef(gqq - gpp, 2.f * gpq);
-                    float z2 = fmaf(zeta, zeta, 1.f);
-                    t = copysignf(__fdividef(1.f, fabsf(zeta) + z2 * rsqrtf(z2)), zeta);
-                    if (fabsf(zeta) > 1e18f) t = __fdividef(0.5f, zeta);  // z2 overflows
-                    c = rsqrtf(fmaf(t, t, 1.f));
-                    sn = t * c;
-                    rot = 1;
-                }
-                s.pair[k] = make_float4(__int_as_float(p), __int_as_float(q), c, sn);
-                s.tn[k] = t;
-            }
-            rotated_any |= __syncthreads_or(rot);
-            // Phase B1: 2x2 blocks of the upper triangle of G
-#pragma unroll
-            for (int i = 0; i < BPT; ++i) {
-                const int al = my_al[i], be = my_be[i];
-                if (al < 0) continue;
-                const float4 A = s.pair[al];
-                const int pa = __float_as_int(A.x), qa = __float_as_int(A.y);
-                if (al == be) {
-                    const float t = s.tn[al];
-                    if (t != 0.f) {
-                        const float g00 = s.G[pa][pa], g01 = s.G[pa][qa], g11 = s.G[qa][qa];
-                        s.G[pa][pa] = g00 - t * g01;
-                        s.G[qa][qa] = g11 + t * g01;
-                        s.G[pa][qa] = 0.f;
-                    }
-                    continue;
-                }
-                const float4 B = s.pair[be];
-                if (A.w == 0.f && B.w == 0.f) continue;
-                const int pb = __float_as_int(B.x), qb = __float_as_int(B.y);
-                // element (x, y) of the symmetric matrix lives at G[min][max]
-                float *e00 = pa < pb ? &s.G[pa][pb] : &s.G[pb][pa];
-                float *e01 = pa < qb ? &s.G[pa][qb] : &s.G[qb][pa];
-                float *e10 = qa < pb ? &s.G[qa][pb] : &s.G[pb][qa];
-                float *e11 = qa < qb ? &s.G[qa][qb] : &s.G[qb][qa];
-                const float ca = A.z, sa = A.w, cb = B.z, sb = B.w;
-                const float g00 = *e00, g01 = *e01, g10 = *e10, g11 = *e11;
-                const float h00 = ca * g00 - sa * g10, h01 = ca * g01 - sa * g11;
-                const float h10 = sa * g00 + ca * g10, h11 = sa * g01 + ca * g11;
-                *e00 = cb * h00 - sb * h01;
-                *e01 = sb * h00 + cb * h01;
-                *e10 = cb * h10 - sb * h11;
-                *e11 = sb * h10 + cb * h11;
-            }
-            // Phase B2: eigenvector rows p, q of each pair, four components at a time
-            for (int e = tid; e < NP * V4; e += NT) {
-                const int k = e / V4, c4 = e % V4;
-                const float4 A = s.pair[k];
-                if (A.w == 0.f) continue;
-                const int p = __float_as_int(A.x), q = __float_as_int(A.y);
-                float4 *vp = reinterpret_cast<float4 *>(&s.Vt[p][0]) + c4;
-                float4 *vq = reinterpret_cast<float4 *>(&s.Vt[q][0]) + c4;
-                const float4 a = *vp, b = *vq;
-                const float c = A.z, sn = A.w;
-                *vp = make_float4(c * a.x - sn * b.x, c * a.y - sn * b.y, c * a.z - sn * b.z, c * a.w - sn * b.w);
-                *vq = make_float4(sn * a.x + c * b.x, sn * a.y + c * b.y, sn * a.z + c * b.z, sn * a.w + c * b.w);
-            }
-            __syncthreads();
+        if (tid == 0) {
+            s.lam[k] = s.G[k][k];
+            s.off[k] = alpha;
+            s.hb[k] = beta;
+            s.hv0[k] = v0;
         }
-        if (!rotated_any) return sweep + 1;
-        // only the top-r subspace is kept: stop once no rotation could add
-        // more than SUBSPACE_TOL of the energy it leaves out (rotations inside
-        // the nearly degenerate noise bulk converge slowly and change nothing)
-        if (r < P && subspace_gain<T, P, D, NT>(s, r) <= SUBSPACE_TOL) return sweep + 1;
+        if (beta == 0.f) continue;  // the same decision in every warp
+        auto vv = [&](int i) { return i == 0 ? v0 : s.G[k + 1 + i][k]; };
+        // p = beta S v: four lanes per row (warp-uniform loop bounds)
+        for (int base = 8 * warp; base < n; base += NT / 4) {
+            const int i = base + (lane >> 2);
+            const float acc =
+                quad_dot(n, i < n, [&](int j, float a) { return fmaf(s.G[k + 1 + i][k + 1 + j], vv(j), a); });
+            if ((lane & 3) == 0 && i < n) s.pv[i] = beta * acc;
+        }
+        __syncthreads();
+        // K = beta v.p / 2 (each warp), w = p - K v, S <- S - v w^T - w v^T,
+        // the entries (i, j) and (j, i) rounded alike
+        float vp = 0.f;
+        for (int i = lane; i < n; i += 32) vp = fmaf(vv(i), s.pv[i], vp);
+        const float K = 0.5f * beta * warp_sum(vp);
+        for (int i = warp; i < n; i += NW)
+            for (int j = lane; j < n; j += 32) {
+                const int a = max(i, j), b = min(i, j);
+                const float va = vv(a), vb = vv(b);
+                const float wa = fmaf(-K, va, s.pv[a]), wb = fmaf(-K, vb, s.pv[b]);
+                s.G[k + 1 + i][k + 1 + j] -= fmaf(va, wb, __fmul_rn(wa, vb));
+            }
+        __syncthreads();
     }
-    return -1;
+    if (tid == 0) {
+        s.lam[P - 2] = s.G[P - 2][P - 2];
+        s.lam[P - 1] = s.G[P - 1][P - 1];
+        s.off[P - 2] = s.G[P - 1][P - 2];
+        s.off[P - 1] = 0.f;
+    }
 }
 
-// INT4 records need the kept vectors to be eigenvectors (their sigma^{1/2}
-// scaling), not just a basis of the kept subspace.  After the subspace stop
-// the subspace is settled, so cyclic Jacobi restricted to the block of the r
-// largest diagonal entries finishes the job: round-robin pairs among the
-// block's indices (a dummy index when r is odd), each rotation applied to the
-// block's entries of G and to the whole eigenvector rows.  Entries between
-// the block and the rest are left alone: nothing reads them afterwards.
-// Leaves s.order as the final ranking -- the block's indices by their
-// polished eigenvalue (ties: lower index first), then the others in index
-// order -- and returns the block sweeps taken (-1 at the cap).
+// Step 2: s.Z = H_0 ... H_{P-3} (H_k Z changes only the trailing block of
+// rows and columns k+1 .. P-1 once the later reflections are in).
 template <typename T, int P, int D, int NT>
-__device__ int polish_block(FactorSmem<T, P, D> &s, int r, int max_sweeps) {
-    constexpr int V4 = P / 4;
-    const int tid = threadIdx.x;
-    const int n = (r + 1) & ~1, np = n / 2;
-    if (tid < P) {
-        const float li = s.G[tid][tid];
-        int rank = 0;
-        for (int j = 0; j < P; ++j) {
-            const float lj = s.G[j][j];
-            rank += (lj > li) || (lj == li && j < tid);
-        }
-        s.red[tid] = rank < r ? 1.f : 0.f;  // block membership
-        if (rank < r) s.order[rank] = tid;
-    }
+__device__ void accumulate_q(FactorSmem<T, P, D> &s) {
+    constexpr int NW = NT / 32;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int e = tid; e < P * P; e += NT) s.Z[e / P][e % P] = e / P == e % P ? 1.f : 0.f;
     __syncthreads();
-    const float tol2 = JACOBI_TOL * JACOBI_TOL;
-    int done = -1;
-    for (int sweep = 0; sweep < max_sweeps && done < 0; ++sweep) {
-        int rotated_any = 0;
-        for (int round = 0; round < n - 1; ++round) {
-            int rot = 0;
-            if (tid < np) {
-                const int k = tid;
-                const int a = k == 0 ? 0 : 1 + ((k - 1 - round + 2 * (n - 1)) % (n - 1));
-                const int kb = n - 1 - k;
-                const int b = 1 + ((kb - 1 - round + 2 * (n - 1)) % (n - 1));
-                int p = -1, q = -1;
-                float c = 1.f, sn = 0.f, t = 0.f;
-                if (a < r && b < r) {
-                    const int ia = s.order[a], ib = s.order[b];
-                    p = ia < ib ? ia : ib;
-                    q = ia < ib ? ib : ia;
-                    const float gpp = s.G[p][p], gqq = s.G[q][q], gpq = s.G[p][q];
-                    if (gpq * gpq > tol2 * fabsf(gpp * gqq) && gpq != 0.f) {
-                        float zeta = __fdividef(gqq - gpp, 2.f * gpq);
-                        float z2 = fmaf(zeta, zeta, 1.f);
-                        t = copysignf(__fdividef(1.f, fabsf(zeta) + z2 * rsqrtf(z2)), zeta);
-                        if (fabsf(zeta) > 1e18f) t = __fdividef(0.5f, zeta);
-                        c = rsqrtf(fmaf(t, t, 1.f));
-                        sn = t * c;
-                        rot = 1;
-                    }
-                }
-                s.pair[k] = make_float4(__int_as_float(p), __int_as_float(q), c, sn);  // p < 0: the dummy
-                s.tn[k] = t;
-            }
-            rotated_any |= __syncthreads_or(rot);
-            const int nblk = np * (np + 1) / 2;
-            for (int e = tid; e < nblk; e += NT) {  // 2x2 blocks (al <= be) of this round's pairs
-                int be = 0;
-                while ((be + 1) * (be + 2) / 2 <= e) ++be;
-                const int al = e - be * (be + 1) / 2;
-                const float4 A = s.pair[al], B = s.pair[be];
-                const int pa = __float_as_int(A.x), qa = __float_as_int(A.y);
-                const int pb = __float_as_int(B.x), qb = __float_as_int(B.y);
-                if (pa < 0 || pb < 0) continue;
-                if (al == be) {
-                    const float t = s.tn[al];
-                    if (t != 0.f) {
-                        const float g00 = s.G[pa][pa], g01 = s.G[pa][qa], g11 = s.G[qa][qa];
-                        s.G[pa][pa] = g00 - t * g01;
-                        s.G[qa][qa] = g11 + t * g01;
-                        s.G[pa][qa] = 0.f;
-                    }
-                    continue;
-                }
-                if (A.w == 0.f && B.w == 0.f) continue;
-                float *e00 = pa < pb ? &s.G[pa][pb] : &s.G[pb][pa];
-                float *e01 = pa < qb ? &s.G[pa][qb] : &s.G[qb][pa];
-                float *e10 = qa < pb ? &s.G[qa][pb] : &s.G[pb][qa];
-                float *e11 = qa < qb ? &s.G[qa][qb] : &s.G[qb][qa];
-                const float ca = A.z, sa = A.w, cb = B.z, sb = B.w;
-                const float g00 = *e00, g01 = *e01, g10 = *e10, g11 = *e11;
-                const float h00 = ca * g00 - sa * g10, h01 = ca * g01 - sa * g11;
-                const float h10 = sa * g00 + ca * g10, h11 = sa * g01 + ca * g11;
-                *e00 = cb * h00 - sb * h01;
-                *e01 = sb * h00 + cb * h01;
-                *e10 = cb * h10 - sb * h11;
-                *e11 = sb * h10 + cb * h11;
-            }
-            for (int e = tid; e < np * V4; e += NT) {  // eigenvector rows p, q of each rotating pair
-                const int k = e / V4, c4 = e % V4;
-                const float4 A = s.pair[k];
-                if (A.w == 0.f) continue;
-                const int p = __float_as_int(A.x), q = __float_as_int(A.y);
-                float4 *vp = reinterpret_cast<float4 *>(&s.Vt[p][0]) + c4;
-                float4 *vq = reinterpret_cast<float4 *>(&s.Vt[q][0]) + c4;
-                const float4 a = *vp, b = *vq;
-                const float c = A.z, sn = A.w;
-                *vp = make_float4(c * a.x - sn * b.x, c * a.y - sn * b.y, c * a.z - sn * b.z, c * a.w - sn * b.w);
-                *vq = make_float4(sn * a.x + c * b.x, sn * a.y + c * b.y, sn * a.z + c * b.z, sn * a.w + c * b.w);
-            }
-            __syncthreads();
+    for (int k = P - 3; k >= 0; --k) {
+        const float beta = s.hb[k];
+        if (beta == 0.f) continue;
+        const int n = P - 1 - k;
+        const float v0 = s.hv0[k];
+        auto vv = [&](int i) { return i == 0 ? v0 : s.G[k + 1 + i][k]; };
+        // u = Z_S^T v (four lanes per column), then Z_S <- Z_S - beta v u^T
+        for (int base = 8 * warp; base < n; base += NT / 4) {
+            const int j = base + (lane >> 2);
+            const float acc =
+                quad_dot(n, j < n, [&](int i, float a) { return fmaf(vv(i), s.Z[k + 1 + i][k + 1 + j], a); });
+            if ((lane & 3) == 0 && j < n) s.pv[j] = beta * acc;
         }
-        if (!rotated_any) done = sweep + 1;
-    }
-    // final ranking: the block by polished eigenvalue, then the rest by index
-    if (tid < P) {
-        const bool member = s.red[tid] != 0.f;
-        const float li = s.G[tid][tid];
-        int pos = member ? 0 : r;
-        for (int j = 0; j < P; ++j) {
-            const bool mj = s.red[j] != 0.f;
-            if (member && mj) {
-                const float lj = s.G[j][j];
-                pos += (lj > li) || (lj == li && j < tid);
-            } else if (!member && !mj) {
-                pos += j < tid;
-            }
+        __syncthreads();
+        for (int i = warp; i < n; i += NW) {
+            const float vi = vv(i);
+            for (int j = lane; j < n; j += 32) s.Z[k + 1 + i][k + 1 + j] = fmaf(-vi, s.pv[j], s.Z[k + 1 + i][k + 1 + j]);
         }
-        s.lam[tid] = li;
-        s.order[pos] = tid;
+        __syncthreads();
     }
-    __syncthreads();
-    return done;
+}
+
+// Step 3, run by one warp: the eigenvalues of the tridiagonal (s.lam, s.off)
+// into s.lam, the rotations applied to the columns of s.Z (each lane its own
+// rows).  Every lane computes the same scalar recurrence; lane 0 alone
+// stores it (nothing in a pass reads back what the pass stored, and a
+// __syncwarp publishes it before the next pass).  Returns the rotations
+// applied, or -1 once an eigenvalue took more than `max_it` QL iterations.
+template <typename T, int P, int D>
+__device__ int ql_implicit(FactorSmem<T, P, D> &s, int max_it) {
+    const int lane = threadIdx.x & 31;
+    float *d = s.lam, *e = s.off;
+    float tst = 0.f;
+    int rotations = 0;
+    for (int l = 0; l < P; ++l) {
+        tst = fmaxf(tst, fabsf(d[l]) + fabsf(e[l]));
+        for (int it = 0;; ++it) {
+            int m = l;  // the first negligible off-diagonal entry from l on
+            while (m < P - 1 && fabsf(e[m]) > QL_EPS * tst) ++m;
+            if (m == l) break;
+            if (it == max_it) return -1;
+            // shift: the eigenvalue of the leading 2 x 2 block nearer d[l]
+            float g = (d[l + 1] - d[l]) / (2.f * e[l]);
+            float r = sqrtf(fmaf(g, g, 1.f));
+            g = d[m] - d[l] + e[l] / (g + copysignf(r, g));
+            float sn = 1.f, c = 1.f, p = 0.f;
+            int i = m - 1;
+            // d[i + 1], d[i] and e[i] of the coming rotation ride in registers
+            // (a rotation stores only d[i + 1] and e[i + 1], which no later
+            // rotation of the pass reads)
+            float dn = d[m], di = d[m - 1], ei = e[m - 1];
+            for (; i >= l; --i) {  // chase the bulge from the bottom of the block up
+                const float di_next = i > l ? d[i - 1] : 0.f, ei_next = i > l ? e[i - 1] : 0.f;
+                const float f = sn * ei, b = c * ei;
+                const float rr = fmaf(f, f, g * g);
+                if (rr < NEGLIGIBLE * NEGLIGIBLE) {  // T splits: deflate and start again
+                    if (lane == 0) e[i + 1] = sqrtf(rr);
+                    break;
+                }
+                const float ir = rsqrtf(rr);  // one reciprocal square root gives r, sin and cos
+                r = rr * ir;
+                if (lane == 0) e[i + 1] = r;
+                sn = f * ir;
+                c = g * ir;
+                g = dn - p;
+                r = fmaf(di - g, sn, 2.f * c * b);
+                p = sn * r;
+                if (lane == 0) d[i + 1] = g + p;
+                g = fmaf(c, r, -b);
+                for (int row = lane; row < P; row += 32) {
+                    const float zi = s.Z[row][i], zn = s.Z[row][i + 1];
+                    s.Z[row][i + 1] = fmaf(sn, zi, __fmul_rn(c, zn));
+                    s.Z[row][i] = fmaf(c, zi, -__fmul_rn(sn, zn));
+                }
+                ++rotations;
+                dn = di;
+                di = di_next;
+                ei = ei_next;
+            }
+            if (lane == 0) {
+                if (i >= l) {  // split at i + 1
+                    d[i + 1] -= p;
+                } else {
+                    d[l] -= p;
+                    e[l] = g;
+                }
+                e[m] = 0.f;
+            }
+            __syncwarp();
+        }
+    }
+    return rotations;
 }
 
 template <typename TO>
@@ -539,8 +462,8 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
     if (v.qR)
         for (int e = tid; e < rp * D; e += NT) v.qR[e] = Rf[e];
     // 3. scales: fp16 in the record (accumulator-column order), their fp32
-    // values in s.Vt for the codes
-    float *scL = &s.Vt[0][0];  // per rank (keys) or per token (values): up to P
+    // values in s.sc for the codes
+    float *scL = s.sc;         // per rank (keys) or per token (values): up to P
     float *scR = scL + P;      // per head-dim column: D
     unsigned char *rec = reinterpret_cast<unsigned char *>(v.rec);
     __half *hL = reinterpret_cast<__half *>(rec + (v.kind == 0 ? y.q_off_sLK : y.q_off_sLV));
@@ -601,53 +524,66 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
     }
 }
 
-// Returns the Jacobi sweeps the page took (the cap if it did not converge).
+// Returns the QL rotations the page took (0 if an eigenvalue hit the
+// iteration cap, which the status word records).
 template <typename T, int P, int D, int NT>
 __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, long job) {
-    const int tid = threadIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31;
     const JobView v = job_view(fp, job);
     load_page<T, P, D, NT>(s, v);
     __syncthreads();
     if constexpr (sizeof(T) == 2) gram_bf16<P, D, NT>(s); else gram_f32<P, D, NT>(s);
     __syncthreads();
-    // the tensor-core tiles of (i, j) and (j, i) may round differently: symmetrise
+    // the tensor-core tiles of (i, j) and (j, i) may round differently:
+    // symmetrise; and scale by a power of two (exact) that brings the largest
+    // diagonal entry into [1, 2), so that no square in the eigensolve can
+    // overflow
+    float mx = 0.f;
+    for (int i = lane; i < P; i += 32) mx = fmaxf(mx, s.G[i][i]);
+    mx = warp_max(mx);
+    const int ex = mx > 0.f ? ilogbf(mx) : 0;
     for (int e = tid; e < P * P; e += NT) {
         int i = e / P, j = e % P;
-        if (j > i) s.G[j][i] = s.G[i][j];
-    }
-    __syncthreads();
-    // with singular values requested every eigenpair must converge; otherwise
-    // only the kept subspace has to, and INT4 records (whose kept vectors
-    // must be eigenvectors) then finish the kept block on its own
-    const bool polish = !v.sigma && v.r < P && v.rec && fp.y.q4;
-    int sweeps = jacobi<T, P, D, NT>(s, fp.max_sweeps, v.sigma ? P : v.r);
-    if (polish && sweeps >= 0 && polish_block<T, P, D, NT>(s, v.r, fp.max_sweeps) < 0) sweeps = -1;
-    if (sweeps < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
-    if (!polish) {
-        if (tid < P) s.lam[tid] = s.G[tid][tid];
-        __syncthreads();
-        if (tid < P) {
-            float li = s.lam[tid];
-            int rank = 0;
-            for (int j = 0; j < P; ++j) {
-                float lj = s.lam[j];
-                rank += (lj > li) || (lj == li && j < tid);
-            }
-            s.order[rank] = tid;
+        if (j >= i) {
+            const float g = ldexpf(s.G[i][j], -ex);
+            s.G[i][j] = g;
+            s.G[j][i] = g;
         }
-        __syncthreads();
     }
-    const int r = v.r;
-    if (v.sigma && tid < P) v.sigma[tid] = sqrtf(fmaxf(s.lam[s.order[tid]], 0.f));
     __syncthreads();
+    tridiagonalize<T, P, D, NT>(s);
+    accumulate_q<T, P, D, NT>(s);  // starts with a barrier; X is dead here (the page comes back below)
+    if (tid < 32) {
+        const int rot = ql_implicit<T, P, D>(s, fp.max_ql_iter);
+        if (tid == 0) s.red[0] = __int_as_float(rot);
+    }
+    __syncthreads();
+    const int rotations = __float_as_int(s.red[0]);
+    if (rotations < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
+    if (tid < P) {  // a NaN eigenvalue ranks below every number: the ranks stay a permutation
+        auto key = [](float x) { return x == x ? x : -INFINITY; };
+        const float li = key(s.lam[tid]);
+        int rank = 0;
+        for (int j = 0; j < P; ++j) {
+            const float lj = key(s.lam[j]);
+            rank += (lj > li) || (lj == li && j < tid);
+        }
+        s.order[rank] = tid;
+    }
+    __syncthreads();
+    const int r = v.r;
+    if (v.sigma && tid < P) v.sigma[tid] = sqrtf(fmaxf(ldexpf(s.lam[s.order[tid]], ex), 0.f));
     for (int e = tid; e < P * P; e += NT) {
         int i = e / P, j = e % P;
-        s.G[i][j] = s.Vt[s.order[j]][i];
+        s.G[i][j] = s.Z[i][s.order[j]];
     }
     __syncthreads();
-    // Hundreds of rounds of fp32 rotations let the eigenvector norms drift by
-    // ~1e-5; scale the kept columns back to unit length (their mutual
-    // orthogonality is already at fp32 rounding level).
+    // the eigenvectors are out: the page again, for the projection (the
+    // barriers below order it before its first read)
+    load_page<T, P, D, NT>(s, v);
+    // A few thousand fp32 rotations leave the eigenvector norms off by about
+    // 1e-6; scale the kept columns back to unit length (their mutual
+    // orthogonality is at the same level).
     if (tid < v.r) {
         float n2 = 0.f;
         for (int i = 0; i < P; ++i) n2 = fmaf(s.G[i][tid], s.G[i][tid], n2);
@@ -664,7 +600,7 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
     const bool rec = v.rec != nullptr;
     if (rec && y.q4) {
         write_q4_record<T, P, D, NT>(s, v, y);
-        return sweeps < 0 ? fp.max_sweeps : sweeps;
+        return rotations < 0 ? 0 : rotations;
     }
     const int rp = rec ? (v.kind == 0 ? y.rkp : y.rvp) : r;
     // L = Q_r  (record: keys LK[token][rank], values LVt[rank][token])
@@ -716,31 +652,31 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
             }
         }
     }
-    return sweeps < 0 ? fp.max_sweeps : sweeps;
+    return rotations < 0 ? 0 : rotations;
 }
 
-// The 256-thread variant keeps four CTAs per SM (64 registers), which its
-// shared memory also allows: four pages in flight keep the shared-memory
-// pipe, which bounds the Jacobi rounds, busy through each round's barriers.
+// The 256-thread variant keeps four CTAs per SM (64 registers): while one
+// CTA's single warp runs the serial QL recurrence, the others' reductions
+// and updates fill the SM.
 template <typename T, int P, int D, int NT>
 __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1) factorize_kernel(const FactorParams fp) {
     extern __shared__ __align__(128) unsigned char smem_raw[];
     auto &s = *reinterpret_cast<FactorSmem<T, P, D> *>(smem_raw);
-    unsigned long long jobs = 0, sweeps = 0;
+    unsigned long long jobs = 0, rotations = 0;
     for (long job = blockIdx.x; job < fp.n_jobs; job += gridDim.x) {
-        sweeps += (unsigned long long)factorize_one<T, P, D, NT>(s, fp, job);
+        rotations += (unsigned long long)factorize_one<T, P, D, NT>(s, fp, job);
         ++jobs;
         __syncthreads();
     }
     if (threadIdx.x == 0 && fp.status && jobs) {  // throughput accounting, once per CTA
         atomicAdd(reinterpret_cast<unsigned long long *>(fp.status + STATUS_JOBS), jobs);
-        atomicAdd(reinterpret_cast<unsigned long long *>(fp.status + STATUS_SWEEPS), sweeps);
+        atomicAdd(reinterpret_cast<unsigned long long *>(fp.status + STATUS_ROTATIONS), rotations);
     }
 }
 
 template <typename T, int P, int D, int NT>
 static cudaError_t launch_t(const FactorParams &fp, int num_sms, cudaStream_t st) {
-    size_t smem = sizeof(FactorSmem<T, P, D>);
+    const size_t smem = sizeof(FactorSmem<T, P, D>);
     auto k = factorize_kernel<T, P, D, NT>;
     // the shared-memory opt-in is set once per device (per launch it costs
     // more host time than a small launch takes on the GPU)
@@ -752,6 +688,11 @@ static cudaError_t launch_t(const FactorParams &fp, int num_sms, cudaStream_t st
     int state = attr_state[dev].load(std::memory_order_acquire);
     if (state == 0) {
         e = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+        // the largest shared split, as the decode kernels ask: an SM set up
+        // by either kernel then takes CTAs of the other beside its own
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(k, cudaFuncAttributePreferredSharedMemoryCarveout,
+                                     cudaSharedmemCarveoutMaxShared);
         state = e == cudaSuccess ? 1 : 2 + (int)e;
         attr_state[dev].store(state, std::memory_order_release);
     }
@@ -768,8 +709,10 @@ static cudaError_t launch_t(const FactorParams &fp, int num_sms, cudaStream_t st
 // A few pages (conversions during decoding) are latency-bound: 1024 threads
 // per page.  Many pages (prefill, batches) are throughput-bound: 256 threads,
 // several pages per SM.  Work capped to run beside decode launches (max_ctas,
-// the background batches) always takes 256 threads: a 1024-thread CTA holds
-// all of an SM's registers, so no decode CTA could share the SM with it.
+// the background batches) never takes 1024 threads, which hold all of an SM's
+// registers; a 256-thread CTA (64 registers, 36 KB of shared memory at
+// P = 64, d = 128, bf16) fits beside any decode CTA.  All variants give the
+// same bits.
 template <typename T, int P, int D>
 static cudaError_t launch_nt(const FactorParams &fp, int num_sms, cudaStream_t st) {
     if (fp.n_jobs <= 2L * num_sms && fp.max_ctas <= 0) return launch_t<T, P, D, 1024>(fp, num_sms, st);

@@ -14,7 +14,7 @@ struct FactorParams {
     int mode;
     long n_jobs;
     int max_ctas;  // grid cap (0: the default, several CTAs per SM)
-    int max_sweeps;
+    int max_ql_iter;  // QL iterations allowed per eigenvalue
     int *status;  // device status words (may be null in batch mode)
     // batch mode: X[n][P][d] -> L[n][P][r], R[n][r][d], sigma[n][P]
     const char *x_base;

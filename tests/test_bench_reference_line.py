@@ -2,6 +2,7 @@
 small workloads of the same structure as the bench's: the keys and units the
 line must carry, and that its three figures are the one timed value."""
 import argparse
+import os
 import json
 
 import pytest
@@ -47,5 +48,9 @@ def test_gpu_arm_cpu_baseline_fields():
     """The cpu_baseline object of the GPU arm's line (host work only)."""
     cb = bench.cpu_baseline_sample(SMALL)
     assert cb["kind"] == "oracle" and cb["unit"] == "us/step" and cb["value"] > 0
-    assert cb["cores"] == 1 and cb["pages_cores"] >= 1 and cb["pages_sample"] > 0
+    assert cb["cores"] == cb["nproc"] == (os.cpu_count() or 1) and cb["pages_cores"] >= 1 and cb["pages_sample"] > 0
     assert cb["pages_factorized_per_s"] > 0 and cb["sample"] and cb["cpu_model"]
+    # decode timed on one core and on all of them; the whole tiny workload through the oracle
+    rates = cb["decode_pairs_per_s"]
+    assert rates["1_core"] > 0 and rates[f"{cb['nproc']}_cores"] > 0 and cb["decode_us_per_step_1_core"] > 0
+    assert cb["tiny_workload_full_oracle_s"] > 0

@@ -112,17 +112,21 @@ def test_bf16_llama_shape_prefill_decode(pkv, T):
 
 def test_factorize_counters_count_every_page_job(pkv):
     """The store's factorization counters: one job per factorized K or V page
-    of every (layer, KV head), between one and the cap of sweeps each;
-    reading clears them."""
+    of every (layer, KV head), and the QL rotations of their eigensolves --
+    at least one pass over the whole tridiagonal (P - 1 rotations: no
+    off-diagonal entry of these pages' tridiagonal form is negligible at
+    first), at most the cap of 30 iterations of P - 1 rotations for each of
+    the P eigenvalues; reading clears them."""
     T = 4097
     cfg = make_cfg(pkv, num_layers=2, num_kv_heads=4, num_q_heads=16)
     store = pkv.Store(cfg)
     assert store.factorize_counters() == (0, 0)
     prefill(pkv, store, cfg, HostCache(), 0, T, rope=5e5)
-    jobs, sweeps = store.factorize_counters()
+    jobs, rotations = store.factorize_counters()
     n_fac = int((oracle.page_kinds(T, cfg.page_size, cfg.sink_tokens, cfg.recent_tokens) == oracle.FACTORED).sum())
     assert jobs == n_fac * cfg.num_layers * cfg.num_kv_heads * 2
-    assert jobs <= sweeps <= 24 * jobs
+    P = cfg.page_size
+    assert (P - 1) * jobs <= rotations <= 30 * P * (P - 1) * jobs
     assert store.factorize_counters() == (0, 0)
     assert store.check_device_status() == 0
 
