@@ -874,7 +874,10 @@ puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
     fp.dense_pool = s->dense_pool;
     fp.conv_list = dev_jobs;
     fp.n_jobs = (long)s->job_host.size() * y.H * 2;
-    fp.max_ctas = s->num_sms;  // one CTA per SM: it runs beside the decode CTAs
+    // one CTA per page job: a conversion CTA holds its SM for one short job
+    // only, so decode CTAs waiting for SMs get them back soon (one CTA per SM
+    // looping over its share of jobs held SMs for whole milliseconds)
+    fp.max_ctas = (int)std::min<long>(fp.n_jobs, 1L << 30);
     e = launch_factorize(fp, s->num_sms, s->conv_stream);
     if (e == cudaSuccess) e = end_batch(s, cb);
     if (e != cudaSuccess) return cuda_fail(e, "batched conversion launch");

@@ -698,8 +698,7 @@ static cudaError_t launch_t(const FactorParams &fp, int num_sms, cudaStream_t st
     }
     if (state != 1) return (cudaError_t)(state - 2);
     long blocks = fp.n_jobs;
-    long cap = (long)num_sms * (NT >= 1024 ? 2 : 8);
-    if (fp.max_ctas > 0 && fp.max_ctas < cap) cap = fp.max_ctas;
+    const long cap = fp.max_ctas > 0 ? fp.max_ctas : (long)num_sms * (NT >= 1024 ? 2 : 8);
     if (blocks > cap) blocks = cap;
     if (blocks < 1) return cudaSuccess;
     k<<<(unsigned)blocks, NT, smem, st>>>(fp);
@@ -708,11 +707,11 @@ static cudaError_t launch_t(const FactorParams &fp, int num_sms, cudaStream_t st
 
 // A few pages (conversions during decoding) are latency-bound: 1024 threads
 // per page.  Many pages (prefill, batches) are throughput-bound: 256 threads,
-// several pages per SM.  Work capped to run beside decode launches (max_ctas,
-// the background batches) never takes 1024 threads, which hold all of an SM's
-// registers; a 256-thread CTA (64 registers, 36 KB of shared memory at
-// P = 64, d = 128, bf16) fits beside any decode CTA.  All variants give the
-// same bits.
+// several pages per SM.  Background batches, which run between and beside
+// decode launches (max_ctas set: one CTA per page job), never take 1024
+// threads, which hold all of an SM's registers: a 256-thread CTA has 64
+// registers and 36 KB of shared memory at P = 64, d = 128, bf16.  All
+// variants give the same bits.
 template <typename T, int P, int D>
 static cudaError_t launch_nt(const FactorParams &fp, int num_sms, cudaStream_t st) {
     if (fp.n_jobs <= 2L * num_sms && fp.max_ctas <= 0) return launch_t<T, P, D, 1024>(fp, num_sms, st);

@@ -13,7 +13,7 @@ enum { FACT_MODE_BATCH = 0, FACT_MODE_PREFILL = 1, FACT_MODE_CONVERT = 2, FACT_M
 struct FactorParams {
     int mode;
     long n_jobs;
-    int max_ctas;  // grid cap (0: the default, several CTAs per SM)
+    int max_ctas;  // grid size cap (0: the default, a few CTAs per SM looping over the jobs)
     int max_ql_iter;  // QL iterations allowed per eigenvalue
     int *status;  // device status words (may be null in batch mode)
     // batch mode: X[n][P][d] -> L[n][P][r], R[n][r][d], sigma[n][P]
