@@ -321,10 +321,14 @@ __device__ void accumulate_q(FactorSmem<T, P, D> &s) {
 // into s.lam, the rotations applied to the columns of s.Z (each lane its own
 // rows).  Every lane computes the same scalar recurrence; lane 0 alone
 // stores it (nothing in a pass reads back what the pass stored, and a
-// __syncwarp publishes it before the next pass).  Returns the rotations
+// __syncwarp publishes it before the next pass).  Shared-memory round trips
+// stay off the recurrence: the search for the first negligible off-diagonal
+// entry is one ballot, each lane carries the column it has just rotated in
+// registers and loads the next one a rotation ahead.  Returns the rotations
 // applied, or -1 once an eigenvalue took more than `max_it` QL iterations.
 template <typename T, int P, int D>
 __device__ int ql_implicit(FactorSmem<T, P, D> &s, int max_it) {
+    constexpr int NR = (P + 31) / 32;  // rows of s.Z per lane
     const int lane = threadIdx.x & 31;
     float *d = s.lam, *e = s.off;
     float tst = 0.f;
@@ -332,53 +336,86 @@ __device__ int ql_implicit(FactorSmem<T, P, D> &s, int max_it) {
     for (int l = 0; l < P; ++l) {
         tst = fmaxf(tst, fabsf(d[l]) + fabsf(e[l]));
         for (int it = 0;; ++it) {
-            int m = l;  // the first negligible off-diagonal entry from l on
-            while (m < P - 1 && fabsf(e[m]) > QL_EPS * tst) ++m;
+            // m: the first negligible off-diagonal entry from l on (e[P-1] = 0);
+            // a NaN counts as negligible, as in a sequential scan
+            int m = P - 1;
+#pragma unroll
+            for (int h = NR - 1; h >= 0; --h) {
+                const int j = lane + 32 * h;
+                const bool neg = j >= l && j < P - 1 && !(fabsf(e[j]) > QL_EPS * tst);
+                const unsigned bal = __ballot_sync(0xffffffffu, neg);
+                if (bal) m = 32 * h + __ffs(bal) - 1;
+            }
             if (m == l) break;
             if (it == max_it) return -1;
             // shift: the eigenvalue of the leading 2 x 2 block nearer d[l]
-            float g = (d[l + 1] - d[l]) / (2.f * e[l]);
+            float g = __fsub_rn(d[l + 1], d[l]) / (2.f * e[l]);
             float r = sqrtf(fmaf(g, g, 1.f));
-            g = d[m] - d[l] + e[l] / (g + copysignf(r, g));
+            g = __fadd_rn(__fsub_rn(d[m], d[l]), e[l] / __fadd_rn(g, copysignf(r, g)));
             float sn = 1.f, c = 1.f, p = 0.f;
             int i = m - 1;
-            // d[i + 1], d[i] and e[i] of the coming rotation ride in registers
-            // (a rotation stores only d[i + 1] and e[i + 1], which no later
-            // rotation of the pass reads)
+            // d[i + 1], d[i] and e[i] of the coming rotation, and this lane's
+            // entries of columns i + 1 (zc, rotated already in this pass)
+            // and i (zi) of s.Z ride in registers (a rotation stores only
+            // d[i + 1], e[i + 1] and column i + 1, which no later rotation of
+            // the pass reads)
             float dn = d[m], di = d[m - 1], ei = e[m - 1];
+            float zc[NR], zi[NR];
+#pragma unroll
+            for (int h = 0; h < NR; ++h) {
+                const int row = lane + 32 * h;
+                zc[h] = row < P ? s.Z[row][m] : 0.f;
+                zi[h] = row < P ? s.Z[row][m - 1] : 0.f;
+            }
             for (; i >= l; --i) {  // chase the bulge from the bottom of the block up
                 const float di_next = i > l ? d[i - 1] : 0.f, ei_next = i > l ? e[i - 1] : 0.f;
-                const float f = sn * ei, b = c * ei;
-                const float rr = fmaf(f, f, g * g);
+                float zi_next[NR];
+#pragma unroll
+                for (int h = 0; h < NR; ++h) {
+                    const int row = lane + 32 * h;
+                    zi_next[h] = i > l && row < P ? s.Z[row][i - 1] : 0.f;
+                }
+                // every rounding is spelled out (no contraction left to the
+                // compiler), so the recurrence gives the same bits however
+                // the loop is scheduled
+                const float f = __fmul_rn(sn, ei), b = __fmul_rn(c, ei);
+                const float rr = fmaf(f, f, __fmul_rn(g, g));
                 if (rr < NEGLIGIBLE * NEGLIGIBLE) {  // T splits: deflate and start again
                     if (lane == 0) e[i + 1] = sqrtf(rr);
                     break;
                 }
                 const float ir = rsqrtf(rr);  // one reciprocal square root gives r, sin and cos
-                r = rr * ir;
+                r = __fmul_rn(rr, ir);
                 if (lane == 0) e[i + 1] = r;
-                sn = f * ir;
-                c = g * ir;
-                g = dn - p;
-                r = fmaf(di - g, sn, 2.f * c * b);
-                p = sn * r;
-                if (lane == 0) d[i + 1] = g + p;
+                sn = __fmul_rn(f, ir);
+                c = __fmul_rn(g, ir);
+                g = __fsub_rn(dn, p);
+                r = fmaf(__fsub_rn(di, g), sn, __fmul_rn(2.f * c, b));
+                p = __fmul_rn(sn, r);
+                if (lane == 0) d[i + 1] = __fadd_rn(g, p);
                 g = fmaf(c, r, -b);
-                for (int row = lane; row < P; row += 32) {
-                    const float zi = s.Z[row][i], zn = s.Z[row][i + 1];
-                    s.Z[row][i + 1] = fmaf(sn, zi, __fmul_rn(c, zn));
-                    s.Z[row][i] = fmaf(c, zi, -__fmul_rn(sn, zn));
+#pragma unroll
+                for (int h = 0; h < NR; ++h) {
+                    const int row = lane + 32 * h;
+                    if (row < P) s.Z[row][i + 1] = fmaf(sn, zi[h], __fmul_rn(c, zc[h]));  // column i + 1 is final
+                    zc[h] = fmaf(c, zi[h], -__fmul_rn(sn, zc[h]));                        // column i, carried
+                    zi[h] = zi_next[h];
                 }
                 ++rotations;
                 dn = di;
                 di = di_next;
                 ei = ei_next;
             }
+#pragma unroll
+            for (int h = 0; h < NR; ++h) {  // the carried column: i + 1 where the chase stopped
+                const int row = lane + 32 * h;
+                if (row < P) s.Z[row][i + 1] = zc[h];
+            }
             if (lane == 0) {
                 if (i >= l) {  // split at i + 1
-                    d[i + 1] -= p;
+                    d[i + 1] = __fsub_rn(d[i + 1], p);
                 } else {
-                    d[l] -= p;
+                    d[l] = __fsub_rn(d[l], p);
                     e[l] = g;
                 }
                 e[m] = 0.f;
