@@ -596,16 +596,12 @@ __device__ __forceinline__ void factored_unit_q4(WarpState<P, D> &w, const unsig
     constexpr int MAXK = RKT ? RKT : P / 16, MAXV = RVT ? RVT : P / 16;
     const int nkt = RKT ? RKT : (y.rkp >> 3), nvt = RVT ? RVT : (y.rvp >> 3);
     const int c = lane & 3;
-    // word wd of this lane's part of a stream: slab wd / 2, word wd % 2.  A
-    // lane's two words of a slab are one 8-byte load (a warp reads the
-    // 256-byte slab without bank conflicts; the repeated loads of a slab for
-    // its eight registers are the same expression and load once)
-    const uint2 *ks_ = reinterpret_cast<const uint2 *>(rec) + lane;
-    const uint2 *vs_ = reinterpret_cast<const uint2 *>(rec + y.q_off_V) + lane;
-    auto breg = [](const uint2 *st, int m) -> uint32_t {
+    // word wd of this lane's part of a stream: slab wd / 2, word wd % 2
+    const uint32_t *ks_ = reinterpret_cast<const uint32_t *>(rec) + 2 * lane;
+    const uint32_t *vs_ = reinterpret_cast<const uint32_t *>(rec + y.q_off_V) + 2 * lane;
+    auto breg = [](const uint32_t *st, int m) -> uint32_t {
         const int wd = m >> 2;
-        const uint2 sl = st[(wd >> 1) * 32];
-        return q4_reg((wd & 1) ? sl.y : sl.x, m & 3);
+        return q4_reg(st[(wd >> 1) * 64 + (wd & 1)], m & 3);
     };
     // 1. t = (q o s_RK) C_RK^T: A = q o s_RK over the head dim (k-step ks holds
     // columns 16 ks + 2c, +1 and 16 ks + 8 + 2c, +1: one uint2 of lane c's scales)
