@@ -191,7 +191,8 @@ size_t decode_smem_bytes(const Layout &y) {
     if (rope) stage += (size_t)y.d * 4;
     stage = (stage + 127) & ~(size_t)127;
     const size_t ns = (size_t)nwc * spw;
-    return ns * stage + ns * sizeof(uint64_t) + sizeof(DecodeShared) + (rope ? 16 + (size_t)y.P * y.d * 4 : 0);
+    const size_t shared_state = du == 4 ? sizeof(DecodeShared<4>) : sizeof(DecodeShared<2>);
+    return ns * stage + ns * sizeof(uint64_t) + shared_state + (rope ? 16 + (size_t)y.P * y.d * 4 : 0);
 }
 
 cudaError_t launch_decode(DecodeParams &p, long total_pages, int max_pages, int num_sms, cudaStream_t st) {

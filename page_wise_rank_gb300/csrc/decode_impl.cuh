@@ -105,17 +105,22 @@ __device__ __forceinline__ int unit_valid(int T, int first, int PU) {
     return v < 0 ? 0 : (v > PU ? PU : v);
 }
 
-// Dense units of one CTA's page range at most: every dense page of a sequence
-// (sink, window, the page being filled) cut into at most four units.
-constexpr int MAX_DENSE_UNITS = MAX_DENSE_PAGES * 4;
-
+// The CTA's shared state beside its slots.  The dense-unit table holds at
+// most every dense page of a sequence (sink, window, the page being filled)
+// cut into DU units; it is sized by DU because a bf16 decode CTA and a
+// background factorization CTA fit one SM's shared memory together only with
+// a few hundred bytes to spare.
+template <int DU>
 struct DecodeShared {
     uint64_t merge_bar;  // completion of the split-merge bulk copies
     int failed;
     int last;
     int n_pre, n_dense;  // dense units before the factorized stretch, and in all
-    int slot_info[NS_MAX];                // per slot: page << 3 | dense << 2 | unit
-    int dense_units[MAX_DENSE_UNITS];     // the same code for each dense unit, in page order
+    int slot_info[NS_MAX];  // per slot: page << 3 | dense << 2 | unit
+    // each dense unit in page order, as rel << 3 | 4 | unit: rel is the page
+    // itself for sink pages (before the factorized stretch) and the page minus
+    // the stretch's end after it; both stay below MAX_DENSE_PAGES
+    short dense_units[MAX_DENSE_PAGES * DU];
 };
 
 
@@ -991,7 +996,7 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     const size_t base_off = decode_unit_bytes<P, D, DU>(y);  // RoPE: the page-start row in a slot
     unsigned char *stages = smem;
     uint64_t *full = reinterpret_cast<uint64_t *>(smem + NS * stage_bytes);
-    DecodeShared &sh = *reinterpret_cast<DecodeShared *>(full + NS);
+    DecodeShared<DU> &sh = *reinterpret_cast<DecodeShared<DU> *>(full + NS);
     // RoPE: the in-page offsets' (cos, sin) table [P][D/2], after the shared state
     float2 *rope_delta = reinterpret_cast<float2 *>(
         (reinterpret_cast<uintptr_t>(&sh + 1) + 15) & ~static_cast<uintptr_t>(15));
@@ -1057,7 +1062,7 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
                 if (p >= pe) break;
             }
             for (int hf = 0; hf < DU; ++hf)
-                if (T > p * P + hf * PU) sh.dense_units[n++] = (p << 3) | 4 | hf;
+                if (T > p * P + hf * PU) sh.dense_units[n++] = (short)(((p < a1 ? p : p - a2) << 3) | 4 | hf);
         }
         if (a1 >= pe) sh.n_pre = n;
         sh.n_dense = n;
@@ -1070,7 +1075,8 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     const int n_pre = sh.n_pre, n_units = sh.n_dense + n_fac;
     const int n_mine = n_units > warp ? (n_units - 1 - warp) / NWC + 1 : 0;
     auto unit_of = [&](int u) -> int {
-        return u < n_pre ? sh.dense_units[u] : (u < n_pre + n_fac ? (a1 + u - n_pre) << 3 : sh.dense_units[u - n_fac]);
+        return u < n_pre ? (int)sh.dense_units[u]
+                         : (u < n_pre + n_fac ? (a1 + u - n_pre) << 3 : (a2 << 3) + sh.dense_units[u - n_fac]);
     };
     if (lane == 0) {
         policy = l2_evict_first();
@@ -1233,7 +1239,7 @@ cudaError_t launch_bf16(DecodeParams &p, long total_pages, int max_pages, int nu
             const size_t tail_bytes = (size_t)Shape::NWC * 8 * (D + 4) * 4;  // the warp states
             if ((size_t)NS * stage_bytes < tail_bytes) return cudaErrorInvalidValue;
             c.stages = NS;
-            c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared) +
+            c.smem = NS * stage_bytes + NS * sizeof(uint64_t) + sizeof(DecodeShared<Shape::DU>) +
                      (ROPE ? 16 + (size_t)P * D * 4 : 0);  // RoPE: the aligned in-page angle table
             c.err = cudaFuncSetAttribute(k, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)c.smem);
             // An SM's shared/L1 split is set when it takes a CTA and holds

@@ -37,22 +37,25 @@ template <typename T, int P, int D>
 struct FactorSmem {
     // The page X is needed for the Gram matrix and again for the projection,
     // the eigenvectors only in between: they share storage, and the page is
-    // loaded a second time once the eigenvectors are taken out.  (At P = 64,
-    // d = 128, bf16, the CTA then takes 36 KB instead of 53 KB, which lets a
-    // background conversion CTA sit beside a decode CTA on one SM.)
+    // loaded a second time once the eigenvectors are taken out.
     union {
         alignas(128) unsigned char X[P * D * sizeof(T)];  // swizzled rows, pitch D * sizeof(T)
         float Z[P][P + 1];  // eigenvectors as columns: Z[i][j] = component i of vector j
     };
-    float G[P][P + 1];  // Gram matrix; after the eigensolve reused for Q[i][j] = Z[i][order[j]]
-    float lam[P];       // diagonal of the tridiagonal, then the eigenvalues
-    float off[P];       // its off-diagonal: off[k] couples k and k + 1
-    float hb[P];        // Householder reflections: beta_k (0: none) ...
-    float hv0[P];       // ... and the first entry of v_k
-    float pv[P];        // a work vector of the reduction
-    int order[P];
-    float sc[P + D];                 // INT4 scales in fp32: per rank or token, then per head-dim column
-    float red[64];                   // per-warp partial sums (up to 32 warps, two sums)
+    // Gram matrix; during the reduction row k above the diagonal keeps beta_k
+    // (G[k][k+1]) and the first entry of v_k (G[k][k+2]); after the
+    // eigensolve, Q with its columns in eigenvalue order
+    float G[P][P + 1];
+    // scratch, each part live at its own time: the tridiagonal's diagonal
+    // (then the eigenvalues, then per-column factors) in w[0, P), its
+    // off-diagonal in w[P, 2P), the reduction's work vector in w[2P, 3P);
+    // INT4 records' scales in w[0, P + D) once those are dead
+    static constexpr int WN = 3 * P > P + D ? 3 * P : P + D;
+    float w[WN];
+    __device__ __forceinline__ float *lam() { return w; }
+    __device__ __forceinline__ float *off() { return w + P; }
+    __device__ __forceinline__ float *pv() { return w + 2 * P; }
+    __device__ __forceinline__ float *sc() { return w; }
 };
 
 // Source page and destination of CTA `job` (mode chosen by the host).
@@ -228,9 +231,9 @@ __device__ __forceinline__ float quad_dot(int n, bool active, F prod) {
     return acc;
 }
 
-// Step 1.  On return s.lam[k] = T_kk, s.off[k] = T_{k,k+1} (off[P-1] = 0);
-// v_k stays in column k of s.G from row k+2 on, its first entry in s.hv0[k],
-// beta_k in s.hb[k] (0: no reflection).
+// Step 1.  On return lam[k] = T_kk, off[k] = T_{k,k+1} (off[P-1] = 0);
+// v_k stays in column k of s.G from row k+2 on, its first entry in
+// G[k][k+2], beta_k in G[k][k+1] (0: no reflection).
 template <typename T, int P, int D, int NT>
 __device__ void tridiagonalize(FactorSmem<T, P, D> &s) {
     constexpr int NW = NT / 32;
@@ -250,10 +253,10 @@ __device__ void tridiagonalize(FactorSmem<T, P, D> &s) {
             beta = -1.f / (alpha * v0);
         }
         if (tid == 0) {
-            s.lam[k] = s.G[k][k];
-            s.off[k] = alpha;
-            s.hb[k] = beta;
-            s.hv0[k] = v0;
+            s.lam()[k] = s.G[k][k];
+            s.off()[k] = alpha;
+            s.G[k][k + 1] = beta;  // row k above the diagonal is no longer read
+            s.G[k][k + 2] = v0;
         }
         if (beta == 0.f) continue;  // the same decision in every warp
         auto vv = [&](int i) { return i == 0 ? v0 : s.G[k + 1 + i][k]; };
@@ -262,28 +265,28 @@ __device__ void tridiagonalize(FactorSmem<T, P, D> &s) {
             const int i = base + (lane >> 2);
             const float acc =
                 quad_dot(n, i < n, [&](int j, float a) { return fmaf(s.G[k + 1 + i][k + 1 + j], vv(j), a); });
-            if ((lane & 3) == 0 && i < n) s.pv[i] = beta * acc;
+            if ((lane & 3) == 0 && i < n) s.pv()[i] = beta * acc;
         }
         __syncthreads();
         // K = beta v.p / 2 (each warp), w = p - K v, S <- S - v w^T - w v^T,
         // the entries (i, j) and (j, i) rounded alike
         float vp = 0.f;
-        for (int i = lane; i < n; i += 32) vp = fmaf(vv(i), s.pv[i], vp);
+        for (int i = lane; i < n; i += 32) vp = fmaf(vv(i), s.pv()[i], vp);
         const float K = 0.5f * beta * warp_sum(vp);
         for (int i = warp; i < n; i += NW)
             for (int j = lane; j < n; j += 32) {
                 const int a = max(i, j), b = min(i, j);
                 const float va = vv(a), vb = vv(b);
-                const float wa = fmaf(-K, va, s.pv[a]), wb = fmaf(-K, vb, s.pv[b]);
+                const float wa = fmaf(-K, va, s.pv()[a]), wb = fmaf(-K, vb, s.pv()[b]);
                 s.G[k + 1 + i][k + 1 + j] -= fmaf(va, wb, __fmul_rn(wa, vb));
             }
         __syncthreads();
     }
     if (tid == 0) {
-        s.lam[P - 2] = s.G[P - 2][P - 2];
-        s.lam[P - 1] = s.G[P - 1][P - 1];
-        s.off[P - 2] = s.G[P - 1][P - 2];
-        s.off[P - 1] = 0.f;
+        s.lam()[P - 2] = s.G[P - 2][P - 2];
+        s.lam()[P - 1] = s.G[P - 1][P - 1];
+        s.off()[P - 2] = s.G[P - 1][P - 2];
+        s.off()[P - 1] = 0.f;
     }
 }
 
@@ -296,29 +299,29 @@ __device__ void accumulate_q(FactorSmem<T, P, D> &s) {
     for (int e = tid; e < P * P; e += NT) s.Z[e / P][e % P] = e / P == e % P ? 1.f : 0.f;
     __syncthreads();
     for (int k = P - 3; k >= 0; --k) {
-        const float beta = s.hb[k];
+        const float beta = s.G[k][k + 1];
         if (beta == 0.f) continue;
         const int n = P - 1 - k;
-        const float v0 = s.hv0[k];
+        const float v0 = s.G[k][k + 2];
         auto vv = [&](int i) { return i == 0 ? v0 : s.G[k + 1 + i][k]; };
         // u = Z_S^T v (four lanes per column), then Z_S <- Z_S - beta v u^T
         for (int base = 8 * warp; base < n; base += NT / 4) {
             const int j = base + (lane >> 2);
             const float acc =
                 quad_dot(n, j < n, [&](int i, float a) { return fmaf(vv(i), s.Z[k + 1 + i][k + 1 + j], a); });
-            if ((lane & 3) == 0 && j < n) s.pv[j] = beta * acc;
+            if ((lane & 3) == 0 && j < n) s.pv()[j] = beta * acc;
         }
         __syncthreads();
         for (int i = warp; i < n; i += NW) {
             const float vi = vv(i);
-            for (int j = lane; j < n; j += 32) s.Z[k + 1 + i][k + 1 + j] = fmaf(-vi, s.pv[j], s.Z[k + 1 + i][k + 1 + j]);
+            for (int j = lane; j < n; j += 32) s.Z[k + 1 + i][k + 1 + j] = fmaf(-vi, s.pv()[j], s.Z[k + 1 + i][k + 1 + j]);
         }
         __syncthreads();
     }
 }
 
-// Step 3, run by one warp: the eigenvalues of the tridiagonal (s.lam, s.off)
-// into s.lam, the rotations applied to the columns of s.Z (each lane its own
+// Step 3, run by one warp: the eigenvalues of the tridiagonal (lam, off)
+// into lam, the rotations applied to the columns of s.Z (each lane its own
 // rows).  Every lane computes the same scalar recurrence; lane 0 alone
 // stores it (nothing in a pass reads back what the pass stored, and a
 // __syncwarp publishes it before the next pass).  Shared-memory round trips
@@ -330,7 +333,7 @@ template <typename T, int P, int D>
 __device__ int ql_implicit(FactorSmem<T, P, D> &s, int max_it) {
     constexpr int NR = (P + 31) / 32;  // rows of s.Z per lane
     const int lane = threadIdx.x & 31;
-    float *d = s.lam, *e = s.off;
+    float *d = s.lam(), *e = s.off();
     float tst = 0.f;
     int rotations = 0;
     for (int l = 0; l < P; ++l) {
@@ -481,16 +484,16 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
         float a = 0.f;
         for (int k = lane; k < D; k += 32) a = fmaf(Rf[j * D + k], Rf[j * D + k], a);
         a = warp_sum(a);
-        if (lane == 0) s.lam[j] = sqrtf(sqrtf(a));
+        if (lane == 0) s.lam()[j] = sqrtf(sqrtf(a));
     }
     __syncthreads();
     for (int e = tid; e < P * rp; e += NT) {
         const int i = e / rp, j = e % rp;
-        const float rs = s.lam[j];
+        const float rs = s.lam()[j];
         s.G[i][j] = (j < r && rs > 0.f) ? s.G[i][j] * rs : 0.f;
     }
     for (int e = tid; e < rp * D; e += NT) {
-        const float rs = s.lam[e / D];
+        const float rs = s.lam()[e / D];
         Rf[e] = rs > 0.f ? Rf[e] / rs : 0.f;
     }
     __syncthreads();
@@ -499,8 +502,8 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
     if (v.qR)
         for (int e = tid; e < rp * D; e += NT) v.qR[e] = Rf[e];
     // 3. scales: fp16 in the record (accumulator-column order), their fp32
-    // values in s.sc for the codes
-    float *scL = s.sc;         // per rank (keys) or per token (values): up to P
+    // values in the scratch for the codes (sigma^{1/2} above is dead by now)
+    float *scL = s.sc();       // per rank (keys) or per token (values): up to P
     float *scR = scL + P;      // per head-dim column: D
     unsigned char *rec = reinterpret_cast<unsigned char *>(v.rec);
     __half *hL = reinterpret_cast<__half *>(rec + (v.kind == 0 ? y.q_off_sLK : y.q_off_sLV));
@@ -592,27 +595,25 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
     accumulate_q<T, P, D, NT>(s);  // starts with a barrier; X is dead here (the page comes back below)
     if (tid < 32) {
         const int rot = ql_implicit<T, P, D>(s, fp.max_ql_iter);
-        if (tid == 0) s.red[0] = __int_as_float(rot);
+        if (tid == 0) s.off()[0] = __int_as_float(rot);  // the off-diagonal is dead after QL
     }
     __syncthreads();
-    const int rotations = __float_as_int(s.red[0]);
+    const int rotations = __float_as_int(s.off()[0]);
     if (rotations < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
-    if (tid < P) {  // a NaN eigenvalue ranks below every number: the ranks stay a permutation
+    // each thread t < P ranks eigenvalue t (descending, ties: lower index
+    // first; a NaN ranks below every number, so the ranks stay a
+    // permutation) and moves eigenvector t into column rank(t) of G
+    const int r = v.r;
+    if (tid < P) {
         auto key = [](float x) { return x == x ? x : -INFINITY; };
-        const float li = key(s.lam[tid]);
+        const float li = key(s.lam()[tid]);
         int rank = 0;
         for (int j = 0; j < P; ++j) {
-            const float lj = key(s.lam[j]);
+            const float lj = key(s.lam()[j]);
             rank += (lj > li) || (lj == li && j < tid);
         }
-        s.order[rank] = tid;
-    }
-    __syncthreads();
-    const int r = v.r;
-    if (v.sigma && tid < P) v.sigma[tid] = sqrtf(fmaxf(ldexpf(s.lam[s.order[tid]], ex), 0.f));
-    for (int e = tid; e < P * P; e += NT) {
-        int i = e / P, j = e % P;
-        s.G[i][j] = s.Z[i][s.order[j]];
+        if (v.sigma) v.sigma[rank] = sqrtf(fmaxf(ldexpf(s.lam()[tid], ex), 0.f));
+        for (int i = 0; i < P; ++i) s.G[i][rank] = s.Z[i][tid];
     }
     __syncthreads();
     // the eigenvectors are out: the page again, for the projection (the
@@ -624,12 +625,12 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
     if (tid < v.r) {
         float n2 = 0.f;
         for (int i = 0; i < P; ++i) n2 = fmaf(s.G[i][tid], s.G[i][tid], n2);
-        s.lam[tid] = n2 > 0.f ? 1.f / sqrtf(n2) : 1.f;  // lam[] is free once order[] is set
+        s.lam()[tid] = n2 > 0.f ? 1.f / sqrtf(n2) : 1.f;  // the eigenvalues are no longer needed
     }
     __syncthreads();
     for (int e = tid; e < P * v.r; e += NT) {
         int i = e / v.r, j = e % v.r;
-        s.G[i][j] *= s.lam[j];
+        s.G[i][j] *= s.lam()[j];
     }
     __syncthreads();
 
