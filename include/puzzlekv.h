@@ -278,8 +278,8 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *store, int32_t layer, 
                                           const int32_t *seq_ids, int32_t B, void *stream);
 
 /*
- * Factorize ahead of time, in one batched launch over all sequences and
- * layers, every page that is complete but has no factors yet (pages inside
+ * Factorize ahead of time, in batched launches over all sequences and
+ * layers, the pages that are complete but have no factors yet (pages inside
  * the local window included) [PuzzleKV §3.3 ⑤].  A page's content is final
  * once its P tokens are present, W tokens before it leaves the window; when
  * it leaves, puzzlekv_append_token / puzzlekv_decode_step then only switch it
@@ -289,10 +289,17 @@ puzzlekv_status puzzlekv_decode_attention(puzzlekv_store *store, int32_t layer, 
  * calling it once per decode step, after the last layer, is the intended use.
  * Pages whose dense slot might be reused are never listed: a page reaches
  * the window's end before its slot comes round again.
- *   Ordering: the batch runs on a low-priority stream internal to the store,
- *   after everything already queued on `stream`, and on at most one CTA per
- *   SM, so that it overlaps the decode steps that follow instead of stalling
- *   them.  A batch's factors are first read when one of its pages becomes
+ *   Pacing: a call starts a new batch only when the store's previous batch
+ *   has finished, and a batch takes the pages nearest their leaving the
+ *   window first, up to about one CTA per SM (num_SMs / (2 num_kv_heads)
+ *   pages of all heads, keys and values).  Pages within 8 steps of leaving
+ *   the window are always taken.  So a page may be converted a few calls
+ *   after it completes, and the page jobs reach the SMs in small numbers
+ *   beside the decode launches instead of all at once.
+ *   Ordering: a batch runs on a low-priority stream internal to the store,
+ *   after everything already queued on `stream`, one CTA per page job, so
+ *   that it overlaps the decode steps that follow instead of stalling them.
+ *   A batch's factors are first read when one of its pages becomes
  *   factorized; the first decode call (puzzlekv_decode_attention,
  *   puzzlekv_decode_step, the static-scratch variant) that reaches that
  *   length, and any prefill call (puzzlekv_load_prefill,

@@ -828,21 +828,53 @@ puzzlekv_status puzzlekv_convert_ready_pages(puzzlekv_store *s, void *stream) {
     NvtxRange nvtx_range("puzzlekv_convert_ready_pages");
     if (!s) return fail(PUZZLEKV_ERR_INVALID_ARG, "store is NULL");
     const Layout &y = s->y;
-    s->job_host.clear();
+    // every complete page without factors, with its slack: the decode steps
+    // left before the page leaves the window (length (p + 1) P + W)
+    struct Ready {
+        int slack, b, l, p;
+    };
+    std::vector<Ready> ready;
     for (int b = 0; b < y.Bmax; ++b) {
         for (int l = 0; l < y.L; ++l) {
             const int T = s->len[(size_t)b * y.L + l];
             if (T < 1) continue;
             const int complete = T / y.P;  // pages whose P tokens are all present
-            for (int p = std::max(s->conv_upto[(size_t)b * y.L + l], y.sink_pages); p < complete; ++p) {
-                if (has_factors(s, b, l, p)) continue;
-                if ((int)s->job_host.size() >= y.max_conv_jobs)
-                    return fail(PUZZLEKV_ERR_CAPACITY, "internal: conversion list overflow");
-                s->job_host.push_back(make_int2((b << 8) | l, p));
-            }
             for (int p = std::max(s->conv_upto[(size_t)b * y.L + l], y.sink_pages); p < complete; ++p)
-                set_factors(s, b, l, p);
+                if (!has_factors(s, b, l, p)) ready.push_back({(p + 1) * y.P + y.W - T, b, l, p});
         }
+    }
+    if (ready.empty()) return PUZZLEKV_OK;
+    // Pacing.  A page is complete W tokens before it leaves the window, so
+    // its conversion can spread over those steps.  A new batch starts only
+    // when the previous one has finished, with about one CTA per SM (page
+    // jobs of H heads x {K, V} per entry), so that few conversion CTAs ever
+    // wait for SMs beside the decode launches; pages within kUrgentSteps of
+    // their deadline go at once whatever else runs.
+    constexpr int kUrgentSteps = 8;
+    bool busy = false;
+    if (s->conv_stream) {
+        const puzzlekv_store::ConvBatch &last = s->batches[(s->next_batch + kConvBatches - 1) % kConvBatches];
+        if (last.pending) {
+            const cudaError_t q = cudaEventQuery(last.done);
+            if (q == cudaErrorNotReady) {
+                busy = true;
+                (void)cudaGetLastError();  // not an error: leave nothing behind for later launch checks
+            } else if (q != cudaSuccess) {
+                return cuda_fail(q, "conversion batch query");
+            }
+        }
+    }
+    std::stable_sort(ready.begin(), ready.end(), [](const Ready &u, const Ready &w) { return u.slack < w.slack; });
+    size_t take = 0;
+    while (take < ready.size() && ready[take].slack <= kUrgentSteps) ++take;
+    if (!busy) take = std::max(take, std::min(ready.size(), (size_t)std::max(1, s->num_sms / (2 * y.H))));
+    if (take == 0) return PUZZLEKV_OK;
+    if ((int)take > y.max_conv_jobs) return fail(PUZZLEKV_ERR_CAPACITY, "internal: conversion list overflow");
+    s->job_host.clear();
+    for (size_t i = 0; i < take; ++i) {
+        const Ready &r = ready[i];
+        s->job_host.push_back(make_int2((r.b << 8) | r.l, r.p));
+        set_factors(s, r.b, r.l, r.p);
     }
     if (s->job_host.empty()) return PUZZLEKV_OK;
     cudaStream_t strm = static_cast<cudaStream_t>(stream);
