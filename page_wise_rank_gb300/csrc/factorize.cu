@@ -370,6 +370,10 @@ __device__ int ql_implicit(FactorSmem<T, P, D> &s, int max_it) {
                 zc[h] = row < P ? s.Z[row][m] : 0.f;
                 zi[h] = row < P ? s.Z[row][m - 1] : 0.f;
             }
+            // unrolled so that the registers carried from one rotation to the
+            // next are renamed instead of copied (a copy waits for the load
+            // it moves): 720 K -> 611 K cycles of QL per 64 x 64 page job
+#pragma unroll 4
             for (; i >= l; --i) {  // chase the bulge from the bottom of the block up
                 const float di_next = i > l ? d[i - 1] : 0.f, ei_next = i > l ? e[i - 1] : 0.f;
                 float zi_next[NR];
