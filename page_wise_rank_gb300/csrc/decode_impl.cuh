@@ -966,8 +966,8 @@ __device__ __forceinline__ void patch_new_row(const DecodeParams &prm, unsigned 
 // copied on demand.  Asking L2 to prefetch the rest of the range as well made
 // back-to-back launches slower (the next launch's prefetches compete with the
 // current one's last copies and its completion) and the single launch no
-// faster, so the kernel does not; a CTA with a short range only keeps each
-// warp's next factor record beyond its slots in flight to L2.
+// faster, so the kernel does not; a CTA with a short range of bf16 records
+// only keeps each warp's next factor record beyond its slots in flight to L2.
 //
 // Overlap with the neighbouring launches (programmatic dependent launch): a
 // CTA lets the next launch start as soon as its own wait for the preceding
@@ -1077,10 +1077,12 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     const int n_mine = n_units > warp ? (n_units - 1 - warp) / NWC + 1 : 0;
     // A short range (a few units per warp) is latency-bound: each warp's
     // factor record one unit beyond its slots also goes to L2 ahead of time
-    // (32K tokens at batch 1: 427.5 -> 423.5 us per 32-layer step).  Long
-    // ranges keep their bandwidth for the slots' own copies (128K tokens and
-    // 16-request batches were 1.5-3 % slower with it).
-    const bool ahead = n_units <= 6 * NWC;
+    // (32K tokens at batch 1: 427.5 -> 423.5 us per 32-layer step; two units
+    // ahead: 444.5).  Long ranges keep their bandwidth for the slots' own
+    // copies (128K tokens and 16-request batches were 1.5-3 % slower with
+    // it), and so do INT4 records, whose kernel is bound by instruction
+    // issue (392.5 -> 412.5 us per step with it).
+    const bool ahead = !Q4 && n_units <= 6 * NWC;
     auto unit_of = [&](int u) -> int {
         return u < n_pre ? (int)sh.dense_units[u]
                          : (u < n_pre + n_fac ? (a1 + u - n_pre) << 3 : (a2 << 3) + sh.dense_units[u - n_fac]);
