@@ -112,18 +112,26 @@ def measured_peak_bf16():
 
 def factorization_roofline(wl, jobs, rotations, ms, sms, sm_mhz):
     """Rates of the prefill factorization against the two peaks that bound it.
-    FLOP conventions per page job (P x d page, P x P Gram):
-      Gram 2 P^2 d; projection 2 r P d (r the mean of r_K and r_V);
-      Householder reduction 2 P^3 (per reflection a matrix-vector product and
-      a rank-2 update of the trailing block, 6 n^2 summed over n < P);
-      forming the reflections' product 4/3 P^3; QL 6 P + 20 per plane
-      rotation (two columns of the eigenvector matrix, and the recurrence)."""
+    FLOP conventions per page job (P x d page, P x P Gram, rank r):
+      Gram 2 P^2 d; projection 2 r P d; Householder reduction 2 P^3 (per
+      reflection a matrix-vector product and a rank-2 update of the trailing
+      block, 6 n^2 summed over n < P).  Then, for r <= P / 2 (the top-r
+      eigenpairs): multisection 6 rounds x 32 Sturm counts x 3 P per
+      eigenvalue; inverse iteration 3 solves x 10 P per vector; Gram-Schmidt
+      3 passes x 2 r^2 P; the reflections applied to r vectors 2 P^2 r.  For
+      r > P / 2: forming the reflections' product 4/3 P^3 and QL 6 P + 20 per
+      plane rotation (two columns of the eigenvector matrix, and the
+      recurrence).  K and V jobs are half each."""
     P, d = wl["P"], wl["d"]
-    r = (wl["rk"] + wl["rv"]) / 2.0
     sec = ms * 1e-3
     gram = jobs * 2.0 * P * P * d
-    proj = jobs * 2.0 * r * P * d
-    eig = jobs * (2.0 + 4.0 / 3.0) * P ** 3 + rotations * (6.0 * P + 20.0)
+    proj, eig = 0.0, jobs * 2.0 * P ** 3 + rotations * (6.0 * P + 20.0)
+    for r in (wl["rk"], wl["rv"]):
+        proj += jobs / 2.0 * 2.0 * r * P * d
+        if 2 * r <= P:
+            eig += jobs / 2.0 * (6 * 32 * 3 * P * r + 3 * 10 * P * r + 3 * 2 * r * r * P + 2 * P * P * r)
+        else:
+            eig += jobs / 2.0 * (4.0 / 3.0) * P ** 3
     bf16_peak, bf16_kind = measured_peak_bf16()
     fp32_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # CUDA-core fp32 FMA lanes x 2 flops
     return {"page_jobs": int(jobs), "ql_rotations_per_job": round(rotations / max(jobs, 1), 1),

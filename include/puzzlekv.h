@@ -205,16 +205,18 @@ puzzlekv_status puzzlekv_background_stream(puzzlekv_store *store, void **stream)
 /*
  * Stateless batched page factorization [PuzzleKV §3.3 ③ and eq. (2)]:
  * for each of n independent pages X_i (P x d), G_i = X_i X_i^T in fp32, its
- * eigenvectors (Householder reduction to tridiagonal form, then implicit QL
- * with Wilkinson shifts, all in fp32), L_i = the top-r eigenvectors (P x r,
- * unit columns), R_i = L_i^T X_i (r x d).
+ * top-r eigenvectors, L_i (P x r, unit columns), and R_i = L_i^T X_i (r x d).
+ * The eigensolve runs in fp32: a Householder reduction to tridiagonal form,
+ * then, for r <= P / 2, multisection on Sturm counts for the eigenvalues
+ * and inverse iteration with partial pivoting for the r vectors, or, for
+ * r > P / 2, implicit QL with Wilkinson shifts on every eigenpair.
  *   X:      device, [n][P][d] in x_dtype (row = token).
  *   L, R:   device, [n][P][r] and [n][r][d] in out_dtype.
  *   sigma:  device fp32 [n][P] or NULL: sqrt of the eigenvalues (clamped at
  *           0), descending -- the singular values of X_i.
  *   status: device int32 or NULL; on return of the stream work, nonzero if
- *           an eigenvalue of any page took more than 30 QL iterations (its
- *           factors are still written).
+ *           an eigenvalue of any page took more than 30 QL iterations (r > P
+ *           / 2 only; its factors are still written).
  */
 puzzlekv_status puzzlekv_factorize_batch(const void *X, int32_t x_dtype, int64_t n, int32_t P, int32_t d,
                                          int32_t r, void *L, void *R, int32_t out_dtype, float *sigma,
@@ -400,7 +402,8 @@ puzzlekv_status puzzlekv_check_device_status(puzzlekv_store *store, void *stream
 /*
  * Synchronise `stream`, then read and clear the store's factorization
  * counters: page jobs factorized (one K or one V page each) and the QL
- * plane rotations their eigensolves applied, summed over every
+ * plane rotations their eigensolves applied (jobs of rank above P / 2: a
+ * smaller rank takes its top eigenpairs without QL), summed over every
  * factorization launch of the store (prefill, per-step and batched
  * conversion) since the last call.  For throughput accounting (the page has
  * no counterpart).  page_jobs and ql_rotations: host pointers, both

@@ -317,7 +317,8 @@ class Store:
 
     def factorize_counters(self, stream=None) -> tuple:
         """(page jobs, QL rotations) of the store's factorization launches since
-        the last call; the counters are cleared."""
+        the last call (rotations come only from jobs of rank above P / 2);
+        the counters are cleared."""
         jobs, rotations = ctypes.c_int64(0), ctypes.c_int64(0)
         check(lib().puzzlekv_factorize_counters(self._h, _stream(stream), ctypes.byref(jobs), ctypes.byref(rotations)))
         return jobs.value, rotations.value

@@ -7,11 +7,14 @@
 //   1. X -> shared memory (bf16 rows in the swizzled layout, or fp32 rows);
 //   2. G = X X^T in fp32: bf16 pages on tensor cores (mma.sync m16n8k16,
 //      bf16 products are exact in fp32), fp32 pages on CUDA cores;
-//   3. the eigenvectors of G: Householder reduction to tridiagonal form, the
-//      reflections' product formed explicitly, then implicit QL on the
-//      tridiagonal with every rotation applied to that product;
-//   4. eigenvalues ranked descending (ties: lower index first);
-//   5. L = Q_r, R = Q_r^T X in fp32, written as bf16 or fp32 into either a
+//   3. the top-r eigenvectors of G: Householder reduction to tridiagonal
+//      form, then for r <= P / 2 multisection for the eigenvalues, inverse
+//      iteration for the r vectors of the tridiagonal and the reflections
+//      applied to them; for larger r the reflections' product formed
+//      explicitly and implicit QL on the tridiagonal with every rotation
+//      applied to that product, eigenvalues ranked descending (ties: lower
+//      index first);
+//   4. L = Q_r, R = Q_r^T X in fp32, written as bf16 or fp32 into either a
 //      factor record (swizzled store layout) or plain row-major arrays.
 #include <cuda_fp16.h>
 
@@ -193,8 +196,9 @@ __device__ void gram_f32(FactorSmem<float, P, D> &s) {
 }
 
 // ---------------------------------------------------------------- eigensolve
-// Eigenvectors of the symmetric P x P matrix in s.G (both triangles), by
-// three classical steps:
+// Eigenvectors of the symmetric P x P matrix in s.G (both triangles).  For
+// ranks above P / 2, by three classical steps (smaller ranks replace steps 2
+// and 3 by the top-r steps further down):
 //   1. Householder reduction to tridiagonal form T = Q^T G Q, with P - 2
 //      reflections H_k = I - beta_k v_k v_k^T (v_k supported on the indices
 //      k+1 .. P-1), each applied to both sides of the trailing block as one
@@ -433,6 +437,267 @@ __device__ int ql_implicit(FactorSmem<T, P, D> &s, int max_it) {
     return rotations;
 }
 
+// ---------------------------------------------------------------- top-r eigenpairs
+// A rank r <= P / 2 needs only the r largest eigenpairs (and every
+// eigenvalue when the caller asks for the singular values), so the QL steps
+// 2 and 3 above give way to three others that cost a fraction of them:
+//   a. eigenvalues by multisection on Sturm counts (the number of negative
+//      pivots of T - x I, formed by the recurrence q_i = (t_ii - x) -
+//      t_{i-1,i}^2 / q_{i-1}, is the number of eigenvalues below x): one
+//      warp per eigenvalue, 32 points a round, BIS_ROUNDS rounds from the
+//      Gershgorin interval (33^6 > 2^30 subintervals, finer than fp32);
+//   b. eigenvectors of T by inverse iteration: INV_ITERS solves with
+//      T - lambda_k I = L D L^T (pivots below |T| 2^-23 moved out to that
+//      size), one thread per vector, from fixed pseudo-random starts, each
+//      round followed by modified Gram-Schmidt over the r vectors in
+//      descending eigenvalue order, which keeps the vectors of a cluster of
+//      eigenvalues apart;
+//   c. the reflections applied to the r vectors: Y <- H_0 ... H_{P-3} Y.
+// (Bisection on Sturm sequences: Barth, Martin and Wilkinson, "Calculation
+// of the eigenvalues of a symmetric tridiagonal matrix by the method of
+// bisection", 1967; inverse iteration: Wilkinson, "The Algebraic Eigenvalue
+// Problem", 1965, ch. 5 and 9.)  As in the QL steps, every sum is taken by
+// a fixed set of lanes in a fixed order and each eigenvalue and vector has
+// its own warp or thread, so the block size does not change a bit.
+constexpr int BIS_ROUNDS = 6;
+constexpr int INV_ITERS = 3;
+constexpr float PIVMIN = 1e-30f;  // a Sturm pivot at or below this counts as negative
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// Entry i of start vector k: a fixed pseudo-random value in [-1, 1) (an
+// integer hash of (i, k)).
+__device__ __forceinline__ float start_entry(int i, int k) {
+    uint32_t h = (uint32_t)i * 0x9E3779B1u + (uint32_t)k * 0x85EBCA77u + 0x165667B1u;
+    h ^= h >> 15;
+    h *= 0x2C1B3C6Du;
+    h ^= h >> 12;
+    return (float)(h & 0xFFFFFFu) * (1.f / 8388608.f) - 1.f;
+}
+
+// Step a for the NC eigenvalues k0 + u * NW (u < NC) of one warp, their
+// multisection chains interleaved.
+template <int P, int NW, int NC>
+__device__ __forceinline__ void bisect_chains(const float *d, const float *e, float gl, float gu, int k0, float *out) {
+    const int lane = threadIdx.x & 31;
+    const float step = (float)(lane + 1) * (1.f / 33.f);
+    float lo[NC], hi[NC];
+#pragma unroll
+    for (int u = 0; u < NC; ++u) {
+        lo[u] = gl;
+        hi[u] = gu;
+    }
+    for (int round = 0; round < BIS_ROUNDS; ++round) {
+        float x[NC], q[NC];
+        int c[NC];
+#pragma unroll
+        for (int u = 0; u < NC; ++u) {
+            x[u] = fmaf(hi[u] - lo[u], step, lo[u]);
+            q[u] = 1.f;
+            c[u] = 0;
+        }
+#pragma unroll 2
+        for (int i = 0; i < P; ++i) {
+            const float di = d[i], e2 = i > 0 ? e[i - 1] * e[i - 1] : 0.f;
+#pragma unroll
+            for (int u = 0; u < NC; ++u) {
+                const float t = fmaf(-e2, rcp_approx(q[u]), di - x[u]);
+                const bool neg = t <= PIVMIN;
+                c[u] += neg;
+                q[u] = neg ? fminf(t, -PIVMIN) : t;
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < NC; ++u) {  // the first point with more than j eigenvalues below it
+            const int j = P - 1 - (k0 + u * NW);
+            const unsigned bal = __ballot_sync(0xffffffffu, c[u] > j);
+            const int a = bal ? __ffs(bal) - 1 : 32;
+            const float xa = __shfl_sync(0xffffffffu, x[u], a & 31), xb = __shfl_sync(0xffffffffu, x[u], (a + 31) & 31);
+            if (a < 32) hi[u] = xa;
+            if (a > 0) lo[u] = xb;
+        }
+    }
+    if (lane == 0)
+#pragma unroll
+        for (int u = 0; u < NC; ++u) out[k0 + u * NW] = 0.5f * (lo[u] + hi[u]);
+}
+
+// Step a: the nk largest eigenvalues of the tridiagonal (lam, off) into
+// pv()[0 .. nk), descending.
+template <typename T, int P, int D, int NT>
+__device__ void eig_bisect(FactorSmem<T, P, D> &s, int nk) {
+    constexpr int NW = NT / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const float *d = s.lam(), *e = s.off();
+    float gl = INFINITY, gu = -INFINITY;
+    for (int i = lane; i < P; i += 32) {
+        const float a = (i > 0 ? fabsf(e[i - 1]) : 0.f) + (i < P - 1 ? fabsf(e[i]) : 0.f);
+        gl = fminf(gl, d[i] - a);
+        gu = fmaxf(gu, d[i] + a);
+    }
+    gl = -warp_max(-gl);
+    gu = warp_max(gu);
+    const float pad = fmaf(2e-6f, fmaxf(fabsf(gl), fabsf(gu)), 1e-30f);
+    gl -= pad;
+    gu += pad;
+    for (int k0 = warp; k0 < nk; k0 += 4 * NW) {
+        const int nc = min(4, (nk - k0 + NW - 1) / NW);
+        if (nc == 4) bisect_chains<P, NW, 4>(d, e, gl, gu, k0, s.pv());
+        else if (nc == 3) bisect_chains<P, NW, 3>(d, e, gl, gu, k0, s.pv());
+        else if (nc == 2) bisect_chains<P, NW, 2>(d, e, gl, gu, k0, s.pv());
+        else bisect_chains<P, NW, 1>(d, e, gl, gu, k0, s.pv());
+    }
+}
+
+// Modified Gram-Schmidt over the r columns of Y (pitch yp), then unit
+// length: column j loses its component along each earlier column k in turn.
+template <int P, int NT>
+__device__ void mgs_columns(float *Y, int yp, int r) {
+    constexpr int NW = NT / 32;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int k = 0; k < r - 1; ++k) {
+        float nk = 0.f;  // |y_k|^2, every warp alike
+        for (int i = lane; i < P; i += 32) nk = fmaf(Y[i * yp + k], Y[i * yp + k], nk);
+        nk = warp_sum(nk);
+        const float inv_nk = nk > 0.f ? 1.f / nk : 0.f;
+        for (int j = k + 1 + warp; j < r; j += NW) {
+            float dot = 0.f;
+            for (int i = lane; i < P; i += 32) dot = fmaf(Y[i * yp + k], Y[i * yp + j], dot);
+            const float c = warp_sum(dot) * inv_nk;
+            for (int i = lane; i < P; i += 32) Y[i * yp + j] = fmaf(-c, Y[i * yp + k], Y[i * yp + j]);
+        }
+        __syncthreads();
+    }
+    for (int k = warp; k < r; k += NW) {
+        float n2 = 0.f;
+        for (int i = lane; i < P; i += 32) n2 = fmaf(Y[i * yp + k], Y[i * yp + k], n2);
+        n2 = warp_sum(n2);
+        const float sc = n2 > 0.f ? 1.f / sqrtf(n2) : 0.f;
+        for (int i = lane; i < P; i += 32) Y[i * yp + k] *= sc;
+    }
+    __syncthreads();
+}
+
+// Step b: eigenvectors of the tridiagonal for the eigenvalues pv()[0 .. r)
+// into the columns of Y (P x r, pitch yp).  Each solve factors
+// T - lambda_k I = Pm L U by Gaussian elimination with partial pivoting
+// (rows i and i + 1 swap when the entry below the pivot is larger; U then
+// has a second superdiagonal, t_{i+1,i+2} at a swapped row), with b carried
+// along, then back-substitutes.  SC (P x nb floats each, pitch nb) hold the
+// reciprocal pivots and first superdiagonal of U for nb vectors at a time;
+// the swap bits stay in the solving thread's registers.  A pivot below
+// |T| 2^-23 is moved out to that size (rows swap at any size above 1e-30:
+// the trailing block of a page of rank r or less holds entries of about
+// that size, and its eigenvectors need the swaps).  Without the pivoting, a cluster of
+// eigenvalues near the fp32 resolution of |T| (a page of rank r or less)
+// comes out as a poorer basis of its subspace.
+template <typename T, int P, int D, int NT>
+__device__ void eig_vectors(FactorSmem<T, P, D> &s, int r, float *Y, int yp, float *SC, int nb) {
+    static_assert(P <= 64, "swap bits of one solve in 64 bits");
+    const int tid = threadIdx.x;
+    const float *d = s.lam(), *e = s.off(), *lam = s.pv();
+    float *IP = SC, *U1 = SC + P * nb;
+    for (int x = tid; x < P * r; x += NT) Y[(x / r) * yp + x % r] = start_entry(x / r, x % r);
+    float tiny = 0.f;
+    if (tid < nb) {
+        float tn = 0.f;
+        for (int i = 0; i < P; ++i)
+            tn = fmaxf(tn, fabsf(d[i]) + (i > 0 ? fabsf(e[i - 1]) : 0.f) + (i < P - 1 ? fabsf(e[i]) : 0.f));
+        tiny = fmaxf(tn * 1.1920929e-7f, 1e-30f);
+    }
+    __syncthreads();
+    for (int it = 0; it < INV_ITERS; ++it) {
+        for (int k0 = 0; k0 < r; k0 += nb) {
+            const int k = k0 + tid;
+            if (tid < nb && k < r) {
+                const float lk = lam[k];
+                auto moved = [&](float x) { return fabsf(x) < tiny ? (x < 0.f ? -tiny : tiny) : x; };
+                // row i of the elimination: pivot cd, superdiagonal cu, right side cb
+                float cd = d[0] - lk, cu = P > 1 ? e[0] : 0.f, cb = Y[k];
+                unsigned long long swaps = 0ull;
+                for (int i = 0; i < P - 1; ++i) {
+                    const float sub = e[i], nd = d[i + 1] - lk, nu = i + 1 < P - 1 ? e[i + 1] : 0.f;
+                    const float nbv = Y[(i + 1) * yp + k];
+                    const bool sw = fabsf(sub) > fmaxf(fabsf(cd), 1e-30f);  // 1 / sub stays finite
+                    const float ip = rcp_approx(sw ? sub : moved(cd));
+                    const float f = (sw ? cd : sub) * ip;
+                    IP[i * nb + tid] = ip;
+                    U1[i * nb + tid] = sw ? nd : cu;
+                    Y[i * yp + k] = sw ? nbv : cb;
+                    swaps |= (unsigned long long)sw << i;
+                    const float a = sw ? cu : nd, bq = sw ? nd : cu;
+                    const float b0 = sw ? cb : nbv, b1 = sw ? nbv : cb;
+                    cd = fmaf(-f, bq, a);
+                    cu = sw ? -f * nu : nu;
+                    cb = fmaf(-f, b1, b0);
+                }
+                const float ipl = rcp_approx(moved(cd));
+                // back substitution: y_i = (b_i - u1_i y_{i+1} - u2_i y_{i+2}) / u_ii,
+                // u2_i = t_{i+1,i+2} where rows i and i + 1 swapped
+                float y1 = cb * ipl, y2 = 0.f, amax = fabsf(y1);
+                Y[(P - 1) * yp + k] = y1;
+                for (int i = P - 2; i >= 0; --i) {
+                    const float u2 = (swaps >> i) & 1ull ? e[i + 1] : 0.f;
+                    const float y = fmaf(-U1[i * nb + tid], y1, fmaf(-u2, y2, Y[i * yp + k])) * IP[i * nb + tid];
+                    Y[i * yp + k] = y;
+                    amax = fmaxf(amax, fabsf(y));
+                    y2 = y1;
+                    y1 = y;
+                }
+                // scaled to max |y| in [1, 2) by a power of two; a vector that
+                // overflowed or vanished starts again from the unit vector e_k
+                const bool ok = amax > 0.f && amax < INFINITY;
+                const float sc = ok ? ldexpf(1.f, -ilogbf(amax)) : 0.f;
+                for (int i = 0; i < P; ++i) Y[i * yp + k] = ok ? Y[i * yp + k] * sc : (i == k ? 1.f : 0.f);
+            }
+            __syncthreads();
+        }
+        mgs_columns<P, NT>(Y, yp, r);
+    }
+}
+
+// Step c: Y <- H_0 H_1 ... H_{P-3} Y, a warp per column (four columns of a
+// warp interleaved); the reflections are read from s.G as the reduction left
+// them.
+template <typename T, int P, int D, int NT>
+__device__ void apply_reflections(FactorSmem<T, P, D> &s, float *Y, int yp, int r) {
+    constexpr int NW = NT / 32, CW = 4;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int k0 = warp; k0 < r; k0 += CW * NW) {
+        for (int m = P - 3; m >= 0; --m) {
+            const float beta = s.G[m][m + 1];
+            if (beta == 0.f) continue;
+            const int n = P - 1 - m;
+            const float v0 = s.G[m][m + 2];
+            float acc[CW];
+#pragma unroll
+            for (int u = 0; u < CW; ++u) acc[u] = 0.f;
+            for (int i = lane; i < n; i += 32) {
+                const float vi = i == 0 ? v0 : s.G[m + 1 + i][m];
+#pragma unroll
+                for (int u = 0; u < CW; ++u)
+                    if (k0 + u * NW < r) acc[u] = fmaf(vi, Y[(m + 1 + i) * yp + k0 + u * NW], acc[u]);
+            }
+#pragma unroll
+            for (int u = 0; u < CW; ++u) acc[u] = beta * warp_sum(acc[u]);
+            for (int i = lane; i < n; i += 32) {
+                const float vi = i == 0 ? v0 : s.G[m + 1 + i][m];
+#pragma unroll
+                for (int u = 0; u < CW; ++u)
+                    if (k0 + u * NW < r) {
+                        float &yv = Y[(m + 1 + i) * yp + k0 + u * NW];
+                        yv = fmaf(-acc[u], vi, yv);
+                    }
+            }
+        }
+    }
+    __syncthreads();
+}
+
 template <typename TO>
 __device__ __forceinline__ void store_elem(char *base, size_t idx, float v) {
     reinterpret_cast<TO *>(base)[idx] = Elem<TO>::from_f32(v);
@@ -568,8 +833,9 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
     }
 }
 
-// Returns the QL rotations the page took (0 if an eigenvalue hit the
-// iteration cap, which the status word records).
+// Returns the QL rotations the page took (0 for a rank up to P / 2, which
+// takes no QL, and if an eigenvalue hit the iteration cap, which the status
+// word records).
 template <typename T, int P, int D, int NT>
 __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, long job) {
     const int tid = threadIdx.x, lane = tid & 31;
@@ -596,30 +862,47 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
     }
     __syncthreads();
     tridiagonalize<T, P, D, NT>(s);
-    accumulate_q<T, P, D, NT>(s);  // starts with a barrier; X is dead here (the page comes back below)
-    if (tid < 32) {
-        const int rot = ql_implicit<T, P, D>(s, fp.max_ql_iter);
-        if (tid == 0) s.off()[0] = __int_as_float(rot);  // the off-diagonal is dead after QL
-    }
-    __syncthreads();
-    const int rotations = __float_as_int(s.off()[0]);
-    if (rotations < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
-    // each thread t < P ranks eigenvalue t (descending, ties: lower index
-    // first; a NaN ranks below every number, so the ranks stay a
-    // permutation) and moves eigenvector t into column rank(t) of G
     const int r = v.r;
-    if (tid < P) {
-        auto key = [](float x) { return x == x ? x : -INFINITY; };
-        const float li = key(s.lam()[tid]);
-        int rank = 0;
-        for (int j = 0; j < P; ++j) {
-            const float lj = key(s.lam()[j]);
-            rank += (lj > li) || (lj == li && j < tid);
+    int rotations = 0;
+    if (2 * r <= P) {  // the top r eigenpairs alone (steps a-c); X is dead here
+        __syncthreads();
+        eig_bisect<T, P, D, NT>(s, v.sigma ? P : r);
+        __syncthreads();
+        // Y (P x r, odd pitch) and the solves' scratch (2 nb floats a row)
+        // in the P x (P + 1) floats of s.Z: nb >= r / 2 as r <= P / 2
+        float *Y = &s.Z[0][0];
+        const int yp = r | 1, nb = min(r, (P + 1 - yp) / 2);
+        eig_vectors<T, P, D, NT>(s, r, Y, yp, Y + P * yp, nb);
+        apply_reflections<T, P, D, NT>(s, Y, yp, r);
+        if (v.sigma)
+            for (int k = tid; k < P; k += NT) v.sigma[k] = sqrtf(fmaxf(ldexpf(s.pv()[k], ex), 0.f));
+        for (int x = tid; x < P * r; x += NT) s.G[x / r][x % r] = Y[(x / r) * yp + x % r];
+        __syncthreads();
+    } else {
+        accumulate_q<T, P, D, NT>(s);  // starts with a barrier; X is dead here (the page comes back below)
+        if (tid < 32) {
+            const int rot = ql_implicit<T, P, D>(s, fp.max_ql_iter);
+            if (tid == 0) s.off()[0] = __int_as_float(rot);  // the off-diagonal is dead after QL
         }
-        if (v.sigma) v.sigma[rank] = sqrtf(fmaxf(ldexpf(s.lam()[tid], ex), 0.f));
-        for (int i = 0; i < P; ++i) s.G[i][rank] = s.Z[i][tid];
+        __syncthreads();
+        rotations = __float_as_int(s.off()[0]);
+        if (rotations < 0 && tid == 0 && fp.status) atomicAdd(fp.status + STATUS_NOT_CONVERGED, 1);
+        // each thread t < P ranks eigenvalue t (descending, ties: lower index
+        // first; a NaN ranks below every number, so the ranks stay a
+        // permutation) and moves eigenvector t into column rank(t) of G
+        if (tid < P) {
+            auto key = [](float x) { return x == x ? x : -INFINITY; };
+            const float li = key(s.lam()[tid]);
+            int rank = 0;
+            for (int j = 0; j < P; ++j) {
+                const float lj = key(s.lam()[j]);
+                rank += (lj > li) || (lj == li && j < tid);
+            }
+            if (v.sigma) v.sigma[rank] = sqrtf(fmaxf(ldexpf(s.lam()[tid], ex), 0.f));
+            for (int i = 0; i < P; ++i) s.G[i][rank] = s.Z[i][tid];
+        }
+        __syncthreads();
     }
-    __syncthreads();
     // the eigenvectors are out: the page again, for the projection (the
     // barriers below order it before its first read)
     load_page<T, P, D, NT>(s, v);
@@ -698,8 +981,8 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
 }
 
 // The 256-thread variant keeps four CTAs per SM (64 registers): while one
-// CTA's single warp runs the serial QL recurrence, the others' reductions
-// and updates fill the SM.
+// CTA's warps wait on a serial recurrence (a Sturm count, a solve, the QL
+// chase) or a barrier, the other CTAs' reductions and updates fill the SM.
 template <typename T, int P, int D, int NT>
 __global__ void __launch_bounds__(NT, NT == 256 ? 4 : 1) factorize_kernel(const FactorParams fp) {
     extern __shared__ __align__(128) unsigned char smem_raw[];

@@ -55,7 +55,7 @@ constexpr int STATUS_WORDS = 16;    // int32 status words at the workspace start
 constexpr int STATUS_NOT_CONVERGED = 0;
 constexpr int STATUS_TIMEOUT = 1;
 constexpr int STATUS_JOBS = 2;      // uint64 at words 2-3: page jobs factorized
-constexpr int STATUS_ROTATIONS = 4; // uint64 at words 4-5: QL rotations those jobs applied
+constexpr int STATUS_ROTATIONS = 4; // uint64 at words 4-5: QL rotations those jobs applied (rank > P / 2)
 
 PKV_HD int gcd8(int c) { return (c & 7) == 0 ? 8 : ((c & 3) == 0 ? 4 : ((c & 1) == 0 ? 2 : 1)); }
 

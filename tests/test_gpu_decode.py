@@ -110,15 +110,18 @@ def test_bf16_llama_shape_prefill_decode(pkv, T):
     run_decode_check(pkv, store, cfg, host, [1], 1, step=3, tol=TOL[torch.bfloat16])
 
 
-def test_factorize_counters_count_every_page_job(pkv):
+@pytest.mark.parametrize("rank", [(16, 24), (40, 8)])
+def test_factorize_counters_count_every_page_job(pkv, rank):
     """The store's factorization counters: one job per factorized K or V page
-    of every (layer, KV head), and the QL rotations of their eigensolves --
-    at least one pass over the whole tridiagonal (P - 1 rotations: no
-    off-diagonal entry of these pages' tridiagonal form is negligible at
-    first), at most the cap of 30 iterations of P - 1 rotations for each of
-    the P eigenvalues; reading clears them."""
+    of every (layer, KV head), and the QL rotations of their eigensolves.
+    Ranks up to P / 2 take the top-r eigenpairs without QL: no rotations.
+    A job of a larger rank (here the keys') runs QL: at least one pass over
+    the whole tridiagonal (P - 1 rotations: no off-diagonal entry of these
+    pages' tridiagonal form is negligible at first), at most the cap of 30
+    iterations of P - 1 rotations for each of the P eigenvalues.  Reading
+    clears them."""
     T = 4097
-    cfg = make_cfg(pkv, num_layers=2, num_kv_heads=4, num_q_heads=16)
+    cfg = make_cfg(pkv, num_layers=2, num_kv_heads=4, num_q_heads=16, rank_k=rank[0], rank_v=rank[1])
     store = pkv.Store(cfg)
     assert store.factorize_counters() == (0, 0)
     prefill(pkv, store, cfg, HostCache(), 0, T, rope=5e5)
@@ -126,7 +129,8 @@ def test_factorize_counters_count_every_page_job(pkv):
     n_fac = int((oracle.page_kinds(T, cfg.page_size, cfg.sink_tokens, cfg.recent_tokens) == oracle.FACTORED).sum())
     assert jobs == n_fac * cfg.num_layers * cfg.num_kv_heads * 2
     P = cfg.page_size
-    assert (P - 1) * jobs <= rotations <= 30 * P * (P - 1) * jobs
+    ql_jobs = sum(jobs // 2 for r in rank if r > P // 2)  # K and V jobs are half each
+    assert (P - 1) * ql_jobs <= rotations <= 30 * P * (P - 1) * ql_jobs
     assert store.factorize_counters() == (0, 0)
     assert store.check_device_status() == 0
 

@@ -58,12 +58,14 @@ def check_c5(X, L, R, S, r, tol=1e-3):
     return worst
 
 
-@pytest.mark.parametrize("P,d,r", [(64, 128, 16), (64, 128, 24), (32, 128, 16), (32, 64, 8), (16, 64, 8), (16, 128, 9)])
+@pytest.mark.parametrize("P,d,r", [(64, 128, 16), (64, 128, 24), (64, 128, 40), (32, 128, 16), (32, 64, 8), (16, 64, 8),
+                                   (16, 128, 9)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_factorize_batch_c5(pkv, P, d, r, dtype):
-    """Both stopping rules: without singular values the eigensolve stops once
-    the kept subspace is converged (the store's path); with them every
-    eigenpair converges.  Either way the reconstruction is within C5."""
+    """With and without singular values (with them every eigenvalue is
+    computed, without them only the kept ones when r <= P / 2, the store's
+    case), on both eigensolver paths (r <= P / 2: bisection and inverse
+    iteration; above: QL).  Either way the reconstruction is within C5."""
     X = pages(150, P, d, dtype, seed=P + d + r)
     L, R, S, status = pkv.factorize_batch(X.cuda(), r, out_dtype=torch.float32)
     torch.cuda.synchronize()
