@@ -235,9 +235,10 @@ __device__ __forceinline__ float quad_dot(int n, bool active, F prod) {
     return acc;
 }
 
-// Step 1.  On return lam[k] = T_kk, off[k] = T_{k,k+1} (off[P-1] = 0);
-// v_k stays in column k of s.G from row k+2 on, its first entry in
-// G[k][k+2], beta_k in G[k][k+1] (0: no reflection).
+// Step 1, on the lower triangle of s.G (the upper one is not read from the
+// first reflection on).  On return lam[k] = T_kk, off[k] = T_{k,k+1}
+// (off[P-1] = 0); v_k stays in column k of s.G from row k+2 on, its first
+// entry in G[k][k+2], beta_k in G[k][k+1] (0: no reflection).
 template <typename T, int P, int D, int NT>
 __device__ void tridiagonalize(FactorSmem<T, P, D> &s) {
     constexpr int NW = NT / 32;
@@ -264,26 +265,34 @@ __device__ void tridiagonalize(FactorSmem<T, P, D> &s) {
         }
         if (beta == 0.f) continue;  // the same decision in every warp
         auto vv = [&](int i) { return i == 0 ? v0 : s.G[k + 1 + i][k]; };
+        // entry (i, j) of S, from the lower triangle (the only one kept)
+        auto S = [&](int i, int j) { return j <= i ? s.G[k + 1 + i][k + 1 + j] : s.G[k + 1 + j][k + 1 + i]; };
         // p = beta S v: four lanes per row (warp-uniform loop bounds)
         for (int base = 8 * warp; base < n; base += NT / 4) {
             const int i = base + (lane >> 2);
-            const float acc =
-                quad_dot(n, i < n, [&](int j, float a) { return fmaf(s.G[k + 1 + i][k + 1 + j], vv(j), a); });
+            const float acc = quad_dot(n, i < n, [&](int j, float a) { return fmaf(S(i, j), vv(j), a); });
             if ((lane & 3) == 0 && i < n) s.pv()[i] = beta * acc;
         }
         __syncthreads();
-        // K = beta v.p / 2 (each warp), w = p - K v, S <- S - v w^T - w v^T,
-        // the entries (i, j) and (j, i) rounded alike
+        // K = beta v.p / 2 (each warp), w = p - K v, S <- S - v w^T - w v^T on
+        // the lower triangle.  Rows i and n - 1 - i share a warp pass (i + 1
+        // and n - i entries: n + 1 together), so that short rows leave no
+        // lanes idle.
         float vp = 0.f;
         for (int i = lane; i < n; i += 32) vp = fmaf(vv(i), s.pv()[i], vp);
         const float K = 0.5f * beta * warp_sum(vp);
-        for (int i = warp; i < n; i += NW)
-            for (int j = lane; j < n; j += 32) {
-                const int a = max(i, j), b = min(i, j);
-                const float va = vv(a), vb = vv(b);
-                const float wa = fmaf(-K, va, s.pv()[a]), wb = fmaf(-K, vb, s.pv()[b]);
-                s.G[k + 1 + i][k + 1 + j] -= fmaf(va, wb, __fmul_rn(wa, vb));
+        for (int pr = warp; 2 * pr < n; pr += NW) {
+            const int i1 = pr, i2 = n - 1 - pr, len1 = i1 + 1, len = i1 == i2 ? len1 : n + 1;
+            const float v1 = vv(i1), w1 = fmaf(-K, v1, s.pv()[i1]);
+            const float v2 = vv(i2), w2 = fmaf(-K, v2, s.pv()[i2]);
+            for (int t = lane; t < len; t += 32) {
+                const bool first = t < len1;
+                const int i = first ? i1 : i2, j = first ? t : t - len1;
+                const float vi = first ? v1 : v2, wi = first ? w1 : w2;
+                const float vj = vv(j), wj = fmaf(-K, vj, s.pv()[j]);
+                s.G[k + 1 + i][k + 1 + j] -= fmaf(vi, wj, __fmul_rn(wi, vj));
             }
+        }
         __syncthreads();
     }
     if (tid == 0) {
