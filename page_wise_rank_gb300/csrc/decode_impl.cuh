@@ -609,14 +609,15 @@ __device__ __forceinline__ void factored_unit_q4(WarpState<P, D> &w, const unsig
         return q4_reg(st[(wd >> 1) * 64 + (wd & 1)], m & 3);
     };
     // 1. t = (q o s_RK) C_RK^T: A = q o s_RK over the head dim (k-step ks holds
-    // columns 16 ks + 2c, +1 and 16 ks + 8 + 2c, +1: one uint2 of lane c's scales)
-    const uint2 *sRK = reinterpret_cast<const uint2 *>(rec + y.q_off_sRK) + c * (D / 16);
+    // columns 16 ks + 2c, +1 and 16 ks + 8 + 2c, +1: one uint2 of lane c's
+    // scales, the four lanes' uint2 contiguous)
+    const uint2 *sRK = reinterpret_cast<const uint2 *>(rec + y.q_off_sRK) + c;
     float t[MAXK][4];
 #pragma unroll
     for (int j = 0; j < MAXK; ++j) t[j][0] = t[j][1] = t[j][2] = t[j][3] = 0.f;
 #pragma unroll
     for (int ks = 0; ks < D / 16; ++ks) {
-        const uint2 sc = sRK[ks];
+        const uint2 sc = sRK[4 * ks];
         uint32_t h0, l0, h1, l1;
         mul_split_f16(w.qh[ks][0], sc.x, h0, l0);
         mul_split_f16(w.qh[ks][1], sc.y, h1, l1);
@@ -695,7 +696,9 @@ __device__ __forceinline__ void factored_unit_q4(WarpState<P, D> &w, const unsig
     uint32_t uhi[MAXV][1], ulo[MAXV][1];
 #pragma unroll
     for (int j = 0; j < MAXV; ++j) O::split(u[j][0] + u[j][2], u[j][1] + u[j][3], uhi[j][0], ulo[j][0]);
-    const __half2 *sRV = reinterpret_cast<const __half2 *>(rec + y.q_off_sRV) + c * (D / 8);
+    // head-dim tile nt's scales for lane c (columns 8 nt + 2c, +1): half2
+    // (nt / 2) 8 + 2c + nt % 2 in k-step order
+    const __half2 *sRV = reinterpret_cast<const __half2 *>(rec + y.q_off_sRV) + 2 * c;
     const int m0 = nvt * (P / 8), kf = nvt >> 1;  // R_V's first register; full k-steps
     uint32_t a0 = 0u, a1 = 0u;                    // the 8-wide last k-step's operand
 #pragma unroll
@@ -725,7 +728,7 @@ __device__ __forceinline__ void factored_unit_q4(WarpState<P, D> &w, const unsig
         }
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            const float2 sc = __half22float2(sRV[n0 + i]);
+            const float2 sc = __half22float2(sRV[((n0 + i) >> 1) * 8 + ((n0 + i) & 1)]);
             w.o[n0 + i][0] = fmaf(acc[i][0], sc.x, w.o[n0 + i][0]);
             w.o[n0 + i][1] = fmaf(acc[i][1], sc.y, w.o[n0 + i][1]);
             w.o[n0 + i][2] = fmaf(acc[i][2], sc.x, w.o[n0 + i][2]);

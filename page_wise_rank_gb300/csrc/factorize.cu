@@ -721,7 +721,8 @@ __device__ __forceinline__ void store_elem(char *base, size_t idx, float v) {
 //      Lt = L sigma^{1/2}, Rt = sigma^{-1/2} R (zero where sigma_j = 0);
 //   3. one fp16 scale per group, max|x| / 7 rounded to fp16: columns of L_K
 //      and of R_K / R_V (head-dim columns), rows of L_V (tokens), stored in
-//      accumulator-column order (q4_scale_index);
+//      accumulator-column order (q4_scale_index; the head-dim vectors in
+//      k-step order, q4_dscale_index);
 //   4. codes round(x / scale) (IEEE division, round half to even) clamped to
 //      [-7, 7], stored as code + 8 in the key or value stream's tensor-core
 //      operand order (q4_operand_elem), one 32-bit word per thread step.
@@ -779,8 +780,9 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
         for (int e = tid; e < P * rp; e += NT) v.qL[e] = s.G[e / rp][e % rp];
     if (v.qR)
         for (int e = tid; e < rp * D; e += NT) v.qR[e] = Rf[e];
-    // 3. scales: fp16 in the record (accumulator-column order), their fp32
-    // values in the scratch for the codes (sigma^{1/2} above is dead by now)
+    // 3. scales: fp16 in the record (accumulator-column order, the head-dim
+    // vectors in k-step order), their fp32 values in the scratch for the
+    // codes (sigma^{1/2} above is dead by now)
     float *scL = s.sc();       // per rank (keys) or per token (values): up to P
     float *scR = scL + P;      // per head-dim column: D
     unsigned char *rec = reinterpret_cast<unsigned char *>(v.rec);
@@ -807,7 +809,7 @@ __device__ void write_q4_record(FactorSmem<T, P, D> &s, const JobView &v, const 
         float m = 0.f;
         for (int j = 0; j < rp; ++j) m = fmaxf(m, fabsf(Rf[j * D + k]));
         const __half h = __float2half_rn(m / 7.f);
-        hR[q4_scale_index(D, k)] = h;
+        hR[q4_dscale_index(k)] = h;
         scR[k] = __half2float(h);
     }
     __syncthreads();

@@ -183,6 +183,12 @@ PKV_HD void q4_operand_elem(int K, int N, int m, int lane, int e, int &k, int &n
 // accumulator-column order: lane c's elements (8 t + 2c, 8 t + 2c + 1) for
 // t = 0 .. K/8 - 1 are contiguous, lanes c = 0..3 one after another.
 PKV_HD int q4_scale_index(int K, int i) { return ((i & 7) >> 1) * (K / 4) + (i >> 3) * 2 + (i & 1); }
+// Position of element n of a head-dim scale vector (s_RK, s_RV; the length
+// is a multiple of 16) in k-step order: per 16 columns, lane c's four
+// elements 2c, 2c + 1, 8 + 2c, 9 + 2c contiguous, lanes c = 0..3 one after
+// another, so the four lanes of a row read 32 contiguous bytes (one bank
+// each) instead of quarters 64 bytes apart (two on each bank).
+PKV_HD int q4_dscale_index(int n) { return (n >> 4) * 16 + ((n & 7) >> 1) * 4 + ((n >> 3) & 1) * 2 + (n & 1); }
 
 struct Layout {
     int L, H, Hq, G, d, P, rk, rv, rkp, rvp, sink_tokens, W, Bmax, Tmax, esz, dtype;
@@ -190,10 +196,11 @@ struct Layout {
     size_t rec_bytes, off_RK, off_LV, off_RV;
     // INT4 factor records [PuzzleKV §4.3] (q4 = 1): a key stream and a value
     // stream of 4-bit codes (code + 8) in tensor-core operand order (Q4Stream
-    // below), each a whole number of 256-byte slabs, then fp16 scales in
-    // accumulator-column order (q4_scale_index): s_RK [d] (per head-dim column
-    // of R_K), s_RV [d] (per head-dim column of R_V), s_LV [P] (per token row
-    // of L_V), s_LK [rkp] (per rank column of L_K).
+    // below), each a whole number of 256-byte slabs, then fp16 scales: s_RK
+    // [d] (per head-dim column of R_K) and s_RV [d] (per head-dim column of
+    // R_V) in k-step order (q4_dscale_index), s_LV [P] (per token row of L_V)
+    // and s_LK [rkp] (per rank column of L_K) in accumulator-column order
+    // (q4_scale_index).
     int q4;
     int q_kslabs, q_vslabs;  // 256-byte slabs of the key / value code streams
     // Keys stored before RoPE (rope = 1), turned at attention by

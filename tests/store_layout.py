@@ -149,6 +149,15 @@ def q4_scales(raw: np.ndarray, K: int) -> np.ndarray:
     return st[((i & 7) >> 1) * (K // 4) + (i >> 3) * 2 + (i & 1)]
 
 
+def q4_dscales(raw: np.ndarray, K: int) -> np.ndarray:
+    """fp16 head-dim scale vector of length K (a multiple of 16) stored in
+    k-step order (per 16 columns, lane c's elements 2c, 2c + 1, 8 + 2c,
+    9 + 2c contiguous), fp64 in natural order."""
+    st = np.frombuffer(np.asarray(raw, dtype=np.uint8)[: 2 * K].tobytes(), dtype=np.float16).astype(np.float64)
+    n = np.arange(K)
+    return st[(n >> 4) * 16 + ((n & 7) >> 1) * 4 + ((n >> 3) & 1) * 2 + (n & 1)]
+
+
 def read_record_q4(rec: np.ndarray, lay: Layout):
     """INT4 record -> codes and fp16 scales of each factor, as a dict
     {name: (codes [rows][cols] int8, scales fp64, per_row)} in the orientation
@@ -162,9 +171,9 @@ def read_record_q4(rec: np.ndarray, lay: Layout):
     LV_B, RV_B = _operand(vs, 0, P, rvp), _operand(vs, nv, rvp, d)  # B[token][rank], B[rank][head dim]
     pad = np.concatenate([ks[:, nk + rkp * P // 64:].ravel(), vs[:, nv + rvp * d // 64:].ravel()])
     return {"LK": (LK_B.T, q4_scales(rec[lay.q_off_sLK:], rkp), False),
-            "RK": (RK_B.T, q4_scales(rec[lay.q_off_sRK:], d), False),
+            "RK": (RK_B.T, q4_dscales(rec[lay.q_off_sRK:], d), False),
             "LVt": (LV_B.T, q4_scales(rec[lay.q_off_sLV:], P), False),
-            "RVt": (RV_B.T, q4_scales(rec[lay.q_off_sRV:], d), True),
+            "RVt": (RV_B.T, q4_dscales(rec[lay.q_off_sRV:], d), True),
             "pad": pad}
 
 

@@ -58,8 +58,8 @@ def check_c5(X, L, R, S, r, tol=1e-3):
     return worst
 
 
-@pytest.mark.parametrize("P,d,r", [(64, 128, 16), (64, 128, 24), (64, 128, 40), (32, 128, 16), (32, 64, 8), (16, 64, 8),
-                                   (16, 128, 9)])
+@pytest.mark.parametrize("P,d,r", [(64, 128, 16), (64, 128, 24), (64, 128, 1), (64, 128, 32), (64, 128, 40), (32, 128, 16),
+                                   (32, 64, 8), (16, 64, 8), (16, 128, 9)])
 @pytest.mark.parametrize("dtype", [torch.bfloat16, torch.float32])
 def test_factorize_batch_c5(pkv, P, d, r, dtype):
     """With and without singular values (with them every eigenvalue is
