@@ -596,23 +596,26 @@ __device__ void mgs_columns(float *Y, int yp, int r) {
 // T - lambda_k I = Pm L U by Gaussian elimination with partial pivoting
 // (rows i and i + 1 swap when the entry below the pivot is larger; U then
 // has a second superdiagonal, t_{i+1,i+2} at a swapped row), with b carried
-// along, then back-substitutes.  SC (P x nb floats each, pitch nb) hold the
-// reciprocal pivots and first superdiagonal of U for nb vectors at a time;
-// the swap bits stay in the solving thread's registers.  A pivot below
-// |T| 2^-23 is moved out to that size (rows swap at any size above 1e-30:
-// the trailing block of a page of rank r or less holds entries of about
-// that size, and its eigenvectors need the swaps).  Without the pivoting, a cluster of
+// along, then back-substitutes.  The swap bits stay in the solving thread's
+// registers and SC (P x r floats, pitch r) keeps one float per row: the
+// multiplier of a swapped row, else the reciprocal pivot.  The back
+// substitution recomputes the rest from the tridiagonal, bit for bit: a
+// swapped row's pivot is t_{i+1,i} and its superdiagonal t_{i+1,i+1} -
+// lambda; an unswapped row's superdiagonal is t_{i,i+1}, times minus the
+// multiplier of row i - 1 if that one swapped.  A pivot below |T| 2^-23 is
+// moved out to that size (rows swap at any size above 1e-30: the trailing
+// block of a page of rank r or less holds entries of about that size, and
+// its eigenvectors need the swaps).  Without the pivoting, a cluster of
 // eigenvalues near the fp32 resolution of |T| (a page of rank r or less)
 // comes out as a poorer basis of its subspace.
 template <typename T, int P, int D, int NT>
-__device__ void eig_vectors(FactorSmem<T, P, D> &s, int r, float *Y, int yp, float *SC, int nb) {
+__device__ void eig_vectors(FactorSmem<T, P, D> &s, int r, float *Y, int yp, float *SC) {
     static_assert(P <= 64, "swap bits of one solve in 64 bits");
     const int tid = threadIdx.x;
     const float *d = s.lam(), *e = s.off(), *lam = s.pv();
-    float *IP = SC, *U1 = SC + P * nb;
     for (int x = tid; x < P * r; x += NT) Y[(x / r) * yp + x % r] = start_entry(x / r, x % r);
     float tiny = 0.f;
-    if (tid < nb) {
+    if (tid < r) {
         float tn = 0.f;
         for (int i = 0; i < P; ++i)
             tn = fmaxf(tn, fabsf(d[i]) + (i > 0 ? fabsf(e[i - 1]) : 0.f) + (i < P - 1 ? fabsf(e[i]) : 0.f));
@@ -620,51 +623,54 @@ __device__ void eig_vectors(FactorSmem<T, P, D> &s, int r, float *Y, int yp, flo
     }
     __syncthreads();
     for (int it = 0; it < INV_ITERS; ++it) {
-        for (int k0 = 0; k0 < r; k0 += nb) {
-            const int k = k0 + tid;
-            if (tid < nb && k < r) {
-                const float lk = lam[k];
-                auto moved = [&](float x) { return fabsf(x) < tiny ? (x < 0.f ? -tiny : tiny) : x; };
-                // row i of the elimination: pivot cd, superdiagonal cu, right side cb
-                float cd = d[0] - lk, cu = P > 1 ? e[0] : 0.f, cb = Y[k];
-                unsigned long long swaps = 0ull;
-                for (int i = 0; i < P - 1; ++i) {
-                    const float sub = e[i], nd = d[i + 1] - lk, nu = i + 1 < P - 1 ? e[i + 1] : 0.f;
-                    const float nbv = Y[(i + 1) * yp + k];
-                    const bool sw = fabsf(sub) > fmaxf(fabsf(cd), 1e-30f);  // 1 / sub stays finite
-                    const float ip = rcp_approx(sw ? sub : moved(cd));
-                    const float f = (sw ? cd : sub) * ip;
-                    IP[i * nb + tid] = ip;
-                    U1[i * nb + tid] = sw ? nd : cu;
-                    Y[i * yp + k] = sw ? nbv : cb;
-                    swaps |= (unsigned long long)sw << i;
-                    const float a = sw ? cu : nd, bq = sw ? nd : cu;
-                    const float b0 = sw ? cb : nbv, b1 = sw ? nbv : cb;
-                    cd = fmaf(-f, bq, a);
-                    cu = sw ? -f * nu : nu;
-                    cb = fmaf(-f, b1, b0);
-                }
-                const float ipl = rcp_approx(moved(cd));
-                // back substitution: y_i = (b_i - u1_i y_{i+1} - u2_i y_{i+2}) / u_ii,
-                // u2_i = t_{i+1,i+2} where rows i and i + 1 swapped
-                float y1 = cb * ipl, y2 = 0.f, amax = fabsf(y1);
-                Y[(P - 1) * yp + k] = y1;
-                for (int i = P - 2; i >= 0; --i) {
-                    const float u2 = (swaps >> i) & 1ull ? e[i + 1] : 0.f;
-                    const float y = fmaf(-U1[i * nb + tid], y1, fmaf(-u2, y2, Y[i * yp + k])) * IP[i * nb + tid];
-                    Y[i * yp + k] = y;
-                    amax = fmaxf(amax, fabsf(y));
-                    y2 = y1;
-                    y1 = y;
-                }
-                // scaled to max |y| in [1, 2) by a power of two; a vector that
-                // overflowed or vanished starts again from the unit vector e_k
-                const bool ok = amax > 0.f && amax < INFINITY;
-                const float sc = ok ? ldexpf(1.f, -ilogbf(amax)) : 0.f;
-                for (int i = 0; i < P; ++i) Y[i * yp + k] = ok ? Y[i * yp + k] * sc : (i == k ? 1.f : 0.f);
+        if (tid < r) {
+            const int k = tid;
+            const float lk = lam[k];
+            auto moved = [&](float x) { return fabsf(x) < tiny ? (x < 0.f ? -tiny : tiny) : x; };
+            // row i of the elimination: pivot cd, superdiagonal cu, right side cb
+            float cd = d[0] - lk, cu = e[0], cb = Y[k];
+            unsigned long long swaps = 0ull;
+            for (int i = 0; i < P - 1; ++i) {
+                const float sub = e[i], nd = d[i + 1] - lk, nu = i + 1 < P - 1 ? e[i + 1] : 0.f;
+                const float nbv = Y[(i + 1) * yp + k];
+                const bool sw = fabsf(sub) > fmaxf(fabsf(cd), 1e-30f);  // 1 / sub stays finite
+                const float ip = rcp_approx(sw ? sub : moved(cd));
+                const float f = (sw ? cd : sub) * ip;
+                SC[i * r + k] = sw ? f : ip;
+                Y[i * yp + k] = sw ? nbv : cb;
+                swaps |= (unsigned long long)sw << i;
+                const float a = sw ? cu : nd, bq = sw ? nd : cu;
+                const float b0 = sw ? cb : nbv, b1 = sw ? nbv : cb;
+                cd = fmaf(-f, bq, a);
+                cu = sw ? -f * nu : nu;
+                cb = fmaf(-f, b1, b0);
             }
-            __syncthreads();
+            const float ipl = rcp_approx(moved(cd));
+            // back substitution: y_i = (b_i - u1_i y_{i+1} - u2_i y_{i+2}) / u_ii,
+            // u2_i = t_{i+1,i+2} where rows i and i + 1 swapped
+            float y1 = cb * ipl, y2 = 0.f, amax = fabsf(y1);
+            Y[(P - 1) * yp + k] = y1;
+            float sl = SC[(P - 2) * r + k];
+            for (int i = P - 2; i >= 0; --i) {
+                const bool sw = (swaps >> i) & 1ull, swp = i > 0 && ((swaps >> (i - 1)) & 1ull);
+                const float slp = i > 0 ? SC[(i - 1) * r + k] : 0.f;
+                const float ip = sw ? rcp_approx(e[i]) : sl;
+                const float u1 = sw ? d[i + 1] - lk : (swp ? -slp * e[i] : e[i]);
+                const float u2 = sw ? e[i + 1] : 0.f;
+                const float y = fmaf(-u1, y1, fmaf(-u2, y2, Y[i * yp + k])) * ip;
+                Y[i * yp + k] = y;
+                amax = fmaxf(amax, fabsf(y));
+                y2 = y1;
+                y1 = y;
+                sl = slp;
+            }
+            // scaled to max |y| in [1, 2) by a power of two; a vector that
+            // overflowed or vanished starts again from the unit vector e_k
+            const bool ok = amax > 0.f && amax < INFINITY;
+            const float sc = ok ? ldexpf(1.f, -ilogbf(amax)) : 0.f;
+            for (int i = 0; i < P; ++i) Y[i * yp + k] = ok ? Y[i * yp + k] * sc : (i == k ? 1.f : 0.f);
         }
+        __syncthreads();
         mgs_columns<P, NT>(Y, yp, r);
     }
 }
@@ -879,11 +885,11 @@ __device__ int factorize_one(FactorSmem<T, P, D> &s, const FactorParams &fp, lon
         __syncthreads();
         eig_bisect<T, P, D, NT>(s, v.sigma ? P : r);
         __syncthreads();
-        // Y (P x r, odd pitch) and the solves' scratch (2 nb floats a row)
-        // in the P x (P + 1) floats of s.Z: nb >= r / 2 as r <= P / 2
+        // Y (P x r, odd pitch) and the solves' scratch (P x r) in the
+        // P x (P + 1) floats of s.Z: P (2r + 1) fits as r <= P / 2
         float *Y = &s.Z[0][0];
-        const int yp = r | 1, nb = min(r, (P + 1 - yp) / 2);
-        eig_vectors<T, P, D, NT>(s, r, Y, yp, Y + P * yp, nb);
+        const int yp = r | 1;
+        eig_vectors<T, P, D, NT>(s, r, Y, yp, Y + P * yp);
         apply_reflections<T, P, D, NT>(s, Y, yp, r);
         if (v.sigma)
             for (int k = tid; k < P; k += NT) v.sigma[k] = sqrtf(fmaxf(ldexpf(s.pv()[k], ex), 0.f));
