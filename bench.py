@@ -461,14 +461,20 @@ def gpu_arm(args, rank, world, local):
                              "step's decode_step calls through the library's C ABI, one of the outputs after"}
         # ---- one batched page conversion alone: decode steps (untimed, no
         # conversion) up to the next page boundary, then the batch that the
-        # boundary makes due, timed with the caller's stream waiting for it
-        while (store_len[0] + 1) % P != 0:
+        # boundary makes due, timed with the caller's stream waiting for it.
+        # The steps cycle through the generated tokens, so the pages they
+        # complete hold distinct rows like the timed steps' pages (one token
+        # repeated would give pages of rank 1, which QL deflates at once)
+        j = 0
+        while True:
+            last = (store_len[0] + 1) % P == 0
             for l in range(L):
-                store.decode_step(l, qs[-1][l], ks[-1][l], vs[-1][l], out[l], seqs, stream=stream)
+                store.decode_step(l, qs[j % len(qs)][l], ks[j % len(ks)][l], vs[j % len(vs)][l], out[l], seqs,
+                                  stream=stream)
             store_len[0] += 1
-        for l in range(L):
-            store.decode_step(l, qs[-1][l], ks[-1][l], vs[-1][l], out[l], seqs, stream=stream)
-        store_len[0] += 1
+            j += 1
+            if last:
+                break
         stream.synchronize()
         # the store paces its batches (a new one starts when the last has
         # finished, about one CTA per SM each): time every batch the boundary
