@@ -456,11 +456,11 @@ __device__ int ql_implicit(FactorSmem<T, P, D> &s, int max_it) {
 //      warp per eigenvalue, 32 points a round, BIS_ROUNDS rounds from the
 //      Gershgorin interval (33^6 > 2^30 subintervals, finer than fp32);
 //   b. eigenvectors of T by inverse iteration: INV_ITERS solves with
-//      T - lambda_k I = L D L^T (pivots below |T| 2^-23 moved out to that
-//      size), one thread per vector, from fixed pseudo-random starts, each
-//      round followed by modified Gram-Schmidt over the r vectors in
-//      descending eigenvalue order, which keeps the vectors of a cluster of
-//      eigenvalues apart;
+//      T - lambda_k I by Gaussian elimination with partial pivoting, one
+//      thread per vector, from fixed pseudo-random starts, each round
+//      followed by modified Gram-Schmidt over the r vectors in descending
+//      eigenvalue order, which keeps the vectors of a cluster of eigenvalues
+//      apart;
 //   c. the reflections applied to the r vectors: Y <- H_0 ... H_{P-3} Y.
 // (Bisection on Sturm sequences: Barth, Martin and Wilkinson, "Calculation
 // of the eigenvalues of a symmetric tridiagonal matrix by the method of
@@ -603,11 +603,11 @@ __device__ void mgs_columns(float *Y, int yp, int r) {
 // swapped row's pivot is t_{i+1,i} and its superdiagonal t_{i+1,i+1} -
 // lambda; an unswapped row's superdiagonal is t_{i,i+1}, times minus the
 // multiplier of row i - 1 if that one swapped.  A pivot below |T| 2^-23 is
-// moved out to that size (rows swap at any size above 1e-30: the trailing
-// block of a page of rank r or less holds entries of about that size, and
-// its eigenvectors need the swaps).  Without the pivoting, a cluster of
-// eigenvalues near the fp32 resolution of |T| (a page of rank r or less)
-// comes out as a poorer basis of its subspace.
+// moved out to that size.  Rows swap whenever the entry below is the larger
+// one and above 1e-30 (so that its reciprocal stays finite), however small:
+// the trailing block of a page of rank r or less holds entries near the
+// fp32 resolution of |T|, and without the swaps the cluster of eigenvalues
+// there came out as a poorer basis of its subspace.
 template <typename T, int P, int D, int NT>
 __device__ void eig_vectors(FactorSmem<T, P, D> &s, int r, float *Y, int yp, float *SC) {
     static_assert(P <= 64, "swap bits of one solve in 64 bits");
