@@ -1081,10 +1081,13 @@ __global__ void __launch_bounds__(DecodeShape<Q4, P, ROPE, D, RKT, RVT>::NWC * 3
     // A short range (a few units per warp) is latency-bound: each warp's
     // factor record one unit beyond its slots also goes to L2 ahead of time
     // (32K tokens at batch 1: 427.5 -> 423.5 us per 32-layer step; two units
-    // ahead: 444.5).  Long ranges keep their bandwidth for the slots' own
-    // copies (128K tokens and 16-request batches were 1.5-3 % slower with
-    // it), and so do INT4 records, whose kernel is bound by instruction
-    // issue (392.5 -> 412.5 us per step with it).
+    // ahead: 444.5).  The first such request goes out with the first copies;
+    // a refill's request pays only when the record that refill copies is in
+    // L2 already (refill requests alone: 463 us).  Long ranges keep their
+    // bandwidth for the slots' own copies (128K tokens and 16-request
+    // batches were 1.5-3 % slower with it), and so do INT4 records, whose
+    // kernel is bound by instruction issue (392.5 -> 412.5 us per step with
+    // it).
     const bool ahead = !Q4 && n_units <= 6 * NWC;
     auto unit_of = [&](int u) -> int {
         return u < n_pre ? (int)sh.dense_units[u]
