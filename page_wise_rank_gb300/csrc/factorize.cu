@@ -677,35 +677,52 @@ __device__ void eig_vectors(FactorSmem<T, P, D> &s, int r, float *Y, int yp, flo
 
 // Step c: Y <- H_0 H_1 ... H_{P-3} Y, a warp per column (four columns of a
 // warp interleaved); the reflections are read from s.G as the reduction left
-// them.
+// them.  They go two at a time, H_{m-1} H_m: with a = v_m^T y, b =
+// v_{m-1}^T y and c = v_{m-1}^T v_m, one pass of sums gives
+// y <- y - v_m (beta_m a) - v_{m-1} beta_{m-1} (b - c beta_m a),
+// so the warp waits on one reduction per pair instead of one per reflection.
 template <typename T, int P, int D, int NT>
 __device__ void apply_reflections(FactorSmem<T, P, D> &s, float *Y, int yp, int r) {
     constexpr int NW = NT / 32, CW = 4;
+    static_assert((P - 2) % 2 == 0, "the reflections pair up");
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     for (int k0 = warp; k0 < r; k0 += CW * NW) {
-        for (int m = P - 3; m >= 0; --m) {
-            const float beta = s.G[m][m + 1];
-            if (beta == 0.f) continue;
-            const int n = P - 1 - m;
-            const float v0 = s.G[m][m + 2];
-            float acc[CW];
+        for (int m = P - 3; m >= 1; m -= 2) {
+            // H_m acts on rows m + 1 .., H_{m-1} on rows m ..; beta 0: no reflection
+            const float b1 = s.G[m][m + 1], b0 = s.G[m - 1][m];
+            if (b1 == 0.f && b0 == 0.f) continue;
+            const float v1_0 = s.G[m][m + 2], v0_0 = s.G[m - 1][m + 1];
+            // entries at absolute row R of v_m (R >= m + 1) and v_{m-1} (R >= m)
+            auto v1 = [&](int R) { return R == m + 1 ? v1_0 : (R > m + 1 ? s.G[R][m] : 0.f); };
+            auto v0 = [&](int R) { return R == m ? v0_0 : s.G[R][m - 1]; };
+            float a[CW], b[CW], c = 0.f;
 #pragma unroll
-            for (int u = 0; u < CW; ++u) acc[u] = 0.f;
-            for (int i = lane; i < n; i += 32) {
-                const float vi = i == 0 ? v0 : s.G[m + 1 + i][m];
-#pragma unroll
-                for (int u = 0; u < CW; ++u)
-                    if (k0 + u * NW < r) acc[u] = fmaf(vi, Y[(m + 1 + i) * yp + k0 + u * NW], acc[u]);
-            }
-#pragma unroll
-            for (int u = 0; u < CW; ++u) acc[u] = beta * warp_sum(acc[u]);
-            for (int i = lane; i < n; i += 32) {
-                const float vi = i == 0 ? v0 : s.G[m + 1 + i][m];
+            for (int u = 0; u < CW; ++u) a[u] = b[u] = 0.f;
+            for (int R = m + lane; R < P; R += 32) {
+                const float x1 = v1(R), x0 = v0(R);
+                c = fmaf(x0, x1, c);
 #pragma unroll
                 for (int u = 0; u < CW; ++u)
                     if (k0 + u * NW < r) {
-                        float &yv = Y[(m + 1 + i) * yp + k0 + u * NW];
-                        yv = fmaf(-acc[u], vi, yv);
+                        const float yv = Y[R * yp + k0 + u * NW];
+                        a[u] = fmaf(x1, yv, a[u]);
+                        b[u] = fmaf(x0, yv, b[u]);
+                    }
+            }
+            c = warp_sum(c);
+            float t1[CW], t0[CW];
+#pragma unroll
+            for (int u = 0; u < CW; ++u) {
+                t1[u] = b1 * warp_sum(a[u]);
+                t0[u] = b0 * fmaf(-c, t1[u], warp_sum(b[u]));
+            }
+            for (int R = m + lane; R < P; R += 32) {
+                const float x1 = v1(R), x0 = v0(R);
+#pragma unroll
+                for (int u = 0; u < CW; ++u)
+                    if (k0 + u * NW < r) {
+                        float &yv = Y[R * yp + k0 + u * NW];
+                        yv = fmaf(-t0[u], x0, fmaf(-t1[u], x1, yv));
                     }
             }
         }
