@@ -97,6 +97,25 @@ def test_int4_operand_order_covers_each_element_once(K, N):
     assert m.max() == K * N // 64 - 1
 
 
+@pytest.mark.parametrize("K", [64, 128])
+def test_int4_head_dim_scales_in_k_step_order(K):
+    """The reader of the head-dim scale vectors (s_RK, s_RV) places column
+    16 ks + 8 b + 2 c + e at 16 ks + 4 c + 2 b + e: per 16 columns the four
+    lanes c of a row own 4 contiguous halves (the uint2 the decode loads at
+    k-step ks), and every column lands once."""
+    from store_layout import q4_dscales
+    raw = np.arange(K, dtype=np.float16).view(np.uint8)  # stored value = storage position
+    got = q4_dscales(raw, K).astype(int)
+    want = np.empty(K, dtype=int)
+    for ks in range(K // 16):
+        for c in range(4):
+            for b in range(2):
+                for e in range(2):
+                    want[16 * ks + 8 * b + 2 * c + e] = 16 * ks + 4 * c + 2 * b + e
+    assert np.array_equal(got, want)
+    assert sorted(got.tolist()) == list(range(K))
+
+
 @pytest.mark.parametrize("bad,status", [
     (dict(head_dim=96), 2), (dict(page_size=128), 2), (dict(num_q_heads=33), 1),
     (dict(num_q_heads=8 * 16), 2), (dict(rank_k=0), 1), (dict(rank_v=65), 1),
